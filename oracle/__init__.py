@@ -1,0 +1,239 @@
+"""Plain CPU oracle for the quantized K/V cache path (ctypes over kvq_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's CPU
+baseline leg may import this package; the product path (the CUDA library and
+its Python binding) never does, and it shares no code with it.
+
+Functions take and return numpy arrays in the layouts documented in
+kvq_oracle.h.  fp16 values travel as their uint16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvq_oracle.c")
+_HDR = os.path.join(_HERE, "kvq_oracle.h")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkvq_oracle.so")
+
+FMT_F16 = 0
+FMT_Q8 = 1
+GROUP = 64
+
+# No FMA contraction and no fast-math: float division, fabsf and rintf keep
+# their IEEE meaning (round-to-nearest-even is the default mode).
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+          "-fno-fast-math", "-fno-strict-aliasing"]
+
+
+def build(force: bool = False) -> str:
+    """Compile kvq_oracle.c into a shared library (gcc); returns its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    newest_src = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= newest_src):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.kvo_fp16_from_float.restype = ctypes.c_uint16
+    lib.kvo_fp16_from_float.argtypes = [ctypes.c_float]
+    lib.kvo_fp16_to_float.restype = ctypes.c_float
+    lib.kvo_fp16_to_float.argtypes = [ctypes.c_uint16]
+    lib.kvo_fp16_from_float_array.restype = None
+    lib.kvo_fp16_from_float_array.argtypes = [P, P, ctypes.c_int64]
+    lib.kvo_fp16_to_float_array.restype = None
+    lib.kvo_fp16_to_float_array.argtypes = [P, P, ctypes.c_int64]
+    lib.kvo_quantize_row_q8.restype = I
+    lib.kvo_quantize_row_q8.argtypes = [P, I, P, P]
+    lib.kvo_append.restype = I
+    lib.kvo_append.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, P, P, P, I]
+    lib.kvo_attention.restype = I
+    lib.kvo_attention.argtypes = [I, I, I, I, I, P, P, P, P, P, I, I, I, P, P, I,
+                                  ctypes.c_float, P]
+    lib.kvo_compact_f16.restype = I
+    lib.kvo_compact_f16.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, P]
+    return lib
+
+
+_lib = None
+_override = None
+
+
+def _load():
+    global _lib
+    if _override is not None:
+        return _override
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+class use_library:
+    """Context manager: route this module's functions to another build of
+    kvq_oracle.c (the tests use it to run the pins against planted mistakes)."""
+
+    def __init__(self, so_path: str):
+        self._lib = _bind(ctypes.CDLL(so_path))
+
+    def __enter__(self):
+        global _override
+        self._prev = _override
+        _override = self._lib
+        return self
+
+    def __exit__(self, *exc):
+        global _override
+        _override = self._prev
+        return False
+
+
+def build_variant(src_text: str, out_dir: str, name: str) -> str:
+    """Compile a (modified) copy of kvq_oracle.c with the oracle's flags."""
+    os.makedirs(out_dir, exist_ok=True)
+    src = os.path.join(out_dir, name + ".c")
+    with open(src, "w") as f:
+        f.write(src_text)
+    so = os.path.join(out_dir, "lib" + name + ".so")
+    subprocess.run(["gcc", *CFLAGS, "-I", _HERE, "-o", so, src, "-lm"], check=True)
+    return so
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --------------------------------------------------------------------------
+# fp16
+# --------------------------------------------------------------------------
+
+def fp16_bits(x) -> np.ndarray:
+    """Round float32 values to IEEE binary16 (nearest, ties to even); bits."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().kvo_fp16_from_float_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def fp16_value(bits) -> np.ndarray:
+    """Decode binary16 bit patterns to float32."""
+    bits = _c(bits, np.uint16)
+    out = np.empty(bits.shape, dtype=np.float32)
+    _load().kvo_fp16_to_float_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+# --------------------------------------------------------------------------
+# quantization
+# --------------------------------------------------------------------------
+
+def quantize_rows_q8(x):
+    """Quantize rows of x [..., hd] -> (codes int8 [..., hd], scales uint16 [..., hd/64])."""
+    x = _c(x, np.float32)
+    hd = x.shape[-1]
+    if hd % GROUP:
+        raise ValueError("head_dim must be a multiple of 64")
+    rows = x.reshape(-1, hd)
+    codes = np.empty(rows.shape, dtype=np.int8)
+    scales = np.empty((rows.shape[0], hd // GROUP), dtype=np.uint16)
+    lib = _load()
+    for i in range(rows.shape[0]):
+        rc = lib.kvo_quantize_row_q8(_ptr(rows[i]), hd, _ptr(codes[i]), _ptr(scales[i]))
+        if rc != 0:
+            raise RuntimeError(f"kvo_quantize_row_q8 failed: {rc}")
+    return codes.reshape(x.shape), scales.reshape(x.shape[:-1] + (hd // GROUP,))
+
+
+# --------------------------------------------------------------------------
+# paged cache image
+# --------------------------------------------------------------------------
+
+class PoolImage:
+    """Host image of one layer's paged pool, in the library's layout."""
+
+    def __init__(self, fmt: int, n_kv: int, head_dim: int, block_size: int, n_blocks: int):
+        self.fmt, self.n_kv, self.head_dim = fmt, n_kv, head_dim
+        self.block_size, self.n_blocks = block_size, n_blocks
+        shape = (n_blocks, n_kv, block_size, head_dim)
+        dt = np.uint16 if fmt == FMT_F16 else np.int8
+        self.k = np.zeros(shape, dtype=dt)
+        self.v = np.zeros(shape, dtype=dt)
+        if fmt == FMT_Q8:
+            sshape = (n_blocks, n_kv, block_size, head_dim // GROUP)
+            self.ks = np.zeros(sshape, dtype=np.uint16)
+            self.vs = np.zeros(sshape, dtype=np.uint16)
+        else:
+            self.ks = None
+            self.vs = None
+
+    def geometry(self):
+        return (self.fmt, self.n_kv, self.head_dim, self.block_size, self.n_blocks)
+
+
+def append(pool: PoolImage, k, v, tok_seq, tok_pos, block_table) -> None:
+    """Quantize-on-write (or fp16 store) of n_tok new cells into the pool image."""
+    k = _c(k, np.float32)
+    v = _c(v, np.float32)
+    tok_seq = _c(tok_seq, np.int32)
+    tok_pos = _c(tok_pos, np.int32)
+    bt = _c(block_table, np.int32)
+    n_tok = tok_seq.shape[0]
+    assert k.shape == (n_tok, pool.n_kv, pool.head_dim) and v.shape == k.shape
+    rc = _load().kvo_append(*pool.geometry(), _ptr(pool.k), _ptr(pool.v),
+                            _ptr(pool.ks), _ptr(pool.vs), _ptr(k), _ptr(v), n_tok,
+                            _ptr(tok_seq), _ptr(tok_pos), _ptr(bt), bt.shape[1])
+    if rc != 0:
+        raise RuntimeError(f"kvo_append failed: {rc}")
+
+
+def attention(pool: PoolImage, q, ctx_lens, block_table, sm_scale: float) -> np.ndarray:
+    """float64 decode attention; q [n_seq][W][n_q][hd] -> out float64, same shape."""
+    q = _c(q, np.float32)
+    n_seq, W, n_q, hd = q.shape
+    assert hd == pool.head_dim
+    ctx = _c(ctx_lens, np.int32)
+    bt = _c(block_table, np.int32)
+    out = np.empty(q.shape, dtype=np.float64)
+    rc = _load().kvo_attention(*pool.geometry(), _ptr(pool.k), _ptr(pool.v),
+                               _ptr(pool.ks), _ptr(pool.vs), _ptr(q), n_seq, W, n_q,
+                               _ptr(ctx), _ptr(bt), bt.shape[1], float(sm_scale),
+                               _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"kvo_attention failed: {rc}")
+    return out
+
+
+def compact_f16(pool: PoolImage, block_table_row, n_cells: int):
+    """Cells [0, n_cells) of one sequence -> (out_k, out_v) uint16 [n_kv][n_cells][hd]."""
+    bt = _c(block_table_row, np.int32)
+    out_k = np.empty((pool.n_kv, n_cells, pool.head_dim), dtype=np.uint16)
+    out_v = np.empty_like(out_k)
+    rc = _load().kvo_compact_f16(*pool.geometry(), _ptr(pool.k), _ptr(pool.v),
+                                 _ptr(pool.ks), _ptr(pool.vs), _ptr(bt), n_cells,
+                                 _ptr(out_k), _ptr(out_v))
+    if rc != 0:
+        raise RuntimeError(f"kvo_compact_f16 failed: {rc}")
+    return out_k, out_v

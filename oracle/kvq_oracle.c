@@ -1,0 +1,395 @@
+/*
+ * kvq_oracle.c -- plain CPU oracle for the quantized K/V cache path.
+ *
+ * TEST INFRASTRUCTURE ONLY (see kvq_oracle.h).  Scalar, single-threaded,
+ * no blocking, no reordering beyond the definitions it restates.
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -fno-fast-math
+ *        (no FMA contraction, IEEE float division and rint in the default
+ *        rounding mode, which is round-to-nearest-even).
+ */
+#include "kvq_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* IEEE-754 binary16 (fp16) from its definition.                             */
+/*                                                                           */
+/* [kv-q8 PR, "Summary"]: the FP16 cache stores K/V as fp16 and the int8     */
+/* cache keeps "one FP16 scale per 64 dims"; [kv-q8 PR, "What changed"]:     */
+/* scale = fp16(max|x| / 127).  fp16() is read as IEEE round-to-nearest,     */
+/* ties-to-even, with subnormals kept and overflow to infinity.             */
+/* ------------------------------------------------------------------------ */
+
+uint16_t kvo_fp16_from_float(float x)
+{
+    uint32_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    const uint16_t sign = (bits >> 31) ? 0x8000u : 0u;
+
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7e00u);
+    if (isinf(x))
+        return (uint16_t)(sign | 0x7c00u);
+
+    const double a = fabs((double)x);
+    /* Largest finite binary16 is 65504; the next grid point would be 65536.
+     * Their midpoint 65520 ties to the even neighbour, which is 65536, i.e.
+     * it overflows.  Everything at or above 65520 becomes infinity. */
+    if (a >= 65520.0)
+        return (uint16_t)(sign | 0x7c00u);
+
+    /* Spacing of the binary16 grid around a: 2^-24 below the smallest normal
+     * 2^-14, else 2^(e-10) for a in [2^e, 2^(e+1)). */
+    double quantum;
+    if (a < ldexp(1.0, -14)) {
+        quantum = ldexp(1.0, -24);
+    } else {
+        int e2;
+        (void)frexp(a, &e2); /* a in [2^(e2-1), 2^e2) */
+        quantum = ldexp(1.0, (e2 - 1) - 10);
+    }
+    const double n = a / quantum;   /* exact: scaling by a power of two */
+    const double r = nearbyint(n);  /* nearest, ties to even (default mode) */
+    const double v = r * quantum;   /* the nearest binary16 value, exact   */
+
+    if (v == 0.0)
+        return sign;
+    if (v < ldexp(1.0, -14)) /* subnormal: v = m * 2^-24 */
+        return (uint16_t)(sign | (uint16_t)r);
+
+    int e;
+    const double f = frexp(v, &e); /* v = f * 2^e, f in [0.5, 1) */
+    const uint32_t exp16 = (uint32_t)((e - 1) + 15);
+    const uint32_t mant = (uint32_t)((f * 2.0 - 1.0) * 1024.0); /* exact */
+    return (uint16_t)(sign | (exp16 << 10) | mant);
+}
+
+float kvo_fp16_to_float(uint16_t h)
+{
+    const int sign = h >> 15;
+    const int e = (h >> 10) & 0x1f;
+    const int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);               /* zero or subnormal */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + (double)m, e - 25);   /* (1 + m/1024) 2^(e-15) */
+    return (float)(sign ? -v : v);
+}
+
+void kvo_fp16_from_float_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_fp16_from_float(x[i]);
+}
+
+void kvo_fp16_to_float_array(const uint16_t *h, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_fp16_to_float(h[i]);
+}
+
+/* All 65536 fp16 values as float, filled from kvo_fp16_to_float on first use
+ * so that dequantization inside the attention loops is a lookup. */
+static float g_fp16_table[65536];
+static int g_fp16_table_ready = 0;
+
+static void fp16_table_init(void)
+{
+    if (g_fp16_table_ready)
+        return;
+    for (int i = 0; i < 65536; ++i)
+        g_fp16_table[i] = kvo_fp16_to_float((uint16_t)i);
+    g_fp16_table_ready = 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantize-on-write.                                                        */
+/*                                                                           */
+/* [kv-q8 PR, "What changed"]: under --kv-q8 a row is quantized on write     */
+/* with scale = fp16(max|x| / 127) and code = clamp(rint(x / scale), -127,   */
+/* 127); [kv-q8 PR, "Summary"]: one scale per 64 dims.  The group maximum    */
+/* covers the whole group before any code is formed (the same section's note */
+/* on the barrier every thread must reach before the stores).                */
+/*                                                                           */
+/* Readings where the page gives only symbols:                               */
+/*  - max|x|/127 and x/scale are IEEE fp32 divisions; x/scale divides by the */
+/*    stored fp16 scale widened to fp32 (the same symbol on both sides).     */
+/*  - rint rounds half to even.                                              */
+/*  - a group whose scale is 0 (all zeros, or max|x|/127 below the fp16      */
+/*    range) gets all-zero codes; an infinite scale gives x/inf = 0 codes.   */
+/*  - NaN inputs are outside the domain; they give code 0 here.             */
+/* ------------------------------------------------------------------------ */
+
+int kvo_quantize_row_q8(const float *x, int hd, int8_t *codes, uint16_t *scales)
+{
+    if (hd <= 0 || hd % KVO_GROUP != 0)
+        return -1;
+    for (int g = 0; g < hd / KVO_GROUP; ++g) {
+        const float *xg = x + (size_t)g * KVO_GROUP;
+        float a = 0.0f;
+        for (int i = 0; i < KVO_GROUP; ++i) {
+            const float ax = fabsf(xg[i]);
+            if (ax > a)
+                a = ax;
+        }
+        const float t = a / 127.0f;
+        const uint16_t s = kvo_fp16_from_float(t);
+        const float sf = kvo_fp16_to_float(s);
+        scales[g] = s;
+        for (int i = 0; i < KVO_GROUP; ++i) {
+            int c = 0;
+            if (sf != 0.0f) {
+                const float ratio = xg[i] / sf;
+                if (ratio == ratio) { /* not NaN */
+                    float rr = rintf(ratio);
+                    if (rr > 127.0f)
+                        rr = 127.0f;
+                    if (rr < -127.0f)
+                        rr = -127.0f;
+                    c = (int)rr;
+                }
+            }
+            codes[(size_t)g * KVO_GROUP + i] = (int8_t)c;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged addressing.                                                         */
+/*                                                                           */
+/* A block holds block_size consecutive cells of one sequence for every KV   */
+/* head; codes and scales are separate runs ([k8v4 PR, "How"]: a block is a  */
+/* list of byte runs, K codes then K scales).  Logical cell p of sequence b  */
+/* is block table[b][p / block_size], slot p % block_size.                   */
+/* ------------------------------------------------------------------------ */
+
+static int64_t cell_row(const int32_t *block_table, int max_blocks_per_seq,
+                        int n_blocks, int n_kv, int block_size,
+                        int seq, int pos, int kvh)
+{
+    if (pos < 0)
+        return -1;
+    const int lb = pos / block_size;
+    if (lb >= max_blocks_per_seq)
+        return -1;
+    const int32_t blk = block_table[(size_t)seq * max_blocks_per_seq + lb];
+    if (blk < 0 || blk >= n_blocks)
+        return -1;
+    const int slot = pos % block_size;
+    return ((int64_t)blk * n_kv + kvh) * block_size + slot;
+}
+
+static int check_geometry(int fmt, int n_kv, int hd, int block_size, int n_blocks)
+{
+    if (fmt != KVO_FMT_F16 && fmt != KVO_FMT_Q8)
+        return -1;
+    if (n_kv <= 0 || hd <= 0 || block_size <= 0 || n_blocks <= 0)
+        return -1;
+    if (fmt == KVO_FMT_Q8 && hd % KVO_GROUP != 0)
+        return -1;
+    return 0;
+}
+
+/* Store one row (one cell, one KV head) of K or V at pool row `row`. */
+static int store_row(int fmt, int hd, void *data, uint16_t *scales, int64_t row,
+                     const float *x)
+{
+    if (fmt == KVO_FMT_F16) {
+        uint16_t *dst = (uint16_t *)data + (size_t)row * hd;
+        for (int d = 0; d < hd; ++d)
+            dst[d] = kvo_fp16_from_float(x[d]);
+        return 0;
+    }
+    int8_t *dst = (int8_t *)data + (size_t)row * hd;
+    uint16_t *sdst = scales + (size_t)row * (hd / KVO_GROUP);
+    return kvo_quantize_row_q8(x, hd, dst, sdst);
+}
+
+int kvo_append(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+               void *k_data, void *v_data, uint16_t *k_scales, uint16_t *v_scales,
+               const float *k, const float *v, int n_tok,
+               const int32_t *tok_seq, const int32_t *tok_pos,
+               const int32_t *block_table, int max_blocks_per_seq)
+{
+    if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0)
+        return -1;
+    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL))
+        return -2;
+    for (int t = 0; t < n_tok; ++t) {
+        for (int kvh = 0; kvh < n_kv; ++kvh) {
+            const int64_t row = cell_row(block_table, max_blocks_per_seq, n_blocks,
+                                         n_kv, block_size, tok_seq[t], tok_pos[t], kvh);
+            if (row < 0)
+                return -3;
+            const size_t src = ((size_t)t * n_kv + kvh) * hd;
+            if (store_row(fmt, hd, k_data, k_scales, row, k + src) != 0)
+                return -4;
+            if (store_row(fmt, hd, v_data, v_scales, row, v + src) != 0)
+                return -4;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization: k_hat = code * scale.  A code has at most 8 significant   */
+/* bits and an fp16 scale 11, so the product is exact in float and in       */
+/* double.  The FP16 cache dequantizes to the stored fp16 value.             */
+/* ------------------------------------------------------------------------ */
+
+static double dequant(int fmt, int hd, const void *data, const uint16_t *scales,
+                      int64_t row, int d)
+{
+    if (fmt == KVO_FMT_F16)
+        return (double)g_fp16_table[((const uint16_t *)data)[(size_t)row * hd + d]];
+    const int8_t c = ((const int8_t *)data)[(size_t)row * hd + d];
+    const uint16_t s = scales[(size_t)row * (hd / KVO_GROUP) + d / KVO_GROUP];
+    return (double)c * (double)g_fp16_table[s];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention, float64.                                                */
+/*                                                                           */
+/* [kv-q8 PR, "What changed" and "Extra Notes"]: the decode of the next      */
+/* token reads the cache through a split-K partial kernel; the split-K      */
+/* combine is an exact re-association of the plain softmax written here:    */
+/*   z_c = sm_scale * sum_d q_d * k_hat_c,d        for visible cells c       */
+/*   out_d = sum_c exp(z_c - max z) v_hat_c,d / sum_c exp(z_c - max z)       */
+/* GQA: query head h reads KV head h / G, G = n_q / n_kv (consecutive query  */
+/* heads share one KV head).  With W query tokens per sequence (a verify     */
+/* window) the W queries are the last W cells already in the cache and token */
+/* w sees cells [0, L - W + w].                                              */
+/* ------------------------------------------------------------------------ */
+
+int kvo_attention(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                  const void *k_data, const void *v_data,
+                  const uint16_t *k_scales, const uint16_t *v_scales,
+                  const float *q, int n_seq, int W, int n_q,
+                  const int32_t *ctx_lens, const int32_t *block_table,
+                  int max_blocks_per_seq, float sm_scale, double *out)
+{
+    if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0)
+        return -1;
+    if (n_seq <= 0 || W <= 0 || n_q <= 0 || n_q % n_kv != 0)
+        return -1;
+    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL))
+        return -2;
+    fp16_table_init();
+    const int G = n_q / n_kv;
+
+    int max_len = 0;
+    for (int b = 0; b < n_seq; ++b)
+        if (ctx_lens[b] > max_len)
+            max_len = ctx_lens[b];
+    double *z = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_len > 0 ? max_len : 1));
+    if (z == NULL || rows == NULL) {
+        free(z);
+        free(rows);
+        return -5;
+    }
+
+    int rc = 0;
+    for (int b = 0; b < n_seq && rc == 0; ++b) {
+        const int L = ctx_lens[b];
+        for (int w = 0; w < W && rc == 0; ++w) {
+            const int last = L - W + w; /* last visible cell */
+            for (int h = 0; h < n_q; ++h) {
+                double *o = out + (((size_t)b * W + w) * n_q + h) * hd;
+                const float *qv = q + (((size_t)b * W + w) * n_q + h) * hd;
+                for (int d = 0; d < hd; ++d)
+                    o[d] = 0.0;
+                if (last < 0)
+                    continue;
+                const int kvh = h / G;
+                const int n_vis = last + 1;
+
+                double zmax = -INFINITY;
+                for (int c = 0; c < n_vis; ++c) {
+                    const int64_t row = cell_row(block_table, max_blocks_per_seq, n_blocks,
+                                                 n_kv, block_size, b, c, kvh);
+                    if (row < 0) {
+                        rc = -3;
+                        break;
+                    }
+                    rows[c] = row;
+                    double dot = 0.0;
+                    for (int d = 0; d < hd; ++d)
+                        dot += (double)qv[d] * dequant(fmt, hd, k_data, k_scales, row, d);
+                    z[c] = (double)sm_scale * dot;
+                    if (z[c] > zmax)
+                        zmax = z[c];
+                }
+                if (rc != 0)
+                    break;
+
+                double den = 0.0;
+                for (int c = 0; c < n_vis; ++c) {
+                    const double e = exp(z[c] - zmax);
+                    den += e;
+                    for (int d = 0; d < hd; ++d)
+                        o[d] += e * dequant(fmt, hd, v_data, v_scales, rows[c], d);
+                }
+                for (int d = 0; d < hd; ++d)
+                    o[d] /= den;
+            }
+        }
+    }
+    free(z);
+    free(rows);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP16 compaction.                                                          */
+/*                                                                           */
+/* [kv-q8 PR, "What changed" and "Extra Notes"]: k_kv_f16 compacts           */
+/* [kvh][ctx][HD] into the contiguous [kvh][P][HD] fp16 halves that the      */
+/* prompt chunk's QK^T and PV products read; on the FP16 cache it is a pure  */
+/* copy.  For the int8 cache each value is fp16(code * scale).               */
+/* ------------------------------------------------------------------------ */
+
+int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                    const void *k_data, const void *v_data,
+                    const uint16_t *k_scales, const uint16_t *v_scales,
+                    const int32_t *block_table_row, int n_cells,
+                    uint16_t *out_k, uint16_t *out_v)
+{
+    if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0)
+        return -1;
+    if (n_cells < 0)
+        return -1;
+    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL))
+        return -2;
+    fp16_table_init();
+    const int max_blocks = (n_cells + block_size - 1) / block_size;
+    for (int kvh = 0; kvh < n_kv; ++kvh) {
+        for (int p = 0; p < n_cells; ++p) {
+            const int64_t row = cell_row(block_table_row, max_blocks, n_blocks, n_kv,
+                                         block_size, 0, p, kvh);
+            if (row < 0)
+                return -3;
+            uint16_t *dk = out_k + ((size_t)kvh * n_cells + p) * hd;
+            uint16_t *dv = out_v + ((size_t)kvh * n_cells + p) * hd;
+            for (int d = 0; d < hd; ++d) {
+                if (fmt == KVO_FMT_F16) {
+                    dk[d] = ((const uint16_t *)k_data)[(size_t)row * hd + d];
+                    dv[d] = ((const uint16_t *)v_data)[(size_t)row * hd + d];
+                } else {
+                    dk[d] = kvo_fp16_from_float(
+                        (float)dequant(fmt, hd, k_data, k_scales, row, d));
+                    dv[d] = kvo_fp16_from_float(
+                        (float)dequant(fmt, hd, v_data, v_scales, row, d));
+                }
+            }
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,81 @@
+/*
+ * kvq_oracle.h -- plain CPU oracle for the quantized K/V cache path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
+ * load or call this code: only the test-suite, the smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or
+ * helper with the CUDA library; the two meet only on the same seeded inputs.
+ *
+ * Everything here is scalar C, written to be read against its sources:
+ *   [kv-q8 PR]  "#3084 qwen35: FP16 K/V cache by default, int8 with --kv-q8
+ *               (262144 fits a 16 GiB card)" -- sections "Summary",
+ *               "What changed", "Extra Notes".
+ *   [k8v4 PR]   "#711 kv: --kv k8v4 streams with --kv-resident" -- section
+ *               "How" (a block moved as byte runs: codes, then scales).
+ *
+ * Layouts (all row-major, element = one K or V value):
+ *   pool codes   [n_blocks][n_kv][block_size][head_dim]   fp16 bits or int8
+ *   pool scales  [n_blocks][n_kv][block_size][head_dim/64] fp16 bits (int8 only)
+ *   q, out       [n_seq][W][n_q][head_dim]
+ *   new k, v     [n_tok][n_kv][head_dim]
+ *   block table  [n_seq][max_blocks_per_seq]
+ * Logical cell p of sequence b lives in block table[b][p / block_size],
+ * slot p % block_size.
+ *
+ * Return value of the int functions: 0 on success, a negative number when an
+ * argument or an index is out of range (nothing is written in that case for
+ * the failing row; the caller treats it as a test failure).
+ */
+#ifndef KVQ_ORACLE_H
+#define KVQ_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVO_FMT_F16 0
+#define KVO_FMT_Q8 1
+#define KVO_GROUP 64
+
+/* IEEE-754 binary16 conversion, round to nearest, ties to even, subnormals
+ * kept, overflow to infinity. */
+uint16_t kvo_fp16_from_float(float x);
+float kvo_fp16_to_float(uint16_t h);
+void kvo_fp16_from_float_array(const float *x, uint16_t *out, int64_t n);
+void kvo_fp16_to_float_array(const uint16_t *h, float *out, int64_t n);
+
+/* Quantize one row of hd values: per group of 64 dims one fp16 scale
+ * s = fp16(max|x| / 127) and codes clamp(rint(x / s), -127, 127). */
+int kvo_quantize_row_q8(const float *x, int hd, int8_t *codes, uint16_t *scales);
+
+/* Write n_tok new cells (K and V) into the paged pool image. */
+int kvo_append(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+               void *k_data, void *v_data, uint16_t *k_scales, uint16_t *v_scales,
+               const float *k, const float *v, int n_tok,
+               const int32_t *tok_seq, const int32_t *tok_pos,
+               const int32_t *block_table, int max_blocks_per_seq);
+
+/* Decode attention in float64 over the dequantized pool.  Query token w of
+ * sequence b sees cells [0, ctx_lens[b] - W + w]; query head h reads KV head
+ * h / (n_q / n_kv).  A query with no visible cell gets an all-zero output. */
+int kvo_attention(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                  const void *k_data, const void *v_data,
+                  const uint16_t *k_scales, const uint16_t *v_scales,
+                  const float *q, int n_seq, int W, int n_q,
+                  const int32_t *ctx_lens, const int32_t *block_table,
+                  int max_blocks_per_seq, float sm_scale, double *out);
+
+/* Copy cells [0, n_cells) of one sequence out to contiguous fp16
+ * out_k/out_v [n_kv][n_cells][hd] (fp16 bits). */
+int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                    const void *k_data, const void *v_data,
+                    const uint16_t *k_scales, const uint16_t *v_scales,
+                    const int32_t *block_table_row, int n_cells,
+                    uint16_t *out_k, uint16_t *out_v);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,92 @@
+"""Negative controls: plant plausible mistakes in a copy of the oracle and
+check that the pins catch every one of them.
+
+Each mutation is a textual edit of kvq_oracle.c, compiled with the oracle's
+own flags into a temporary library; the pins (the same test functions that
+run against the real oracle) must fail on it.  This is the check that the
+pins are strong enough to catch a dropped term, a wrong sign or index, or a
+transposed operand, in the spirit of the negative control described in
+#711 kv: --kv k8v4 streams with --kv-resident, "Tests".
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle_attention as att
+from tests import test_oracle_fp16 as f16
+from tests import test_oracle_quant as qt
+
+F16, Q8 = oracle.FMT_F16, oracle.FMT_Q8
+
+MUTATIONS = {
+    "round_half_away": ("float rr = rintf(ratio);", "float rr = roundf(ratio);"),
+    "times_reciprocal": ("const float ratio = xg[i] / sf;",
+                         "const float ratio = xg[i] * (1.0f / sf);"),
+    "unrounded_scale": ("const float ratio = xg[i] / sf;", "const float ratio = xg[i] / t;"),
+    "max_not_abs": ("const float ax = fabsf(xg[i]);", "const float ax = xg[i];"),
+    "clamp_128": ("if (rr < -127.0f)\n                        rr = -127.0f;",
+                  "if (rr < -128.0f)\n                        rr = -128.0f;"),
+    "fp16_ties_away": ("const double r = nearbyint(n);", "const double r = floor(n + 0.5);"),
+    "fp16_subnormal_edge": ("if (a < ldexp(1.0, -14)) {", "if (a < ldexp(1.0, -15)) {"),
+    "gqa_modulo": ("const int kvh = h / G;", "const int kvh = h % n_kv;"),
+    "causal_drop_diagonal": ("const int last = L - W + w; /* last visible cell */",
+                             "const int last = L - W + w - 1;"),
+    "no_softmax_scale": ("z[c] = (double)sm_scale * dot;", "z[c] = dot;"),
+    "scale_group_index": ("+ d / KVO_GROUP];", "+ 0];"),
+    "slot_off_by_one": ("const int slot = pos % block_size;",
+                        "const int slot = (pos + 1) % block_size;"),
+    "k_reads_v": ("dot += (double)qv[d] * dequant(fmt, hd, k_data, k_scales, row, d);",
+                  "dot += (double)qv[d] * dequant(fmt, hd, v_data, v_scales, row, d);"),
+    "no_normalisation": ("o[d] /= den;", "o[d] /= (den + 1.0);"),
+    "compact_k_from_v": ("(float)dequant(fmt, hd, k_data, k_scales, row, d));",
+                         "(float)dequant(fmt, hd, v_data, v_scales, row, d));"),
+}
+
+
+def _all_pins():
+    """Every pin, as zero-argument callables."""
+    pins = [f16.test_decode_every_bit_pattern,
+            f16.test_encode_grid_points_midpoints_and_neighbours,
+            qt.test_scale_one_ties_round_half_even, qt.test_scale_two_and_half,
+            qt.test_negative_maximum_uses_absolute_value,
+            qt.test_zero_group_and_underflowing_scale,
+            qt.test_scale_is_rounded_to_fp16_before_dividing,
+            qt.test_subnormal_scale_and_clamp, qt.test_overflowing_scale_gives_zero_codes,
+            qt.test_division_is_by_the_scale_not_times_its_reciprocal,
+            lambda: qt.test_invariants_on_random_rows(256),
+            att.test_shuffled_block_table_moves_whole_blocks,
+            att.test_two_cells_closed_form,
+            att.test_queries_without_visible_cells_are_zero]
+    for fmt in (F16, Q8):
+        pins += [lambda fmt=fmt: att.test_fp16_store_and_q8_roundtrip(fmt),
+                 lambda fmt=fmt: att.test_one_visible_cell_returns_its_value(fmt),
+                 lambda fmt=fmt: att.test_equal_keys_give_mean_of_values(fmt),
+                 lambda fmt=fmt: att.test_compaction(fmt)]
+    for args in [(F16, 4, 2, 64, 3), (Q8, 3, 4, 128, 4), (Q8, 2, 8, 256, 1)]:
+        pins.append(lambda args=args: att.test_matches_torch_sdpa(*args))
+    return pins
+
+
+def _failures(so_path):
+    failed = 0
+    with oracle.use_library(so_path):
+        for pin in _all_pins():
+            try:
+                pin()
+            except (AssertionError, RuntimeError, ValueError, FloatingPointError):
+                failed += 1
+    return failed
+
+
+def test_unmodified_copy_passes_every_pin(tmp_path):
+    so = oracle.build_variant(oracle.source_text(), str(tmp_path), "kvq_oracle_copy")
+    assert _failures(so) == 0
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation anchor not found exactly once: {name}"
+    so = oracle.build_variant(src.replace(old, new), str(tmp_path), "kvq_oracle_" + name)
+    assert _failures(so) > 0, f"no pin caught the planted mistake '{name}'"
