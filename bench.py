@@ -1,0 +1,496 @@
+"""Benchmark: decode-attention KV bytes read (GB/s) on the gqa32k workload.
+
+Workload (one step): batch 1, 32 query / 8 KV heads, head_dim 128, a
+32768-cell context; append one cell (K and V) and decode one token, on an
+FP16 cache and on an int8 cache (both formats every step).  The context
+grows by one cell per step for 64 steps, as the workload states.  Eight
+layer caches (8 x 203 MB = 1.6 GB, far above the 129 MB L2) are visited in
+turn, so no step reads a cache that is still in L2.
+
+Printed: one JSON line.  `value` = cache bytes the two decodes read per step
+(every visible cell, K + V, codes + scales) / step time, over all ranks.
+The timed region replays CUDA graphs of the captured steps (the library's C
+entry points, called through the binding while capturing); `e2e` repeats
+the measurement through the same public calls without graphs, with the
+step's inputs copied from pinned host memory and the outputs read back every
+step.  `--impl reference` times the CPU oracle on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("decode-attn KV bytes read GB/s (% of HBM peak); append Mcells/s; FP16 & int8")
+LAYERS = 8
+STEPS_PER_LAYER = 64
+WORKLOAD_DESC = ("gqa32k: batch 1, n_q 32, n_kv 8, head_dim 128, 32768-cell context + 1 "
+                 "appended cell per step (64 steps), K with 4 outlier channels x20; "
+                 "each step = append + decode on an FP16 cache and on an int8 cache")
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _row_bytes(fmt_q8: bool, hd: int) -> int:
+    """Cache bytes per (cell, KV head): K and V codes (+ fp16 scale per 64 dims)."""
+    return 2 * (hd + 2 * (hd // 64)) if fmt_q8 else 2 * 2 * hd
+
+
+def _step_ctx(s: int, L: int) -> int:
+    return L + (s // LAYERS) % STEPS_PER_LAYER + 1
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_on = None
+        self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def mark(self, on: bool):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for t, ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        during = [p for t, p in rows if self.t_on and self.t_off and
+                  self.t_on - 0.15 <= t <= self.t_off + 0.15]
+        use = during if during else rows
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in use if num(p[1]) is not None]
+        smax = [num(p[2]) for p in use if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4)
+                          if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(during)}
+
+
+# --------------------------------------------------------------------------
+# the CUDA library arm
+# --------------------------------------------------------------------------
+
+def run_kvq(args):
+    import torch
+    import torch.distributed as dist
+
+    import quantized_kv_cache_append_gb300 as kvq
+    import workloads
+    from quantized_kv_cache_append_gb300.pool import PagedPool
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    kvq.build()
+    kvq.load_library()
+
+    wl = workloads.make("gqa32k")
+    L, n_kv, hd, n_q, bs = int(wl.ctx_lens[0]), wl.n_kv, wl.head_dim, wl.n_q, wl.block_size
+    cap = L + STEPS_PER_LAYER
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bt = dev(wl.block_table)
+
+    # 8 layers x (FP16 pool, int8 pool), each prefilled with the workload's cells
+    k_pre, v_pre = dev(wl.k), dev(wl.v)
+    seq_pre, pos_pre = dev(wl.tok_seq), dev(wl.tok_pos)
+    layers = []
+    for _ in range(LAYERS):
+        pair = {}
+        for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8)):
+            pool = PagedPool(fmt, n_kv, hd, bs, wl.n_blocks)
+            pool.append(k_pre, v_pre, seq_pre, pos_pre, bt)
+            ws_bytes = pool.workspace_bytes(1, 1, n_q, cap)
+            pair[name] = (pool, torch.empty(ws_bytes, dtype=torch.uint8, device="cuda"),
+                          torch.empty((1, 1, n_q, hd), dtype=torch.float32, device="cuda"))
+        layers.append(pair)
+    torch.cuda.synchronize()
+
+    # append throughput (bulk: the 32768-cell prefill), outside the timed steps
+    append_mcells = {}
+    for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8)):
+        pool = layers[0][name][0]
+        for _ in range(3):
+            pool.append(k_pre, v_pre, seq_pre, pos_pre, bt)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        e0.record()
+        for _ in range(reps):
+            pool.append(k_pre, v_pre, seq_pre, pos_pre, bt)
+        e1.record()
+        torch.cuda.synchronize()
+        append_mcells[name] = L * reps / (e0.elapsed_time(e1) * 1e-3) / 1e6
+
+    # per-step inputs (64 distinct new cells and queries), resident in HBM
+    sk = dev(np.stack([st["k"] for st in wl.steps]))          # [64][1][n_kv][hd]
+    sv = dev(np.stack([st["v"] for st in wl.steps]))
+    sq = dev(np.stack([st["q"] for st in wl.steps]))          # [64][1][1][n_q][hd]
+    spos = dev(np.stack([st["tok_pos"] for st in wl.steps]))  # [64][1]
+    sctx = dev(np.stack([st["ctx_lens"] for st in wl.steps]))  # [64][1]
+    seq0 = dev(np.zeros(1, np.int32))
+
+    def step(s, formats=("f16", "q8"), do_append=True, do_decode=True):
+        j = (s // LAYERS) % STEPS_PER_LAYER
+        for name in formats:
+            pool, ws, out = layers[s % LAYERS][name]
+            if do_append:
+                pool.append(sk[j], sv[j], seq0, spos[j], bt)
+            if do_decode:
+                pool.decode(sq[j], sctx[j], cap, bt, wl.sm_scale, out=out, workspace=ws)
+
+    def capture(n, **kw):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step(0, **kw)                      # warm the binding outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                step(i, **kw)
+        return g
+
+    chunk = LAYERS * STEPS_PER_LAYER            # 512 steps: every layer through 64 steps
+    g_full = capture(chunk)
+    K, W = args.steps, args.warmup
+    rem = K % chunk
+    g_rem = capture(rem) if rem else None
+
+    def run_steps(n):
+        for _ in range(n // chunk):
+            g_full.replay()
+        if n % chunk:
+            if n % chunk == rem and g_rem is not None:
+                g_rem.replay()
+            else:
+                for i in range(n % chunk):
+                    step(i)
+
+    bytes_per_step = {"f16": [], "q8": []}
+    for s in range(chunk):
+        ctx = _step_ctx(s, L)
+        bytes_per_step["f16"].append(ctx * n_kv * _row_bytes(False, hd))
+        bytes_per_step["q8"].append(ctx * n_kv * _row_bytes(True, hd))
+    total_bytes = sum(bytes_per_step["f16"][s % chunk] + bytes_per_step["q8"][s % chunk]
+                      for s in range(K))
+
+    # warm-up (untimed), then exactly K timed steps between barriers
+    run_steps(W)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    run_steps(K)
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    clock_info = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = total_bytes * world / (ms * 1e-3) / 1e9
+
+    # per-kernel durations: graphs of decode-only steps, one format at a time
+    kernel_ms = {}
+    for name in ("f16", "q8"):
+        g = capture(chunk, formats=(name,), do_append=False)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        kernel_ms[name] = a.elapsed_time(b) / chunk
+    g = capture(chunk, formats=("f16", "q8"), do_decode=False)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    append_step_us = a.elapsed_time(b) / chunk / 2 * 1e3
+
+    peak, peak_kind = _peaks()
+    avg_bytes = {n: sum(v) / len(v) for n, v in bytes_per_step.items()}
+    gbs = {n: avg_bytes[n] / (kernel_ms[n] * 1e-3) / 1e9 for n in kernel_ms}
+    dominant = max(kernel_ms, key=kernel_ms.get)
+    traffic = _ncu_traffic(dominant)
+
+    # end to end through the public calls, host buffers, no graphs
+    e2e = _e2e(step_fn=None, torch=torch, layers=layers, wl=wl, bt=bt, cap=cap, L=L,
+               n_kv=n_kv, hd=hd, K=min(K, 512), W=min(W, 32), world=world, dist=dist)
+
+    result = None
+    if rank == 0:
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "storage": ["f16", "int8+fp16 scale/64"], "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": WORKLOAD_DESC, "layers": LAYERS,
+                       "l2": "inputs larger than L2: 8 layer caches rotated, 1.6 GB",
+                       "graph": "CUDA graphs of 512 captured steps", "parallelism":
+                       f"replicas x{world}"},
+            "gpu_launches": 6 * K,
+            "roofline": {"kernel": f"decode partial+combine ({dominant})", "bound": "hbm",
+                         "achieved": round(gbs[dominant], 1), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(gbs[dominant] / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": int(avg_bytes[dominant]),
+                         "launch_us": round(kernel_ms[dominant] * 1e3, 3)},
+            "decode": {n: {"us": round(kernel_ms[n] * 1e3, 3), "GB/s": round(gbs[n], 1),
+                           "frac_of_measured_hbm": round(gbs[n] / peak, 4),
+                           "frac_of_nominal_8TBs": round(gbs[n] / 8000.0, 4)}
+                       for n in kernel_ms},
+            "append": {"bulk_Mcells_per_s": {n: round(v, 1) for n, v in append_mcells.items()},
+                       "one_cell_step_us": round(append_step_us, 3)},
+            "clocks": clock_info,
+            "e2e": e2e,
+        }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def _ncu_traffic(fmt: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current decode kernel source (else null)."""
+    path = os.path.join(ROOT, "profiles", "decode_gqa32k_traffic.txt")
+    src = os.path.join(ROOT, "quantized_kv_cache_append_gb300", "csrc", "kvq_decode.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fields = {}
+        for ln in open(path):
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("decode_source_sha256_16") != sha:
+            return None
+        return int(float(fields[f"traffic_bytes_per_launch_{fmt}"]))
+    except Exception:
+        return None
+
+
+def _e2e(step_fn, torch, layers, wl, bt, cap, L, n_kv, hd, K, W, world, dist):
+    """Per step: pinned host -> device copies of the new cell and the query,
+    append + decode on both formats through the public calls, device -> host
+    copy of both outputs, synchronize."""
+    n_q = wl.n_q
+    hk = torch.from_numpy(np.stack([st["k"] for st in wl.steps])).pin_memory()
+    hv = torch.from_numpy(np.stack([st["v"] for st in wl.steps])).pin_memory()
+    hq = torch.from_numpy(np.stack([st["q"] for st in wl.steps])).pin_memory()
+    hpos = torch.from_numpy(np.stack([st["tok_pos"] for st in wl.steps])).pin_memory()
+    hctx = torch.from_numpy(np.stack([st["ctx_lens"] for st in wl.steps])).pin_memory()
+    hout = torch.empty((2, 1, 1, n_q, hd), dtype=torch.float32).pin_memory()
+    dk = torch.empty_like(hk[0], device="cuda")
+    dv = torch.empty_like(hv[0], device="cuda")
+    dq = torch.empty_like(hq[0], device="cuda")
+    dpos = torch.empty_like(hpos[0], device="cuda")
+    dctx = torch.empty_like(hctx[0], device="cuda")
+    seq0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h2d = (hk[0].numel() + hv[0].numel() + hq[0].numel()) * 4 + 2 * 4
+    d2h = hout.numel() * 4
+
+    def one(s):
+        j = (s // LAYERS) % STEPS_PER_LAYER
+        dk.copy_(hk[j], non_blocking=True)
+        dv.copy_(hv[j], non_blocking=True)
+        dq.copy_(hq[j], non_blocking=True)
+        dpos.copy_(hpos[j], non_blocking=True)
+        dctx.copy_(hctx[j], non_blocking=True)
+        for i, name in enumerate(("f16", "q8")):
+            pool, ws, out = layers[s % LAYERS][name]
+            pool.append(dk, dv, seq0, dpos, bt)
+            pool.decode(dq, dctx, cap, bt, wl.sm_scale, out=out, workspace=ws)
+            hout[i].copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for s in range(W):
+        one(s)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    total = 0
+    for s in range(K):
+        one(s)
+        ctx = _step_ctx(s, L)
+        total += ctx * n_kv * (_row_bytes(False, hd) + _row_bytes(True, hd))
+    dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": round(total * world / dt / 1e9, 2), "unit": "GB/s", "steps": K,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(dt / K * 1e3, 4)}
+
+
+# --------------------------------------------------------------------------
+# the reference arm: the CPU oracle on the same workload
+# --------------------------------------------------------------------------
+
+def _oracle_steps(n_steps: int, budget_s: float = None):
+    """Prefill both oracle caches, then run oracle steps (append one cell +
+    float64 decode, FP16 and int8).  Returns (bytes, seconds, steps)."""
+    import oracle
+    import workloads
+
+    wl = workloads.make("gqa32k")
+    L, n_kv, hd = int(wl.ctx_lens[0]), wl.n_kv, wl.head_dim
+    imgs = {}
+    for name, fmt in (("f16", oracle.FMT_F16), ("q8", oracle.FMT_Q8)):
+        img = oracle.PoolImage(fmt, n_kv, hd, wl.block_size, wl.n_blocks)
+        oracle.append(img, wl.k, wl.v, wl.tok_seq, wl.tok_pos, wl.block_table)
+        imgs[name] = img
+    t0 = time.perf_counter()
+    total = 0
+    done = 0
+    for s in range(n_steps):
+        j = s % STEPS_PER_LAYER
+        st = wl.steps[j]
+        for name in ("f16", "q8"):
+            oracle.append(imgs[name], st["k"], st["v"], st["tok_seq"], st["tok_pos"],
+                          wl.block_table)
+            oracle.attention(imgs[name], st["q"], st["ctx_lens"], wl.block_table, wl.sm_scale)
+        total += int(st["ctx_lens"][0]) * n_kv * (_row_bytes(False, hd) + _row_bytes(True, hd))
+        done += 1
+        if budget_s is not None and time.perf_counter() - t0 > budget_s:
+            break
+    return total, time.perf_counter() - t0, done
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    total, dt, done = _oracle_steps(10_000, budget_s)
+    return {"value": round(total / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{done} steps of the same workload (append 1 cell + float64 decode over "
+                      f"32769+ cells, FP16 and int8), single-threaded C oracle"}
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; its prefill is untimed
+    total, dt, done = _oracle_steps(args.steps)
+    value = total / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": done, "warmup": args.warmup,
+            "ms_per_step": dt / done * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": WORKLOAD_DESC},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"{done} steps, single-threaded C oracle"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8192)
+    ap.add_argument("--warmup", type=int, default=512)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        res = run_reference(args)
+    else:
+        res = run_kvq(args)
+        rank, world, _ = _dist()
+        if res is not None and world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

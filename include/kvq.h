@@ -1,0 +1,207 @@
+/*
+ * kvq.h -- C ABI of the quantized K/V cache library (one GB300, sm_103a).
+ *
+ * The library keeps a transformer's K/V cache in a paged pool, as FP16 or as
+ * int8 codes with one FP16 scale per 64 head dims, and runs the three calls
+ * that touch it on the decode / verify / prompt paths:
+ *
+ *   kvq_append       quantize-on-write of new K/V rows into the pool
+ *   kvq_decode_attn  GQA attention of 1..W query tokens against the pool,
+ *                    as split-K partials merged by a log-sum-exp combine
+ *   kvq_compact_f16  the pool copied out to contiguous FP16 staging
+ *
+ * Sources (page title, section):
+ *   [kv-q8 PR]  "#3084 qwen35: FP16 K/V cache by default, int8 with --kv-q8
+ *               (262144 fits a 16 GiB card)": "Summary" (the two formats,
+ *               one FP16 scale per 64 dims), "What changed" (the formula
+ *               scale = fp16(max|x|/127), code = clamp(rint(x/scale),
+ *               -127, 127); k_attn_prep / k_attn_part / k_kv_f16 templated on
+ *               the cache format; scale arrays carried beside the code
+ *               arrays), "Extra Notes" (split-K decode; k_kv_f16 compacts
+ *               [kvh][ctx][HD] into [kvh][P][HD] halves for the prompt).
+ *   [k8v4 PR]   "#711 kv: --kv k8v4 streams with --kv-resident": "How"
+ *               (a block is a list of byte runs -- codes, then scales; the
+ *               decode, verify-window and prompt appends; a writer that
+ *               tests one pointer and silently skips the other), "Tests"
+ *               (the negative control that catches that skip).
+ *   [Path F v3] "Path F format v3: persist per-head INT8 KV scales for
+ *               INT8 + persistent KV interop": "Why", "Scope" (int8 bytes
+ *               without their scales are refused, not used).
+ *
+ * Conventions for every call
+ *   - All device arrays are owned and allocated by the caller; the library
+ *     allocates nothing and keeps no state between calls.  Pointers marked
+ *     "device" must be device (or managed) memory of the current device.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  No call reads device memory on the host or
+ *     synchronizes.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid argument returns KVQ_ERR_ARG (or KVQ_ERR_UNSUPPORTED for a
+ *     valid but unimplemented shape) and launches nothing.  No call aborts,
+ *     exits, throws or traps on the device.  A launch failure reported by
+ *     the runtime returns KVQ_ERR_CUDA.
+ *   - Device-side preconditions (not checked on the host, since the values
+ *     live on the device): block ids in the block table lie in
+ *     [0, n_blocks) for every cell that is read or written; token positions
+ *     are < max_blocks_per_seq * block_size; W <= ctx_lens[b] <= max_ctx.
+ *     Breaking them gives unspecified values for the cells involved but no
+ *     out-of-bounds access: every kernel checks each block id it reads
+ *     against [0, n_blocks) and skips (append, compaction) or reads as
+ *     zeros (attention) a cell whose id is out of range; the append kernel
+ *     checks tok_seq against [0, n_seq) and tok_pos against the table width;
+ *     the attention kernels clamp ctx_lens[b] to [0, max_blocks_per_seq *
+ *     block_size].
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Cache formats ([kv-q8 PR], "Summary"). */
+typedef enum {
+    KVQ_F16 = 0, /* K and V stored as IEEE fp16 (round to nearest even)      */
+    KVQ_Q8 = 1   /* int8 codes + one fp16 scale per 64 dims of a row         */
+} kvq_format;
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_ARG = 1,         /* null / misaligned pointer, bad size or shape  */
+    KVQ_ERR_UNSUPPORTED = 2, /* valid request outside the implemented shapes */
+    KVQ_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required   */
+    KVQ_ERR_CUDA = 4         /* the CUDA runtime reported a launch error     */
+} kvq_status;
+
+/* Group of head dims sharing one fp16 scale in KVQ_Q8. */
+#define KVQ_GROUP 64
+
+/*
+ * One layer's paged K/V pool.  A physical block holds block_size consecutive
+ * cells of one sequence for all n_kv_heads KV heads; K and V, codes and
+ * scales are four separate arrays ("byte runs", [k8v4 PR] "How"):
+ *
+ *   k_data, v_data     [n_blocks][n_kv_heads][block_size][head_dim]
+ *                      fp16 (KVQ_F16) or int8 (KVQ_Q8)
+ *   k_scales, v_scales [n_blocks][n_kv_heads][block_size][head_dim / 64]
+ *                      fp16 bits; KVQ_Q8 only (must be NULL-free for Q8,
+ *                      ignored for F16)
+ *
+ * Cell p of sequence b is block block_table[b * max_blocks_per_seq +
+ * p / block_size], slot p % block_size; its row of KV head h starts at
+ * element ((block * n_kv_heads + h) * block_size + slot) * head_dim.
+ *
+ * Limits: head_dim in {64, 128, 256}; block_size a power of two in
+ * [16, 1024]; all four pointers 256-byte aligned (torch allocations are);
+ * n_blocks * n_kv_heads * block_size < 2^31.
+ */
+typedef struct kvq_cache {
+    int32_t fmt;        /* kvq_format */
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t n_blocks;
+    int32_t reserved;   /* must be 0 */
+    void *k_data;
+    void *v_data;
+    void *k_scales;
+    void *v_scales;
+} kvq_cache;
+
+/*
+ * Bytes one physical block occupies in the pool: K and V codes plus, for
+ * KVQ_Q8, their scales (2 bytes per 64 dims).  Per element that is 2 bytes
+ * (F16) or 1 + 2/64 bytes (Q8) -- the 6.0 GiB and 3.1 GiB of a 262144-cell
+ * cache in [kv-q8 PR], "Summary".  Returns 0 for an invalid geometry.
+ */
+size_t kvq_block_bytes(int fmt, int n_kv_heads, int head_dim, int block_size);
+
+/*
+ * Quantize-on-write of n_tok new cells ([kv-q8 PR], "What changed";
+ * [k8v4 PR], "How": one call serves the decode step (n_tok = number of
+ * sequences), a verify window and a prompt chunk).
+ *
+ *   k, v        device fp32 [n_tok][n_kv_heads][head_dim], 16-byte aligned
+ *   tok_seq     device int32 [n_tok]: sequence of each new cell
+ *   tok_pos     device int32 [n_tok]: its position (cell index) in that
+ *               sequence
+ *   block_table device int32 [n_seq][max_blocks_per_seq]
+ *   n_seq       host int: rows of block_table (bounds tok_seq)
+ *
+ * KVQ_F16 stores fp16_rne(x).  KVQ_Q8 stores, per row and per group of 64
+ * dims, s = fp16_rne(max|x| / 127) and codes clamp(rint(x / float(s)), -127,
+ * 127): both divisions are IEEE fp32 divisions, rint rounds half to even; a
+ * group whose scale is 0 gets zero codes.  The result is bit-identical to
+ * that definition.  A cell written twice holds the last write; two tokens of
+ * one call must not name the same cell.  n_tok == 0 is a no-op returning
+ * KVQ_OK.
+ */
+kvq_status kvq_append(const kvq_cache *cache, const float *k, const float *v, int n_tok,
+                      const int32_t *tok_seq, const int32_t *tok_pos,
+                      const int32_t *block_table, int n_seq, int max_blocks_per_seq,
+                      void *stream);
+
+/*
+ * Workspace bytes kvq_decode_attn needs for these sizes on the current
+ * device (the split plan depends on its SM count).  Returns 0 for invalid
+ * arguments.
+ */
+size_t kvq_decode_workspace_bytes(const kvq_cache *cache, int n_seq, int W, int n_q,
+                                  int max_ctx);
+
+/*
+ * Decode attention of W query tokens per sequence against the cache
+ * ([kv-q8 PR], "What changed" and "Extra Notes": the split-K partial kernel
+ * k_attn_part and its combine).
+ *
+ *   q           device fp32 [n_seq][W][n_q][head_dim], 16-byte aligned
+ *   ctx_lens    device int32 [n_seq]: cells in each sequence, the W query
+ *               tokens' own cells included (they are appended first)
+ *   max_ctx     host int: an upper bound of ctx_lens, used to plan splits
+ *   block_table device int32 [n_seq][max_blocks_per_seq]
+ *   sm_scale    softmax scale (usually 1/sqrt(head_dim))
+ *   out         device fp32 [n_seq][W][n_q][head_dim], 16-byte aligned
+ *   workspace   device scratch of at least kvq_decode_workspace_bytes(),
+ *               256-byte aligned; no initial contents are needed.  It
+ *               holds the split-K partials between the two kernels of one
+ *               call, so calls sharing a workspace must be ordered (same
+ *               stream, or events).
+ *
+ * Query head h reads KV head h / (n_q / n_kv_heads); n_q must be a
+ * multiple of n_kv_heads.  Query token w of sequence b is the cell
+ * ctx_lens[b] - W + w and attends to cells [0, ctx_lens[b] - W + w]
+ * (causal inside the window).  out = softmax(sm_scale * q . K^T) V over the
+ * dequantized cache, computed in fp32; a query with no visible cell gets 0.
+ * W in [1, 16], n_q / n_kv_heads * W <= 32.
+ */
+kvq_status kvq_decode_attn(const kvq_cache *cache, const float *q, int n_seq, int W, int n_q,
+                           const int32_t *ctx_lens, int max_ctx, const int32_t *block_table,
+                           int max_blocks_per_seq, float sm_scale, float *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * FP16 compaction of cells [0, n_cells) of one sequence ([kv-q8 PR],
+ * "Extra Notes": k_kv_f16 compacts [kvh][ctx][HD] into [kvh][P][HD]
+ * halves; on the FP16 cache it is a pure copy).
+ *
+ *   block_table_row device int32 [ceil(n_cells / block_size)]: the
+ *                   sequence's row of the block table
+ *   out_k, out_v    device fp16 [n_kv_heads][n_cells][head_dim], 16-byte
+ *                   aligned
+ *
+ * KVQ_F16 copies the stored bits; KVQ_Q8 writes fp16_rne(code * scale)
+ * (the product is exact in fp32).  n_cells == 0 is a no-op.
+ */
+kvq_status kvq_compact_f16(const kvq_cache *cache, const int32_t *block_table_row, int n_cells,
+                           void *out_k, void *out_v, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *kvq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

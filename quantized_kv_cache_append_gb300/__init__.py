@@ -1,0 +1,164 @@
+"""Python binding of the quantized K/V cache library (include/kvq.h).
+
+Thin ctypes marshalling over libkvq.so: every function has the name of the C
+entry point it calls and only converts arguments (torch tensors -> device
+pointers, the current torch CUDA stream -> cudaStream_t).  All work happens
+in the library's CUDA kernels; there is no fallback of any kind.  If the
+library has not been built, importing the binding's functions raises.
+
+    from quantized_kv_cache_append_gb300 import (
+        KVQ_F16, KVQ_Q8, kvq_cache, kvq_append, kvq_decode_attn, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from .build import LIB_PATH, build  # noqa: F401  (build() is the in-tree nvcc build)
+
+KVQ_F16 = 0
+KVQ_Q8 = 1
+KVQ_GROUP = 64
+
+KVQ_OK = 0
+KVQ_ERR_ARG = 1
+KVQ_ERR_UNSUPPORTED = 2
+KVQ_ERR_WORKSPACE = 3
+KVQ_ERR_CUDA = 4
+
+# Every symbol the C header declares, in the order it declares them.
+EXPORTED_SYMBOLS = (
+    "kvq_block_bytes",
+    "kvq_append",
+    "kvq_decode_workspace_bytes",
+    "kvq_decode_attn",
+    "kvq_compact_f16",
+    "kvq_status_string",
+)
+
+
+class kvq_cache(ctypes.Structure):
+    """Mirror of `struct kvq_cache` (one layer's paged pool descriptor)."""
+
+    _fields_ = [
+        ("fmt", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("n_blocks", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("k_data", ctypes.c_void_p),
+        ("v_data", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+    ]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {kvq_status_string(status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load libkvq.so (raises if it is missing: there is no other path)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library not built: {p} is missing "
+            "(run quantized_kv_cache_append_gb300.build.build())")
+    lib = ctypes.CDLL(p)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    CP = ctypes.POINTER(kvq_cache)
+    lib.kvq_block_bytes.restype = Z
+    lib.kvq_block_bytes.argtypes = [I, I, I, I]
+    lib.kvq_append.restype = I
+    lib.kvq_append.argtypes = [CP, P, P, I, P, P, P, I, I, P]
+    lib.kvq_decode_workspace_bytes.restype = Z
+    lib.kvq_decode_workspace_bytes.argtypes = [CP, I, I, I, I]
+    lib.kvq_decode_attn.restype = I
+    lib.kvq_decode_attn.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P, Z, P]
+    lib.kvq_compact_f16.restype = I
+    lib.kvq_compact_f16.argtypes = [CP, P, I, P, P, P]
+    lib.kvq_status_string.restype = ctypes.c_char_p
+    lib.kvq_status_string.argtypes = [I]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(x):
+    """Device (or host) address of a tensor / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_cache(fmt: int, n_kv_heads: int, head_dim: int, block_size: int, n_blocks: int,
+               k_data, v_data, k_scales=None, v_scales=None) -> kvq_cache:
+    """Fill a kvq_cache from tensors (or raw device addresses)."""
+    return kvq_cache(fmt, n_kv_heads, head_dim, block_size, n_blocks, 0,
+                     _ptr(k_data), _ptr(v_data), _ptr(k_scales), _ptr(v_scales))
+
+
+def kvq_block_bytes(fmt: int, n_kv_heads: int, head_dim: int, block_size: int) -> int:
+    return int(load_library().kvq_block_bytes(fmt, n_kv_heads, head_dim, block_size))
+
+
+def kvq_append(cache: kvq_cache, k, v, n_tok: int, tok_seq, tok_pos, block_table,
+               n_seq: int, max_blocks_per_seq: int, stream=None) -> int:
+    return load_library().kvq_append(ctypes.byref(cache), _ptr(k), _ptr(v), n_tok,
+                                     _ptr(tok_seq), _ptr(tok_pos), _ptr(block_table),
+                                     n_seq, max_blocks_per_seq, _stream(stream))
+
+
+def kvq_decode_workspace_bytes(cache: kvq_cache, n_seq: int, W: int, n_q: int,
+                               max_ctx: int) -> int:
+    return int(load_library().kvq_decode_workspace_bytes(ctypes.byref(cache), n_seq, W, n_q,
+                                                         max_ctx))
+
+
+def kvq_decode_attn(cache: kvq_cache, q, n_seq: int, W: int, n_q: int, ctx_lens, max_ctx: int,
+                    block_table, max_blocks_per_seq: int, sm_scale: float, out, workspace,
+                    workspace_bytes: int, stream=None) -> int:
+    return load_library().kvq_decode_attn(ctypes.byref(cache), _ptr(q), n_seq, W, n_q,
+                                          _ptr(ctx_lens), max_ctx, _ptr(block_table),
+                                          max_blocks_per_seq, float(sm_scale), _ptr(out),
+                                          _ptr(workspace), int(workspace_bytes),
+                                          _stream(stream))
+
+
+def kvq_compact_f16(cache: kvq_cache, block_table_row, n_cells: int, out_k, out_v,
+                    stream=None) -> int:
+    return load_library().kvq_compact_f16(ctypes.byref(cache), _ptr(block_table_row), n_cells,
+                                          _ptr(out_k), _ptr(out_v), _stream(stream))
+
+
+def kvq_status_string(status: int) -> str:
+    return load_library().kvq_status_string(int(status)).decode()
+
+
+def check(status: int, where: str = "kvq") -> None:
+    """Raise KvqError unless status is KVQ_OK."""
+    if status != KVQ_OK:
+        raise KvqError(status, where)

@@ -1,0 +1,242 @@
+// kvq_api.cu -- the C ABI (include/kvq.h): host-side validation, split
+// planning and launches.  Nothing here reads device memory or synchronizes.
+//
+// Error rules follow the pages' "refuse rather than silently skip":
+// #711 kv: --kv k8v4 streams with --kv-resident, "How" (a writer that tested
+// one pointer and silently skipped the other) and "Tests" (the negative
+// control that catches it); Path F format v3: persist per-head INT8 KV
+// scales, "Why" and "Scope" (int8 bytes without their scales are refused).
+// So a missing scale pointer, like every other invalid argument, is an
+// error returned before any launch.
+#include <math.h>
+#include <stdint.h>
+
+#include "kvq_internal.cuh"
+
+#define KVQ_API extern "C" __attribute__((visibility("default")))
+
+namespace kvq {
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int log2_exact(int v) {
+  int l = 0;
+  while ((1 << l) < v) ++l;
+  return (1 << l) == v ? l : -1;
+}
+
+// Geometry checks shared by every call.
+kvq_status check_cache(const kvq_cache* c) {
+  if (c == nullptr) return KVQ_ERR_ARG;
+  if (c->fmt != KVQ_F16 && c->fmt != KVQ_Q8) return KVQ_ERR_ARG;
+  if (c->reserved != 0) return KVQ_ERR_ARG;
+  if (c->n_kv_heads <= 0 || c->n_blocks <= 0) return KVQ_ERR_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_ARG;
+  if (c->block_size < 16 || c->block_size > 1024 || log2_exact(c->block_size) < 0)
+    return KVQ_ERR_ARG;
+  if ((long long)c->n_blocks * c->n_kv_heads * c->block_size >= (1LL << 31)) return KVQ_ERR_ARG;
+  if (c->k_data == nullptr || c->v_data == nullptr) return KVQ_ERR_ARG;
+  if (!aligned(c->k_data, 256) || !aligned(c->v_data, 256)) return KVQ_ERR_ARG;
+  if (c->fmt == KVQ_Q8) {
+    // int8 codes without their scales are refused, never half-written.
+    if (c->k_scales == nullptr || c->v_scales == nullptr) return KVQ_ERR_ARG;
+    if (!aligned(c->k_scales, 256) || !aligned(c->v_scales, 256)) return KVQ_ERR_ARG;
+  }
+  return KVQ_OK;
+}
+
+Pool make_pool(const kvq_cache* c) {
+  Pool p;
+  p.k = c->k_data;
+  p.v = c->v_data;
+  p.ks = static_cast<const __half*>(c->k_scales);
+  p.vs = static_cast<const __half*>(c->v_scales);
+  p.n_kv = c->n_kv_heads;
+  p.bs_log2 = log2_exact(c->block_size);
+  p.n_blocks = c->n_blocks;
+  return p;
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Split plan: about four partial CTAs per SM over all (sequence, KV head)
+// pairs, each split a whole number of cell tiles.
+bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, DecodePlan* p) {
+  const int G = n_q / c->n_kv_heads;
+  p->rows = G * W;
+  p->rows_pad = decode_rows_pad(c->head_dim, p->rows);
+  const int tile = decode_cell_tile();
+  const long long units = (long long)n_seq * c->n_kv_heads;
+  const int tiles = (max_ctx + tile - 1) / tile;
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  const long long target = 4LL * sms;
+  long long ns = (target + units - 1) / units;
+  if (ns < 1) ns = 1;
+  if (ns > tiles) ns = tiles;
+  const int split_tiles = (int)((tiles + ns - 1) / ns);
+  p->split_cells = split_tiles * tile;
+  p->nsplit = (max_ctx + p->split_cells - 1) / p->split_cells;
+  const size_t parts = (size_t)n_seq * c->n_kv_heads * p->nsplit * p->rows;
+  p->off_o = 0;
+  p->off_ml = round_up(parts * c->head_dim * sizeof(float), 256);
+  p->bytes = p->off_ml + round_up(parts * 2 * sizeof(float), 256);
+  return true;
+}
+
+kvq_status check_decode_shape(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx,
+                              int max_blocks) {
+  if (n_seq <= 0 || n_q <= 0 || max_ctx <= 0 || max_blocks <= 0) return KVQ_ERR_ARG;
+  if (W < 1 || W > 16) return KVQ_ERR_ARG;
+  if (n_q % c->n_kv_heads != 0) return KVQ_ERR_ARG;
+  if (max_ctx < W) return KVQ_ERR_ARG;
+  if ((long long)max_ctx > (long long)max_blocks * c->block_size) return KVQ_ERR_ARG;
+  if (n_seq > 65535 || c->n_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+  const int rows = (n_q / c->n_kv_heads) * W;
+  if (!decode_supported(c->fmt, c->head_dim, rows)) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+KVQ_API size_t kvq_block_bytes(int fmt, int n_kv_heads, int head_dim, int block_size) {
+  if (n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return 0;
+  const size_t elems = (size_t)n_kv_heads * head_dim * block_size;  // per K (or V)
+  if (fmt == KVQ_F16) return 2 * elems * 2;
+  if (fmt == KVQ_Q8) {
+    if (head_dim % KVQ_GROUP != 0) return 0;
+    return 2 * (elems + (elems / KVQ_GROUP) * 2);
+  }
+  return 0;
+}
+
+KVQ_API kvq_status kvq_append(const kvq_cache* cache, const float* k, const float* v, int n_tok,
+                              const int32_t* tok_seq, const int32_t* tok_pos,
+                              const int32_t* block_table, int n_seq, int max_blocks_per_seq,
+                              void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_tok < 0) return KVQ_ERR_ARG;
+  if (n_tok == 0) return KVQ_OK;
+  if (k == nullptr || v == nullptr || tok_seq == nullptr || tok_pos == nullptr ||
+      block_table == nullptr)
+    return KVQ_ERR_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(tok_seq, 4) || !aligned(tok_pos, 4) ||
+      !aligned(block_table, 4))
+    return KVQ_ERR_ARG;
+  if (n_seq <= 0 || max_blocks_per_seq <= 0) return KVQ_ERR_ARG;
+  if ((long long)n_tok * cache->n_kv_heads * 2 >= (1LL << 36)) return KVQ_ERR_UNSUPPORTED;
+  AppendArgs a;
+  a.k_dst = cache->k_data;
+  a.v_dst = cache->v_data;
+  a.ks_dst = static_cast<__half*>(cache->k_scales);
+  a.vs_dst = static_cast<__half*>(cache->v_scales);
+  a.k = k;
+  a.v = v;
+  a.tok_seq = tok_seq;
+  a.tok_pos = tok_pos;
+  a.block_table = block_table;
+  a.n_tok = n_tok;
+  a.n_kv = cache->n_kv_heads;
+  a.bs_log2 = log2_exact(cache->block_size);
+  a.n_blocks = cache->n_blocks;
+  a.n_seq = n_seq;
+  a.max_blocks = max_blocks_per_seq;
+  const cudaError_t e =
+      launch_append(cache->fmt, cache->head_dim, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+KVQ_API size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int n_seq, int W, int n_q,
+                                          int max_ctx) {
+  if (check_cache(cache) != KVQ_OK) return 0;
+  const int max_blocks = (max_ctx + cache->block_size - 1) / cache->block_size;
+  if (check_decode_shape(cache, n_seq, W, n_q, max_ctx, max_blocks > 0 ? max_blocks : 1) !=
+      KVQ_OK)
+    return 0;
+  DecodePlan p;
+  if (!plan_decode(cache, n_seq, W, n_q, max_ctx, &p)) return 0;
+  return p.bytes;
+}
+
+KVQ_API kvq_status kvq_decode_attn(const kvq_cache* cache, const float* q, int n_seq, int W,
+                                   int n_q, const int32_t* ctx_lens, int max_ctx,
+                                   const int32_t* block_table, int max_blocks_per_seq,
+                                   float sm_scale, float* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  st = check_decode_shape(cache, n_seq, W, n_q, max_ctx, max_blocks_per_seq);
+  if (st != KVQ_OK) return st;
+  if (q == nullptr || out == nullptr || ctx_lens == nullptr || block_table == nullptr)
+    return KVQ_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ctx_lens, 4) || !aligned(block_table, 4))
+    return KVQ_ERR_ARG;
+  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return KVQ_ERR_ARG;
+  DecodePlan plan;
+  if (!plan_decode(cache, n_seq, W, n_q, max_ctx, &plan)) return KVQ_ERR_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < plan.bytes)
+    return KVQ_ERR_WORKSPACE;
+  DecodeArgs a;
+  a.pool = make_pool(cache);
+  a.q = q;
+  a.out = out;
+  a.ctx_lens = ctx_lens;
+  a.block_table = block_table;
+  a.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_o);
+  a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_ml);
+  a.n_seq = n_seq;
+  a.W = W;
+  a.n_q = n_q;
+  a.G = n_q / cache->n_kv_heads;
+  a.R = plan.rows;
+  a.max_blocks = max_blocks_per_seq;
+  a.split_cells = plan.split_cells;
+  a.nsplit = plan.nsplit;
+  a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
+  const cudaError_t e =
+      launch_decode(cache->fmt, cache->head_dim, plan, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+KVQ_API kvq_status kvq_compact_f16(const kvq_cache* cache, const int32_t* block_table_row,
+                                   int n_cells, void* out_k, void* out_v, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_cells < 0) return KVQ_ERR_ARG;
+  if (n_cells == 0) return KVQ_OK;
+  if (block_table_row == nullptr || out_k == nullptr || out_v == nullptr) return KVQ_ERR_ARG;
+  if (!aligned(block_table_row, 4) || !aligned(out_k, 16) || !aligned(out_v, 16))
+    return KVQ_ERR_ARG;
+  CompactArgs a;
+  a.pool = make_pool(cache);
+  a.block_row = block_table_row;
+  a.n_cells = n_cells;
+  a.out_k = static_cast<__half*>(out_k);
+  a.out_v = static_cast<__half*>(out_v);
+  const cudaError_t e =
+      launch_compact(cache->fmt, cache->head_dim, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+KVQ_API const char* kvq_status_string(int status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_ARG: return "KVQ_ERR_ARG: invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED: shape outside the implemented set";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE: workspace missing or too small";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA: CUDA launch error";
+    default: return "unknown kvq_status";
+  }
+}

@@ -1,0 +1,66 @@
+"""A paged K/V pool held in torch device tensors, driven through the C ABI.
+
+PyTorch only provides the device memory and the stream here; every step of
+append, decode attention and compaction runs in libkvq.so.  The methods are
+argument marshalling over the entry points of the same names.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (KVQ_F16, KVQ_GROUP, KVQ_Q8, check, kvq_append, kvq_compact_f16,
+               kvq_decode_attn, kvq_decode_workspace_bytes, make_cache)
+
+
+class PagedPool:
+    """One layer's pool: codes [n_blocks][n_kv][bs][hd] (+ fp16 scales for int8)."""
+
+    def __init__(self, fmt: int, n_kv: int, head_dim: int, block_size: int, n_blocks: int,
+                 device="cuda", fill: int = 0):
+        self.fmt, self.n_kv, self.head_dim = fmt, n_kv, head_dim
+        self.block_size, self.n_blocks = block_size, n_blocks
+        shape = (n_blocks, n_kv, block_size, head_dim)
+        dt = torch.float16 if fmt == KVQ_F16 else torch.int8
+        self.k = torch.full(shape, fill, dtype=dt, device=device) if fill else \
+            torch.zeros(shape, dtype=dt, device=device)
+        self.v = torch.zeros_like(self.k) if not fill else torch.full_like(self.k, fill)
+        if fmt == KVQ_Q8:
+            sshape = (n_blocks, n_kv, block_size, head_dim // KVQ_GROUP)
+            self.ks = torch.zeros(sshape, dtype=torch.float16, device=device)
+            self.vs = torch.zeros_like(self.ks)
+        else:
+            self.ks = self.vs = None
+        self.cache = make_cache(fmt, n_kv, head_dim, block_size, n_blocks,
+                                self.k, self.v, self.ks, self.vs)
+
+    def append(self, k, v, tok_seq, tok_pos, block_table, stream=None) -> None:
+        n_tok = int(tok_seq.shape[0])
+        check(kvq_append(self.cache, k, v, n_tok, tok_seq, tok_pos, block_table,
+                         int(block_table.shape[0]), int(block_table.shape[1]), stream),
+              "kvq_append")
+
+    def workspace_bytes(self, n_seq: int, W: int, n_q: int, max_ctx: int) -> int:
+        return kvq_decode_workspace_bytes(self.cache, n_seq, W, n_q, max_ctx)
+
+    def decode(self, q, ctx_lens, max_ctx: int, block_table, sm_scale: float, out=None,
+               workspace=None, stream=None):
+        n_seq, W, n_q, hd = q.shape
+        if out is None:
+            out = torch.empty_like(q)
+        need = self.workspace_bytes(n_seq, W, n_q, max_ctx)
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        check(kvq_decode_attn(self.cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
+                              int(block_table.shape[1]), sm_scale, out, workspace,
+                              workspace.numel(), stream), "kvq_decode_attn")
+        return out
+
+    def compact(self, block_table_row, n_cells: int, out_k=None, out_v=None, stream=None):
+        shape = (self.n_kv, n_cells, self.head_dim)
+        if out_k is None:
+            out_k = torch.empty(shape, dtype=torch.float16, device=self.k.device)
+        if out_v is None:
+            out_v = torch.empty(shape, dtype=torch.float16, device=self.k.device)
+        check(kvq_compact_f16(self.cache, block_table_row, n_cells, out_k, out_v, stream),
+              "kvq_compact_f16")
+        return out_k, out_v
