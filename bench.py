@@ -471,8 +471,43 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(args):
+    """A few launches of each kernel on one layer of the workload, for ncu
+    (small device footprint, no graphs, no timing)."""
+    import torch
+
+    import quantized_kv_cache_append_gb300 as kvq
+    import workloads
+    from quantized_kv_cache_append_gb300.pool import PagedPool
+
+    kvq.build()
+    kvq.load_library()
+    wl = workloads.make(args.profile_workload)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bt = dev(wl.block_table)
+    L = int(wl.ctx_lens[0])
+    k, v, seq, pos = dev(wl.k), dev(wl.v), dev(wl.tok_seq), dev(wl.tok_pos)
+    q, ctx = dev(wl.q), dev(wl.ctx_lens)
+    for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8)):
+        if name not in wl.formats:
+            continue
+        pool = PagedPool(fmt, wl.n_kv, wl.head_dim, wl.block_size, wl.n_blocks)
+        for _ in range(args.profile_reps):
+            pool.append(k, v, seq, pos, bt)
+        for _ in range(args.profile_reps):
+            pool.decode(q, ctx, int(wl.ctx_lens.max()), bt, wl.sm_scale)
+        for _ in range(args.profile_reps):
+            pool.compact(bt[0], L)
+        torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_workload, "reps": args.profile_reps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run a few launches of every kernel on one layer (for ncu)")
+    ap.add_argument("--profile-workload", default="gqa32k")
+    ap.add_argument("--profile-reps", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=8192)
     ap.add_argument("--warmup", type=int, default=512)
@@ -481,6 +516,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.impl == "reference":
         res = run_reference(args)
     else:

@@ -93,7 +93,8 @@ def _random_pair(fmt, lens, n_kv, hd, bs, seed, shuffle=True):
     rng = np.random.default_rng(seed)
     nbs = [max(1, -(-L // bs)) for L in lens]
     nb = sum(nbs)
-    perm = rng.permutation(nb).astype(np.int32) if shuffle else np.arange(nb, dtype=np.int32)
+    perm_rng = np.random.default_rng(seed + 7919)          # data draws do not depend on it
+    perm = perm_rng.permutation(nb).astype(np.int32) if shuffle else np.arange(nb, dtype=np.int32)
     table = np.full((len(lens), max(nbs)), -1, np.int32)
     at = 0
     for b, n in enumerate(nbs):
