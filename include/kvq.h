@@ -198,6 +198,36 @@ kvq_status kvq_decode_attn(const kvq_cache *cache, const float *q, int n_seq, in
 kvq_status kvq_compact_f16(const kvq_cache *cache, const int32_t *block_table_row, int n_cells,
                            void *out_k, void *out_v, void *stream);
 
+/*
+ * Bytes of device scratch that kvq_decode_attn_static keeps in the library
+ * (one array per device that loads the library, held until the process
+ * exits).
+ */
+#define KVQ_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * kvq_decode_attn without a workspace argument, for callers that cannot
+ * allocate device memory: code running during CUDA graph capture (where
+ * cudaMalloc is not allowed), plugins inside a framework whose allocator
+ * owns the device memory, real-time loops whose memory is fixed at
+ * start-up.  The paper has no counterpart to this call; it exists for
+ * such callers only.
+ *
+ * Arguments, results and errors are those of kvq_decode_attn.  The scratch
+ * is a file-scope device array of KVQ_STATIC_SCRATCH_BYTES inside the
+ * library; a request whose split plan needs more (what
+ * kvq_decode_workspace_bytes reports) returns KVQ_ERR_WORKSPACE and
+ * launches nothing.  The first call on a device looks up the array's
+ * address and caches it: make that first call before any stream capture.
+ * Every call uses the same array, so calls whose kernels may overlap on
+ * the GPU (unordered streams) race on it; order them.  The array needs no
+ * clearing between calls.
+ */
+kvq_status kvq_decode_attn_static(const kvq_cache *cache, const float *q, int n_seq, int W,
+                                  int n_q, const int32_t *ctx_lens, int max_ctx,
+                                  const int32_t *block_table, int max_blocks_per_seq,
+                                  float sm_scale, float *out, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *kvq_status_string(int status);
 

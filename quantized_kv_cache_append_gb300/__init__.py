@@ -34,8 +34,12 @@ EXPORTED_SYMBOLS = (
     "kvq_decode_workspace_bytes",
     "kvq_decode_attn",
     "kvq_compact_f16",
+    "kvq_decode_attn_static",
     "kvq_status_string",
 )
+
+# Size of the library-held scratch used by kvq_decode_attn_static.
+KVQ_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class kvq_cache(ctypes.Structure):
@@ -87,6 +91,8 @@ def load_library(path: Optional[str] = None):
     lib.kvq_decode_attn.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P, Z, P]
     lib.kvq_compact_f16.restype = I
     lib.kvq_compact_f16.argtypes = [CP, P, I, P, P, P]
+    lib.kvq_decode_attn_static.restype = I
+    lib.kvq_decode_attn_static.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P]
     lib.kvq_status_string.restype = ctypes.c_char_p
     lib.kvq_status_string.argtypes = [I]
     if path is None:
@@ -152,6 +158,17 @@ def kvq_compact_f16(cache: kvq_cache, block_table_row, n_cells: int, out_k, out_
                     stream=None) -> int:
     return load_library().kvq_compact_f16(ctypes.byref(cache), _ptr(block_table_row), n_cells,
                                           _ptr(out_k), _ptr(out_v), _stream(stream))
+
+
+def kvq_decode_attn_static(cache: kvq_cache, q, n_seq: int, W: int, n_q: int, ctx_lens,
+                           max_ctx: int, block_table, max_blocks_per_seq: int,
+                           sm_scale: float, out, stream=None) -> int:
+    """kvq_decode_attn with the library's own device scratch, for callers that
+    cannot allocate (graph capture, framework-owned memory, fixed budgets)."""
+    return load_library().kvq_decode_attn_static(ctypes.byref(cache), _ptr(q), n_seq, W, n_q,
+                                                 _ptr(ctx_lens), max_ctx, _ptr(block_table),
+                                                 max_blocks_per_seq, float(sm_scale), _ptr(out),
+                                                 _stream(stream))
 
 
 def kvq_status_string(status: int) -> str:

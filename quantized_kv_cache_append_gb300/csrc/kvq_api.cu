@@ -240,3 +240,63 @@ KVQ_API const char* kvq_status_string(int status) {
     default: return "unknown kvq_status";
   }
 }
+
+// ---------------------------------------------------------------------------
+// kvq_decode_attn_static: decode attention for callers that cannot allocate.
+//
+// Some callers have no way to hand us a workspace: code that runs while a
+// CUDA graph is being captured (cudaMalloc is not allowed there), plugins
+// hosted by a framework whose allocator owns all device memory, and
+// real-time loops whose memory is fixed once at start-up.  For them this
+// entry point keeps its scratch in one file-scope device array of
+// KVQ_STATIC_SCRATCH_BYTES, which exists on every device that loads the
+// library for as long as the process lives.  The first call on a device
+// looks the array's device address up (cudaGetSymbolAddress) and caches
+// it; make that first call before any stream capture.  All calls share the
+// array: two calls whose kernels overlap on the GPU (different streams,
+// no ordering between them) race on it.  Nothing in the array has to start
+// at zero: the partial kernel writes every slot the combine kernel reads.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace kvq {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[KVQ_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_decode_scratch on the current device (set up once).
+kvq_status static_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+      return KVQ_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+}  // namespace kvq
+
+KVQ_API kvq_status kvq_decode_attn_static(const kvq_cache* cache, const float* q, int n_seq,
+                                          int W, int n_q, const int32_t* ctx_lens, int max_ctx,
+                                          const int32_t* block_table, int max_blocks_per_seq,
+                                          float sm_scale, float* out, void* stream) {
+  void* scratch = nullptr;
+  const kvq_status st = kvq::static_scratch_address(&scratch);
+  if (st != KVQ_OK) return st;
+  // Same validation, plan and kernels as kvq_decode_attn; a plan that needs
+  // more than the array holds comes back as KVQ_ERR_WORKSPACE.
+  return kvq_decode_attn(cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
+                         max_blocks_per_seq, sm_scale, out, scratch,
+                         (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
+}
