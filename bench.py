@@ -171,7 +171,7 @@ def run_kvq(args):
             pool = PagedPool(fmt, n_kv, hd, bs, wl.n_blocks)
             pool.append(k_pre, v_pre, seq_pre, pos_pre, bt)
             ws_bytes = pool.workspace_bytes(1, 1, n_q, cap)
-            pair[name] = (pool, torch.empty(ws_bytes, dtype=torch.uint8, device="cuda"),
+            pair[name] = (pool, torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda"),
                           torch.empty((1, 1, n_q, hd), dtype=torch.float32, device="cuda"))
         layers.append(pair)
     torch.cuda.synchronize()

@@ -166,9 +166,9 @@ size_t kvq_decode_workspace_bytes(const kvq_cache *cache, int n_seq, int W, int 
  *   out         device fp32 [n_seq][W][n_q][head_dim], 16-byte aligned
  *   workspace   device scratch of at least kvq_decode_workspace_bytes(),
  *               256-byte aligned; no initial contents are needed.  It
- *               holds the split-K partials between the two kernels of one
- *               call, so calls sharing a workspace must be ordered (same
- *               stream, or events).
+ *               holds the split-K partials between the partial kernel and
+ *               the combine kernel of one call, so calls sharing a
+ *               workspace must be ordered (same stream, or events).
  *
  * Query head h reads KV head h / (n_q / n_kv_heads); n_q must be a
  * multiple of n_kv_heads.  Query token w of sequence b is the cell

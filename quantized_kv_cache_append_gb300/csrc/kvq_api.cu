@@ -67,25 +67,59 @@ int sm_count() {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Split plan: about four partial CTAs per SM over all (sequence, KV head)
-// pairs, each split a whole number of cell tiles.
+// Split plan: one wave of partial CTAs (as many as are resident per SM, on
+// every SM; twice that for batches, whose ragged lengths leave CTAs short)
+// over all (sequence, KV head) pairs, each split a whole number of cell
+// tiles.  The tensor-core kernel takes the shapes it covers; the CUDA-core
+// kernel the rest.
 bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, DecodePlan* p) {
   const int G = n_q / c->n_kv_heads;
   p->rows = G * W;
   p->rows_pad = decode_rows_pad(c->head_dim, p->rows);
-  const int tile = decode_cell_tile();
+  int per_sm = 0;
+  p->use_mma = 0;
+  if (mma_decode_supported(c->fmt, c->head_dim, p->rows)) {
+    per_sm = mma_ctas_per_sm(c->fmt, c->head_dim, p->rows);
+    p->use_mma = per_sm > 0;
+  }
+  if (!p->use_mma) per_sm = 4;
+  const int tile = p->use_mma ? mma_cell_tile() : decode_cell_tile();
   const long long units = (long long)n_seq * c->n_kv_heads;
   const int tiles = (max_ctx + tile - 1) / tile;
   int sms = sm_count();
   if (sms <= 0) sms = 148;
-  const long long target = 4LL * sms;
-  long long ns = (target + units - 1) / units;
+  // The tensor-core kernel runs the splits of one (sequence, KV head) as
+  // thread-block clusters of up to 8 CTAs that merge on chip; one partial
+  // per cluster goes to the workspace.  Clusters are placed whole, inside a
+  // GPC, so the resident capacity comes from the cluster occupancy query
+  // and the cluster size is the one (of 8, 4, 2) with the most resident
+  // CTAs.  The split count is a whole number of clusters within one wave.
+  long long capacity = (long long)per_sm * sms;
+  p->cluster = 1;
+  if (p->use_mma) {
+    long long best = 0;
+    for (int cl = 8; cl >= 2; cl /= 2) {
+      const long long cap = (long long)mma_active_clusters(c->fmt, c->head_dim, p->rows, cl) * cl;
+      if (cap > best) {
+        best = cap;
+        p->cluster = cl;
+      }
+    }
+    if (best > 0) capacity = best;
+    else p->cluster = 1;
+  }
+  const long long target = capacity * (n_seq > 1 ? 2 : 1);
+  long long ns = target / units;
   if (ns < 1) ns = 1;
   if (ns > tiles) ns = tiles;
+  while (p->cluster > 1 && p->cluster > ns) p->cluster /= 2;
+  ns = ns / p->cluster * p->cluster;
   const int split_tiles = (int)((tiles + ns - 1) / ns);
   p->split_cells = split_tiles * tile;
   p->nsplit = (max_ctx + p->split_cells - 1) / p->split_cells;
-  const size_t parts = (size_t)n_seq * c->n_kv_heads * p->nsplit * p->rows;
+  p->nsplit = (p->nsplit + p->cluster - 1) / p->cluster * p->cluster;  // whole clusters
+  p->ncl = p->nsplit / p->cluster;
+  const size_t parts = (size_t)n_seq * c->n_kv_heads * p->ncl * p->rows;
   p->off_o = 0;
   p->off_ml = round_up(parts * c->head_dim * sizeof(float), 256);
   p->bytes = p->off_ml + round_up(parts * 2 * sizeof(float), 256);
@@ -204,6 +238,7 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache* cache, const float* q, int n
   a.max_blocks = max_blocks_per_seq;
   a.split_cells = plan.split_cells;
   a.nsplit = plan.nsplit;
+  a.ncl = plan.ncl;
   a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
   const cudaError_t e =
       launch_decode(cache->fmt, cache->head_dim, plan, a, static_cast<cudaStream_t>(stream));

@@ -307,15 +307,29 @@ __global__ void __launch_bounds__(256) decode_combine(DecodeArgs a) {
   float* dst = a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + g) * HD;
   const size_t base = ((size_t)b * a.pool.n_kv + kvh) * a.nsplit;
 
+  // A partial whose producer lost an mbarrier wait carries m = NaN: the
+  // row's output becomes NaN instead of a silently wrong value.
   float mx = kNegInf;
-  for (int j = t; j < ns; j += 256) mx = fmaxf(mx, __ldcg(a.ws_ml + ((base + j) * a.R + r) * 2));
+  int lost = 0;
+  for (int j = t; j < ns; j += 256) {
+    const float mj = __ldcg(a.ws_ml + ((base + j) * a.R + r) * 2);
+    lost |= mj != mj;
+    mx = fmaxf(mx, mj);
+  }
   s_red[t] = mx;
-  __syncthreads();
+  lost = __syncthreads_or(lost);
   for (int s = 128; s >= 1; s >>= 1) {
     if (t < s) s_red[t] = fmaxf(s_red[t], s_red[t + s]);
     __syncthreads();
   }
   const float M = s_red[0];
+  if (lost) {
+    if (t < TPR) {
+      const float nan = __int_as_float(0x7fc00000);
+      *reinterpret_cast<float4*>(dst + t * 4) = make_float4(nan, nan, nan, nan);
+    }
+    return;
+  }
 
   const int d4 = (t % TPR) * 4, js = t / TPR;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -409,6 +423,7 @@ int decode_rows_pad(int hd, int rows) {
 bool decode_supported(int fmt, int hd, int rows) {
   if (fmt != KVQ_F16 && fmt != KVQ_Q8) return false;
   if (hd != 64 && hd != 128 && hd != 256) return false;
+  if (mma_decode_supported(fmt, hd, rows)) return true;
   const int rp = decode_rows_pad(hd, rows);
   return rows >= 1 && rp <= 32 && rp * (hd / 32) <= 64;
 }
@@ -416,7 +431,10 @@ bool decode_supported(int fmt, int hd, int rows) {
 cudaError_t launch_decode(int fmt, int hd, const DecodePlan& plan, const DecodeArgs& a,
                           cudaStream_t s) {
   cudaError_t e = cudaErrorInvalidValue;
-  if (fmt == KVQ_F16) {
+  if (plan.use_mma) {
+    // the tensor-core kernel merges its own splits (last CTA per row group)
+    return launch_decode_mma_partial(fmt, hd, plan, a, s);
+  } else if (fmt == KVQ_F16) {
     if (hd == 64) e = launch_rows<KVQ_F16, 64>(plan, a, s);
     else if (hd == 128) e = launch_rows<KVQ_F16, 128>(plan, a, s);
     else if (hd == 256) e = launch_rows<KVQ_F16, 256>(plan, a, s);

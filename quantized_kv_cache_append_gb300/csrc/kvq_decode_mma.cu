@@ -1,0 +1,1128 @@
+// kvq_decode_mma.cu -- split-K decode attention on tensor cores, fed by TMA.
+//
+// The partial kernel of the split-K decode (#3084 qwen35: FP16 K/V cache by
+// default, int8 with --kv-q8, "What changed" and "Extra Notes": k_attn_part
+// templated on the cache format, read by the decode of the next token).  One
+// CTA per (split, KV head, sequence):
+//
+//   producer warp   one elected lane streams the split's cells through a
+//                   ring of STAGES shared-memory stages.  A stage is 64
+//                   cells: K and V codes arrive by TMA tensor copies
+//                   (cp.async.bulk.tensor, 128-byte swizzle, straight from
+//                   the paged pool through the block table), the int8
+//                   scales by bulk copies; an mbarrier per stage counts the
+//                   bytes in ("full") and the consumer warps out ("empty").
+//   4 consumer warps  each owns 16 cells of every stage.  S^T = K . Q^T is a
+//                   16-cell x 8-row mma.sync.m16n8k16 per 16 dims; the int8
+//                   codes are widened to fp16 exactly in registers and the
+//                   per-64-dim scales multiply the per-group partial dot
+//                   products.  Online softmax runs in the log2 domain with a
+//                   lazily raised reference maximum.  O^T += V^T . P^T is
+//                   another m16n8k16 per 16 dims, with the V scales folded
+//                   into P per group.  q and p enter the tensor cores as
+//                   fp16 hi + lo pairs (about 22 significant bits), K and V
+//                   as exact fp16 (int8 codes, or the FP16 cache itself).
+//
+// The warps' partial states are merged in shared memory and written as one
+// (o, m, l) partial per row; the combine kernel (kvq_decode.cu) merges the
+// splits.  Masked cells (beyond the context, beyond the causal limit of a
+// verify-window row, or in a block whose id is out of range) get logit -inf
+// and contribute exact zeros.  Every mbarrier wait is bounded: a wait that
+// runs out marks the partial as NaN (the combine passes NaN to the output)
+// and the producer still waits, bounded, for its own copies before the CTA
+// exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <string.h>
+
+#include <mutex>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = kConsumerWarps * 32;  // thread 0 also issues the copies
+constexpr int kTC = 64;                      // cells per pipeline stage
+constexpr int kCellsPerWarp = kTC / kConsumerWarps;
+constexpr uint32_t kWaitLimit = 1u << 25;    // polls before a wait is declared lost
+constexpr float kTau = 8.0f;                 // lazy rescale threshold (log2 units)
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int FMT, int HD, int NT>
+struct Cfg {
+  static constexpr int ESZ = FMT == KVQ_F16 ? 2 : 1;
+  static constexpr int ROWB = HD * ESZ;                  // code bytes per cell row
+  static constexpr int SWB = ROWB < 128 ? ROWB : 128;    // swizzle span (64 or 128 B)
+  static constexpr int NCH = ROWB / SWB;                 // swizzle spans per row
+  static constexpr int NG = HD / kGroup;
+  static constexpr int TILE_B = kTC * ROWB;              // K (or V) codes of a stage
+  static constexpr int SCALE_B = FMT == KVQ_Q8 ? kTC * NG * 2 : 0;
+  static constexpr int STAGE_RAW = 2 * TILE_B + 2 * SCALE_B;
+  static constexpr int STAGE_B = (STAGE_RAW + 1023) / 1024 * 1024;
+  // Stages per CTA and CTAs per SM: keep about 100 KB or more of copies in
+  // flight per SM while fitting as many 4-warp CTAs as the 227 KB allow.
+  static constexpr int STAGES = STAGE_B <= 20 * 1024 ? 3 : (STAGE_B <= 32 * 1024 ? 2 : 3);
+  static constexpr int OFF_V = TILE_B;
+  static constexpr int OFF_KS = 2 * TILE_B;
+  static constexpr int OFF_VS = 2 * TILE_B + SCALE_B;
+  // q as fp16 hi / lo rows, padded by 16 bytes so ldmatrix rows hit distinct banks
+  static constexpr int QROW = HD * 2 + 16;
+  static constexpr int QBYTES_MAX = 2 * NT * 8 * QROW;   // hi and lo, NT*8 padded rows
+  static constexpr int SMEM_Q = STAGES * STAGE_B;
+  static constexpr int SMEM_BAR = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
+  static constexpr int SMEM = SMEM_BAR + 2 * STAGES * 8 + 1024 /*align*/;
+  static constexpr int MIN_CTAS = (227 * 1024) / SMEM >= 3 ? 3 : ((227 * 1024) / SMEM >= 2 ? 2 : 1);
+  // merge buffers (20 x 32 row values, o for rows x dims <= 2048, two flags)
+  static_assert(STAGES * STAGE_B >= (20 * 32 + 2048 + 2) * 4, "merge buffers fit");
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false if it never came.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// One 2D tensor map per SWB-byte span of a cell row: [rows][SWB], row
+// stride = the row's bytes.  A piece of pc cells lands as [span][cell][SWB].
+struct TmaMaps {
+  CUtensorMap k[4];
+  CUtensorMap v[4];
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Thread-block cluster helpers: rank, barrier, distributed shared memory.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// Plain (not volatile) loads: the peers' values are fixed between the two
+// cluster barriers, so the compiler may batch them.
+__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
+  float v;
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
+  float4 v;
+  asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d = a . b (no accumulator input).
+__device__ __forceinline__ void mma16816_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                            uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float half_lo(uint32_t h) {
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xffff)));
+}
+__device__ __forceinline__ float half_hi(uint32_t h) {
+  return __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+}
+
+// x = hi + lo with hi, lo fp16 (about 22 significant bits together).
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_half2(x0, x1);
+  lo = pack_half2(x0 - half_lo(hi), x1 - half_hi(hi));
+}
+
+// int8 -> fp16, exactly: with u = c ^ 0x80 (= c + 128 as an unsigned byte),
+// the fp16 bit pattern 0x6400 | u is 1024 + u, and (1024 + u) - 1152 = c.
+constexpr uint32_t kMagic = 0x64646464u;
+constexpr uint32_t kBias = 0x64806480u;  // fp16 1152 in both halves
+
+// Pairs (byte 0, byte 1) and (byte 2, byte 3) of one biased word.
+__device__ __forceinline__ void widen_same(uint32_t wx, uint32_t& p01, uint32_t& p23) {
+  p01 = hsub2(prmt(wx, kMagic, 0x4140u), kBias);
+  p23 = hsub2(prmt(wx, kMagic, 0x4342u), kBias);
+}
+
+// Swizzled shared-memory byte offset of logical byte `b` of cell `c` (0..63)
+// in a K or V tile laid out [span][cell][SWB]: every TMA box (one piece of
+// cells, one span) is placed at its [span][first cell] slot, so the layout
+// and the swizzle (XOR of the 16-byte chunk with the line index mod 8 or 4)
+// do not depend on the block size.
+template <int FMT, int HD>
+__device__ __forceinline__ uint32_t tile_off(int c, int b) {
+  using C = Cfg<FMT, HD, 1>;
+  const uint32_t off = ((uint32_t)(b / C::SWB) * kTC + (uint32_t)c) * C::SWB + (uint32_t)(b % C::SWB);
+  // 128-byte swizzle: chunk bits [4:6] ^= address bits [7:9]; 64-byte: [4:5] ^= [7:8]
+  return off ^ (((off >> 7) & (C::SWB == 128 ? 7u : 3u)) << 4);
+}
+
+__device__ __forceinline__ int clamp_len_mma(int L, const DecodeArgs& a) {
+  const long long cap_table = (long long)a.max_blocks << a.pool.bs_log2;
+  const long long cap_plan = (long long)a.nsplit * a.split_cells;
+  const long long cap = cap_table < cap_plan ? cap_table : cap_plan;
+  return L < 0 ? 0 : (int)((long long)L < cap ? L : cap);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Block id of cell c (-1 past the end).  Loaded a tile ahead of its use and
+// only tested when used, so the load latency stays hidden.
+__device__ __forceinline__ int block_of(const DecodeArgs& a, const int32_t* bt, int c, int c_end) {
+  return c < c_end ? __ldg(bt + (c >> a.pool.bs_log2)) : -1;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int FMT, int HD, int NT>
+__global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
+    decode_mma(const __grid_constant__ TmaMaps maps, DecodeArgs a) {
+  using C = Cfg<FMT, HD, NT>;
+  constexpr int KS = HD / 16;   // k-steps of q.k, and m-tiles of p.v
+  constexpr int RP = NT * 8;    // padded rows
+  constexpr int MAXP = kTC / 16;
+  constexpr float kNegInf = -INFINITY;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t qbase = sbase + C::SMEM_Q;                 // q hi rows, then lo rows
+  const uint32_t bar_full = sbase + C::SMEM_BAR;
+  const uint32_t bar_empty = bar_full + 8 * C::STAGES;
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
+  const int c_begin = split * a.split_cells;
+  // An empty split (past the end of the context) still runs to the cluster
+  // merge below, contributing nothing, because every CTA of a cluster has
+  // to reach the cluster barriers.
+  const bool empty = c_begin >= L;
+  const int c_end = empty ? c_begin : min(L, c_begin + a.split_cells);
+  const int n_tiles = (c_end - c_begin + kTC - 1) / kTC;
+  const int pc_log2 = a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6;  // cells per TMA piece
+  const int n_pieces = kTC >> pc_log2;
+  const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
+  const bool producer = threadIdx.x == 0;
+  // Let the combine grid be scheduled as soon as SMs free up; it still waits
+  // (griddepcontrol.wait) for this whole grid to finish before reading.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // Producer state (thread 0): pool rows of the pieces of the next tile to
+  // issue, read one tile ahead so the block-table load latency is hidden.
+  int next_blk[MAXP];
+  auto fetch_rows = [&](int it) {
+    const int c0 = c_begin + it * kTC;
+    for (int p = 0; p < MAXP; ++p)
+      next_blk[p] = (p < n_pieces && it < n_tiles) ? block_of(a, bt, c0 + (p << pc_log2), c_end) : -1;
+  };
+  auto issue = [&](int it) {
+    const int s = it % C::STAGES;
+    const int pc = 1 << pc_log2;
+    const int bsz = 1 << a.pool.bs_log2;
+    const int c0 = c_begin + it * kTC;
+    int rows[MAXP];
+    uint32_t bytes = 0;
+    for (int p = 0; p < MAXP; ++p) {
+      const int blk = next_blk[p];
+      const int c = c0 + (p << pc_log2);
+      rows[p] = (p < n_pieces && blk >= 0 && blk < a.pool.n_blocks)
+                    ? (blk * a.pool.n_kv + kvh) * bsz + (c & (bsz - 1))
+                    : -1;
+      if (rows[p] >= 0) bytes += 2u * pc * C::ROWB + (FMT == KVQ_Q8 ? 2u * pc * C::NG * 2 : 0u);
+    }
+    const uint32_t full = bar_full + 8 * s;
+    mbar_expect_tx(full, bytes);
+    const uint32_t st = sbase + s * C::STAGE_B;
+    for (int p = 0; p < n_pieces; ++p) {
+      const int row = rows[p];
+      if (row < 0) continue;
+#pragma unroll
+      for (int sp = 0; sp < C::NCH; ++sp) {
+        const uint32_t so = (uint32_t)(sp * kTC + (p << pc_log2)) * C::SWB;
+        tma_load_2d(st + so, &maps.k[sp], 0, row, full);
+        tma_load_2d(st + C::OFF_V + so, &maps.v[sp], 0, row, full);
+      }
+      if constexpr (FMT == KVQ_Q8) {
+        const uint32_t sb = (uint32_t)pc * C::NG * 2;
+        const uint32_t soff = (uint32_t)p * sb;
+        bulk_load(st + C::OFF_KS + soff, a.pool.ks + (size_t)row * C::NG, sb, full);
+        bulk_load(st + C::OFF_VS + soff, a.pool.vs + (size_t)row * C::NG, sb, full);
+      }
+    }
+  };
+
+  // The producer initialises the barriers and starts the first copies
+  // before anything else, so their latency overlaps the q load below.
+  int issued = 0;
+  bool lost = false;
+  if (producer) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fetch_rows(0);
+    for (int it = 0; it < n_tiles && it < C::STAGES; ++it) {
+      issue(it);
+      fetch_rows(it + 1);
+      ++issued;
+    }
+  }
+  // q * sm_scale * log2(e) as fp16 hi + lo, rows [RP][HD] in k order: FP16
+  // uses the natural dim order; int8 permutes each 16-wide k-step so that
+  // k = 2t + e -> dim 64 gq + 16 t + 4 kk + e and k = 2t + 8 + e -> that + 2
+  // (t = k-pair lane, kk = k-step inside the 64-dim group gq), the order in
+  // which a lane widens its 4-byte code words.
+  {
+    unsigned char* qs = smem + C::SMEM_Q;
+    for (int i = threadIdx.x; i < RP * HD; i += kThreads) {
+      const int r = i / HD, k = i - r * HD;
+      int dim = k;
+      if constexpr (FMT == KVQ_Q8) {
+        const int ks = k >> 4, kq = k & 15;
+        const int tt = (kq & 7) >> 1, e = kq & 1, hi8 = kq >> 3;
+        dim = (ks >> 2) * 64 + 16 * tt + 4 * (ks & 3) + 2 * hi8 + e;
+      }
+      float x = 0.f;
+      if (r < a.R) {
+        const int w = r / a.G, gg = r - w * a.G;
+        x = __ldg(a.q + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + dim) * a.qscale;
+      }
+      const __half h = __float2half_rn(x);
+      const __half lo = __float2half_rn(x - __half2float(h));
+      *reinterpret_cast<__half*>(qs + r * C::QROW + k * 2) = h;
+      *reinterpret_cast<__half*>(qs + (RP + r) * C::QROW + k * 2) = lo;
+    }
+  }
+  __syncthreads();
+
+  // ---------------- consumer setup ----------------
+  const int g = lane >> 2, t = lane & 3;
+
+  // ldmatrix lane addressing of q: matrix lane>>3 = {hi k0-7, hi k8-15, lo
+  // k0-7, lo k8-15}, row lane&7.
+  const uint32_t q_lane = qbase + (uint32_t)((lane >> 4) * RP + (lane & 7)) * C::QROW +
+                          (uint32_t)((lane >> 3) & 1) * 16;
+
+  // Last visible cell of each of this thread's rows (the verify window's
+  // causal limit), or -1 for padding rows.
+  int row_last[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = nt * 8 + 2 * t + j;
+      row_last[nt][j] = r < a.R ? L - a.W + r / a.G : -1;
+    }
+
+  float m[NT][2], l[NT][2];
+  float o[KS][NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = kNegInf;
+    l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+  }
+
+  const int cl = warp * kCellsPerWarp;  // first cell of this warp's slice in a stage
+  // block id of this warp's slice, loaded one tile ahead
+  auto slice_blk = [&](int it) -> int {
+    return it < n_tiles ? block_of(a, bt, c_begin + it * kTC + cl, c_end) : -1;
+  };
+  int blk_next = slice_blk(0);
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int s = it % C::STAGES;
+    const int blk_here = blk_next;
+    blk_next = slice_blk(it + 1);
+    const int nvalid = (blk_here >= 0 && blk_here < a.pool.n_blocks)
+                           ? min(kCellsPerWarp, c_end - (c_begin + it * kTC + cl))
+                           : 0;
+    if (!mbar_wait(bar_full + 8 * s, (it / C::STAGES) & 1)) {
+      lost = true;
+      break;
+    }
+    const int cw0 = c_begin + it * kTC + cl;  // this warp's first cell
+    if (nvalid > 0) {
+      const uint32_t st = sbase + s * C::STAGE_B;
+      const unsigned char* sp = smem + s * C::STAGE_B;
+
+      // ---------------- S^T = K . Q^T (four independent accumulators) ----------------
+      float z[NT][4];
+      if constexpr (FMT == KVQ_F16) {
+        float acc[4][NT][4];
+        const int mi = lane >> 3, rr = lane & 7;
+        const int cell = cl + ((mi & 1) << 3) + rr;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t af[4];
+          ldsm_x4(af, st + tile_off<FMT, HD>(cell, (ks * 16 + ((mi >> 1) << 3)) * 2));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            uint32_t qf[4];
+            ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + ks * 32);
+            if (ks < 2) {
+              mma16816_zc(acc[(ks & 1) * 2 + 0][nt], af, qf[0], qf[1]);
+              mma16816_zc(acc[(ks & 1) * 2 + 1][nt], af, qf[2], qf[3]);
+            } else {
+              mma16816(acc[(ks & 1) * 2 + 0][nt], af, qf[0], qf[1]);
+              mma16816(acc[(ks & 1) * 2 + 1][nt], af, qf[2], qf[3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            z[nt][k] = (acc[0][nt][k] + acc[2][nt][k]) + (acc[1][nt][k] + acc[3][nt][k]);
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) z[nt][0] = z[nt][1] = z[nt][2] = z[nt][3] = 0.f;
+        const unsigned short* ksc = reinterpret_cast<const unsigned short*>(sp + C::OFF_KS);
+#pragma unroll
+        for (int gq = 0; gq < C::NG; ++gq) {
+          const uint4 k0 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g, gq * 64 + 16 * t));
+          const uint4 k8 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g + 8, gq * 64 + 16 * t));
+          const uint32_t w0[4] = {k0.x ^ 0x80808080u, k0.y ^ 0x80808080u, k0.z ^ 0x80808080u,
+                                  k0.w ^ 0x80808080u};
+          const uint32_t w8[4] = {k8.x ^ 0x80808080u, k8.y ^ 0x80808080u, k8.z ^ 0x80808080u,
+                                  k8.w ^ 0x80808080u};
+          float acc[2][NT][4];  // hi chain, lo chain
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            uint32_t af[4];
+            widen_same(w0[kk], af[0], af[2]);
+            widen_same(w8[kk], af[1], af[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              uint32_t qf[4];
+              ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + (gq * 4 + kk) * 32);
+              if (kk == 0) {
+                mma16816_zc(acc[0][nt], af, qf[0], qf[1]);
+                mma16816_zc(acc[1][nt], af, qf[2], qf[3]);
+              } else {
+                mma16816(acc[0][nt], af, qf[0], qf[1]);
+                mma16816(acc[1][nt], af, qf[2], qf[3]);
+              }
+            }
+          }
+          const float s0 = __half2float(__ushort_as_half(ksc[(cl + g) * C::NG + gq]));
+          const float s8 = __half2float(__ushort_as_half(ksc[(cl + g + 8) * C::NG + gq]));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            z[nt][0] = fmaf(s0, acc[0][nt][0] + acc[1][nt][0], z[nt][0]);
+            z[nt][1] = fmaf(s0, acc[0][nt][1] + acc[1][nt][1], z[nt][1]);
+            z[nt][2] = fmaf(s8, acc[0][nt][2] + acc[1][nt][2], z[nt][2]);
+            z[nt][3] = fmaf(s8, acc[0][nt][3] + acc[1][nt][3], z[nt][3]);
+          }
+        }
+      }
+
+      // ---------------- masks and online softmax ----------------
+      float p[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int vis = min(nvalid - 1, row_last[nt][j] - cw0);  // last visible slice index
+          if (g > vis) z[nt][j] = kNegInf;
+          if (g + 8 > vis) z[nt][2 + j] = kNegInf;
+          float tmax = fmaxf(z[nt][j], z[nt][2 + j]);
+          tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
+          tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+          tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+          if (tmax > m[nt][j] + kTau) {  // also true for the first finite maximum
+            const float alpha = m[nt][j] == kNegInf ? 0.f : fast_exp2(m[nt][j] - tmax);
+            m[nt][j] = tmax;
+            l[nt][j] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              o[mt][nt][j] *= alpha;
+              o[mt][nt][2 + j] *= alpha;
+            }
+          }
+          const bool none = m[nt][j] == kNegInf;
+          p[nt][j] = none ? 0.f : fast_exp2(z[nt][j] - m[nt][j]);
+          p[nt][2 + j] = none ? 0.f : fast_exp2(z[nt][2 + j] - m[nt][j]);
+          l[nt][j] += p[nt][j] + p[nt][2 + j];
+        }
+      }
+
+      // ---------------- O^T += V^T . P^T ----------------
+      if constexpr (FMT == KVQ_F16) {
+        uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t h01, l01, h23, l23;
+          split_pair(p[nt][0], p[nt][1], h01, l01);
+          split_pair(p[nt][2], p[nt][3], h23, l23);
+          bh[nt][0] = movmatrix_t(h01);
+          bh[nt][1] = movmatrix_t(h23);
+          bl[nt][0] = movmatrix_t(l01);
+          bl[nt][1] = movmatrix_t(l23);
+        }
+        // V rows of cells past the valid ones may hold anything: zero them.
+        const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t mhi =
+            (2 * t + 8 < nvalid ? 0xffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
+        const int mi = lane >> 3, rr = lane & 7;
+        const int cell = cl + ((mi >> 1) << 3) + rr;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t af[4];
+          ldsm_x4_t(af, st + C::OFF_V + tile_off<FMT, HD>(cell, (mt * 16 + ((mi & 1) << 3)) * 2));
+          if (nvalid < kCellsPerWarp) {
+            af[0] &= mlo;
+            af[1] &= mlo;
+            af[2] &= mhi;
+            af[3] &= mhi;
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(o[mt][nt], af, bh[nt][0], bh[nt][1]);
+            mma16816(o[mt][nt], af, bl[nt][0], bl[nt][1]);
+          }
+        }
+      } else {
+        const unsigned short* vsc = reinterpret_cast<const unsigned short*>(sp + C::OFF_VS);
+        const unsigned char* vt = sp + C::OFF_V;
+#pragma unroll
+        for (int gv = 0; gv < C::NG; ++gv) {
+          // p = 0 exactly for masked cells, whose scale bits may be anything
+          // (even inf / NaN): clamping keeps 0 * s == 0.  Finite fp16
+          // scales are below 65504 and pass unchanged.
+          const float s0 = fminf(__half2float(__ushort_as_half(vsc[(cl + g) * C::NG + gv])), 65504.f);
+          const float s8 = fminf(__half2float(__ushort_as_half(vsc[(cl + g + 8) * C::NG + gv])), 65504.f);
+          uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float x0 = p[nt][0] * s0;
+            const float x1 = p[nt][1] * s0;
+            const float x2 = p[nt][2] * s8;
+            const float x3 = p[nt][3] * s8;
+            uint32_t h01, l01, h23, l23;
+            split_pair(x0, x1, h01, l01);
+            split_pair(x2, x3, h23, l23);
+            bh[nt][0] = movmatrix_t(h01);
+            bh[nt][1] = movmatrix_t(h23);
+            bl[nt][0] = movmatrix_t(l01);
+            bl[nt][1] = movmatrix_t(l23);
+          }
+          // two 32-dim chunks per 64-dim group; m-tile 2jj row g <-> dim
+          // 32jj + 4g, row g+8 <-> +1; m-tile 2jj+1 rows <-> +2, +3.
+#pragma unroll
+          for (int jh = 0; jh < 2; ++jh) {
+            const int jj = gv * 2 + jh;
+            const int db = 32 * jj + 4 * g;
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t, db)) ^ 0x80808080u;
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 1, db)) ^ 0x80808080u;
+            const uint32_t wc = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 8, db)) ^ 0x80808080u;
+            const uint32_t wd = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 9, db)) ^ 0x80808080u;
+            const uint32_t ab01 = prmt(wa, wb, 0x5140u), ab23 = prmt(wa, wb, 0x7362u);
+            const uint32_t cd01 = prmt(wc, wd, 0x5140u), cd23 = prmt(wc, wd, 0x7362u);
+            uint32_t a0[4], a1[4];
+            a0[0] = hsub2(prmt(ab01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t, 2t+1
+            a0[1] = hsub2(prmt(ab01, kMagic, 0x4342u), kBias);  // dim +1
+            a0[2] = hsub2(prmt(cd01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t+8, 2t+9
+            a0[3] = hsub2(prmt(cd01, kMagic, 0x4342u), kBias);  // dim +1
+            a1[0] = hsub2(prmt(ab23, kMagic, 0x4140u), kBias);  // dim +2
+            a1[1] = hsub2(prmt(ab23, kMagic, 0x4342u), kBias);  // dim +3
+            a1[2] = hsub2(prmt(cd23, kMagic, 0x4140u), kBias);
+            a1[3] = hsub2(prmt(cd23, kMagic, 0x4342u), kBias);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma16816(o[2 * jj][nt], a0, bh[nt][0], bh[nt][1]);
+              mma16816(o[2 * jj][nt], a0, bl[nt][0], bl[nt][1]);
+              mma16816(o[2 * jj + 1][nt], a1, bh[nt][0], bh[nt][1]);
+              mma16816(o[2 * jj + 1][nt], a1, bl[nt][0], bl[nt][1]);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    // Refill this stage with tile it + STAGES once every warp has let it go.
+    if (producer && issued < n_tiles) {
+      if (!mbar_wait(bar_empty + 8 * s, (it / C::STAGES) & 1)) {
+        lost = true;
+      } else {
+        issue(issued);
+        fetch_rows(issued + 1);
+        ++issued;
+      }
+    }
+  }
+  if (producer) {
+    // Every copy this CTA issued has landed before the CTA can exit.
+    for (int it = issued > C::STAGES ? issued - C::STAGES : 0; it < issued; ++it)
+      (void)mbar_wait(bar_full + 8 * (it % C::STAGES), (it / C::STAGES) & 1);
+  }
+
+  // ---------------- merge the warps ----------------
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float v = l[nt][j];
+      v += __shfl_xor_sync(kFull, v, 4);
+      v += __shfl_xor_sync(kFull, v, 8);
+      v += __shfl_xor_sync(kFull, v, 16);
+      l[nt][j] = v;
+    }
+  __syncthreads();  // the pipeline's shared memory is free now
+  float* s_m = reinterpret_cast<float*>(smem);   // [4][RP] warp maxima, then 4*RP + 8*RP spare
+  float* s_l = s_m + 16 * RP;                      // [4][RP] warp sums
+  float* s_o = s_l + kConsumerWarps * RP;          // [RP][HD]
+  int* s_lost = reinterpret_cast<int*>(s_o + RP * HD);
+  if (threadIdx.x == 0) *s_lost = 0;
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        s_m[warp * RP + nt * 8 + 2 * t + j] = m[nt][j];
+        s_l[warp * RP + nt * 8 + 2 * t + j] = l[nt][j];
+      }
+  }
+  __syncthreads();
+  if (lost) atomicOr(s_lost, 1);
+  float wgt[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = nt * 8 + 2 * t + j;
+      float M = s_m[r];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * RP + r]);
+      wgt[nt][j] = (M == kNegInf || m[nt][j] == kNegInf) ? 0.f : fast_exp2(m[nt][j] - M);
+    }
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int j = k & 1;
+            const int r = nt * 8 + 2 * t + j;
+            int d;
+            if constexpr (FMT == KVQ_F16) {
+              d = mt * 16 + g + ((k >> 1) << 3);
+            } else {
+              d = 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) + (k >> 1);
+            }
+            const float v = wgt[nt][j] * o[mt][nt][k];
+            s_o[r * HD + d] = (w == 0) ? v : s_o[r * HD + d] + v;
+          }
+    }
+    __syncthreads();
+  }
+
+  // CTA-level partial: per row the CTA maximum and sum (in shared memory
+  // next to the CTA's weighted o rows), read by the cluster leader.
+  const int tid = threadIdx.x;
+  float* c_M = s_m + 4 * RP;      // [RP] (s_m's second half is free after the warp merge)
+  float* c_L = c_M + RP;          // [RP]
+  if (tid < RP) {
+    const int r = tid;
+    float M = s_m[r];
+    for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * RP + r]);
+    float lsum = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w)
+      if (s_m[w * RP + r] != kNegInf) lsum = fmaf(s_l[w * RP + r], fast_exp2(s_m[w * RP + r] - M), lsum);
+    c_M[r] = *s_lost ? __int_as_float(0x7fc00000) : M;  // a lost wait poisons the row
+    c_L[r] = lsum;
+  }
+
+  // ---------------- cluster merge over distributed shared memory ----------------
+  const uint32_t crank = cluster_rank(), csize = cluster_size();
+  const int ci = split / (int)csize;                       // this cluster's partial slot
+  cluster_sync_all();
+  if (crank == 0) {
+    // leader: fold the other CTAs' (M, L, o) into its own, row by row; all
+    // remote loads of a batch are issued before any is used.
+    float* f_M = c_L + RP;        // [RP] merged maximum
+    float* f_w = f_M + RP;        // [8][RP] weight of each rank
+    if (tid < RP) {
+      const int r = tid;
+      float mq[8], lq[8];
+      mq[0] = c_M[r];
+      lq[0] = c_L[r];
+#pragma unroll
+      for (int q = 1; q < 8; ++q) {
+        if (q < (int)csize) {
+          mq[q] = dsmem_ld(dsmem_addr(smem_u32(c_M + r), q));
+          lq[q] = dsmem_ld(dsmem_addr(smem_u32(c_L + r), q));
+        }
+      }
+      float M = kNegInf;
+      int bad = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < (int)csize) {
+          bad |= mq[q] != mq[q];
+          M = fmaxf(M, mq[q]);
+        }
+      float lsum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float wq = (q >= (int)csize || M == kNegInf || mq[q] == kNegInf || bad) ? 0.f
+                                                                                         : fast_exp2(mq[q] - M);
+        f_w[q * RP + r] = wq;
+        if (q < (int)csize) lsum = fmaf(lq[q], wq, lsum);
+      }
+      f_M[r] = bad ? __int_as_float(0x7fc00000) : M;
+      c_L[r] = lsum;
+    }
+    __syncthreads();
+    const size_t slot = (((size_t)b * a.pool.n_kv + kvh) * a.ncl + ci) * a.R;
+    for (int i4 = tid; i4 < a.R * HD / 4; i4 += kThreads) {
+      const int i = i4 * 4, r = i / HD;
+      float4 v[8];
+      v[0] = *reinterpret_cast<const float4*>(s_o + i);
+#pragma unroll
+      for (int q = 1; q < 8; ++q)
+        if (q < (int)csize) v[q] = dsmem_ld4(dsmem_addr(smem_u32(s_o + i), q));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (q < (int)csize) {
+          const float wq = f_w[q * RP + r];
+          acc.x = fmaf(wq, v[q].x, acc.x);
+          acc.y = fmaf(wq, v[q].y, acc.y);
+          acc.z = fmaf(wq, v[q].z, acc.z);
+          acc.w = fmaf(wq, v[q].w, acc.w);
+        }
+      }
+      *reinterpret_cast<float4*>(a.ws_o + slot * HD + i) = acc;
+    }
+    if (tid < a.R) {
+      a.ws_ml[(slot + tid) * 2 + 0] = f_M[tid];
+      a.ws_ml[(slot + tid) * 2 + 1] = c_L[tid];
+    }
+  }
+  cluster_sync_all();  // the other CTAs keep their shared memory until the leader has read it
+}
+
+// ---------------------------------------------------------------------------
+// Final combine of the per-cluster partials (one CTA per sequence x KV head),
+// launched as a programmatic dependent of the partial kernel: its CTAs wait
+// on griddepcontrol until every partial is written.
+// ---------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(128) combine_clusters(DecodeArgs a, int cl) {
+  constexpr float kNegInf = -INFINITY;
+  constexpr int D4 = HD / 4;
+  __shared__ float s_M[32], s_inv[32];
+  __shared__ int s_nan[32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
+  const int ns = (L + a.split_cells - 1) / a.split_cells;  // non-empty splits
+  const int nlive = (ns + cl - 1) / cl;                      // clusters holding them
+  const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.ncl;
+  for (int r = warp; r < a.R; r += 4) {
+    float mx = kNegInf;
+    int bad = 0;
+    for (int j = lane; j < nlive; j += 32) {
+      const float mj = __ldcg(a.ws_ml + ((base0 + j) * a.R + r) * 2);
+      bad |= mj != mj;
+      mx = fmaxf(mx, mj);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+      bad |= __shfl_xor_sync(kFull, bad, off);
+    }
+    float lsum = 0.f;
+    for (int j = lane; j < nlive; j += 32) {
+      const size_t rj = (base0 + j) * a.R + r;
+      const float mj = __ldcg(a.ws_ml + rj * 2);
+      if (mx != kNegInf && mj != kNegInf) lsum = fmaf(__ldcg(a.ws_ml + rj * 2 + 1), fast_exp2(mj - mx), lsum);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+    if (lane == 0) {
+      s_M[r] = mx;
+      s_inv[r] = (mx != kNegInf && lsum > 0.f) ? 1.f / lsum : 0.f;
+      s_nan[r] = bad;
+    }
+  }
+  __syncthreads();
+  constexpr int BATCH = 8;  // partial loads in flight per thread
+  for (int i = tid; i < a.R * D4; i += 128) {
+    const int r = i / D4, d4 = (i - r * D4) * 4;
+    const float Mr = s_M[r], inv = s_inv[r];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (inv != 0.f) {
+      for (int j0 = 0; j0 < nlive; j0 += BATCH) {
+        float4 oj[BATCH];
+        float mj[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+          if (j0 + u < nlive) {
+            const size_t rj = (base0 + j0 + u) * a.R + r;
+            oj[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + rj * HD + d4));
+            mj[u] = __ldcg(a.ws_ml + rj * 2);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+          if (j0 + u < nlive) {
+            const float wj = mj[u] == kNegInf ? 0.f : fast_exp2(mj[u] - Mr);
+            acc.x = fmaf(wj, oj[u].x, acc.x);
+            acc.y = fmaf(wj, oj[u].y, acc.y);
+            acc.z = fmaf(wj, oj[u].z, acc.z);
+            acc.w = fmaf(wj, oj[u].w, acc.w);
+          }
+        }
+      }
+    }
+    const int w = r / a.G, gg = r - w * a.G;
+    float* dst = a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + d4;
+    float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (s_nan[r]) {
+      const float nan = __int_as_float(0x7fc00000);
+      res = make_float4(nan, nan, nan, nan);
+    }
+    *reinterpret_cast<float4*>(dst) = res;   // rows of an empty sequence come out 0
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// Span sp of one codes array: [total rows][SWB bytes] starting at byte
+// sp * SWB of each row, box = one piece of cells.
+template <int FMT, int HD>
+bool make_map(CUtensorMap* map, const void* base, int sp, long long rows, int piece_cells) {
+  using C = Cfg<FMT, HD, 1>;
+  auto enc = encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)C::SWB, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)C::ROWB};
+  const cuuint32_t box[2] = {(cuuint32_t)C::SWB, (cuuint32_t)piece_cells};
+  const cuuint32_t estr[2] = {1, 1};
+  void* span_base = static_cast<char*>(const_cast<void*>(base)) + (size_t)sp * C::SWB;
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, span_base, dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         C::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int FMT, int HD, int NT>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&decode_mma<FMT, HD, NT>);
+}
+
+template <int FMT, int HD, int NT>
+int ctas_per_sm_impl() {
+  static int occ = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    using C = Cfg<FMT, HD, NT>;
+    if (cudaFuncSetAttribute(decode_mma<FMT, HD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess) {
+      occ = 0;
+      return;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma<FMT, HD, NT>, kThreads,
+                                                      C::SMEM) != cudaSuccess)
+      n = 0;
+    occ = n;
+  });
+  return occ;
+}
+
+template <int FMT, int HD, int NT>
+cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s) {
+  using C = Cfg<FMT, HD, NT>;
+  if (ctas_per_sm_impl<FMT, HD, NT>() <= 0) return cudaErrorInvalidConfiguration;
+  const long long rows = (long long)a.pool.n_blocks * a.pool.n_kv << a.pool.bs_log2;
+  const int piece = 1 << (a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6);
+  TmaMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int sp = 0; sp < C::NCH; ++sp) {
+    if (!make_map<FMT, HD>(&maps.k[sp], a.pool.k, sp, rows, piece) ||
+        !make_map<FMT, HD>(&maps.v[sp], a.pool.v, sp, rows, piece))
+      return cudaErrorInvalidValue;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nsplit, a.pool.n_kv, a.n_seq);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma<FMT, HD, NT>, maps, a);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cc = {};
+  cc.gridDim = dim3(a.pool.n_kv, a.n_seq, 1);
+  cc.blockDim = dim3(128);
+  cc.stream = s;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cc.attrs = pdl;
+  cc.numAttrs = 1;
+  return cudaLaunchKernelEx(&cc, combine_clusters<HD>, a, p.cluster);
+}
+
+// Clusters of `cl` CTAs that can be resident on the device at once.
+template <int FMT, int HD, int NT>
+int active_clusters_impl(int cl) {
+  static int cache[4] = {-1, -1, -1, -1};  // cl = 1, 2, 4, 8
+  static std::mutex mu;
+  const int idx = cl == 1 ? 0 : cl == 2 ? 1 : cl == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[idx] >= 0) return cache[idx];
+  using C = Cfg<FMT, HD, NT>;
+  int n = 0;
+  if (ctas_per_sm_impl<FMT, HD, NT>() > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl * 64, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_mma<FMT, HD, NT>, &cfg) != cudaSuccess) n = 0;
+  }
+  cache[idx] = n;
+  return n;
+}
+
+template <int FMT, int HD>
+int active_clusters_hd(int nt, int cl) {
+  switch (nt) {
+    case 1: return active_clusters_impl<FMT, HD, 1>(cl);
+    case 2: if constexpr (HD <= 128) return active_clusters_impl<FMT, HD, 2>(cl); break;
+    case 4: if constexpr (HD <= 64) return active_clusters_impl<FMT, HD, 4>(cl); break;
+  }
+  return 0;
+}
+
+template <int FMT, int HD>
+int ctas_per_sm_hd(int nt) {
+  switch (nt) {
+    case 1: return ctas_per_sm_impl<FMT, HD, 1>();
+    case 2: if constexpr (HD <= 128) return ctas_per_sm_impl<FMT, HD, 2>(); break;
+    case 4: if constexpr (HD <= 64) return ctas_per_sm_impl<FMT, HD, 4>(); break;
+  }
+  return 0;
+}
+
+template <int FMT, int HD>
+cudaError_t launch_hd(int nt, const DecodePlan& p, const DecodeArgs& a, cudaStream_t s) {
+  switch (nt) {
+    case 1: return launch_impl<FMT, HD, 1>(p, a, s);
+    case 2: if constexpr (HD <= 128) return launch_impl<FMT, HD, 2>(p, a, s); break;
+    case 4: if constexpr (HD <= 64) return launch_impl<FMT, HD, 4>(p, a, s); break;
+  }
+  return cudaErrorInvalidValue;
+}
+
+int n_tiles_for(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 0; }
+
+}  // namespace
+
+bool mma_decode_supported(int fmt, int hd, int rows) {
+  const int nt = n_tiles_for(rows);
+  if (nt == 0 || rows < 1) return false;
+  if (hd != 64 && hd != 128 && hd != 256) return false;
+  if (fmt != KVQ_F16 && fmt != KVQ_Q8) return false;
+  return nt * hd <= 256;
+}
+
+int mma_cell_tile() { return kTC; }
+
+int mma_active_clusters(int fmt, int hd, int rows, int cl) {
+  const int nt = n_tiles_for(rows);
+  if (fmt == KVQ_F16) {
+    if (hd == 64) return active_clusters_hd<KVQ_F16, 64>(nt, cl);
+    if (hd == 128) return active_clusters_hd<KVQ_F16, 128>(nt, cl);
+    return active_clusters_hd<KVQ_F16, 256>(nt, cl);
+  }
+  if (hd == 64) return active_clusters_hd<KVQ_Q8, 64>(nt, cl);
+  if (hd == 128) return active_clusters_hd<KVQ_Q8, 128>(nt, cl);
+  return active_clusters_hd<KVQ_Q8, 256>(nt, cl);
+}
+
+int mma_ctas_per_sm(int fmt, int hd, int rows) {
+  const int nt = n_tiles_for(rows);
+  if (fmt == KVQ_F16) {
+    if (hd == 64) return ctas_per_sm_hd<KVQ_F16, 64>(nt);
+    if (hd == 128) return ctas_per_sm_hd<KVQ_F16, 128>(nt);
+    return ctas_per_sm_hd<KVQ_F16, 256>(nt);
+  }
+  if (hd == 64) return ctas_per_sm_hd<KVQ_Q8, 64>(nt);
+  if (hd == 128) return ctas_per_sm_hd<KVQ_Q8, 128>(nt);
+  return ctas_per_sm_hd<KVQ_Q8, 256>(nt);
+}
+
+cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, const DecodeArgs& a,
+                                      cudaStream_t s) {
+  const int nt = n_tiles_for(p.rows);
+  if (fmt == KVQ_F16) {
+    if (hd == 64) return launch_hd<KVQ_F16, 64>(nt, p, a, s);
+    if (hd == 128) return launch_hd<KVQ_F16, 128>(nt, p, a, s);
+    return launch_hd<KVQ_F16, 256>(nt, p, a, s);
+  }
+  if (hd == 64) return launch_hd<KVQ_Q8, 64>(nt, p, a, s);
+  if (hd == 128) return launch_hd<KVQ_Q8, 128>(nt, p, a, s);
+  return launch_hd<KVQ_Q8, 256>(nt, p, a, s);
+}
+
+}  // namespace kvq

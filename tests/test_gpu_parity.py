@@ -231,7 +231,7 @@ def test_validation_with_real_buffers():
     out = torch.empty_like(q)
     ctx = dev(np.array([64], np.int32))
     ws_bytes = p.gpu.workspace_bytes(1, 1, 4, 64)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     c = p.gpu.cache
     call = lambda **kw: kvq.kvq_decode_attn(
         kw.get("cache", c), kw.get("q", q), 1, kw.get("W", 1), kw.get("n_q", 4), ctx,

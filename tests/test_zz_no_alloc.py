@@ -70,7 +70,7 @@ def _with_workspace(pool, q, ctx, max_ctx, bt, sm):
     n_seq, W, n_q, _ = q.shape
     out = torch.full_like(q, float("nan"))
     need = kvq.kvq_decode_workspace_bytes(pool.cache, n_seq, W, n_q, max_ctx)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     st = kvq.kvq_decode_attn(pool.cache, q, n_seq, W, n_q, ctx, max_ctx, bt, bt.shape[1], sm,
                              out, ws, need)
     assert st == kvq.KVQ_OK, kvq.kvq_status_string(st)
