@@ -44,6 +44,11 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   constexpr int LANES_PER_GROUP = kGroup / VEC;
   constexpr int NG = HD / kGroup;
 
+  // Launched as a programmatic dependent: wait for the previous kernel's
+  // writes (k, v, positions may come from it), then let the next kernel's
+  // launch begin.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   const long long n_rows = (long long)a.n_tok * a.n_kv * 2;
@@ -130,14 +135,21 @@ cudaError_t launch_fmt(int hd, const AppendArgs& a, cudaStream_t s) {
   const int warps_per_block = 8;
   const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)blocks), block(32 * warps_per_block);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(32 * warps_per_block);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (hd) {
-    case 64: append_kernel<FMT, 64><<<grid, block, 0, s>>>(a); break;
-    case 128: append_kernel<FMT, 128><<<grid, block, 0, s>>>(a); break;
-    case 256: append_kernel<FMT, 256><<<grid, block, 0, s>>>(a); break;
+    case 64: return cudaLaunchKernelEx(&cfg, append_kernel<FMT, 64>, a);
+    case 128: return cudaLaunchKernelEx(&cfg, append_kernel<FMT, 128>, a);
+    case 256: return cudaLaunchKernelEx(&cfg, append_kernel<FMT, 256>, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

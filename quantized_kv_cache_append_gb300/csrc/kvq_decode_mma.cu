@@ -66,7 +66,12 @@ struct Cfg {
   static constexpr int STAGE_B = (STAGE_RAW + 1023) / 1024 * 1024;
   // Stages per CTA and CTAs per SM: keep about 100 KB or more of copies in
   // flight per SM while fitting as many 4-warp CTAs as the 227 KB allow.
-  static constexpr int STAGES = STAGE_B <= 20 * 1024 ? 3 : (STAGE_B <= 32 * 1024 ? 2 : 3);
+  // merge buffers reuse the stages after the loop: 20 row values x 32 rows,
+  // o rows plus four warp slabs (5 x RP x HD floats), flags
+  static constexpr int MERGE_B = (20 * 32 + 5 * NT * 8 * HD + 4) * 4;
+  // at least three stages (one in flight while two are held), more when the
+  // merge buffers need the room
+  static constexpr int STAGES = (MERGE_B + STAGE_B - 1) / STAGE_B > 3 ? (MERGE_B + STAGE_B - 1) / STAGE_B : 3;
   static constexpr int OFF_V = TILE_B;
   static constexpr int OFF_KS = 2 * TILE_B;
   static constexpr int OFF_VS = 2 * TILE_B + SCALE_B;
@@ -75,10 +80,13 @@ struct Cfg {
   static constexpr int QBYTES_MAX = 2 * NT * 8 * QROW;   // hi and lo, NT*8 padded rows
   static constexpr int SMEM_Q = STAGES * STAGE_B;
   static constexpr int SMEM_BAR = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
-  static constexpr int SMEM = SMEM_BAR + 2 * STAGES * 8 + 1024 /*align*/;
+  // block ids of the split's pieces, staged once so any warp can issue a refill
+  static constexpr int ROWS_CAP = 512;
+  static constexpr int SMEM_REL = SMEM_BAR + STAGES * 8;        // release counters [STAGES]
+  static constexpr int SMEM_BLK = SMEM_REL + 16 * 4;            // block ids [ROWS_CAP]
+  static constexpr int SMEM = SMEM_BLK + ROWS_CAP * 4 + 1024 /*align*/;
   static constexpr int MIN_CTAS = (227 * 1024) / SMEM >= 3 ? 3 : ((227 * 1024) / SMEM >= 2 ? 2 : 1);
-  // merge buffers (20 x 32 row values, o for rows x dims <= 2048, two flags)
-  static_assert(STAGES * STAGE_B >= (20 * 32 + 2048 + 2) * 4, "merge buffers fit");
+  static_assert(STAGES * STAGE_B >= MERGE_B, "merge buffers fit");
 };
 
 // ---------------------------------------------------------------------------
@@ -307,10 +315,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t qbase = sbase + C::SMEM_Q;                 // q hi rows, then lo rows
   const uint32_t bar_full = sbase + C::SMEM_BAR;
-  const uint32_t bar_empty = bar_full + 8 * C::STAGES;
+  int* s_rel = reinterpret_cast<int*>(smem + C::SMEM_REL);
+  int* s_blk = reinterpret_cast<int*>(smem + C::SMEM_BLK);
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream: nothing it may have written is read before this wait.
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.k[0])) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.v[0])) : "memory");
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
   const int c_begin = split * a.split_cells;
   // An empty split (past the end of the context) still runs to the cluster
@@ -327,15 +343,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // (griddepcontrol.wait) for this whole grid to finish before reading.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // Producer state (thread 0): pool rows of the pieces of the next tile to
-  // issue, read one tile ahead so the block-table load latency is hidden.
-  int next_blk[MAXP];
-  auto fetch_rows = [&](int it) {
-    const int c0 = c_begin + it * kTC;
-    for (int p = 0; p < MAXP; ++p)
-      next_blk[p] = (p < n_pieces && it < n_tiles) ? block_of(a, bt, c0 + (p << pc_log2), c_end) : -1;
+  // Copies of a stage are issued by whichever warp releases the stage last
+  // (a shared-memory counter per stage), so no warp ever blocks waiting for
+  // the others.  The block id of every piece of the split is staged in
+  // shared memory once (when it fits), so an issuing warp needs no global
+  // load on that path.
+  const int n_entries = n_tiles * n_pieces;
+  const bool blk_in_smem = n_entries <= C::ROWS_CAP;
+  auto piece_blk = [&](int it, int p, bool from_smem) -> int {
+    return from_smem ? s_blk[it * n_pieces + p]
+                     : block_of(a, bt, c_begin + it * kTC + (p << pc_log2), c_end);
   };
-  auto issue = [&](int it) {
+  auto issue = [&](int it, bool from_smem) {
     const int s = it % C::STAGES;
     const int pc = 1 << pc_log2;
     const int bsz = 1 << a.pool.bs_log2;
@@ -343,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     int rows[MAXP];
     uint32_t bytes = 0;
     for (int p = 0; p < MAXP; ++p) {
-      const int blk = next_blk[p];
+      const int blk = p < n_pieces ? piece_blk(it, p, from_smem) : -1;
       const int c = c0 + (p << pc_log2);
       rows[p] = (p < n_pieces && blk >= 0 && blk < a.pool.n_blocks)
                     ? (blk * a.pool.n_kv + kvh) * bsz + (c & (bsz - 1))
@@ -371,31 +390,24 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     }
   };
 
-  // The producer initialises the barriers and starts the first copies
-  // before anything else, so their latency overlaps the q load below.
-  int issued = 0;
-  bool lost = false;
-  if (producer) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kConsumerWarps);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    fetch_rows(0);
-    for (int it = 0; it < n_tiles && it < C::STAGES; ++it) {
-      issue(it);
-      fetch_rows(it + 1);
-      ++issued;
-    }
-  }
-  // q * sm_scale * log2(e) as fp16 hi + lo, rows [RP][HD] in k order: FP16
-  // uses the natural dim order; int8 permutes each 16-wide k-step so that
-  // k = 2t + e -> dim 64 gq + 16 t + 4 kk + e and k = 2t + 8 + e -> that + 2
-  // (t = k-pair lane, kk = k-step inside the 64-dim group gq), the order in
-  // which a lane widens its 4-byte code words.
-  {
-    unsigned char* qs = smem + C::SMEM_Q;
-    for (int i = threadIdx.x; i < RP * HD; i += kThreads) {
+  // Prologue.  Every small load (q, the split's block ids) is issued first,
+  // into registers; only then does thread 0 start the first stages' bulk
+  // copies.  Issued the other way round, these few latency-critical loads
+  // would queue behind tens of megabytes of copies from all CTAs.
+  //
+  // q * sm_scale * log2(e) goes to shared memory as fp16 hi + lo, rows
+  // [RP][HD] in k order: FP16 uses the natural dim order; int8 permutes each
+  // 16-wide k-step so that k = 2t + e -> dim 64 gq + 16 t + 4 kk + e and
+  // k = 2t + 8 + e -> that + 2 (t = k-pair lane, kk = k-step inside the
+  // 64-dim group gq), the order in which a lane widens its 4-byte code words.
+  constexpr int QPT = (RP * HD + kThreads - 1) / kThreads;  // q values per thread
+  constexpr int BPT = (C::ROWS_CAP + kThreads - 1) / kThreads;
+  float qv[QPT];
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    const int i = threadIdx.x + u * kThreads;
+    qv[u] = 0.f;
+    if (i < RP * HD) {
       const int r = i / HD, k = i - r * HD;
       int dim = k;
       if constexpr (FMT == KVQ_Q8) {
@@ -403,15 +415,47 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         const int tt = (kq & 7) >> 1, e = kq & 1, hi8 = kq >> 3;
         dim = (ks >> 2) * 64 + 16 * tt + 4 * (ks & 3) + 2 * hi8 + e;
       }
-      float x = 0.f;
       if (r < a.R) {
         const int w = r / a.G, gg = r - w * a.G;
-        x = __ldg(a.q + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + dim) * a.qscale;
+        qv[u] = __ldg(a.q + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + dim);
       }
-      const __half h = __float2half_rn(x);
-      const __half lo = __float2half_rn(x - __half2float(h));
-      *reinterpret_cast<__half*>(qs + r * C::QROW + k * 2) = h;
-      *reinterpret_cast<__half*>(qs + (RP + r) * C::QROW + k * 2) = lo;
+    }
+  }
+  int bv[BPT];
+#pragma unroll
+  for (int u = 0; u < BPT; ++u) {
+    const int i = threadIdx.x + u * kThreads;
+    bv[u] = (blk_in_smem && i < n_entries)
+                ? block_of(a, bt, c_begin + (i / n_pieces) * kTC + ((i % n_pieces) << pc_log2), c_end)
+                : -1;
+  }
+  bool lost = false;
+  if (producer) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      s_rel[s] = 0;
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int it = 0; it < n_tiles && it < C::STAGES; ++it) issue(it, false);
+  }
+  {
+    unsigned char* qs = smem + C::SMEM_Q;
+#pragma unroll
+    for (int u = 0; u < QPT; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      if (i < RP * HD) {
+        const int r = i / HD, k = i - r * HD;
+        const float x = qv[u] * a.qscale;
+        const __half h = __float2half_rn(x);
+        const __half lo = __float2half_rn(x - __half2float(h));
+        *reinterpret_cast<__half*>(qs + r * C::QROW + k * 2) = h;
+        *reinterpret_cast<__half*>(qs + (RP + r) * C::QROW + k * 2) = lo;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < BPT; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      if (blk_in_smem && i < n_entries) s_blk[i] = bv[u];
     }
   }
   __syncthreads();
@@ -446,237 +490,281 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   }
 
   const int cl = warp * kCellsPerWarp;  // first cell of this warp's slice in a stage
-  // block id of this warp's slice, loaded one tile ahead
   auto slice_blk = [&](int it) -> int {
     return it < n_tiles ? block_of(a, bt, c_begin + it * kTC + cl, c_end) : -1;
   };
-  int blk_next = slice_blk(0);
+  auto slice_nvalid = [&](int it, int blk) -> int {
+    return (blk >= 0 && blk < a.pool.n_blocks) ? min(kCellsPerWarp, c_end - (c_begin + it * kTC + cl)) : 0;
+  };
 
-  for (int it = 0; it < n_tiles; ++it) {
-    const int s = it % C::STAGES;
-    const int blk_here = blk_next;
-    blk_next = slice_blk(it + 1);
-    const int nvalid = (blk_here >= 0 && blk_here < a.pool.n_blocks)
-                           ? min(kCellsPerWarp, c_end - (c_begin + it * kTC + cl))
-                           : 0;
-    if (!mbar_wait(bar_full + 8 * s, (it / C::STAGES) & 1)) {
-      lost = true;
-      break;
-    }
-    const int cw0 = c_begin + it * kTC + cl;  // this warp's first cell
-    if (nvalid > 0) {
-      const uint32_t st = sbase + s * C::STAGE_B;
-      const unsigned char* sp = smem + s * C::STAGE_B;
-
-      // ---------------- S^T = K . Q^T (four independent accumulators) ----------------
-      float z[NT][4];
-      if constexpr (FMT == KVQ_F16) {
-        float acc[4][NT][4];
-        const int mi = lane >> 3, rr = lane & 7;
-        const int cell = cl + ((mi & 1) << 3) + rr;
+  // q . k of one stage for this warp's 16 cells -> z (log2-domain logits)
+  auto qk = [&](int s, float (&z)[NT][4]) {
+    const uint32_t st = sbase + s * C::STAGE_B;
+    const unsigned char* sp = smem + s * C::STAGE_B;
+  // ---------------- S^T = K . Q^T (four independent accumulators) ----------------
+  if constexpr (FMT == KVQ_F16) {
+    float acc[4][NT][4];
+    const int mi = lane >> 3, rr = lane & 7;
+    const int cell = cl + ((mi & 1) << 3) + rr;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t af[4];
-          ldsm_x4(af, st + tile_off<FMT, HD>(cell, (ks * 16 + ((mi >> 1) << 3)) * 2));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            uint32_t qf[4];
-            ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + ks * 32);
-            if (ks < 2) {
-              mma16816_zc(acc[(ks & 1) * 2 + 0][nt], af, qf[0], qf[1]);
-              mma16816_zc(acc[(ks & 1) * 2 + 1][nt], af, qf[2], qf[3]);
-            } else {
-              mma16816(acc[(ks & 1) * 2 + 0][nt], af, qf[0], qf[1]);
-              mma16816(acc[(ks & 1) * 2 + 1][nt], af, qf[2], qf[3]);
-            }
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            z[nt][k] = (acc[0][nt][k] + acc[2][nt][k]) + (acc[1][nt][k] + acc[3][nt][k]);
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) z[nt][0] = z[nt][1] = z[nt][2] = z[nt][3] = 0.f;
-        const unsigned short* ksc = reinterpret_cast<const unsigned short*>(sp + C::OFF_KS);
-#pragma unroll
-        for (int gq = 0; gq < C::NG; ++gq) {
-          const uint4 k0 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g, gq * 64 + 16 * t));
-          const uint4 k8 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g + 8, gq * 64 + 16 * t));
-          const uint32_t w0[4] = {k0.x ^ 0x80808080u, k0.y ^ 0x80808080u, k0.z ^ 0x80808080u,
-                                  k0.w ^ 0x80808080u};
-          const uint32_t w8[4] = {k8.x ^ 0x80808080u, k8.y ^ 0x80808080u, k8.z ^ 0x80808080u,
-                                  k8.w ^ 0x80808080u};
-          float acc[2][NT][4];  // hi chain, lo chain
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            uint32_t af[4];
-            widen_same(w0[kk], af[0], af[2]);
-            widen_same(w8[kk], af[1], af[3]);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              uint32_t qf[4];
-              ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + (gq * 4 + kk) * 32);
-              if (kk == 0) {
-                mma16816_zc(acc[0][nt], af, qf[0], qf[1]);
-                mma16816_zc(acc[1][nt], af, qf[2], qf[3]);
-              } else {
-                mma16816(acc[0][nt], af, qf[0], qf[1]);
-                mma16816(acc[1][nt], af, qf[2], qf[3]);
-              }
-            }
-          }
-          const float s0 = __half2float(__ushort_as_half(ksc[(cl + g) * C::NG + gq]));
-          const float s8 = __half2float(__ushort_as_half(ksc[(cl + g + 8) * C::NG + gq]));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            z[nt][0] = fmaf(s0, acc[0][nt][0] + acc[1][nt][0], z[nt][0]);
-            z[nt][1] = fmaf(s0, acc[0][nt][1] + acc[1][nt][1], z[nt][1]);
-            z[nt][2] = fmaf(s8, acc[0][nt][2] + acc[1][nt][2], z[nt][2]);
-            z[nt][3] = fmaf(s8, acc[0][nt][3] + acc[1][nt][3], z[nt][3]);
-          }
-        }
-      }
-
-      // ---------------- masks and online softmax ----------------
-      float p[NT][4];
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t af[4];
+      ldsm_x4(af, st + tile_off<FMT, HD>(cell, (ks * 16 + ((mi >> 1) << 3)) * 2));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int vis = min(nvalid - 1, row_last[nt][j] - cw0);  // last visible slice index
-          if (g > vis) z[nt][j] = kNegInf;
-          if (g + 8 > vis) z[nt][2 + j] = kNegInf;
-          float tmax = fmaxf(z[nt][j], z[nt][2 + j]);
-          tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
-          tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
-          tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-          if (tmax > m[nt][j] + kTau) {  // also true for the first finite maximum
-            const float alpha = m[nt][j] == kNegInf ? 0.f : fast_exp2(m[nt][j] - tmax);
-            m[nt][j] = tmax;
-            l[nt][j] *= alpha;
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-              o[mt][nt][j] *= alpha;
-              o[mt][nt][2 + j] *= alpha;
-            }
-          }
-          const bool none = m[nt][j] == kNegInf;
-          p[nt][j] = none ? 0.f : fast_exp2(z[nt][j] - m[nt][j]);
-          p[nt][2 + j] = none ? 0.f : fast_exp2(z[nt][2 + j] - m[nt][j]);
-          l[nt][j] += p[nt][j] + p[nt][2 + j];
-        }
-      }
-
-      // ---------------- O^T += V^T . P^T ----------------
-      if constexpr (FMT == KVQ_F16) {
-        uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          uint32_t h01, l01, h23, l23;
-          split_pair(p[nt][0], p[nt][1], h01, l01);
-          split_pair(p[nt][2], p[nt][3], h23, l23);
-          bh[nt][0] = movmatrix_t(h01);
-          bh[nt][1] = movmatrix_t(h23);
-          bl[nt][0] = movmatrix_t(l01);
-          bl[nt][1] = movmatrix_t(l23);
-        }
-        // V rows of cells past the valid ones may hold anything: zero them.
-        const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t mhi =
-            (2 * t + 8 < nvalid ? 0xffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
-        const int mi = lane >> 3, rr = lane & 7;
-        const int cell = cl + ((mi >> 1) << 3) + rr;
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          uint32_t af[4];
-          ldsm_x4_t(af, st + C::OFF_V + tile_off<FMT, HD>(cell, (mt * 16 + ((mi & 1) << 3)) * 2));
-          if (nvalid < kCellsPerWarp) {
-            af[0] &= mlo;
-            af[1] &= mlo;
-            af[2] &= mhi;
-            af[3] &= mhi;
-          }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma16816(o[mt][nt], af, bh[nt][0], bh[nt][1]);
-            mma16816(o[mt][nt], af, bl[nt][0], bl[nt][1]);
-          }
-        }
-      } else {
-        const unsigned short* vsc = reinterpret_cast<const unsigned short*>(sp + C::OFF_VS);
-        const unsigned char* vt = sp + C::OFF_V;
-#pragma unroll
-        for (int gv = 0; gv < C::NG; ++gv) {
-          // p = 0 exactly for masked cells, whose scale bits may be anything
-          // (even inf / NaN): clamping keeps 0 * s == 0.  Finite fp16
-          // scales are below 65504 and pass unchanged.
-          const float s0 = fminf(__half2float(__ushort_as_half(vsc[(cl + g) * C::NG + gv])), 65504.f);
-          const float s8 = fminf(__half2float(__ushort_as_half(vsc[(cl + g + 8) * C::NG + gv])), 65504.f);
-          uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float x0 = p[nt][0] * s0;
-            const float x1 = p[nt][1] * s0;
-            const float x2 = p[nt][2] * s8;
-            const float x3 = p[nt][3] * s8;
-            uint32_t h01, l01, h23, l23;
-            split_pair(x0, x1, h01, l01);
-            split_pair(x2, x3, h23, l23);
-            bh[nt][0] = movmatrix_t(h01);
-            bh[nt][1] = movmatrix_t(h23);
-            bl[nt][0] = movmatrix_t(l01);
-            bl[nt][1] = movmatrix_t(l23);
-          }
-          // two 32-dim chunks per 64-dim group; m-tile 2jj row g <-> dim
-          // 32jj + 4g, row g+8 <-> +1; m-tile 2jj+1 rows <-> +2, +3.
-#pragma unroll
-          for (int jh = 0; jh < 2; ++jh) {
-            const int jj = gv * 2 + jh;
-            const int db = 32 * jj + 4 * g;
-            const uint32_t wa = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t, db)) ^ 0x80808080u;
-            const uint32_t wb = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 1, db)) ^ 0x80808080u;
-            const uint32_t wc = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 8, db)) ^ 0x80808080u;
-            const uint32_t wd = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 9, db)) ^ 0x80808080u;
-            const uint32_t ab01 = prmt(wa, wb, 0x5140u), ab23 = prmt(wa, wb, 0x7362u);
-            const uint32_t cd01 = prmt(wc, wd, 0x5140u), cd23 = prmt(wc, wd, 0x7362u);
-            uint32_t a0[4], a1[4];
-            a0[0] = hsub2(prmt(ab01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t, 2t+1
-            a0[1] = hsub2(prmt(ab01, kMagic, 0x4342u), kBias);  // dim +1
-            a0[2] = hsub2(prmt(cd01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t+8, 2t+9
-            a0[3] = hsub2(prmt(cd01, kMagic, 0x4342u), kBias);  // dim +1
-            a1[0] = hsub2(prmt(ab23, kMagic, 0x4140u), kBias);  // dim +2
-            a1[1] = hsub2(prmt(ab23, kMagic, 0x4342u), kBias);  // dim +3
-            a1[2] = hsub2(prmt(cd23, kMagic, 0x4140u), kBias);
-            a1[3] = hsub2(prmt(cd23, kMagic, 0x4342u), kBias);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              mma16816(o[2 * jj][nt], a0, bh[nt][0], bh[nt][1]);
-              mma16816(o[2 * jj][nt], a0, bl[nt][0], bl[nt][1]);
-              mma16816(o[2 * jj + 1][nt], a1, bh[nt][0], bh[nt][1]);
-              mma16816(o[2 * jj + 1][nt], a1, bl[nt][0], bl[nt][1]);
-            }
-          }
+        uint32_t qf[4];
+        ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + ks * 32);
+        if (ks < 2) {
+          mma16816_zc(acc[(ks & 1) * 2 + 0][nt], af, qf[0], qf[1]);
+          mma16816_zc(acc[(ks & 1) * 2 + 1][nt], af, qf[2], qf[3]);
+        } else {
+          mma16816(acc[(ks & 1) * 2 + 0][nt], af, qf[0], qf[1]);
+          mma16816(acc[(ks & 1) * 2 + 1][nt], af, qf[2], qf[3]);
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-    // Refill this stage with tile it + STAGES once every warp has let it go.
-    if (producer && issued < n_tiles) {
-      if (!mbar_wait(bar_empty + 8 * s, (it / C::STAGES) & 1)) {
-        lost = true;
-      } else {
-        issue(issued);
-        fetch_rows(issued + 1);
-        ++issued;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        z[nt][k] = (acc[0][nt][k] + acc[2][nt][k]) + (acc[1][nt][k] + acc[3][nt][k]);
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) z[nt][0] = z[nt][1] = z[nt][2] = z[nt][3] = 0.f;
+    const unsigned short* ksc = reinterpret_cast<const unsigned short*>(sp + C::OFF_KS);
+#pragma unroll
+    for (int gq = 0; gq < C::NG; ++gq) {
+      const uint4 k0 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g, gq * 64 + 16 * t));
+      const uint4 k8 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g + 8, gq * 64 + 16 * t));
+      const uint32_t w0[4] = {k0.x ^ 0x80808080u, k0.y ^ 0x80808080u, k0.z ^ 0x80808080u,
+                              k0.w ^ 0x80808080u};
+      const uint32_t w8[4] = {k8.x ^ 0x80808080u, k8.y ^ 0x80808080u, k8.z ^ 0x80808080u,
+                              k8.w ^ 0x80808080u};
+      float acc[2][NT][4];  // hi chain, lo chain
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t af[4];
+        widen_same(w0[kk], af[0], af[2]);
+        widen_same(w8[kk], af[1], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t qf[4];
+          ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + (gq * 4 + kk) * 32);
+          if (kk == 0) {
+            mma16816_zc(acc[0][nt], af, qf[0], qf[1]);
+            mma16816_zc(acc[1][nt], af, qf[2], qf[3]);
+          } else {
+            mma16816(acc[0][nt], af, qf[0], qf[1]);
+            mma16816(acc[1][nt], af, qf[2], qf[3]);
+          }
+        }
+      }
+      const float s0 = __half2float(__ushort_as_half(ksc[(cl + g) * C::NG + gq]));
+      const float s8 = __half2float(__ushort_as_half(ksc[(cl + g + 8) * C::NG + gq]));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        z[nt][0] = fmaf(s0, acc[0][nt][0] + acc[1][nt][0], z[nt][0]);
+        z[nt][1] = fmaf(s0, acc[0][nt][1] + acc[1][nt][1], z[nt][1]);
+        z[nt][2] = fmaf(s8, acc[0][nt][2] + acc[1][nt][2], z[nt][2]);
+        z[nt][3] = fmaf(s8, acc[0][nt][3] + acc[1][nt][3], z[nt][3]);
       }
     }
   }
+
+  };
+
+  // causal / length masks, online softmax -> p (rescales o when the maximum rises)
+  auto softmax = [&](int nvalid, int cw0, float (&z)[NT][4], float (&p)[NT][4]) {
+  // ---------------- masks and online softmax ----------------
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int vis = min(nvalid - 1, row_last[nt][j] - cw0);  // last visible slice index
+      if (g > vis) z[nt][j] = kNegInf;
+      if (g + 8 > vis) z[nt][2 + j] = kNegInf;
+      float tmax = fmaxf(z[nt][j], z[nt][2 + j]);
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+      if (tmax > m[nt][j] + kTau) {  // also true for the first finite maximum
+        const float alpha = m[nt][j] == kNegInf ? 0.f : fast_exp2(m[nt][j] - tmax);
+        m[nt][j] = tmax;
+        l[nt][j] *= alpha;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][nt][j] *= alpha;
+          o[mt][nt][2 + j] *= alpha;
+        }
+      }
+      const bool none = m[nt][j] == kNegInf;
+      p[nt][j] = none ? 0.f : fast_exp2(z[nt][j] - m[nt][j]);
+      p[nt][2 + j] = none ? 0.f : fast_exp2(z[nt][2 + j] - m[nt][j]);
+      l[nt][j] += p[nt][j] + p[nt][2 + j];
+    }
+  }
+
+  };
+
+  // o += V^T . P^T for one stage
+  auto pv = [&](int s, int nvalid, const float (&p)[NT][4]) {
+    const uint32_t st = sbase + s * C::STAGE_B;
+    const unsigned char* sp = smem + s * C::STAGE_B;
+  // ---------------- O^T += V^T . P^T ----------------
+  if constexpr (FMT == KVQ_F16) {
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint32_t h01, l01, h23, l23;
+      split_pair(p[nt][0], p[nt][1], h01, l01);
+      split_pair(p[nt][2], p[nt][3], h23, l23);
+      bh[nt][0] = movmatrix_t(h01);
+      bh[nt][1] = movmatrix_t(h23);
+      bl[nt][0] = movmatrix_t(l01);
+      bl[nt][1] = movmatrix_t(l23);
+    }
+    // V rows of cells past the valid ones may hold anything: zero them.
+    const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
+    const uint32_t mhi =
+        (2 * t + 8 < nvalid ? 0xffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
+    const int mi = lane >> 3, rr = lane & 7;
+    const int cell = cl + ((mi >> 1) << 3) + rr;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t af[4];
+      ldsm_x4_t(af, st + C::OFF_V + tile_off<FMT, HD>(cell, (mt * 16 + ((mi & 1) << 3)) * 2));
+      if (nvalid < kCellsPerWarp) {
+        af[0] &= mlo;
+        af[1] &= mlo;
+        af[2] &= mhi;
+        af[3] &= mhi;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816(o[mt][nt], af, bh[nt][0], bh[nt][1]);
+        mma16816(o[mt][nt], af, bl[nt][0], bl[nt][1]);
+      }
+    }
+  } else {
+    const unsigned short* vsc = reinterpret_cast<const unsigned short*>(sp + C::OFF_VS);
+    const unsigned char* vt = sp + C::OFF_V;
+#pragma unroll
+    for (int gv = 0; gv < C::NG; ++gv) {
+      // p = 0 exactly for masked cells, whose scale bits may be anything
+      // (even inf / NaN): clamping keeps 0 * s == 0.  Finite fp16
+      // scales are below 65504 and pass unchanged.
+      const float s0 = fminf(__half2float(__ushort_as_half(vsc[(cl + g) * C::NG + gv])), 65504.f);
+      const float s8 = fminf(__half2float(__ushort_as_half(vsc[(cl + g + 8) * C::NG + gv])), 65504.f);
+      uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float x0 = p[nt][0] * s0;
+        const float x1 = p[nt][1] * s0;
+        const float x2 = p[nt][2] * s8;
+        const float x3 = p[nt][3] * s8;
+        uint32_t h01, l01, h23, l23;
+        split_pair(x0, x1, h01, l01);
+        split_pair(x2, x3, h23, l23);
+        bh[nt][0] = movmatrix_t(h01);
+        bh[nt][1] = movmatrix_t(h23);
+        bl[nt][0] = movmatrix_t(l01);
+        bl[nt][1] = movmatrix_t(l23);
+      }
+      // two 32-dim chunks per 64-dim group; m-tile 2jj row g <-> dim
+      // 32jj + 4g, row g+8 <-> +1; m-tile 2jj+1 rows <-> +2, +3.
+#pragma unroll
+      for (int jh = 0; jh < 2; ++jh) {
+        const int jj = gv * 2 + jh;
+        const int db = 32 * jj + 4 * g;
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t, db)) ^ 0x80808080u;
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 1, db)) ^ 0x80808080u;
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 8, db)) ^ 0x80808080u;
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 9, db)) ^ 0x80808080u;
+        const uint32_t ab01 = prmt(wa, wb, 0x5140u), ab23 = prmt(wa, wb, 0x7362u);
+        const uint32_t cd01 = prmt(wc, wd, 0x5140u), cd23 = prmt(wc, wd, 0x7362u);
+        uint32_t a0[4], a1[4];
+        a0[0] = hsub2(prmt(ab01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t, 2t+1
+        a0[1] = hsub2(prmt(ab01, kMagic, 0x4342u), kBias);  // dim +1
+        a0[2] = hsub2(prmt(cd01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t+8, 2t+9
+        a0[3] = hsub2(prmt(cd01, kMagic, 0x4342u), kBias);  // dim +1
+        a1[0] = hsub2(prmt(ab23, kMagic, 0x4140u), kBias);  // dim +2
+        a1[1] = hsub2(prmt(ab23, kMagic, 0x4342u), kBias);  // dim +3
+        a1[2] = hsub2(prmt(cd23, kMagic, 0x4140u), kBias);
+        a1[3] = hsub2(prmt(cd23, kMagic, 0x4342u), kBias);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816(o[2 * jj][nt], a0, bh[nt][0], bh[nt][1]);
+          mma16816(o[2 * jj][nt], a0, bl[nt][0], bl[nt][1]);
+          mma16816(o[2 * jj + 1][nt], a1, bh[nt][0], bh[nt][1]);
+          mma16816(o[2 * jj + 1][nt], a1, bl[nt][0], bl[nt][1]);
+        }
+      }
+    }
+  }
+  };
+
+  auto release = [&](int it) {
+    // the last warp to let the stage go issues its refill
+    __syncwarp();
+    if (lane == 0) {
+      const int s = it % C::STAGES;
+      __threadfence_block();  // this warp's reads of the stage come first
+      const int prev = atomicAdd(s_rel + s, 1);
+      if (prev == kConsumerWarps - 1) {
+        s_rel[s] = 0;
+        __threadfence_block();
+        if (it + C::STAGES < n_tiles) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(it + C::STAGES, blk_in_smem);
+        }
+      }
+    }
+  };
+
+  // Software pipeline: q.k of tile it+1 is issued next to p.v of tile it
+  // (independent work the scheduler can interleave); the softmax of tile
+  // it+1 follows p.v of tile it because it may rescale o.
+  int blk_n = slice_blk(0);
+  int nv_cur = 0;
+  float p_cur[NT][4];
+  if (n_tiles > 0) {
+    if (!mbar_wait(bar_full, 0)) {
+      lost = true;
+    } else {
+      nv_cur = slice_nvalid(0, blk_n);
+      blk_n = slice_blk(1);
+      if (nv_cur > 0) {
+        float z[NT][4];
+        qk(0, z);
+        softmax(nv_cur, c_begin + cl, z, p_cur);
+      }
+    }
+  }
+  for (int it = 0; it < n_tiles && !lost; ++it) {
+    const int s = it % C::STAGES;
+    float zn[NT][4];
+    int nv_next = 0;
+    const bool more = it + 1 < n_tiles;
+    if (more) {
+      const int sn = (it + 1) % C::STAGES;
+      if (!mbar_wait(bar_full + 8 * sn, ((it + 1) / C::STAGES) & 1)) {
+        lost = true;
+      } else {
+        nv_next = slice_nvalid(it + 1, blk_n);
+        blk_n = slice_blk(it + 2);
+        if (nv_next > 0) qk(sn, zn);
+      }
+    }
+    if (nv_cur > 0) pv(s, nv_cur, p_cur);
+    release(it);
+    if (lost) break;
+    if (more && nv_next > 0) softmax(nv_next, c_begin + (it + 1) * kTC + cl, zn, p_cur);
+    nv_cur = nv_next;
+  }
   if (producer) {
-    // Every copy this CTA issued has landed before the CTA can exit.
-    for (int it = issued > C::STAGES ? issued - C::STAGES : 0; it < issued; ++it)
+    // Every copy this CTA issued has landed before the CTA can exit (waits
+    // return at once in normal runs; they are bounded after a lost wait).
+    for (int it = n_tiles > C::STAGES ? n_tiles - C::STAGES : 0; it < n_tiles; ++it)
       (void)mbar_wait(bar_full + 8 * (it % C::STAGES), (it / C::STAGES) & 1);
   }
 
@@ -719,29 +807,29 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * RP + r]);
       wgt[nt][j] = (M == kNegInf || m[nt][j] == kNegInf) ? 0.f : fast_exp2(m[nt][j] - M);
     }
+  // every warp writes its weighted rows to a slab of its own; one barrier;
+  // the slabs are summed in parallel into s_o
+  float* s_slab = s_o + RP * HD + 4;  // [4][RP][HD] after s_o and the flags
 #pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) {
-    if (warp == w) {
+  for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int j = k & 1;
-            const int r = nt * 8 + 2 * t + j;
-            int d;
-            if constexpr (FMT == KVQ_F16) {
-              d = mt * 16 + g + ((k >> 1) << 3);
-            } else {
-              d = 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) + (k >> 1);
-            }
-            const float v = wgt[nt][j] * o[mt][nt][k];
-            s_o[r * HD + d] = (w == 0) ? v : s_o[r * HD + d] + v;
-          }
-    }
-    __syncthreads();
-  }
+      for (int k = 0; k < 4; ++k) {
+        const int j = k & 1;
+        const int r = nt * 8 + 2 * t + j;
+        int d;
+        if constexpr (FMT == KVQ_F16) {
+          d = mt * 16 + g + ((k >> 1) << 3);
+        } else {
+          d = 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) + (k >> 1);
+        }
+        s_slab[(warp * RP + r) * HD + d] = wgt[nt][j] * o[mt][nt][k];
+      }
+  __syncthreads();
+  for (int i = threadIdx.x; i < RP * HD; i += kThreads)
+    s_o[i] = (s_slab[i] + s_slab[RP * HD + i]) + (s_slab[2 * RP * HD + i] + s_slab[3 * RP * HD + i]);
+  __syncthreads();
 
   // CTA-level partial: per row the CTA maximum and sum (in shared memory
   // next to the CTA's weighted o rows), read by the cluster leader.
@@ -835,25 +923,46 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 // on griddepcontrol until every partial is written.
 // ---------------------------------------------------------------------------
 template <int HD>
-__global__ void __launch_bounds__(128) combine_clusters(DecodeArgs a, int cl) {
+__global__ void __launch_bounds__(256) combine_clusters(DecodeArgs a, int cl) {
+  // One CTA per (KV head, sequence, row).  Thread (js, d4) owns dims
+  // [4 d4, 4 d4 + 4) of the partials j = js, js + JS, ...; all its partial
+  // loads are issued before any is used, while warp 0 forms the row's
+  // maximum and sum over every partial.  One round trip to L2 in total.
+  constexpr int TPR = HD / 4;        // threads per row vector
+  constexpr int JS = 256 / TPR;      // split slices
+  constexpr int MAXJ = 8;            // partials held in registers per thread
   constexpr float kNegInf = -INFINITY;
-  constexpr int D4 = HD / 4;
-  __shared__ float s_M[32], s_inv[32];
-  __shared__ int s_nan[32];
+  __shared__ float s_M, s_inv;
+  __shared__ int s_bad;
+  __shared__ float4 s_acc[JS][TPR];
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int kvh = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int kvh = blockIdx.x, b = blockIdx.y, r = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int js = tid / TPR, d4 = (tid % TPR) * 4;
   const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
   const int ns = (L + a.split_cells - 1) / a.split_cells;  // non-empty splits
   const int nlive = (ns + cl - 1) / cl;                      // clusters holding them
   const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.ncl;
-  for (int r = warp; r < a.R; r += 4) {
+
+  float4 oj[MAXJ];
+  float mj[MAXJ];
+#pragma unroll
+  for (int u = 0; u < MAXJ; ++u) {
+    const int j = js + u * JS;
+    if (j < nlive) {
+      const size_t rj = (base0 + j) * a.R + r;
+      oj[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + rj * HD + d4));
+      mj[u] = __ldcg(a.ws_ml + rj * 2);
+    }
+  }
+  if (tid < 32) {
     float mx = kNegInf;
     int bad = 0;
     for (int j = lane; j < nlive; j += 32) {
-      const float mj = __ldcg(a.ws_ml + ((base0 + j) * a.R + r) * 2);
-      bad |= mj != mj;
-      mx = fmaxf(mx, mj);
+      const float m = __ldcg(a.ws_ml + ((base0 + j) * a.R + r) * 2);
+      bad |= m != m;
+      mx = fmaxf(mx, m);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
@@ -863,55 +972,63 @@ __global__ void __launch_bounds__(128) combine_clusters(DecodeArgs a, int cl) {
     float lsum = 0.f;
     for (int j = lane; j < nlive; j += 32) {
       const size_t rj = (base0 + j) * a.R + r;
-      const float mj = __ldcg(a.ws_ml + rj * 2);
-      if (mx != kNegInf && mj != kNegInf) lsum = fmaf(__ldcg(a.ws_ml + rj * 2 + 1), fast_exp2(mj - mx), lsum);
+      const float m = __ldcg(a.ws_ml + rj * 2);
+      if (mx != kNegInf && m != kNegInf) lsum = fmaf(__ldcg(a.ws_ml + rj * 2 + 1), fast_exp2(m - mx), lsum);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
     if (lane == 0) {
-      s_M[r] = mx;
-      s_inv[r] = (mx != kNegInf && lsum > 0.f) ? 1.f / lsum : 0.f;
-      s_nan[r] = bad;
+      s_M = mx;
+      s_inv = (mx != kNegInf && lsum > 0.f) ? 1.f / lsum : 0.f;
+      s_bad = bad;
     }
   }
   __syncthreads();
-  constexpr int BATCH = 8;  // partial loads in flight per thread
-  for (int i = tid; i < a.R * D4; i += 128) {
-    const int r = i / D4, d4 = (i - r * D4) * 4;
-    const float Mr = s_M[r], inv = s_inv[r];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (inv != 0.f) {
-      for (int j0 = 0; j0 < nlive; j0 += BATCH) {
-        float4 oj[BATCH];
-        float mj[BATCH];
+  const float M = s_M;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (s_inv != 0.f) {
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-          if (j0 + u < nlive) {
-            const size_t rj = (base0 + j0 + u) * a.R + r;
-            oj[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + rj * HD + d4));
-            mj[u] = __ldcg(a.ws_ml + rj * 2);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-          if (j0 + u < nlive) {
-            const float wj = mj[u] == kNegInf ? 0.f : fast_exp2(mj[u] - Mr);
-            acc.x = fmaf(wj, oj[u].x, acc.x);
-            acc.y = fmaf(wj, oj[u].y, acc.y);
-            acc.z = fmaf(wj, oj[u].z, acc.z);
-            acc.w = fmaf(wj, oj[u].w, acc.w);
-          }
-        }
+    for (int u = 0; u < MAXJ; ++u) {
+      if (js + u * JS < nlive && mj[u] != kNegInf) {
+        const float w = fast_exp2(mj[u] - M);
+        acc.x = fmaf(w, oj[u].x, acc.x);
+        acc.y = fmaf(w, oj[u].y, acc.y);
+        acc.z = fmaf(w, oj[u].z, acc.z);
+        acc.w = fmaf(w, oj[u].w, acc.w);
       }
     }
-    const int w = r / a.G, gg = r - w * a.G;
-    float* dst = a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + d4;
-    float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (s_nan[r]) {
+    for (int j = js + MAXJ * JS; j < nlive; j += JS) {  // more partials than registers
+      const size_t rj = (base0 + j) * a.R + r;
+      const float m = __ldcg(a.ws_ml + rj * 2);
+      if (m == kNegInf) continue;
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(a.ws_o + rj * HD + d4));
+      const float w = fast_exp2(m - M);
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
+  }
+  s_acc[js][tid % TPR] = acc;
+  __syncthreads();
+  if (js == 0) {
+    float4 sum = s_acc[0][tid];
+#pragma unroll
+    for (int q = 1; q < JS; ++q) {
+      const float4 v = s_acc[q][tid];
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
+    const float inv = s_inv;
+    float4 res = make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
+    if (s_bad) {
       const float nan = __int_as_float(0x7fc00000);
       res = make_float4(nan, nan, nan, nan);
     }
-    *reinterpret_cast<float4*>(dst) = res;   // rows of an empty sequence come out 0
+    const int w = r / a.G, gg = r - w * a.G;
+    *reinterpret_cast<float4*>(a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + d4) = res;
   }
 }
 
@@ -995,18 +1112,20 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma<FMT, HD, NT>, maps, a);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cc = {};
-  cc.gridDim = dim3(a.pool.n_kv, a.n_seq, 1);
-  cc.blockDim = dim3(128);
+  cc.gridDim = dim3(a.pool.n_kv, a.n_seq, a.R);
+  cc.blockDim = dim3(256);
   cc.stream = s;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
