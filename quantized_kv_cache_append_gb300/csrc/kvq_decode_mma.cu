@@ -33,6 +33,7 @@
 // exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -62,8 +63,10 @@ struct Cfg {
   static constexpr int NG = HD / kGroup;
   static constexpr int TILE_B = kTC * ROWB;              // K (or V) codes of a stage
   static constexpr int SCALE_B = FMT == KVQ_Q8 ? kTC * NG * 2 : 0;
-  static constexpr int STAGE_RAW = 2 * TILE_B + 2 * SCALE_B;
-  static constexpr int STAGE_B = (STAGE_RAW + 1023) / 1024 * 1024;
+  // A stage holds the K and V code tiles (each a whole number of 1 KB
+  // swizzle atoms); the int8 scales of all stages live in a region of their
+  // own so no stage is padded.
+  static constexpr int STAGE_B = 2 * TILE_B;
   // Stages per CTA and CTAs per SM: keep about 100 KB or more of copies in
   // flight per SM while fitting as many 4-warp CTAs as the 227 KB allow.
   // merge buffers reuse the stages after the loop: 20 row values x 32 rows,
@@ -73,19 +76,19 @@ struct Cfg {
   // merge buffers need the room
   static constexpr int STAGES = (MERGE_B + STAGE_B - 1) / STAGE_B > 3 ? (MERGE_B + STAGE_B - 1) / STAGE_B : 3;
   static constexpr int OFF_V = TILE_B;
-  static constexpr int OFF_KS = 2 * TILE_B;
-  static constexpr int OFF_VS = 2 * TILE_B + SCALE_B;
+  static constexpr int SMEM_SC = STAGES * STAGE_B;           // [STAGES][K, V][64 cells][NG] fp16
   // q as fp16 hi / lo rows, padded by 16 bytes so ldmatrix rows hit distinct banks
   static constexpr int QROW = HD * 2 + 16;
   static constexpr int QBYTES_MAX = 2 * NT * 8 * QROW;   // hi and lo, NT*8 padded rows
-  static constexpr int SMEM_Q = STAGES * STAGE_B;
+  static constexpr int SMEM_Q = SMEM_SC + STAGES * 2 * SCALE_B;
   static constexpr int SMEM_BAR = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
   // block ids of the split's pieces, staged once so any warp can issue a refill
-  static constexpr int ROWS_CAP = 512;
+  static constexpr int ROWS_CAP = 256;
   static constexpr int SMEM_REL = SMEM_BAR + STAGES * 8;        // release counters [STAGES]
   static constexpr int SMEM_BLK = SMEM_REL + 16 * 4;            // block ids [ROWS_CAP]
   static constexpr int SMEM = SMEM_BLK + ROWS_CAP * 4 + 1024 /*align*/;
-  static constexpr int MIN_CTAS = (227 * 1024) / SMEM >= 3 ? 3 : ((227 * 1024) / SMEM >= 2 ? 2 : 1);
+  static constexpr int FIT = (227 * 1024) / SMEM;
+  static constexpr int MIN_CTAS = FIT >= 4 ? 4 : (FIT >= 3 ? 3 : (FIT >= 2 ? 2 : 1));
   static_assert(STAGES * STAGE_B >= MERGE_B, "merge buffers fit");
 };
 
@@ -384,8 +387,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       if constexpr (FMT == KVQ_Q8) {
         const uint32_t sb = (uint32_t)pc * C::NG * 2;
         const uint32_t soff = (uint32_t)p * sb;
-        bulk_load(st + C::OFF_KS + soff, a.pool.ks + (size_t)row * C::NG, sb, full);
-        bulk_load(st + C::OFF_VS + soff, a.pool.vs + (size_t)row * C::NG, sb, full);
+        const uint32_t sc = sbase + C::SMEM_SC + (uint32_t)s * 2 * C::SCALE_B;
+        bulk_load(sc + soff, a.pool.ks + (size_t)row * C::NG, sb, full);
+        bulk_load(sc + C::SCALE_B + soff, a.pool.vs + (size_t)row * C::NG, sb, full);
       }
     }
   };
@@ -479,6 +483,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       row_last[nt][j] = r < a.R ? L - a.W + r / a.G : -1;
     }
 
+  int row_last_min = INT_MAX;  // smallest causal limit among this thread's real rows
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (nt * 8 + 2 * t + j < a.R) row_last_min = min(row_last_min, row_last[nt][j]);
+
   float m[NT][2], l[NT][2];
   float o[KS][NT][4];
 #pragma unroll
@@ -491,11 +502,43 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 
   const int cl = warp * kCellsPerWarp;  // first cell of this warp's slice in a stage
   auto slice_blk = [&](int it) -> int {
-    return it < n_tiles ? block_of(a, bt, c_begin + it * kTC + cl, c_end) : -1;
+    if (it >= n_tiles) return -1;
+    if (blk_in_smem) return c_begin + it * kTC + cl < c_end ? s_blk[it * n_pieces + (cl >> pc_log2)] : -1;
+    return block_of(a, bt, c_begin + it * kTC + cl, c_end);
   };
   auto slice_nvalid = [&](int it, int blk) -> int {
     return (blk >= 0 && blk < a.pool.n_blocks) ? min(kCellsPerWarp, c_end - (c_begin + it * kTC + cl)) : 0;
   };
+
+  // Swizzled shared-memory addresses.  With a 128-byte swizzle the XOR term
+  // of every address this thread reads splits into a per-thread constant and
+  // a compile-time part, so a few base registers replace the full
+  // computation per load (the spans of a row are whole 64-cell x 128-byte
+  // blocks, reached by immediate offsets).
+  constexpr uint32_t kSpanB = kTC * 128;
+  uint32_t kx[4], vx[4];   // FP16 ldmatrix bases (K, V^T)
+  uint32_t kq[2], vq[2][4];  // int8 bases (K words, V words)
+  {
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t ck = (uint32_t)(cl + ((mi & 1) << 3) + rr), cv = (uint32_t)(cl + ((mi >> 1) << 3) + rr);
+    const uint32_t xk = ((uint32_t)(mi >> 1) << 4) ^ ((uint32_t)rr << 4);
+    const uint32_t xv = ((uint32_t)(mi & 1) << 4) ^ ((uint32_t)rr << 4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      kx[k] = ck * 128 + (xk ^ (32u * k));
+      vx[k] = C::OFF_V + cv * 128 + (xv ^ (32u * k));
+    }
+    const uint32_t yk = (16u * t) ^ ((uint32_t)g << 4);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) kq[k] = (uint32_t)(cl + g) * 128 + (yk ^ (64u * k));
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t c = (uint32_t)(cl + 2 * t + e);
+      const uint32_t w = (4u * g) ^ ((c & 7u) << 4);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vq[e][k] = C::OFF_V + c * 128 + (w ^ (32u * k));
+    }
+  }
 
   // q . k of one stage for this warp's 16 cells -> z (log2-domain logits)
   auto qk = [&](int s, float (&z)[NT][4]) {
@@ -509,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t af[4];
-      ldsm_x4(af, st + tile_off<FMT, HD>(cell, (ks * 16 + ((mi >> 1) << 3)) * 2));
+      ldsm_x4(af, st + kx[ks & 3] + (uint32_t)(ks >> 2) * kSpanB);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         uint32_t qf[4];
@@ -531,11 +574,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   } else {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) z[nt][0] = z[nt][1] = z[nt][2] = z[nt][3] = 0.f;
-    const unsigned short* ksc = reinterpret_cast<const unsigned short*>(sp + C::OFF_KS);
+    const unsigned short* ksc = reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * 2 * C::SCALE_B);
 #pragma unroll
     for (int gq = 0; gq < C::NG; ++gq) {
-      const uint4 k0 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g, gq * 64 + 16 * t));
-      const uint4 k8 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g + 8, gq * 64 + 16 * t));
+      uint4 k0, k8;
+      if constexpr (C::SWB == 128) {
+        const unsigned char* kp = sp + kq[gq & 1] + (gq >> 1) * kSpanB;
+        k0 = *reinterpret_cast<const uint4*>(kp);
+        k8 = *reinterpret_cast<const uint4*>(kp + 8 * 128);  // cell g + 8: same swizzle
+      } else {
+        k0 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g, gq * 64 + 16 * t));
+        k8 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g + 8, gq * 64 + 16 * t));
+      }
       const uint32_t w0[4] = {k0.x ^ 0x80808080u, k0.y ^ 0x80808080u, k0.z ^ 0x80808080u,
                               k0.w ^ 0x80808080u};
       const uint32_t w8[4] = {k8.x ^ 0x80808080u, k8.y ^ 0x80808080u, k8.z ^ 0x80808080u,
@@ -575,14 +625,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 
   // causal / length masks, online softmax -> p (rescales o when the maximum rises)
   auto softmax = [&](int nvalid, int cw0, float (&z)[NT][4], float (&p)[NT][4]) {
+    // padding rows never reach the output, so only a short slice or a causal
+    // limit inside it needs masks
+    const bool need_mask = nvalid < kCellsPerWarp || row_last_min - cw0 < kCellsPerWarp - 1;
   // ---------------- masks and online softmax ----------------
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int vis = min(nvalid - 1, row_last[nt][j] - cw0);  // last visible slice index
-      if (g > vis) z[nt][j] = kNegInf;
-      if (g + 8 > vis) z[nt][2 + j] = kNegInf;
+      if (need_mask) {
+        const int vis = min(nvalid - 1, row_last[nt][j] - cw0);  // last visible slice index
+        if (g > vis) z[nt][j] = kNegInf;
+        if (g + 8 > vis) z[nt][2 + j] = kNegInf;
+      }
       float tmax = fmaxf(z[nt][j], z[nt][2 + j]);
       tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
       tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
@@ -632,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       uint32_t af[4];
-      ldsm_x4_t(af, st + C::OFF_V + tile_off<FMT, HD>(cell, (mt * 16 + ((mi & 1) << 3)) * 2));
+      ldsm_x4_t(af, st + vx[mt & 3] + (uint32_t)(mt >> 2) * kSpanB);
       if (nvalid < kCellsPerWarp) {
         af[0] &= mlo;
         af[1] &= mlo;
@@ -646,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       }
     }
   } else {
-    const unsigned short* vsc = reinterpret_cast<const unsigned short*>(sp + C::OFF_VS);
+    const unsigned short* vsc =
+        reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * 2 * C::SCALE_B + C::SCALE_B);
     const unsigned char* vt = sp + C::OFF_V;
 #pragma unroll
     for (int gv = 0; gv < C::NG; ++gv) {
@@ -676,10 +732,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       for (int jh = 0; jh < 2; ++jh) {
         const int jj = gv * 2 + jh;
         const int db = 32 * jj + 4 * g;
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t, db)) ^ 0x80808080u;
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 1, db)) ^ 0x80808080u;
-        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 8, db)) ^ 0x80808080u;
-        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 9, db)) ^ 0x80808080u;
+        uint32_t wa, wb, wc, wd;
+        if constexpr (C::SWB == 128) {
+          const unsigned char* v0 = sp + vq[0][jj & 3] + (jj >> 2) * kSpanB;
+          const unsigned char* v1 = sp + vq[1][jj & 3] + (jj >> 2) * kSpanB;
+          wa = *reinterpret_cast<const uint32_t*>(v0) ^ 0x80808080u;
+          wb = *reinterpret_cast<const uint32_t*>(v1) ^ 0x80808080u;
+          wc = *reinterpret_cast<const uint32_t*>(v0 + 8 * 128) ^ 0x80808080u;  // cells +8
+          wd = *reinterpret_cast<const uint32_t*>(v1 + 8 * 128) ^ 0x80808080u;
+        } else {
+          wa = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t, db)) ^ 0x80808080u;
+          wb = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 1, db)) ^ 0x80808080u;
+          wc = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 8, db)) ^ 0x80808080u;
+          wd = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 9, db)) ^ 0x80808080u;
+        }
         const uint32_t ab01 = prmt(wa, wb, 0x5140u), ab23 = prmt(wa, wb, 0x7362u);
         const uint32_t cd01 = prmt(wc, wd, 0x5140u), cd23 = prmt(wc, wd, 0x7362u);
         uint32_t a0[4], a1[4];
@@ -708,11 +774,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     __syncwarp();
     if (lane == 0) {
       const int s = it % C::STAGES;
-      __threadfence_block();  // this warp's reads of the stage come first
-      const int prev = atomicAdd(s_rel + s, 1);
+      // acquire-release: this warp's reads of the stage happen before the
+      // count moves, and the last warp sees every other warp's reads done
+      int prev;
+      asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "r"(smem_u32(s_rel + s))
+                   : "memory");
       if (prev == kConsumerWarps - 1) {
         s_rel[s] = 0;
-        __threadfence_block();
         if (it + C::STAGES < n_tiles) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           issue(it + C::STAGES, blk_in_smem);
