@@ -336,19 +336,27 @@ def run_kvq(args):
     return result
 
 
+def _decode_sources_sha() -> str:
+    """sha256[:16] over the decode kernel sources (the SIMT and tensor-core
+    partial kernels and the combine)."""
+    h = hashlib.sha256()
+    for f in ("kvq_decode.cu", "kvq_decode_mma.cu"):
+        h.update(open(os.path.join(ROOT, "quantized_kv_cache_append_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
 def _ncu_traffic(fmt: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current decode kernel source (else null)."""
-    path = os.path.join(ROOT, "profiles", "decode_gqa32k_traffic.txt")
-    src = os.path.join(ROOT, "quantized_kv_cache_append_gb300", "csrc", "kvq_decode.cu")
+    """DRAM bytes per launch of the decode kernels from the committed ncu
+    summary, if it was taken on the current decode sources (else null)."""
+    path = os.path.join(ROOT, "profiles", "decode_mma_gqa32k_traffic.txt")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         fields = {}
         for ln in open(path):
-            if ":" in ln:
+            if ":" in ln and not ln.startswith("#"):
                 k, v = ln.split(":", 1)
                 fields[k.strip()] = v.strip()
-        if fields.get("decode_source_sha256_16") != sha:
+        if fields.get("decode_sources_sha256_16") != _decode_sources_sha():
             return None
         return int(float(fields[f"traffic_bytes_per_launch_{fmt}"]))
     except Exception:
