@@ -169,6 +169,30 @@ def test_degenerate_quantization_groups():
         p.assert_cache_equal()
 
 
+def test_quantization_ties_and_near_ties():
+    # Groups whose maximum is exactly 127 s (s an fp16 value, so the stored
+    # scale is s itself) and whose other elements are (k + 1/2) s exactly or
+    # 1-3 fp32 ulps away: x / s is an exact half-integer (round half to even)
+    # or so close to one that only the IEEE quotient decides.
+    rng = np.random.default_rng(11)
+    n, n_kv, hd = 96, 2, 128
+    s = rng.uniform(2.0 ** -10, 16.0, size=(n, n_kv, hd // 64)).astype(np.float16)
+    s = s.astype(np.float32)
+    half = rng.integers(-127, 127, size=(n, n_kv, hd)).astype(np.float32) + np.float32(0.5)
+    x = (half * np.repeat(s, 64, axis=-1)).astype(np.float32)
+    steps = rng.integers(-3, 4, size=x.shape)
+    for k in (1, 2, 3):
+        up, dn = steps >= k, steps <= -k
+        x[up] = np.nextafter(x[up], np.float32(np.inf))
+        x[dn] = np.nextafter(x[dn], np.float32(-np.inf))
+    x[..., ::64] = (np.float32(127.0) * s).astype(np.float32)   # the group maxima
+    v = -x[::-1].copy()
+    table = np.arange(6, dtype=np.int32)[None]
+    p = Pair("q8", n_kv, hd, 16, 6, table)
+    p.append(x, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32))
+    p.assert_cache_equal()
+
+
 def test_paged_equals_contiguous_bitwise():
     lens = [700, 1500]
     for fmt in ("f16", "q8"):
