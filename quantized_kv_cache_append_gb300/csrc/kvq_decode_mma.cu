@@ -81,7 +81,10 @@ struct Cfg {
   static constexpr int QROW = HD * 2 + 16;
   static constexpr int QBYTES_MAX = 2 * NT * 8 * QROW;   // hi and lo, NT*8 padded rows
   static constexpr int SMEM_Q = SMEM_SC + STAGES * 2 * SCALE_B;
-  static constexpr int SMEM_BAR = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
+  // int8: per (padded row, 64-dim group) 1152 * sum of q (hi + lo), fp32
+  static constexpr int SMEM_QC = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
+  static constexpr int QC_BYTES = FMT == KVQ_Q8 ? (NT * 8 * NG * 4 + 15) / 16 * 16 : 0;
+  static constexpr int SMEM_BAR = SMEM_QC + QC_BYTES;
   // block ids of the split's pieces, staged once so any warp can issue a refill
   static constexpr int ROWS_CAP = 256;
   static constexpr int SMEM_REL = SMEM_BAR + STAGES * 8;        // release counters [STAGES]
@@ -401,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   //
   // q * sm_scale * log2(e) goes to shared memory as fp16 hi + lo, rows
   // [RP][HD] in k order: FP16 uses the natural dim order; int8 permutes each
-  // 16-wide k-step so that k = 2t + e -> dim 64 gq + 16 t + 4 kk + e and
-  // k = 2t + 8 + e -> that + 2 (t = k-pair lane, kk = k-step inside the
-  // 64-dim group gq), the order in which a lane widens its 4-byte code words.
+  // 16-wide k-step ks so that k = 2t + e -> dim 16 ks + 4 t + e and
+  // k = 2t + 8 + e -> that + 2 (t = k-pair lane): a lane's ldmatrix word
+  // holds the 4 code bytes of dims 16 ks + 4t .. + 3.
   constexpr int QPT = (RP * HD + kThreads - 1) / kThreads;  // q values per thread
   constexpr int BPT = (C::ROWS_CAP + kThreads - 1) / kThreads;
   float qv[QPT];
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       if constexpr (FMT == KVQ_Q8) {
         const int ks = k >> 4, kq = k & 15;
         const int tt = (kq & 7) >> 1, e = kq & 1, hi8 = kq >> 3;
-        dim = (ks >> 2) * 64 + 16 * tt + 4 * (ks & 3) + 2 * hi8 + e;
+        dim = 16 * ks + 4 * tt + 2 * hi8 + e;
       }
       if (r < a.R) {
         const int w = r / a.G, gg = r - w * a.G;
@@ -467,6 +470,32 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // ---------------- consumer setup ----------------
   const int g = lane >> 2, t = lane & 3;
 
+  // int8 K enters the MMA as fp16 (1152 + code) (no subtraction per
+  // element); the 1152 * sum(q) of each (row, 64-dim group) is taken off
+  // once, as the starting value of that group's hi accumulator.
+  float qcorr[C::NG > 0 ? (FMT == KVQ_Q8 ? C::NG : 1) : 1][NT][2];
+  if constexpr (FMT == KVQ_Q8) {
+    float* s_qc = reinterpret_cast<float*>(smem + C::SMEM_QC);
+    const unsigned char* qs = smem + C::SMEM_Q;
+    for (int pr = warp; pr < RP * C::NG; pr += kConsumerWarps) {
+      const int r = pr / C::NG, gq = pr - r * C::NG;
+      const int k = gq * 64 + 2 * lane;
+      const __half2 h = *reinterpret_cast<const __half2*>(qs + r * C::QROW + k * 2);
+      const __half2 lo = *reinterpret_cast<const __half2*>(qs + (RP + r) * C::QROW + k * 2);
+      float v = (__low2float(h) + __high2float(h)) + (__low2float(lo) + __high2float(lo));
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      if (lane == 0) s_qc[pr] = 1152.0f * v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int gq = 0; gq < C::NG; ++gq)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) qcorr[gq][nt][j] = -s_qc[(nt * 8 + 2 * t + j) * C::NG + gq];
+  }
+
   // ldmatrix lane addressing of q: matrix lane>>3 = {hi k0-7, hi k8-15, lo
   // k0-7, lo k8-15}, row lane&7.
   const uint32_t q_lane = qbase + (uint32_t)((lane >> 4) * RP + (lane & 7)) * C::QROW +
@@ -515,30 +544,38 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // a compile-time part, so a few base registers replace the full
   // computation per load (the spans of a row are whole 64-cell x 128-byte
   // blocks, reached by immediate offsets).
+  //
+  // ldmatrix x4 lane addressing: matrix mi = lane >> 3 reads row rr = lane & 7.
+  // kx: matrices (cells +0, chunk 2k), (cells +8, chunk 2k), (cells +0,
+  // chunk 2k+1), (cells +8, chunk 2k+1) of the k-th 32-byte step of a row --
+  // K for q.k in both formats and, as byte pairs, int8 V for p.v.  vx (FP16
+  // V^T): (cells +0, chunk 2k), (+0, 2k+1), (+8, 2k), (+8, 2k+1).
   constexpr uint32_t kSpanB = kTC * 128;
-  uint32_t kx[4], vx[4];   // FP16 ldmatrix bases (K, V^T)
-  uint32_t kq[2], vq[2][4];  // int8 bases (K words, V words)
+  uint32_t kx[4], vx[4];
   {
     const int mi = lane >> 3, rr = lane & 7;
     const uint32_t ck = (uint32_t)(cl + ((mi & 1) << 3) + rr), cv = (uint32_t)(cl + ((mi >> 1) << 3) + rr);
-    const uint32_t xk = ((uint32_t)(mi >> 1) << 4) ^ ((uint32_t)rr << 4);
-    const uint32_t xv = ((uint32_t)(mi & 1) << 4) ^ ((uint32_t)rr << 4);
+    if constexpr (C::SWB == 128) {
+      const uint32_t xk = ((uint32_t)(mi >> 1) << 4) ^ ((uint32_t)rr << 4);
+      const uint32_t xv = ((uint32_t)(mi & 1) << 4) ^ ((uint32_t)rr << 4);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      kx[k] = ck * 128 + (xk ^ (32u * k));
-      vx[k] = C::OFF_V + cv * 128 + (xv ^ (32u * k));
-    }
-    const uint32_t yk = (16u * t) ^ ((uint32_t)g << 4);
+      for (int k = 0; k < 4; ++k) {
+        kx[k] = ck * 128 + (xk ^ (32u * k));
+        vx[k] = C::OFF_V + cv * 128 + (xv ^ (32u * k));
+      }
+    } else {  // 64-byte rows (int8, HD 64): two 32-byte steps
 #pragma unroll
-    for (int k = 0; k < 2; ++k) kq[k] = (uint32_t)(cl + g) * 128 + (yk ^ (64u * k));
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const uint32_t c = (uint32_t)(cl + 2 * t + e);
-      const uint32_t w = (4u * g) ^ ((c & 7u) << 4);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) vq[e][k] = C::OFF_V + c * 128 + (w ^ (32u * k));
+      for (int k = 0; k < 4; ++k) {
+        kx[k] = tile_off<FMT, HD>((int)ck, (32 * k + 16 * (mi >> 1)) & (C::ROWB - 1));
+        vx[k] = 0;
+      }
     }
   }
+  // shared-memory offset of the k-th 32-byte step of the kx row set
+  auto kstep = [&](int k) -> uint32_t {
+    if constexpr (C::SWB == 128) return kx[k & 3] + (uint32_t)(k >> 2) * kSpanB;
+    else return kx[k & 1];
+  };
 
   // q . k of one stage for this warp's 16 cells -> z (log2-domain logits)
   auto qk = [&](int s, float (&z)[NT][4]) {
@@ -577,36 +614,38 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     const unsigned short* ksc = reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * 2 * C::SCALE_B);
 #pragma unroll
     for (int gq = 0; gq < C::NG; ++gq) {
-      uint4 k0, k8;
-      if constexpr (C::SWB == 128) {
-        const unsigned char* kp = sp + kq[gq & 1] + (gq >> 1) * kSpanB;
-        k0 = *reinterpret_cast<const uint4*>(kp);
-        k8 = *reinterpret_cast<const uint4*>(kp + 8 * 128);  // cell g + 8: same swizzle
-      } else {
-        k0 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g, gq * 64 + 16 * t));
-        k8 = *reinterpret_cast<const uint4*>(sp + tile_off<FMT, HD>(cl + g + 8, gq * 64 + 16 * t));
+      // words: [k-step kk][cells +0 | +8], each the 4 code bytes of dims
+      // 16 (4 gq + kk) + 4t .. + 3 of cell g (or g + 8)
+      uint32_t w[4][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[4];
+        ldsm_x4(r, st + kstep(2 * gq + h));
+        w[2 * h][0] = r[0] ^ 0x80808080u;
+        w[2 * h][1] = r[1] ^ 0x80808080u;
+        w[2 * h + 1][0] = r[2] ^ 0x80808080u;
+        w[2 * h + 1][1] = r[3] ^ 0x80808080u;
       }
-      const uint32_t w0[4] = {k0.x ^ 0x80808080u, k0.y ^ 0x80808080u, k0.z ^ 0x80808080u,
-                              k0.w ^ 0x80808080u};
-      const uint32_t w8[4] = {k8.x ^ 0x80808080u, k8.y ^ 0x80808080u, k8.z ^ 0x80808080u,
-                              k8.w ^ 0x80808080u};
-      float acc[2][NT][4];  // hi chain, lo chain
+      float acc[2][NT][4];  // hi chain (starts at -1152 sum q), lo chain
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[0][nt][0] = acc[0][nt][2] = qcorr[gq][nt][0];
+        acc[0][nt][1] = acc[0][nt][3] = qcorr[gq][nt][1];
+      }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t af[4];
-        widen_same(w0[kk], af[0], af[2]);
-        widen_same(w8[kk], af[1], af[3]);
+        uint32_t af[4];  // fp16 1152 + code, exact
+        af[0] = prmt(w[kk][0], kMagic, 0x4140u);
+        af[2] = prmt(w[kk][0], kMagic, 0x4342u);
+        af[1] = prmt(w[kk][1], kMagic, 0x4140u);
+        af[3] = prmt(w[kk][1], kMagic, 0x4342u);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           uint32_t qf[4];
           ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + (gq * 4 + kk) * 32);
-          if (kk == 0) {
-            mma16816_zc(acc[0][nt], af, qf[0], qf[1]);
-            mma16816_zc(acc[1][nt], af, qf[2], qf[3]);
-          } else {
-            mma16816(acc[0][nt], af, qf[0], qf[1]);
-            mma16816(acc[1][nt], af, qf[2], qf[3]);
-          }
+          mma16816(acc[0][nt], af, qf[0], qf[1]);
+          if (kk == 0) mma16816_zc(acc[1][nt], af, qf[2], qf[3]);
+          else mma16816(acc[1][nt], af, qf[2], qf[3]);
         }
       }
       const float s0 = __half2float(__ushort_as_half(ksc[(cl + g) * C::NG + gq]));
@@ -703,7 +742,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   } else {
     const unsigned short* vsc =
         reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * 2 * C::SCALE_B + C::SCALE_B);
-    const unsigned char* vt = sp + C::OFF_V;
 #pragma unroll
     for (int gv = 0; gv < C::NG; ++gv) {
       // p = 0 exactly for masked cells, whose scale bits may be anything
@@ -726,43 +764,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         bl[nt][0] = movmatrix_t(l01);
         bl[nt][1] = movmatrix_t(l23);
       }
-      // two 32-dim chunks per 64-dim group; m-tile 2jj row g <-> dim
-      // 32jj + 4g, row g+8 <-> +1; m-tile 2jj+1 rows <-> +2, +3.
+      // Two ldmatrix.trans x4 per 64-dim group, on byte pairs: register
+      // i of chunk c holds (cell 2t, dims 16c + 2g, +1) and (cell 2t + 1,
+      // same dims) for cells +0 (i = 0) or +8 (i = 1), so m-tile c row g is
+      // dim 16c + 2g and row g + 8 is dim 16c + 2g + 1.
 #pragma unroll
       for (int jh = 0; jh < 2; ++jh) {
-        const int jj = gv * 2 + jh;
-        const int db = 32 * jj + 4 * g;
-        uint32_t wa, wb, wc, wd;
-        if constexpr (C::SWB == 128) {
-          const unsigned char* v0 = sp + vq[0][jj & 3] + (jj >> 2) * kSpanB;
-          const unsigned char* v1 = sp + vq[1][jj & 3] + (jj >> 2) * kSpanB;
-          wa = *reinterpret_cast<const uint32_t*>(v0) ^ 0x80808080u;
-          wb = *reinterpret_cast<const uint32_t*>(v1) ^ 0x80808080u;
-          wc = *reinterpret_cast<const uint32_t*>(v0 + 8 * 128) ^ 0x80808080u;  // cells +8
-          wd = *reinterpret_cast<const uint32_t*>(v1 + 8 * 128) ^ 0x80808080u;
-        } else {
-          wa = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t, db)) ^ 0x80808080u;
-          wb = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 1, db)) ^ 0x80808080u;
-          wc = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 8, db)) ^ 0x80808080u;
-          wd = *reinterpret_cast<const uint32_t*>(vt + tile_off<FMT, HD>(cl + 2 * t + 9, db)) ^ 0x80808080u;
-        }
-        const uint32_t ab01 = prmt(wa, wb, 0x5140u), ab23 = prmt(wa, wb, 0x7362u);
-        const uint32_t cd01 = prmt(wc, wd, 0x5140u), cd23 = prmt(wc, wd, 0x7362u);
-        uint32_t a0[4], a1[4];
-        a0[0] = hsub2(prmt(ab01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t, 2t+1
-        a0[1] = hsub2(prmt(ab01, kMagic, 0x4342u), kBias);  // dim +1
-        a0[2] = hsub2(prmt(cd01, kMagic, 0x4140u), kBias);  // dim +0, cells 2t+8, 2t+9
-        a0[3] = hsub2(prmt(cd01, kMagic, 0x4342u), kBias);  // dim +1
-        a1[0] = hsub2(prmt(ab23, kMagic, 0x4140u), kBias);  // dim +2
-        a1[1] = hsub2(prmt(ab23, kMagic, 0x4342u), kBias);  // dim +3
-        a1[2] = hsub2(prmt(cd23, kMagic, 0x4140u), kBias);
-        a1[3] = hsub2(prmt(cd23, kMagic, 0x4342u), kBias);
+        const int c0 = gv * 4 + jh * 2;  // first 16-dim chunk of this pair
+        uint32_t r[4];
+        ldsm_x4_t(r, st + C::OFF_V + kstep(c0 >> 1));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma16816(o[2 * jj][nt], a0, bh[nt][0], bh[nt][1]);
-          mma16816(o[2 * jj][nt], a0, bl[nt][0], bl[nt][1]);
-          mma16816(o[2 * jj + 1][nt], a1, bh[nt][0], bh[nt][1]);
-          mma16816(o[2 * jj + 1][nt], a1, bl[nt][0], bl[nt][1]);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t w0 = r[2 * h] ^ 0x80808080u, w8 = r[2 * h + 1] ^ 0x80808080u;
+          uint32_t af[4];
+          af[0] = hsub2(prmt(w0, kMagic, 0x4240u), kBias);  // dim 2g, cells 2t, 2t+1
+          af[1] = hsub2(prmt(w0, kMagic, 0x4341u), kBias);  // dim 2g+1
+          af[2] = hsub2(prmt(w8, kMagic, 0x4240u), kBias);  // dim 2g, cells 2t+8, 2t+9
+          af[3] = hsub2(prmt(w8, kMagic, 0x4341u), kBias);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(o[c0 + h][nt], af, bh[nt][0], bh[nt][1]);
+            mma16816(o[c0 + h][nt], af, bl[nt][0], bl[nt][1]);
+          }
         }
       }
     }
@@ -892,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         if constexpr (FMT == KVQ_F16) {
           d = mt * 16 + g + ((k >> 1) << 3);
         } else {
-          d = 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) + (k >> 1);
+          d = 16 * mt + 2 * g + (k >> 1);
         }
         s_slab[(warp * RP + r) * HD + d] = wgt[nt][j] * o[mt][nt][k];
       }
