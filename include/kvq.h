@@ -215,9 +215,10 @@ kvq_status kvq_compact_f16(const kvq_cache *cache, const int32_t *block_table_ro
  *
  * Arguments, results and errors are those of kvq_decode_attn.  The scratch
  * is a file-scope device array of KVQ_STATIC_SCRATCH_BYTES inside the
- * library; a request whose split plan needs more (what
- * kvq_decode_workspace_bytes reports) returns KVQ_ERR_WORKSPACE and
- * launches nothing.  The first call on a device looks up the array's
+ * library; when the split plan kvq_decode_workspace_bytes describes needs
+ * more, the context is cut into fewer splits until it fits, and a request
+ * that does not fit even with one split per (sequence, KV head) returns
+ * KVQ_ERR_WORKSPACE and launches nothing.  The first call on a device looks up the array's
  * address and caches it: make that first call before any stream capture.
  * Every call uses the same array, so calls whose kernels may overlap on
  * the GPU (unordered streams) race on it; order them.  The array needs no

@@ -71,8 +71,10 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // every SM; twice that for batches, whose ragged lengths leave CTAs short)
 // over all (sequence, KV head) pairs, each split a whole number of cell
 // tiles.  The tensor-core kernel takes the shapes it covers; the CUDA-core
-// kernel the rest.
-bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, DecodePlan* p) {
+// kernel the rest.  With max_bytes set, the split count is lowered until
+// the workspace fits (false if even one split per pair does not).
+bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, DecodePlan* p,
+                 size_t max_bytes = SIZE_MAX) {
   const int G = n_q / c->n_kv_heads;
   p->rows = G * W;
   p->rows_pad = decode_rows_pad(c->head_dim, p->rows);
@@ -84,46 +86,32 @@ bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, Dec
   }
   if (!p->use_mma) per_sm = 4;
   const int tile = p->use_mma ? mma_cell_tile() : decode_cell_tile();
+  const int slots_per_split = p->use_mma ? mma_warps_per_split() : 1;
   const long long units = (long long)n_seq * c->n_kv_heads;
   const int tiles = (max_ctx + tile - 1) / tile;
   int sms = sm_count();
   if (sms <= 0) sms = 148;
-  // The tensor-core kernel runs the splits of one (sequence, KV head) as
-  // thread-block clusters of up to 8 CTAs that merge on chip; one partial
-  // per cluster goes to the workspace.  Clusters are placed whole, inside a
-  // GPC, so the resident capacity comes from the cluster occupancy query
-  // and the cluster size is the one (of 8, 4, 2) with the most resident
-  // CTAs.  The split count is a whole number of clusters within one wave.
-  long long capacity = (long long)per_sm * sms;
-  p->cluster = 1;
-  if (p->use_mma) {
-    long long best = 0;
-    for (int cl = 8; cl >= 2; cl /= 2) {
-      const long long cap = (long long)mma_active_clusters(c->fmt, c->head_dim, p->rows, cl) * cl;
-      if (cap > best) {
-        best = cap;
-        p->cluster = cl;
-      }
-    }
-    if (best > 0) capacity = best;
-    else p->cluster = 1;
-  }
+  const long long capacity = (long long)per_sm * sms;
   const long long target = capacity * (n_seq > 1 ? 2 : 1);
   long long ns = target / units;
   if (ns < 1) ns = 1;
   if (ns > tiles) ns = tiles;
-  while (p->cluster > 1 && p->cluster > ns) p->cluster /= 2;
-  ns = ns / p->cluster * p->cluster;
-  const int split_tiles = (int)((tiles + ns - 1) / ns);
-  p->split_cells = split_tiles * tile;
-  p->nsplit = (max_ctx + p->split_cells - 1) / p->split_cells;
-  p->nsplit = (p->nsplit + p->cluster - 1) / p->cluster * p->cluster;  // whole clusters
-  p->ncl = p->nsplit / p->cluster;
-  const size_t parts = (size_t)n_seq * c->n_kv_heads * p->ncl * p->rows;
-  p->off_o = 0;
-  p->off_ml = round_up(parts * c->head_dim * sizeof(float), 256);
-  p->bytes = p->off_ml + round_up(parts * 2 * sizeof(float), 256);
-  return true;
+  for (;;) {
+    const int split_tiles = (int)((tiles + ns - 1) / ns);
+    p->split_cells = split_tiles * tile;
+    p->nsplit = (max_ctx + p->split_cells - 1) / p->split_cells;
+    p->nslot = p->nsplit * slots_per_split;
+    const size_t parts = (size_t)n_seq * c->n_kv_heads * p->nslot * p->rows;
+    p->off_o = 0;
+    p->off_ml = round_up(parts * c->head_dim * sizeof(float), 256);
+    p->bytes = p->off_ml + round_up(parts * 2 * sizeof(float), 256);
+    if (p->bytes <= max_bytes) return true;
+    if (p->nsplit <= 1) return false;
+    // shrink in proportion, at least by one split
+    long long next = (long long)((double)p->nsplit * (double)max_bytes / (double)p->bytes);
+    ns = next < p->nsplit - 1 ? next : p->nsplit - 1;
+    if (ns < 1) ns = 1;
+  }
 }
 
 kvq_status check_decode_shape(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx,
@@ -204,11 +192,16 @@ KVQ_API size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int n_seq, int
   return p.bytes;
 }
 
-KVQ_API kvq_status kvq_decode_attn(const kvq_cache* cache, const float* q, int n_seq, int W,
-                                   int n_q, const int32_t* ctx_lens, int max_ctx,
-                                   const int32_t* block_table, int max_blocks_per_seq,
-                                   float sm_scale, float* out, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+namespace kvq {
+namespace {
+
+// Validation, plan and launch of one decode call.  fit_plan: lower the split
+// count until the plan fits workspace_bytes (the static-scratch entry
+// point); otherwise the full plan must fit.
+kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W, int n_q,
+                       const int32_t* ctx_lens, int max_ctx, const int32_t* block_table,
+                       int max_blocks_per_seq, float sm_scale, float* out, void* workspace,
+                       size_t workspace_bytes, void* stream, bool fit_plan) {
   kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
   st = check_decode_shape(cache, n_seq, W, n_q, max_ctx, max_blocks_per_seq);
@@ -218,10 +211,11 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache* cache, const float* q, int n
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ctx_lens, 4) || !aligned(block_table, 4))
     return KVQ_ERR_ARG;
   if (!(sm_scale == sm_scale) || isinf(sm_scale)) return KVQ_ERR_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
   DecodePlan plan;
-  if (!plan_decode(cache, n_seq, W, n_q, max_ctx, &plan)) return KVQ_ERR_ARG;
-  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < plan.bytes)
-    return KVQ_ERR_WORKSPACE;
+  if (!plan_decode(cache, n_seq, W, n_q, max_ctx, &plan, fit_plan ? workspace_bytes : SIZE_MAX))
+    return fit_plan ? KVQ_ERR_WORKSPACE : KVQ_ERR_ARG;
+  if (workspace_bytes < plan.bytes) return KVQ_ERR_WORKSPACE;
   DecodeArgs a;
   a.pool = make_pool(cache);
   a.q = q;
@@ -238,11 +232,24 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache* cache, const float* q, int n
   a.max_blocks = max_blocks_per_seq;
   a.split_cells = plan.split_cells;
   a.nsplit = plan.nsplit;
-  a.ncl = plan.ncl;
+  a.nslot = plan.nslot;
   a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
   const cudaError_t e =
       launch_decode(cache->fmt, cache->head_dim, plan, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace kvq
+
+KVQ_API kvq_status kvq_decode_attn(const kvq_cache* cache, const float* q, int n_seq, int W,
+                                   int n_q, const int32_t* ctx_lens, int max_ctx,
+                                   const int32_t* block_table, int max_blocks_per_seq,
+                                   float sm_scale, float* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return kvq::decode_impl(cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
+                          max_blocks_per_seq, sm_scale, out, workspace, workspace_bytes, stream,
+                          false);
 }
 
 KVQ_API kvq_status kvq_compact_f16(const kvq_cache* cache, const int32_t* block_table_row,
@@ -329,9 +336,10 @@ KVQ_API kvq_status kvq_decode_attn_static(const kvq_cache* cache, const float* q
   void* scratch = nullptr;
   const kvq_status st = kvq::static_scratch_address(&scratch);
   if (st != KVQ_OK) return st;
-  // Same validation, plan and kernels as kvq_decode_attn; a plan that needs
-  // more than the array holds comes back as KVQ_ERR_WORKSPACE.
-  return kvq_decode_attn(cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
-                         max_blocks_per_seq, sm_scale, out, scratch,
-                         (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
+  // Same validation and kernels as kvq_decode_attn, with the split count
+  // lowered until the plan fits the array; a request that does not fit even
+  // with one split per (sequence, KV head) comes back as KVQ_ERR_WORKSPACE.
+  return kvq::decode_impl(cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
+                          max_blocks_per_seq, sm_scale, out, scratch,
+                          (size_t)KVQ_STATIC_SCRATCH_BYTES, stream, true);
 }

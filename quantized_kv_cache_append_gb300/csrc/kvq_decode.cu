@@ -432,7 +432,7 @@ cudaError_t launch_decode(int fmt, int hd, const DecodePlan& plan, const DecodeA
                           cudaStream_t s) {
   cudaError_t e = cudaErrorInvalidValue;
   if (plan.use_mma) {
-    // the tensor-core kernel merges its own splits (last CTA per row group)
+    // the tensor-core partial kernel and its combine
     return launch_decode_mma_partial(fmt, hd, plan, a, s);
   } else if (fmt == KVQ_F16) {
     if (hd == 64) e = launch_rows<KVQ_F16, 64>(plan, a, s);

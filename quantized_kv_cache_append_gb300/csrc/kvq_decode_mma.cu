@@ -3,33 +3,38 @@
 // The partial kernel of the split-K decode (#3084 qwen35: FP16 K/V cache by
 // default, int8 with --kv-q8, "What changed" and "Extra Notes": k_attn_part
 // templated on the cache format, read by the decode of the next token).  One
-// CTA per (split, KV head, sequence):
+// CTA of 4 warps per (split, KV head, sequence):
 //
-//   producer warp   one elected lane streams the split's cells through a
-//                   ring of STAGES shared-memory stages.  A stage is 64
-//                   cells: K and V codes arrive by TMA tensor copies
-//                   (cp.async.bulk.tensor, 128-byte swizzle, straight from
-//                   the paged pool through the block table), the int8
-//                   scales by bulk copies; an mbarrier per stage counts the
-//                   bytes in ("full") and the consumer warps out ("empty").
-//   4 consumer warps  each owns 16 cells of every stage.  S^T = K . Q^T is a
-//                   16-cell x 8-row mma.sync.m16n8k16 per 16 dims; the int8
-//                   codes are widened to fp16 exactly in registers and the
-//                   per-64-dim scales multiply the per-group partial dot
-//                   products.  Online softmax runs in the log2 domain with a
-//                   lazily raised reference maximum.  O^T += V^T . P^T is
-//                   another m16n8k16 per 16 dims, with the V scales folded
-//                   into P per group.  q and p enter the tensor cores as
-//                   fp16 hi + lo pairs (about 22 significant bits), K and V
-//                   as exact fp16 (int8 codes, or the FP16 cache itself).
+//   copies      the split's cells stream through a ring of STAGES
+//               shared-memory stages of 64 cells: K and V codes by TMA
+//               tensor copies (cp.async.bulk.tensor, 128-byte swizzle,
+//               straight from the paged pool through the block table), the
+//               int8 scales by bulk copies; an mbarrier per stage counts the
+//               bytes in.  Thread 0 issues the first stages; after that the
+//               warp that releases a stage last (a shared-memory counter)
+//               issues its refill.
+//   q.k         each warp owns 16 cells of every stage.  S^T = K . Q^T is a
+//               16-cell x 8-row mma.sync.m16n8k16 per 16 dims.  int8 K
+//               enters as the exact fp16 value 1152 + code, and 1152 * sum(q)
+//               per 64-dim group is taken off through the accumulator's
+//               starting value; the per-64-dim scales multiply the group
+//               partial dot products.
+//   softmax     online, in the log2 domain, with a lazily raised reference
+//               maximum.
+//   p.v         O^T += V^T . P^T, another m16n8k16 per 16 dims; int8 V is
+//               widened to fp16 exactly in registers and the V scales are
+//               folded into P per group.
 //
-// The warps' partial states are merged in shared memory and written as one
-// (o, m, l) partial per row; the combine kernel (kvq_decode.cu) merges the
-// splits.  Masked cells (beyond the context, beyond the causal limit of a
+// q and p enter the tensor cores as fp16 hi + lo pairs (about 22 significant
+// bits), K and V as exact fp16 values.
+//
+// Each warp writes its partial state, one (o, m, l) per row, straight from
+// registers; the combine kernel below merges the partials of every warp of
+// every split.  Masked cells (beyond the context, beyond the causal limit of a
 // verify-window row, or in a block whose id is out of range) get logit -inf
 // and contribute exact zeros.  Every mbarrier wait is bounded: a wait that
 // runs out marks the partial as NaN (the combine passes NaN to the output)
-// and the producer still waits, bounded, for its own copies before the CTA
+// and thread 0 still waits, bounded, for the CTA's copies before the CTA
 // exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -67,14 +72,10 @@ struct Cfg {
   // swizzle atoms); the int8 scales of all stages live in a region of their
   // own so no stage is padded.
   static constexpr int STAGE_B = 2 * TILE_B;
-  // Stages per CTA and CTAs per SM: keep about 100 KB or more of copies in
-  // flight per SM while fitting as many 4-warp CTAs as the 227 KB allow.
-  // merge buffers reuse the stages after the loop: 20 row values x 32 rows,
-  // o rows plus four warp slabs (5 x RP x HD floats), flags
-  static constexpr int MERGE_B = (20 * 32 + 5 * NT * 8 * HD + 4) * 4;
-  // at least three stages (one in flight while two are held), more when the
-  // merge buffers need the room
-  static constexpr int STAGES = (MERGE_B + STAGE_B - 1) / STAGE_B > 3 ? (MERGE_B + STAGE_B - 1) / STAGE_B : 3;
+  // Three stages per CTA (one landing while two are read) and as many
+  // 4-warp CTAs per SM as the 227 KB allow keep about 100 KB or more of
+  // copies in flight per SM.
+  static constexpr int STAGES = 3;
   static constexpr int OFF_V = TILE_B;
   static constexpr int SMEM_SC = STAGES * STAGE_B;           // [STAGES][K, V][64 cells][NG] fp16
   // q as fp16 hi / lo rows, padded by 16 bytes so ldmatrix rows hit distinct banks
@@ -91,8 +92,10 @@ struct Cfg {
   static constexpr int SMEM_BLK = SMEM_REL + 16 * 4;            // block ids [ROWS_CAP]
   static constexpr int SMEM = SMEM_BLK + ROWS_CAP * 4 + 1024 /*align*/;
   static constexpr int FIT = (227 * 1024) / SMEM;
-  static constexpr int MIN_CTAS = FIT >= 4 ? 4 : (FIT >= 3 ? 3 : (FIT >= 2 ? 2 : 1));
-  static_assert(STAGES * STAGE_B >= MERGE_B, "merge buffers fit");
+  // 32-row tiles (NT 4) hold 4x the accumulators: at most 3 CTAs (168
+  // registers a thread) so they do not spill
+  static constexpr int FIT_R = NT >= 4 ? (FIT < 3 ? FIT : 3) : FIT;
+  static constexpr int MIN_CTAS = FIT_R >= 4 ? 4 : (FIT_R >= 3 ? 3 : (FIT_R >= 2 ? 2 : 1));
 };
 
 // ---------------------------------------------------------------------------
@@ -109,10 +112,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Bounded wait for the phase with the given parity; false if it never came.
@@ -153,44 +152,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           "r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
-}
-
-// Thread-block cluster helpers: rank, barrier, distributed shared memory.
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-// Plain (not volatile) loads: the peers' values are fixed between the two
-// cluster barriers, so the compiler may batch them.
-__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
-  float v;
-  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
-  float4 v;
-  asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -266,12 +227,6 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 constexpr uint32_t kMagic = 0x64646464u;
 constexpr uint32_t kBias = 0x64806480u;  // fp16 1152 in both halves
 
-// Pairs (byte 0, byte 1) and (byte 2, byte 3) of one biased word.
-__device__ __forceinline__ void widen_same(uint32_t wx, uint32_t& p01, uint32_t& p23) {
-  p01 = hsub2(prmt(wx, kMagic, 0x4140u), kBias);
-  p23 = hsub2(prmt(wx, kMagic, 0x4342u), kBias);
-}
-
 // Swizzled shared-memory byte offset of logical byte `b` of cell `c` (0..63)
 // in a K or V tile laid out [span][cell][SWB]: every TMA box (one piece of
 // cells, one span) is placed at its [span][first cell] slot, so the layout
@@ -335,11 +290,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
   const int c_begin = split * a.split_cells;
-  // An empty split (past the end of the context) still runs to the cluster
-  // merge below, contributing nothing, because every CTA of a cluster has
-  // to reach the cluster barriers.
-  const bool empty = c_begin >= L;
-  const int c_end = empty ? c_begin : min(L, c_begin + a.split_cells);
+  // A split past the end of this sequence's context has nothing to do; the
+  // combine kernel reads only the slots of splits that hold cells.
+  if (c_begin >= L) return;
+  const int c_end = min(L, c_begin + a.split_cells);
   const int n_tiles = (c_end - c_begin + kTC - 1) / kTC;
   const int pc_log2 = a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6;  // cells per TMA piece
   const int n_pieces = kTC >> pc_log2;
@@ -580,12 +534,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // q . k of one stage for this warp's 16 cells -> z (log2-domain logits)
   auto qk = [&](int s, float (&z)[NT][4]) {
     const uint32_t st = sbase + s * C::STAGE_B;
-    const unsigned char* sp = smem + s * C::STAGE_B;
   // ---------------- S^T = K . Q^T (four independent accumulators) ----------------
   if constexpr (FMT == KVQ_F16) {
     float acc[4][NT][4];
-    const int mi = lane >> 3, rr = lane & 7;
-    const int cell = cl + ((mi & 1) << 3) + rr;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t af[4];
@@ -703,7 +654,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // o += V^T . P^T for one stage
   auto pv = [&](int s, int nvalid, const float (&p)[NT][4]) {
     const uint32_t st = sbase + s * C::STAGE_B;
-    const unsigned char* sp = smem + s * C::STAGE_B;
   // ---------------- O^T += V^T . P^T ----------------
   if constexpr (FMT == KVQ_F16) {
     uint32_t bh[NT][2], bl[NT][2];
@@ -721,8 +671,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
     const uint32_t mhi =
         (2 * t + 8 < nvalid ? 0xffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
-    const int mi = lane >> 3, rr = lane & 7;
-    const int cell = cl + ((mi >> 1) << 3) + rr;
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       uint32_t af[4];
@@ -861,7 +809,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       (void)mbar_wait(bar_full + 8 * (it % C::STAGES), (it / C::STAGES) & 1);
   }
 
-  // ---------------- merge the warps ----------------
+  // ---------------- this warp's partial ----------------
+  // Every warp writes its own (o, m, l) rows straight from registers: no
+  // block barrier, no merge on chip.  The combine kernel merges the slots
+  // of all warps of all splits.  A lost wait poisons the warp's rows (NaN).
+  const bool wlost = __any_sync(kFull, lost);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -872,256 +824,164 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       v += __shfl_xor_sync(kFull, v, 16);
       l[nt][j] = v;
     }
-  __syncthreads();  // the pipeline's shared memory is free now
-  float* s_m = reinterpret_cast<float*>(smem);   // [4][RP] warp maxima, then 4*RP + 8*RP spare
-  float* s_l = s_m + 16 * RP;                      // [4][RP] warp sums
-  float* s_o = s_l + kConsumerWarps * RP;          // [RP][HD]
-  int* s_lost = reinterpret_cast<int*>(s_o + RP * HD);
-  if (threadIdx.x == 0) *s_lost = 0;
-  if (g == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        s_m[warp * RP + nt * 8 + 2 * t + j] = m[nt][j];
-        s_l[warp * RP + nt * 8 + 2 * t + j] = l[nt][j];
-      }
-  }
-  __syncthreads();
-  if (lost) atomicOr(s_lost, 1);
-  float wgt[NT][2];
+  const size_t slot0 =
+      (((size_t)b * a.pool.n_kv + kvh) * a.nslot + (size_t)split * kConsumerWarps + warp) * a.R;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int r = nt * 8 + 2 * t + j;
-      float M = s_m[r];
+      if (r < a.R) {
+        float* orow = a.ws_o + (slot0 + r) * HD;
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * RP + r]);
-      wgt[nt][j] = (M == kNegInf || m[nt][j] == kNegInf) ? 0.f : fast_exp2(m[nt][j] - M);
-    }
-  // every warp writes its weighted rows to a slab of its own; one barrier;
-  // the slabs are summed in parallel into s_o
-  float* s_slab = s_o + RP * HD + 4;  // [4][RP][HD] after s_o and the flags
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int j = k & 1;
-        const int r = nt * 8 + 2 * t + j;
-        int d;
-        if constexpr (FMT == KVQ_F16) {
-          d = mt * 16 + g + ((k >> 1) << 3);
-        } else {
-          d = 16 * mt + 2 * g + (k >> 1);
+        for (int mt = 0; mt < KS; ++mt) {
+          if constexpr (FMT == KVQ_F16) {  // m-tile rows g, g + 8 are dims 16 mt + g, + 8
+            orow[mt * 16 + g] = o[mt][nt][j];
+            orow[mt * 16 + g + 8] = o[mt][nt][2 + j];
+          } else {                        // int8: dims 16 mt + 2g, + 1
+            *reinterpret_cast<float2*>(orow + mt * 16 + 2 * g) =
+                make_float2(o[mt][nt][j], o[mt][nt][2 + j]);
+          }
         }
-        s_slab[(warp * RP + r) * HD + d] = wgt[nt][j] * o[mt][nt][k];
+        if (g == 0)
+          *reinterpret_cast<float2*>(a.ws_ml + (slot0 + r) * 2) =
+              make_float2(wlost ? __int_as_float(0x7fc00000) : m[nt][j], l[nt][j]);
       }
-  __syncthreads();
-  for (int i = threadIdx.x; i < RP * HD; i += kThreads)
-    s_o[i] = (s_slab[i] + s_slab[RP * HD + i]) + (s_slab[2 * RP * HD + i] + s_slab[3 * RP * HD + i]);
-  __syncthreads();
-
-  // CTA-level partial: per row the CTA maximum and sum (in shared memory
-  // next to the CTA's weighted o rows), read by the cluster leader.
-  const int tid = threadIdx.x;
-  float* c_M = s_m + 4 * RP;      // [RP] (s_m's second half is free after the warp merge)
-  float* c_L = c_M + RP;          // [RP]
-  if (tid < RP) {
-    const int r = tid;
-    float M = s_m[r];
-    for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * RP + r]);
-    float lsum = 0.f;
-    for (int w = 0; w < kConsumerWarps; ++w)
-      if (s_m[w * RP + r] != kNegInf) lsum = fmaf(s_l[w * RP + r], fast_exp2(s_m[w * RP + r] - M), lsum);
-    c_M[r] = *s_lost ? __int_as_float(0x7fc00000) : M;  // a lost wait poisons the row
-    c_L[r] = lsum;
-  }
-
-  // ---------------- cluster merge over distributed shared memory ----------------
-  const uint32_t crank = cluster_rank(), csize = cluster_size();
-  const int ci = split / (int)csize;                       // this cluster's partial slot
-  cluster_sync_all();
-  if (crank == 0) {
-    // leader: fold the other CTAs' (M, L, o) into its own, row by row; all
-    // remote loads of a batch are issued before any is used.
-    float* f_M = c_L + RP;        // [RP] merged maximum
-    float* f_w = f_M + RP;        // [8][RP] weight of each rank
-    if (tid < RP) {
-      const int r = tid;
-      float mq[8], lq[8];
-      mq[0] = c_M[r];
-      lq[0] = c_L[r];
-#pragma unroll
-      for (int q = 1; q < 8; ++q) {
-        if (q < (int)csize) {
-          mq[q] = dsmem_ld(dsmem_addr(smem_u32(c_M + r), q));
-          lq[q] = dsmem_ld(dsmem_addr(smem_u32(c_L + r), q));
-        }
-      }
-      float M = kNegInf;
-      int bad = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q < (int)csize) {
-          bad |= mq[q] != mq[q];
-          M = fmaxf(M, mq[q]);
-        }
-      float lsum = 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float wq = (q >= (int)csize || M == kNegInf || mq[q] == kNegInf || bad) ? 0.f
-                                                                                         : fast_exp2(mq[q] - M);
-        f_w[q * RP + r] = wq;
-        if (q < (int)csize) lsum = fmaf(lq[q], wq, lsum);
-      }
-      f_M[r] = bad ? __int_as_float(0x7fc00000) : M;
-      c_L[r] = lsum;
     }
-    __syncthreads();
-    const size_t slot = (((size_t)b * a.pool.n_kv + kvh) * a.ncl + ci) * a.R;
-    for (int i4 = tid; i4 < a.R * HD / 4; i4 += kThreads) {
-      const int i = i4 * 4, r = i / HD;
-      float4 v[8];
-      v[0] = *reinterpret_cast<const float4*>(s_o + i);
-#pragma unroll
-      for (int q = 1; q < 8; ++q)
-        if (q < (int)csize) v[q] = dsmem_ld4(dsmem_addr(smem_u32(s_o + i), q));
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (q < (int)csize) {
-          const float wq = f_w[q * RP + r];
-          acc.x = fmaf(wq, v[q].x, acc.x);
-          acc.y = fmaf(wq, v[q].y, acc.y);
-          acc.z = fmaf(wq, v[q].z, acc.z);
-          acc.w = fmaf(wq, v[q].w, acc.w);
-        }
-      }
-      *reinterpret_cast<float4*>(a.ws_o + slot * HD + i) = acc;
-    }
-    if (tid < a.R) {
-      a.ws_ml[(slot + tid) * 2 + 0] = f_M[tid];
-      a.ws_ml[(slot + tid) * 2 + 1] = c_L[tid];
-    }
-  }
-  cluster_sync_all();  // the other CTAs keep their shared memory until the leader has read it
 }
 
 // ---------------------------------------------------------------------------
-// Final combine of the per-cluster partials (one CTA per sequence x KV head),
-// launched as a programmatic dependent of the partial kernel: its CTAs wait
-// on griddepcontrol until every partial is written.
+// Final combine of the per-warp partials, launched as a programmatic
+// dependent of the partial kernel: its CTAs wait on griddepcontrol until
+// every partial is written.
 // ---------------------------------------------------------------------------
+constexpr int kCombineJS = 64;     // partial slices per CTA
+constexpr int kCombineDV = 8;      // float4 columns per CTA (32 dims)
+constexpr int kCombineBatch = 8;   // partial loads in flight per thread
+
 template <int HD>
-__global__ void __launch_bounds__(256) combine_clusters(DecodeArgs a, int cl) {
-  // One CTA per (KV head, sequence, row).  Thread (js, d4) owns dims
-  // [4 d4, 4 d4 + 4) of the partials j = js, js + JS, ...; all its partial
-  // loads are issued before any is used, while warp 0 forms the row's
-  // maximum and sum over every partial.  One round trip to L2 in total.
-  constexpr int TPR = HD / 4;        // threads per row vector
-  constexpr int JS = 256 / TPR;      // split slices
-  constexpr int MAXJ = 8;            // partials held in registers per thread
+__global__ void __launch_bounds__(kCombineJS * kCombineDV) combine_partials(DecodeArgs a) {
+  // One CTA per (KV head, sequence, row, 32-dim slice).  Thread (js, dv)
+  // merges float4 column dv of the partials j = js, js + 64, ... online
+  // (running maximum, rescaled sums; loads of a batch issued together);
+  // the 64 slices then meet through warp shuffles and shared memory.
+  constexpr int NW = kCombineJS * kCombineDV / 32;
   constexpr float kNegInf = -INFINITY;
-  __shared__ float s_M, s_inv;
-  __shared__ int s_bad;
-  __shared__ float4 s_acc[JS][TPR];
+  __shared__ float s_wm[NW];
+  __shared__ float s_wl[NW];
+  __shared__ float4 s_wacc[NW][kCombineDV];
+  __shared__ int s_wbad[NW];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int kvh = blockIdx.x, b = blockIdx.y, r = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int js = tid / TPR, d4 = (tid % TPR) * 4;
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int r = blockIdx.z / (HD / 32), d4 = (blockIdx.z % (HD / 32)) * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int dv = tid % kCombineDV, js = tid / kCombineDV;
+  const int d = d4 + 4 * dv;
   const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
-  const int ns = (L + a.split_cells - 1) / a.split_cells;  // non-empty splits
-  const int nlive = (ns + cl - 1) / cl;                      // clusters holding them
-  const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.ncl;
+  const int nlive = (L + a.split_cells - 1) / a.split_cells * kConsumerWarps;
+  const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.nslot;
 
-  float4 oj[MAXJ];
-  float mj[MAXJ];
-#pragma unroll
-  for (int u = 0; u < MAXJ; ++u) {
-    const int j = js + u * JS;
-    if (j < nlive) {
-      const size_t rj = (base0 + j) * a.R + r;
-      oj[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + rj * HD + d4));
-      mj[u] = __ldcg(a.ws_ml + rj * 2);
-    }
-  }
-  if (tid < 32) {
-    float mx = kNegInf;
-    int bad = 0;
-    for (int j = lane; j < nlive; j += 32) {
-      const float m = __ldcg(a.ws_ml + ((base0 + j) * a.R + r) * 2);
-      bad |= m != m;
-      mx = fmaxf(mx, m);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-      bad |= __shfl_xor_sync(kFull, bad, off);
-    }
-    float lsum = 0.f;
-    for (int j = lane; j < nlive; j += 32) {
-      const size_t rj = (base0 + j) * a.R + r;
-      const float m = __ldcg(a.ws_ml + rj * 2);
-      if (mx != kNegInf && m != kNegInf) lsum = fmaf(__ldcg(a.ws_ml + rj * 2 + 1), fast_exp2(m - mx), lsum);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
-    if (lane == 0) {
-      s_M = mx;
-      s_inv = (mx != kNegInf && lsum > 0.f) ? 1.f / lsum : 0.f;
-      s_bad = bad;
-    }
-  }
-  __syncthreads();
-  const float M = s_M;
+  float M = kNegInf, lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (s_inv != 0.f) {
+  bool bad = false;
+  for (int j0 = js; j0 < nlive; j0 += kCombineJS * kCombineBatch) {
+    float mb[kCombineBatch], lb[kCombineBatch];
+    float4 ob[kCombineBatch];
 #pragma unroll
-    for (int u = 0; u < MAXJ; ++u) {
-      if (js + u * JS < nlive && mj[u] != kNegInf) {
-        const float w = fast_exp2(mj[u] - M);
-        acc.x = fmaf(w, oj[u].x, acc.x);
-        acc.y = fmaf(w, oj[u].y, acc.y);
-        acc.z = fmaf(w, oj[u].z, acc.z);
-        acc.w = fmaf(w, oj[u].w, acc.w);
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const int j = j0 + u * kCombineJS;
+      mb[u] = kNegInf;
+      lb[u] = 0.f;
+      ob[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < nlive) {
+        const size_t rj = (base0 + j) * a.R + r;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + rj * 2));
+        mb[u] = ml.x;
+        lb[u] = ml.y;
+        ob[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + rj * HD + d));
       }
     }
-    for (int j = js + MAXJ * JS; j < nlive; j += JS) {  // more partials than registers
-      const size_t rj = (base0 + j) * a.R + r;
-      const float m = __ldcg(a.ws_ml + rj * 2);
-      if (m == kNegInf) continue;
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(a.ws_o + rj * HD + d4));
-      const float w = fast_exp2(m - M);
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
-    }
-  }
-  s_acc[js][tid % TPR] = acc;
-  __syncthreads();
-  if (js == 0) {
-    float4 sum = s_acc[0][tid];
+    float bm = M;
 #pragma unroll
-    for (int q = 1; q < JS; ++q) {
-      const float4 v = s_acc[q][tid];
+    for (int u = 0; u < kCombineBatch; ++u) {
+      bad |= mb[u] != mb[u];
+      bm = fmaxf(bm, mb[u]);
+    }
+    if (bm == kNegInf) continue;
+    const float sc = M == kNegInf ? 0.f : fast_exp2(M - bm);
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+    lsum *= sc;
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      if (mb[u] != kNegInf) {
+        const float w = fast_exp2(mb[u] - bm);
+        acc.x = fmaf(w, ob[u].x, acc.x);
+        acc.y = fmaf(w, ob[u].y, acc.y);
+        acc.z = fmaf(w, ob[u].z, acc.z);
+        acc.w = fmaf(w, ob[u].w, acc.w);
+        lsum = fmaf(w, lb[u], lsum);
+      }
+    }
+    M = bm;
+  }
+  // block maximum: lanes of a warp cover 4 slices x 8 columns
+  float wm = M;
+  wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, 8));
+  wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, 16));
+  const bool wbad = __any_sync(kFull, bad);
+  if (lane == 0) {
+    s_wm[warp] = wm;
+    s_wbad[warp] = wbad;
+  }
+  __syncthreads();
+  float Mall = s_wm[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) Mall = fmaxf(Mall, s_wm[w]);
+  const float sc = (M == kNegInf || Mall == kNegInf) ? 0.f : fast_exp2(M - Mall);
+  acc.x *= sc;
+  acc.y *= sc;
+  acc.z *= sc;
+  acc.w *= sc;
+  lsum *= sc;
+#pragma unroll
+  for (int off = 8; off <= 16; off <<= 1) {
+    acc.x += __shfl_xor_sync(kFull, acc.x, off);
+    acc.y += __shfl_xor_sync(kFull, acc.y, off);
+    acc.z += __shfl_xor_sync(kFull, acc.z, off);
+    acc.w += __shfl_xor_sync(kFull, acc.w, off);
+    lsum += __shfl_xor_sync(kFull, lsum, off);
+  }
+  if (lane < kCombineDV) s_wacc[warp][lane] = acc;
+  if (lane == 0) s_wl[warp] = lsum;
+  __syncthreads();
+  if (tid < kCombineDV) {
+    float4 sum = s_wacc[0][tid];
+    float lam = s_wl[0];
+    int any_bad = s_wbad[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+      const float4 v = s_wacc[w][tid];
       sum.x += v.x;
       sum.y += v.y;
       sum.z += v.z;
       sum.w += v.w;
+      lam += s_wl[w];
+      any_bad |= s_wbad[w];
     }
-    const float inv = s_inv;
+    // an empty context (no live partial) gives 0; a lost wait gives NaN
+    const float inv = lam > 0.f ? 1.f / lam : 0.f;
     float4 res = make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
-    if (s_bad) {
+    if (any_bad) {
       const float nan = __int_as_float(0x7fc00000);
       res = make_float4(nan, nan, nan, nan);
     }
     const int w = r / a.G, gg = r - w * a.G;
-    *reinterpret_cast<float4*>(a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + d4) = res;
+    *reinterpret_cast<float4*>(a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD +
+                               d4 + 4 * tid) = res;
   }
 }
 
@@ -1205,65 +1065,23 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma<FMT, HD, NT>, maps, a);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cc = {};
-  cc.gridDim = dim3(a.pool.n_kv, a.n_seq, a.R);
-  cc.blockDim = dim3(256);
+  cc.gridDim = dim3(a.pool.n_kv, a.n_seq, a.R * (HD / 32));
+  cc.blockDim = dim3(kCombineJS * kCombineDV);
   cc.stream = s;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cc.attrs = pdl;
   cc.numAttrs = 1;
-  return cudaLaunchKernelEx(&cc, combine_clusters<HD>, a, p.cluster);
-}
-
-// Clusters of `cl` CTAs that can be resident on the device at once.
-template <int FMT, int HD, int NT>
-int active_clusters_impl(int cl) {
-  static int cache[4] = {-1, -1, -1, -1};  // cl = 1, 2, 4, 8
-  static std::mutex mu;
-  const int idx = cl == 1 ? 0 : cl == 2 ? 1 : cl == 4 ? 2 : 3;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache[idx] >= 0) return cache[idx];
-  using C = Cfg<FMT, HD, NT>;
-  int n = 0;
-  if (ctas_per_sm_impl<FMT, HD, NT>() > 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cl * 64, 1, 1);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_mma<FMT, HD, NT>, &cfg) != cudaSuccess) n = 0;
-  }
-  cache[idx] = n;
-  return n;
-}
-
-template <int FMT, int HD>
-int active_clusters_hd(int nt, int cl) {
-  switch (nt) {
-    case 1: return active_clusters_impl<FMT, HD, 1>(cl);
-    case 2: if constexpr (HD <= 128) return active_clusters_impl<FMT, HD, 2>(cl); break;
-    case 4: if constexpr (HD <= 64) return active_clusters_impl<FMT, HD, 4>(cl); break;
-  }
-  return 0;
+  return cudaLaunchKernelEx(&cc, combine_partials<HD>, a);
 }
 
 template <int FMT, int HD>
@@ -1300,17 +1118,7 @@ bool mma_decode_supported(int fmt, int hd, int rows) {
 
 int mma_cell_tile() { return kTC; }
 
-int mma_active_clusters(int fmt, int hd, int rows, int cl) {
-  const int nt = n_tiles_for(rows);
-  if (fmt == KVQ_F16) {
-    if (hd == 64) return active_clusters_hd<KVQ_F16, 64>(nt, cl);
-    if (hd == 128) return active_clusters_hd<KVQ_F16, 128>(nt, cl);
-    return active_clusters_hd<KVQ_F16, 256>(nt, cl);
-  }
-  if (hd == 64) return active_clusters_hd<KVQ_Q8, 64>(nt, cl);
-  if (hd == 128) return active_clusters_hd<KVQ_Q8, 128>(nt, cl);
-  return active_clusters_hd<KVQ_Q8, 256>(nt, cl);
-}
+int mma_warps_per_split() { return kConsumerWarps; }
 
 int mma_ctas_per_sm(int fmt, int hd, int rows) {
   const int nt = n_tiles_for(rows);
