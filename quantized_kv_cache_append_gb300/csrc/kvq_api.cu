@@ -68,7 +68,8 @@ int sm_count() {
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Split plan: one wave of partial CTAs (as many as are resident per SM, on
-// every SM; twice that for batches, whose ragged lengths leave CTAs short)
+// every SM; four times that for batches, whose ragged lengths need short
+// splits to fill the tail of the launch)
 // over all (sequence, KV head) pairs, each split a whole number of cell
 // tiles.  The tensor-core kernel takes the shapes it covers; the CUDA-core
 // kernel the rest.  With max_bytes set, the split count is lowered until
@@ -86,13 +87,12 @@ bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, Dec
   }
   if (!p->use_mma) per_sm = 4;
   const int tile = p->use_mma ? mma_cell_tile() : decode_cell_tile();
-  const int slots_per_split = p->use_mma ? mma_warps_per_split() : 1;
   const long long units = (long long)n_seq * c->n_kv_heads;
   const int tiles = (max_ctx + tile - 1) / tile;
   int sms = sm_count();
   if (sms <= 0) sms = 148;
   const long long capacity = (long long)per_sm * sms;
-  const long long target = capacity * (n_seq > 1 ? 2 : 1);
+  const long long target = capacity * (n_seq > 1 ? 4 : 1);
   long long ns = target / units;
   if (ns < 1) ns = 1;
   if (ns > tiles) ns = tiles;
@@ -100,8 +100,7 @@ bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, Dec
     const int split_tiles = (int)((tiles + ns - 1) / ns);
     p->split_cells = split_tiles * tile;
     p->nsplit = (max_ctx + p->split_cells - 1) / p->split_cells;
-    p->nslot = p->nsplit * slots_per_split;
-    const size_t parts = (size_t)n_seq * c->n_kv_heads * p->nslot * p->rows;
+    const size_t parts = (size_t)n_seq * c->n_kv_heads * p->nsplit * p->rows;
     p->off_o = 0;
     p->off_ml = round_up(parts * c->head_dim * sizeof(float), 256);
     p->bytes = p->off_ml + round_up(parts * 2 * sizeof(float), 256);
@@ -232,7 +231,6 @@ kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W,
   a.max_blocks = max_blocks_per_seq;
   a.split_cells = plan.split_cells;
   a.nsplit = plan.nsplit;
-  a.nslot = plan.nslot;
   a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
   const cudaError_t e =
       launch_decode(cache->fmt, cache->head_dim, plan, a, static_cast<cudaStream_t>(stream));

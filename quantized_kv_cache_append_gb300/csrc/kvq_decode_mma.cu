@@ -75,7 +75,10 @@ struct Cfg {
   // Three stages per CTA (one landing while two are read) and as many
   // 4-warp CTAs per SM as the 227 KB allow keep about 100 KB or more of
   // copies in flight per SM.
-  static constexpr int STAGES = 3;
+  // (the merge at the end reuses the stages for 4 warp slabs of RP x HD
+  // fp32, which takes a fourth stage for 32-row int8 HD 64 tiles)
+  static constexpr int SLAB_B = kConsumerWarps * NT * 8 * HD * 4;
+  static constexpr int STAGES = (SLAB_B + STAGE_B - 1) / STAGE_B > 3 ? (SLAB_B + STAGE_B - 1) / STAGE_B : 3;
   static constexpr int OFF_V = TILE_B;
   static constexpr int SMEM_SC = STAGES * STAGE_B;           // [STAGES][K, V][64 cells][NG] fp16
   // q as fp16 hi / lo rows, padded by 16 bytes so ldmatrix rows hit distinct banks
@@ -85,17 +88,22 @@ struct Cfg {
   // int8: per (padded row, 64-dim group) 1152 * sum of q (hi + lo), fp32
   static constexpr int SMEM_QC = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
   static constexpr int QC_BYTES = FMT == KVQ_Q8 ? (NT * 8 * NG * 4 + 15) / 16 * 16 : 0;
-  static constexpr int SMEM_BAR = SMEM_QC + QC_BYTES;
+  // per-warp row maxima and sums for the merge at the end: [4][RP][2] fp32
+  static constexpr int SMEM_WML = SMEM_QC + QC_BYTES;
+  static constexpr int SMEM_BAR = SMEM_WML + kConsumerWarps * NT * 8 * 2 * 4;
   // block ids of the split's pieces, staged once so any warp can issue a refill
-  static constexpr int ROWS_CAP = 256;
+  static constexpr int ROWS_CAP = 128;
   static constexpr int SMEM_REL = SMEM_BAR + STAGES * 8;        // release counters [STAGES]
   static constexpr int SMEM_BLK = SMEM_REL + 16 * 4;            // block ids [ROWS_CAP]
   static constexpr int SMEM = SMEM_BLK + ROWS_CAP * 4 + 1024 /*align*/;
-  static constexpr int FIT = (227 * 1024) / SMEM;
+  static constexpr int FIT = (228 * 1024) / (SMEM + 1024);  // 1 KB reserved per CTA
   // 32-row tiles (NT 4) hold 4x the accumulators: at most 3 CTAs (168
   // registers a thread) so they do not spill
   static constexpr int FIT_R = NT >= 4 ? (FIT < 3 ? FIT : 3) : FIT;
   static constexpr int MIN_CTAS = FIT_R >= 4 ? 4 : (FIT_R >= 3 ? 3 : (FIT_R >= 2 ? 2 : 1));
+  static_assert(STAGES * STAGE_B >= SLAB_B, "merge slabs fit in the stages");
+  // the SM's 228 KB hold MIN_CTAS of these CTAs (1 KB of each is reserved)
+  static_assert(MIN_CTAS * (SMEM + 1024) <= 228 * 1024, "CTAs per SM fit the shared memory");
 };
 
 // ---------------------------------------------------------------------------
@@ -259,6 +267,52 @@ __device__ __forceinline__ int block_of(const DecodeArgs& a, const int32_t* bt, 
   return c < c_end ? __ldg(bt + (c >> a.pool.bs_log2)) : -1;
 }
 
+// Work item of CTA c.  The grid is one CTA per possible (sequence, KV head,
+// split); the items that hold cells are numbered so that every full-length
+// split comes first (in sequence, split, KV head order) and the last,
+// shorter split of each sequence after them.  CTAs are dispatched roughly in
+// index order, so the short splits fill the tail of the launch instead of
+// full-length splits starting last.  Every warp computes this itself, a
+// warp-wide scan over 32 sequences at a time.  Returns false past the end.
+__device__ __forceinline__ bool item_of(const DecodeArgs& a, int c, int& b, int& kvh, int& split) {
+  const int lane = threadIdx.x & 31;
+  const int S = a.split_cells, nkv = a.pool.n_kv;
+  for (int pass = 0; pass < 2; ++pass) {   // 0: full splits, 1: last partial splits
+    for (int b0 = 0; b0 < a.n_seq; b0 += 32) {
+      const int bb = b0 + lane;
+      int n = 0, Lb = 0;
+      if (bb < a.n_seq) {
+        Lb = clamp_len_mma(__ldg(a.ctx_lens + bb), a);
+        n = pass == 0 ? Lb / S * nkv : (Lb % S != 0 ? nkv : 0);
+      }
+      int incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const int total = __shfl_sync(kFull, incl, 31);
+      if (c < total) {
+        const unsigned m = __ballot_sync(kFull, bb < a.n_seq && incl > c);
+        const int src = __ffs(m) - 1;
+        const int k = c - __shfl_sync(kFull, incl - n, src);
+        const int Ls = __shfl_sync(kFull, Lb, src);
+        b = b0 + src;
+        if (pass == 0) {
+          split = k / nkv;
+          kvh = k - split * nkv;
+        } else {
+          split = Ls / S;
+          kvh = k;
+        }
+        return true;
+      }
+      c -= total;
+    }
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -279,7 +333,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   int* s_rel = reinterpret_cast<int*>(smem + C::SMEM_REL);
   int* s_blk = reinterpret_cast<int*>(smem + C::SMEM_BLK);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Launched as a programmatic dependent of the previous kernel on the
   // stream: nothing it may have written is read before this wait.
@@ -288,11 +341,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.v[0])) : "memory");
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // CTAs past the last item (splits beyond a sequence's context) have
+  // nothing to do; the combine kernel reads only the slots of live splits.
+  int b, kvh, split;
+  if (!item_of(a, blockIdx.x, b, kvh, split)) return;
   const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
   const int c_begin = split * a.split_cells;
-  // A split past the end of this sequence's context has nothing to do; the
-  // combine kernel reads only the slots of splits that hold cells.
-  if (c_begin >= L) return;
   const int c_end = min(L, c_begin + a.split_cells);
   const int n_tiles = (c_end - c_begin + kTC - 1) / kTC;
   const int pc_log2 = a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6;  // cells per TMA piece
@@ -809,11 +863,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       (void)mbar_wait(bar_full + 8 * (it % C::STAGES), (it / C::STAGES) & 1);
   }
 
-  // ---------------- this warp's partial ----------------
-  // Every warp writes its own (o, m, l) rows straight from registers: no
-  // block barrier, no merge on chip.  The combine kernel merges the slots
-  // of all warps of all splits.  A lost wait poisons the warp's rows (NaN).
-  const bool wlost = __any_sync(kFull, lost);
+  // ---------------- merge the 4 warps, write the split's partial ----------------
+  // Each warp's row maxima and sums go to shared memory; after one barrier
+  // (every warp is past the loop, so the stages are free) each warp writes
+  // its rows scaled to the CTA maximum into a slab of its own in the stage
+  // memory; after a second barrier the 4 slabs are summed straight into the
+  // split's partial in global memory.  A lost wait poisons the rows (NaN).
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -824,30 +879,73 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       v += __shfl_xor_sync(kFull, v, 16);
       l[nt][j] = v;
     }
-  const size_t slot0 =
-      (((size_t)b * a.pool.n_kv + kvh) * a.nslot + (size_t)split * kConsumerWarps + warp) * a.R;
+  float* s_wml = reinterpret_cast<float*>(smem + C::SMEM_WML);  // [warp][RP][m, l]
+  const bool wlost = __any_sync(kFull, lost);
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = nt * 8 + 2 * t + j;
+        s_wml[(warp * RP + r) * 2 + 0] = wlost ? __int_as_float(0x7fc00000) : m[nt][j];
+        s_wml[(warp * RP + r) * 2 + 1] = l[nt][j];
+      }
+  }
+  __syncthreads();
+  float* s_slab = reinterpret_cast<float*>(smem);  // [warp][R][HD] over the free stages
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int r = nt * 8 + 2 * t + j;
       if (r < a.R) {
-        float* orow = a.ws_o + (slot0 + r) * HD;
+        float M = s_wml[r * 2];
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_wml[(w * RP + r) * 2]);
+        const float wgt = (M == kNegInf || m[nt][j] == kNegInf) ? 0.f : fast_exp2(m[nt][j] - M);
+        float* orow = s_slab + (warp * a.R + r) * HD;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           if constexpr (FMT == KVQ_F16) {  // m-tile rows g, g + 8 are dims 16 mt + g, + 8
-            orow[mt * 16 + g] = o[mt][nt][j];
-            orow[mt * 16 + g + 8] = o[mt][nt][2 + j];
+            orow[mt * 16 + g] = wgt * o[mt][nt][j];
+            orow[mt * 16 + g + 8] = wgt * o[mt][nt][2 + j];
           } else {                        // int8: dims 16 mt + 2g, + 1
             *reinterpret_cast<float2*>(orow + mt * 16 + 2 * g) =
-                make_float2(o[mt][nt][j], o[mt][nt][2 + j]);
+                make_float2(wgt * o[mt][nt][j], wgt * o[mt][nt][2 + j]);
           }
         }
-        if (g == 0)
-          *reinterpret_cast<float2*>(a.ws_ml + (slot0 + r) * 2) =
-              make_float2(wlost ? __int_as_float(0x7fc00000) : m[nt][j], l[nt][j]);
       }
     }
+  __syncthreads();
+  const size_t slot0 = (((size_t)b * a.pool.n_kv + kvh) * a.nsplit + split) * a.R;
+  for (int i4 = threadIdx.x; i4 < a.R * HD / 4; i4 += kThreads) {
+    const float4 v0 = reinterpret_cast<const float4*>(s_slab)[i4];
+    const float4 v1 = reinterpret_cast<const float4*>(s_slab + a.R * HD)[i4];
+    const float4 v2 = reinterpret_cast<const float4*>(s_slab + 2 * a.R * HD)[i4];
+    const float4 v3 = reinterpret_cast<const float4*>(s_slab + 3 * a.R * HD)[i4];
+    reinterpret_cast<float4*>(a.ws_o + slot0 * HD)[i4] =
+        make_float4((v0.x + v1.x) + (v2.x + v3.x), (v0.y + v1.y) + (v2.y + v3.y),
+                    (v0.z + v1.z) + (v2.z + v3.z), (v0.w + v1.w) + (v2.w + v3.w));
+  }
+  if (threadIdx.x < a.R) {
+    const int r = threadIdx.x;
+    float M = s_wml[r * 2];
+    bool bad = M != M;
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) {
+      const float mw = s_wml[(w * RP + r) * 2];
+      bad |= mw != mw;
+      M = fmaxf(M, mw);
+    }
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = s_wml[(w * RP + r) * 2];
+      if (M != kNegInf && mw != kNegInf) lsum = fmaf(s_wml[(w * RP + r) * 2 + 1], fast_exp2(mw - M), lsum);
+    }
+    *reinterpret_cast<float2*>(a.ws_ml + (slot0 + r) * 2) =
+        make_float2(bad ? __int_as_float(0x7fc00000) : M, lsum);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -855,42 +953,45 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 // dependent of the partial kernel: its CTAs wait on griddepcontrol until
 // every partial is written.
 // ---------------------------------------------------------------------------
-constexpr int kCombineJS = 64;     // partial slices per CTA
-constexpr int kCombineDV = 8;      // float4 columns per CTA (32 dims)
-constexpr int kCombineBatch = 8;   // partial loads in flight per thread
+constexpr int kCombineThreads = 256;
+constexpr int kCombineBatch = 4;   // partial loads in flight per thread
 
-template <int HD>
-__global__ void __launch_bounds__(kCombineJS * kCombineDV) combine_partials(DecodeArgs a) {
-  // One CTA per (KV head, sequence, row, 32-dim slice).  Thread (js, dv)
-  // merges float4 column dv of the partials j = js, js + 64, ... online
-  // (running maximum, rescaled sums; loads of a batch issued together);
-  // the 64 slices then meet through warp shuffles and shared memory.
-  constexpr int NW = kCombineJS * kCombineDV / 32;
+template <int HD, int DV>
+__global__ void __launch_bounds__(kCombineThreads, 4) combine_partials(DecodeArgs a) {
+  // One CTA per (KV head, sequence, row, DV float4 columns).  Thread (js,
+  // dv) merges column dv of the partials j = js, js + JS, ... online
+  // (running maximum, rescaled sums; the loads of a batch issued together);
+  // the JS slices then meet through warp shuffles and shared memory.  The
+  // host picks DV so that one batch usually covers every partial.
+  constexpr int JS = kCombineThreads / DV;
+  constexpr int NW = kCombineThreads / 32;
+  constexpr int CHUNKS = HD / 4 / DV;   // CTAs per row
   constexpr float kNegInf = -INFINITY;
+  static_assert(DV <= 32 && HD / 4 % DV == 0, "combine shape");
   __shared__ float s_wm[NW];
   __shared__ float s_wl[NW];
-  __shared__ float4 s_wacc[NW][kCombineDV];
   __shared__ int s_wbad[NW];
+  __shared__ float4 s_wacc[NW][DV];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int kvh = blockIdx.x, b = blockIdx.y;
-  const int r = blockIdx.z / (HD / 32), d4 = (blockIdx.z % (HD / 32)) * 32;
+  const int r = blockIdx.z / CHUNKS, d0 = (blockIdx.z % CHUNKS) * DV * 4;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int dv = tid % kCombineDV, js = tid / kCombineDV;
-  const int d = d4 + 4 * dv;
+  const int dv = tid % DV, js = tid / DV;
+  const int d = d0 + 4 * dv;
   const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
-  const int nlive = (L + a.split_cells - 1) / a.split_cells * kConsumerWarps;
-  const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.nslot;
+  const int nlive = (L + a.split_cells - 1) / a.split_cells;
+  const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.nsplit;
 
   float M = kNegInf, lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   bool bad = false;
-  for (int j0 = js; j0 < nlive; j0 += kCombineJS * kCombineBatch) {
+  for (int j0 = js; j0 < nlive; j0 += JS * kCombineBatch) {
     float mb[kCombineBatch], lb[kCombineBatch];
     float4 ob[kCombineBatch];
 #pragma unroll
     for (int u = 0; u < kCombineBatch; ++u) {
-      const int j = j0 + u * kCombineJS;
+      const int j = j0 + u * JS;
       mb[u] = kNegInf;
       lb[u] = 0.f;
       ob[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -928,10 +1029,10 @@ __global__ void __launch_bounds__(kCombineJS * kCombineDV) combine_partials(Deco
     }
     M = bm;
   }
-  // block maximum: lanes of a warp cover 4 slices x 8 columns
+  // block maximum (a warp holds 32 / DV slices; their columns share M)
   float wm = M;
-  wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, 8));
-  wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, 16));
+#pragma unroll
+  for (int off = DV; off < 32; off <<= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, off));
   const bool wbad = __any_sync(kFull, bad);
   if (lane == 0) {
     s_wm[warp] = wm;
@@ -948,17 +1049,17 @@ __global__ void __launch_bounds__(kCombineJS * kCombineDV) combine_partials(Deco
   acc.w *= sc;
   lsum *= sc;
 #pragma unroll
-  for (int off = 8; off <= 16; off <<= 1) {
+  for (int off = DV; off < 32; off <<= 1) {
     acc.x += __shfl_xor_sync(kFull, acc.x, off);
     acc.y += __shfl_xor_sync(kFull, acc.y, off);
     acc.z += __shfl_xor_sync(kFull, acc.z, off);
     acc.w += __shfl_xor_sync(kFull, acc.w, off);
     lsum += __shfl_xor_sync(kFull, lsum, off);
   }
-  if (lane < kCombineDV) s_wacc[warp][lane] = acc;
+  if (lane < DV) s_wacc[warp][lane] = acc;
   if (lane == 0) s_wl[warp] = lsum;
   __syncthreads();
-  if (tid < kCombineDV) {
+  if (tid < DV) {
     float4 sum = s_wacc[0][tid];
     float lam = s_wl[0];
     int any_bad = s_wbad[0];
@@ -981,8 +1082,34 @@ __global__ void __launch_bounds__(kCombineJS * kCombineDV) combine_partials(Deco
     }
     const int w = r / a.G, gg = r - w * a.G;
     *reinterpret_cast<float4*>(a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD +
-                               d4 + 4 * tid) = res;
+                               d0 + 4 * tid) = res;
   }
+}
+
+template <int HD, int DV>
+cudaError_t launch_combine_dv(const DecodeArgs& a, cudaStream_t s) {
+  cudaLaunchConfig_t cc = {};
+  cc.gridDim = dim3(a.pool.n_kv, a.n_seq, a.R * (HD / 4 / DV));
+  cc.blockDim = dim3(kCombineThreads);
+  cc.stream = s;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cc.attrs = pdl;
+  cc.numAttrs = 1;
+  return cudaLaunchKernelEx(&cc, combine_partials<HD, DV>, a);
+}
+
+// Widest column block (fewest CTAs) whose slices still cover every partial
+// slot in one batch of loads; 4 columns (64 slices) when none does.
+template <int HD>
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
+  const int need_js = (a.nsplit + kCombineBatch - 1) / kCombineBatch;
+  constexpr int MAXDV = HD / 4 < 32 ? HD / 4 : 32;
+  if (need_js <= kCombineThreads / 32 && MAXDV >= 32) return launch_combine_dv<HD, MAXDV>(a, s);
+  if (need_js <= kCombineThreads / 16 && MAXDV >= 16) return launch_combine_dv<HD, 16>(a, s);
+  if (need_js <= kCombineThreads / 8) return launch_combine_dv<HD, 8>(a, s);
+  return launch_combine_dv<HD, 4>(a, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -1061,7 +1188,9 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
       return cudaErrorInvalidValue;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.nsplit, a.pool.n_kv, a.n_seq);
+  const long long items = (long long)p.nsplit * a.pool.n_kv * a.n_seq;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  cfg.gridDim = dim3((unsigned)items);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
@@ -1072,16 +1201,7 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma<FMT, HD, NT>, maps, a);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cc = {};
-  cc.gridDim = dim3(a.pool.n_kv, a.n_seq, a.R * (HD / 32));
-  cc.blockDim = dim3(kCombineJS * kCombineDV);
-  cc.stream = s;
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  cc.attrs = pdl;
-  cc.numAttrs = 1;
-  return cudaLaunchKernelEx(&cc, combine_partials<HD>, a);
+  return launch_combine<HD>(a, s);
 }
 
 template <int FMT, int HD>
@@ -1117,8 +1237,6 @@ bool mma_decode_supported(int fmt, int hd, int rows) {
 }
 
 int mma_cell_tile() { return kTC; }
-
-int mma_warps_per_split() { return kConsumerWarps; }
 
 int mma_ctas_per_sm(int fmt, int hd, int rows) {
   const int nt = n_tiles_for(rows);

@@ -46,9 +46,7 @@ struct DecodePlan {
   int rows;            // R = G * W query rows per (sequence, KV head)
   int rows_pad;        // R rounded up to the kernel's row tile
   int split_cells;     // cells per split (a multiple of the cell tile)
-  int nsplit;          // splits per (sequence, KV head)
-  int nslot;           // partial slots per (sequence, KV head): one per split
-                       // (CUDA-core kernel) or one per warp of a split
+  int nsplit;          // splits per (sequence, KV head), one partial each
   size_t off_o, off_ml, bytes;  // workspace layout
 };
 
@@ -58,10 +56,9 @@ struct DecodeArgs {
   float* out;          // [n_seq][W][n_q][hd]
   const int32_t* ctx_lens;
   const int32_t* block_table;
-  float* ws_o;         // [n_seq][n_kv][nslot][R][hd]   unnormalised partial outputs
-  float* ws_ml;        // [n_seq][n_kv][nslot][R][2]    (running max, sum), log2 domain
+  float* ws_o;         // [n_seq][n_kv][nsplit][R][hd]   unnormalised partial outputs
+  float* ws_ml;        // [n_seq][n_kv][nsplit][R][2]    (running max, sum), log2 domain
   int n_seq, W, n_q, G, R, max_blocks, split_cells, nsplit;
-  int nslot;           // partial slots per (sequence, KV head)
   float qscale;        // sm_scale * log2(e): logits come out in the log2 domain
 };
 
@@ -84,11 +81,10 @@ cudaError_t launch_decode(int fmt, int hd, const DecodePlan& plan, const DecodeA
                           cudaStream_t s);
 
 // Tensor-core partial kernel (kvq_decode_mma.cu): shapes it covers, its cell
-// tile, partial slots per split (one per consumer warp), resident CTAs per SM
-// (0 if unavailable), and its launcher (partial + combine).
+// tile, resident CTAs per SM (0 if unavailable), and its launcher (partial +
+// combine).
 bool mma_decode_supported(int fmt, int hd, int rows);
 int mma_cell_tile();
-int mma_warps_per_split();
 int mma_ctas_per_sm(int fmt, int hd, int rows);
 cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, const DecodeArgs& a,
                                       cudaStream_t s);
