@@ -48,8 +48,8 @@ class PagedPool:
         if out is None:
             out = torch.empty_like(q)
         need = self.workspace_bytes(n_seq, W, n_q, max_ctx)
-        if workspace is None:   # zero-filled: the arrival counters start at zero
-            workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
+        if workspace is None:   # needs no initial contents
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
         check(kvq_decode_attn(self.cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
                               int(block_table.shape[1]), sm_scale, out, workspace,
                               workspace.numel(), stream), "kvq_decode_attn")
