@@ -816,9 +816,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     }
   };
 
-  // Software pipeline: q.k of tile it+1 is issued next to p.v of tile it
-  // (independent work the scheduler can interleave); the softmax of tile
-  // it+1 follows p.v of tile it because it may rescale o.
+  // Software pipeline: q.k of tile it+1 and p.v of tile it form one
+  // straight-line block, so the compiler can interleave the two; the
+  // softmax of tile it+1 follows because it may rescale o.  Neither is
+  // skipped for a slice without valid cells (stale or unloaded stage
+  // memory): its logits are masked to -inf, so p = 0, FP16 V rows are
+  // zeroed by mask and int8 V scales are clamped to finite values.
   int blk_n = slice_blk(0);
   int nv_cur = 0;
   float p_cur[NT][4];
@@ -828,33 +831,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     } else {
       nv_cur = slice_nvalid(0, blk_n);
       blk_n = slice_blk(1);
-      if (nv_cur > 0) {
-        float z[NT][4];
-        qk(0, z);
-        softmax(nv_cur, c_begin + cl, z, p_cur);
-      }
+      float z[NT][4];
+      qk(0, z);
+      softmax(nv_cur, c_begin + cl, z, p_cur);
     }
   }
-  for (int it = 0; it < n_tiles && !lost; ++it) {
-    const int s = it % C::STAGES;
-    float zn[NT][4];
-    int nv_next = 0;
-    const bool more = it + 1 < n_tiles;
-    if (more) {
-      const int sn = (it + 1) % C::STAGES;
-      if (!mbar_wait(bar_full + 8 * sn, ((it + 1) / C::STAGES) & 1)) {
-        lost = true;
-      } else {
-        nv_next = slice_nvalid(it + 1, blk_n);
-        blk_n = slice_blk(it + 2);
-        if (nv_next > 0) qk(sn, zn);
-      }
+  int it = 0;
+  for (; it + 1 < n_tiles && !lost; ++it) {
+    const int sn = (it + 1) % C::STAGES;
+    if (!mbar_wait(bar_full + 8 * sn, ((it + 1) / C::STAGES) & 1)) {
+      lost = true;
+      break;
     }
-    if (nv_cur > 0) pv(s, nv_cur, p_cur);
+    const int nv_next = slice_nvalid(it + 1, blk_n);
+    blk_n = slice_blk(it + 2);
+    float zn[NT][4];
+    qk(sn, zn);
+    pv(it % C::STAGES, nv_cur, p_cur);
     release(it);
-    if (lost) break;
-    if (more && nv_next > 0) softmax(nv_next, c_begin + (it + 1) * kTC + cl, zn, p_cur);
+    softmax(nv_next, c_begin + (it + 1) * kTC + cl, zn, p_cur);
     nv_cur = nv_next;
+  }
+  if (!lost && n_tiles > 0) {  // the last tile
+    pv(it % C::STAGES, nv_cur, p_cur);
+    release(it);
   }
   if (producer) {
     // Every copy this CTA issued has landed before the CTA can exit (waits
