@@ -85,9 +85,9 @@ struct Cfg {
   static constexpr int QROW = HD * 2 + 16;
   static constexpr int QBYTES_MAX = 2 * NT * 8 * QROW;   // hi and lo, NT*8 padded rows
   static constexpr int SMEM_Q = SMEM_SC + STAGES * 2 * SCALE_B;
-  // int8: per (padded row, 64-dim group) 1152 * sum of q (hi + lo), fp32
+  // int8: per (padded row, 64-dim group, 32-dim half) 1152 * sum of q (hi + lo)
   static constexpr int SMEM_QC = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
-  static constexpr int QC_BYTES = FMT == KVQ_Q8 ? (NT * 8 * NG * 4 + 15) / 16 * 16 : 0;
+  static constexpr int QC_BYTES = FMT == KVQ_Q8 ? (NT * 8 * NG * 2 * 4 + 15) / 16 * 16 : 0;
   // per-warp row maxima and sums for the merge at the end: [4][RP][2] fp32
   static constexpr int SMEM_WML = SMEM_QC + QC_BYTES;
   static constexpr int SMEM_BAR = SMEM_WML + kConsumerWarps * NT * 8 * 2 * 4;
@@ -368,15 +368,21 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     return from_smem ? s_blk[it * n_pieces + p]
                      : block_of(a, bt, c_begin + it * kTC + (p << pc_log2), c_end);
   };
-  auto issue = [&](int it, bool from_smem) {
+  // block ids of the pieces of tile it
+  auto tile_blks = [&](int it, bool from_smem, int (&blk)[MAXP]) {
+#pragma unroll
+    for (int p = 0; p < MAXP; ++p) blk[p] = p < n_pieces ? piece_blk(it, p, from_smem) : -1;
+  };
+  auto issue = [&](int it, const int (&blks)[MAXP]) {
     const int s = it % C::STAGES;
     const int pc = 1 << pc_log2;
     const int bsz = 1 << a.pool.bs_log2;
     const int c0 = c_begin + it * kTC;
     int rows[MAXP];
     uint32_t bytes = 0;
+#pragma unroll
     for (int p = 0; p < MAXP; ++p) {
-      const int blk = p < n_pieces ? piece_blk(it, p, from_smem) : -1;
+      const int blk = blks[p];
       const int c = c0 + (p << pc_log2);
       rows[p] = (p < n_pieces && blk >= 0 && blk < a.pool.n_blocks)
                     ? (blk * a.pool.n_kv + kvh) * bsz + (c & (bsz - 1))
@@ -446,12 +452,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   }
   bool lost = false;
   if (producer) {
+    // the block ids of every first-wave piece are loaded together, before
+    // the first copy is issued
+    int fb[C::STAGES][MAXP];
+#pragma unroll
+    for (int it = 0; it < C::STAGES; ++it) tile_blks(it, false, fb[it]);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       s_rel[s] = 0;
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    for (int it = 0; it < n_tiles && it < C::STAGES; ++it) issue(it, false);
+#pragma unroll
+    for (int it = 0; it < C::STAGES; ++it)
+      if (it < n_tiles) issue(it, fb[it]);
   }
   {
     unsigned char* qs = smem + C::SMEM_Q;
@@ -465,6 +478,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         const __half lo = __float2half_rn(x - __half2float(h));
         *reinterpret_cast<__half*>(qs + r * C::QROW + k * 2) = h;
         *reinterpret_cast<__half*>(qs + (RP + r) * C::QROW + k * 2) = lo;
+        if constexpr (FMT == KVQ_Q8) {
+          // The 32 lanes of a warp hold 32 consecutive k of one row and one
+          // 64-dim group (RP * HD is a multiple of 128): their sum of q,
+          // times 1152, fills the (row, group, half) slot of the int8 bias.
+          float v = __half2float(h) + __half2float(lo);
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+          if (lane == 0)
+            reinterpret_cast<float*>(smem + C::SMEM_QC)[(r * C::NG + k / 64) * 2 + ((k >> 5) & 1)] =
+                1152.0f * v;
+        }
       }
     }
 #pragma unroll
@@ -483,25 +507,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // once, as the starting value of that group's hi accumulator.
   float qcorr[C::NG > 0 ? (FMT == KVQ_Q8 ? C::NG : 1) : 1][NT][2];
   if constexpr (FMT == KVQ_Q8) {
-    float* s_qc = reinterpret_cast<float*>(smem + C::SMEM_QC);
-    const unsigned char* qs = smem + C::SMEM_Q;
-    for (int pr = warp; pr < RP * C::NG; pr += kConsumerWarps) {
-      const int r = pr / C::NG, gq = pr - r * C::NG;
-      const int k = gq * 64 + 2 * lane;
-      const __half2 h = *reinterpret_cast<const __half2*>(qs + r * C::QROW + k * 2);
-      const __half2 lo = *reinterpret_cast<const __half2*>(qs + (RP + r) * C::QROW + k * 2);
-      float v = (__low2float(h) + __high2float(h)) + (__low2float(lo) + __high2float(lo));
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-      if (lane == 0) s_qc[pr] = 1152.0f * v;
-    }
-    __syncthreads();
+    const float* s_qc = reinterpret_cast<const float*>(smem + C::SMEM_QC);
 #pragma unroll
     for (int gq = 0; gq < C::NG; ++gq)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) qcorr[gq][nt][j] = -s_qc[(nt * 8 + 2 * t + j) * C::NG + gq];
+        for (int j = 0; j < 2; ++j) {
+          const int i = ((nt * 8 + 2 * t + j) * C::NG + gq) * 2;
+          qcorr[gq][nt][j] = -(s_qc[i] + s_qc[i + 1]);
+        }
   }
 
   // ldmatrix lane addressing of q: matrix lane>>3 = {hi k0-7, hi k8-15, lo
@@ -810,7 +825,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         s_rel[s] = 0;
         if (it + C::STAGES < n_tiles) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue(it + C::STAGES, blk_in_smem);
+          int nb[MAXP];
+          tile_blks(it + C::STAGES, blk_in_smem, nb);
+          issue(it + C::STAGES, nb);
         }
       }
     }
