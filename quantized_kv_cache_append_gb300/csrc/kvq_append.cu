@@ -4,84 +4,150 @@
 // under --kv-q8 a row is written as scale = fp16(max|x| / 127) per 64 dims and
 // code = clamp(rint(x / scale), -127, 127); the FP16 cache stores fp16(x).
 // The same section notes that the group maximum needs every thread to reach
-// a barrier before the stores.  Here one half-warp owns one 64-dim group, so
-// the group maximum is a warp-shuffle butterfly that every lane executes: no
-// __syncthreads exists in this kernel and no early return can skip one.
+// a barrier before the stores.  Here a quad of lanes owns one 64-dim group,
+// so the group maximum is a warp-shuffle butterfly that every lane executes:
+// no __syncthreads exists in these kernels and no early return can skip one.
 //
-// Bit-exactness: max|x| is exact; a / 127.0f is an IEEE fp32 division (the
-// library is built without fast-math, so '/' is div.rn.f32); x / s is
-// replaced by a reciprocal multiply only where that provably rounds to the
-// same integer (quantize_one); __float2half_rn rounds to nearest even with
-// subnormals; rintf rounds half to even, so clamping afterwards equals
-// clamping the rounded value.
+// Bit-exactness: max|x| is exact; a / 127 and x / s are the IEEE fp32
+// quotients the pages define (the library is built without fast-math, so
+// '/' is div.rn.f32), replaced by multiplies only where those provably give
+// the same fp16 scale (group_scale) or the same integer code (code_byte);
+// __float2half_rn rounds to nearest even with subnormals; rounding is to
+// nearest even, and clamping before rounding equals clamping after it for
+// the bound 127.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 namespace {
 
-// Butterfly max over the `kLanes` lanes that share one 64-dim group.
-template <int kLanes>
-__device__ __forceinline__ float group_max(float v) {
-#pragma unroll
-  for (int off = kLanes / 2; off >= 1; off >>= 1)
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
+// The group scale fp16_rne(fl32(a / 127)) from a multiply: y = a * fl(1/127)
+// is within 2 fp32 ulps of fl32(a / 127), so the two round to the same fp16
+// value unless an fp16 rounding midpoint (13 discarded bits equal to 0x1000)
+// lies within that distance, or the result leaves the fp16 normal range;
+// only then is the quotient itself computed.
+__device__ __forceinline__ __half group_scale(float a) {
+  const float y = a * (1.0f / 127.0f);
+  const uint32_t low = __float_as_uint(y) & 0x1fffu;
+  const bool exact_needed = (low > 0x1000u - 4u && low < 0x1000u + 4u) || !(y >= 6.103515625e-05f) ||
+                            !(y < 65504.0f);
+  return __float2half_rn(exact_needed ? a / 127.0f : y);
 }
 
-// code = clamp(rint(x / sf), -127, 127) with x / sf the IEEE fp32 quotient.
-// y = x * (1 / sf) is within about 2^-22 |x / sf| of the real quotient (both
-// roundings together), and |x / sf| stays below 256, so wherever y lies
-// more than 2.5e-4 away from a half-integer, the real quotient, its fp32
-// rounding and y all round to the same integer.  Only inside that band is
-// the quotient itself computed (a few elements in ten thousand), so ties
-// and near-ties resolve exactly as the division defines them.
-__device__ __forceinline__ int quantize_one(float x, float sf, float rs) {
-  if (sf == 0.0f) return 0;
-  const float y = x * rs;
-  float n = rintf(y);
-  if (fabsf(fabsf(y - n) - 0.5f) < 2.5e-4f) n = rintf(x / sf);
-  const int c = __float2int_rn(n);  // NaN (out-of-domain input) gives 0
-  return max(-127, min(127, c));
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
-// The K and V inputs are flat arrays of n_tok * n_kv * HD floats, read as
-// 16-byte chunks; a 64-dim group is 16 consecutive chunks, so one half-warp
-// owns one group and finds its maximum with a 4-step butterfly.  Each thread
-// handles U chunk positions of K and the same positions of V (2U loads in
-// flight before the first use), warp j covering chunks [32 U j, 32 U (j+1));
-// a CTA has W warps.
-// The destination of a row comes from the token's sequence, position and
-// block-table entry; those small loads are issued beside the data loads.
+// Packed fp32 pairs (two lanes of work per instruction).
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  return ((unsigned long long)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo2(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// The int8 code clamp(rint(x / sf), -127, 127) from the IEEE fp32 quotient
+// itself, as a byte (0 for a zero scale or a NaN quotient).
+__device__ __forceinline__ uint32_t exact_code(float x, float sf) {
+  if (sf == 0.0f) return 0u;
+  const float qv = x / sf;
+  if (!(qv == qv)) return 0u;
+  return (uint32_t)(int)fminf(fmaxf(rintf(qv), -127.0f), 127.0f) & 0xffu;
+}
+
+// Codes of 4 values of one group (finite group maximum, so x is finite), as
+// 4 bytes.  y = x * rs (rs = 1 / sf within one ulp) is within 2^-21 |x / sf|
+// of the real quotient, and |x / sf| < 256, so wherever y lies more than
+// 2.5e-4 from a half-integer the real quotient, its fp32 rounding and y
+// round to the same integer; only inside that band are the quotients
+// themselves used.  After clamping y to [-127, 127], y + 1.5 * 2^23 rounds y
+// to an integer (to nearest, ties to even) in the low mantissa bits, whose
+// low byte is the two's-complement code.
+__device__ __forceinline__ uint32_t codes4(const float4& x, float sf, float rs) {
+  if (sf == 0.0f) return 0u;
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const unsigned long long r2 = pack2(rs, rs), m2 = pack2(kMagic, kMagic);
+  const unsigned long long p01 = mul2(pack2(x.x, x.y), r2), p23 = mul2(pack2(x.z, x.w), r2);
+  const unsigned long long y01 = pack2(fminf(fmaxf(lo2(p01), -127.0f), 127.0f),
+                                       fminf(fmaxf(hi2(p01), -127.0f), 127.0f));
+  const unsigned long long y23 = pack2(fminf(fmaxf(lo2(p23), -127.0f), 127.0f),
+                                       fminf(fmaxf(hi2(p23), -127.0f), 127.0f));
+  const unsigned long long t01 = add2(y01, m2), t23 = add2(y23, m2);
+  const unsigned long long d01 = sub2(y01, sub2(t01, m2)), d23 = sub2(y23, sub2(t23, m2));
+  constexpr float kBand = 0.5f - 2.5e-4f;
+  const bool tie = fabsf(lo2(d01)) > kBand || fabsf(hi2(d01)) > kBand || fabsf(lo2(d23)) > kBand ||
+                   fabsf(hi2(d23)) > kBand;
+  if (tie)  // near a tie: the quotients decide (a few groups in a thousand)
+    return exact_code(x.x, sf) | (exact_code(x.y, sf) << 8) | (exact_code(x.z, sf) << 16) |
+           (exact_code(x.w, sf) << 24);
+  return prmt(prmt((uint32_t)t01, (uint32_t)(t01 >> 32), 0x0040u),
+              prmt((uint32_t)t23, (uint32_t)(t23 >> 32), 0x0040u), 0x5410u);
+}
+
+// Destination row of row index `row` (= token * n_kv + kvh): the token's
+// sequence, position and block-table entry; -1 when a precondition is
+// broken (then nothing is written).
+__device__ __forceinline__ long long dest_row(const AppendArgs& a, long long row, bool rows32) {
+  int tok, kvh;
+  if (rows32) {  // 32-bit division where the row count fits
+    tok = (int)((unsigned)row / (unsigned)a.n_kv);
+    kvh = (int)row - tok * a.n_kv;
+  } else {
+    tok = (int)(row / a.n_kv);
+    kvh = (int)(row - (long long)tok * a.n_kv);
+  }
+  const int seq = __ldg(a.tok_seq + tok);
+  const int pos = __ldg(a.tok_pos + tok);
+  if (seq < 0 || seq >= a.n_seq || pos < 0 || (pos >> a.bs_log2) >= a.max_blocks) return -1;
+  const int blk = __ldg(a.block_table + (size_t)seq * a.max_blocks + (pos >> a.bs_log2));
+  if (blk < 0 || blk >= a.n_blocks) return -1;
+  return ((long long)blk * a.n_kv + kvh) * (1LL << a.bs_log2) + (pos & ((1 << a.bs_log2) - 1));
+}
+
+// FP16 append.  The K and V inputs are flat arrays of n_tok * n_kv * HD
+// floats, read as 16-byte chunks; each thread handles U chunk positions of
+// K and the same positions of V (2U loads in flight before the first use),
+// warp j of the grid covering chunks [32 U j, 32 U (j + 1)); W warps a CTA.
 template <int HD, int U, int W>
-struct AppendShape {
-  static constexpr int CPR = HD / 4;   // 16-byte chunks per row
-  static constexpr int WARPS = W;      // warps per CTA
-  static constexpr long long CHUNKS_PER_CTA = 32LL * U * WARPS;
-};
-
-template <int FMT, int HD, int U, int W>
-__global__ void __launch_bounds__(W * 32) append_kernel(AppendArgs a) {
-  using S = AppendShape<HD, U, W>;
-  constexpr int NG = HD / kGroup;
-
+__global__ void __launch_bounds__(W * 32) append_f16_kernel(AppendArgs a) {
+  constexpr int CPR = HD / 4;  // 16-byte chunks per row
   // Launched as a programmatic dependent: wait for the previous kernel's
   // writes (k, v, positions may come from it), then let the next kernel's
   // launch begin.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const long long n_chunks = (long long)a.n_tok * a.n_kv * S::CPR;  // a multiple of 16
-  const long long base = (long long)blockIdx.x * S::CHUNKS_PER_CTA + (threadIdx.x >> 5) * 32LL * U;
+  const long long n_chunks = (long long)a.n_tok * a.n_kv * CPR;
+  const bool rows32 = n_chunks / CPR <= 0x7fffffffLL;
+  const long long base = ((long long)blockIdx.x * W + (threadIdx.x >> 5)) * 32LL * U;
   const float4* k4 = reinterpret_cast<const float4*>(a.k);
   const float4* v4 = reinterpret_cast<const float4*>(a.v);
 
   float4 xk[U], xv[U];
-  long long dst_row[U];
 #pragma unroll
   for (int j = 0; j < U; ++j) {
     const long long f = base + 32LL * j + lane;
     xk[j] = xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    dst_row[j] = -1;
     if (f < n_chunks) {
       xk[j] = __ldcs(k4 + f);
       xv[j] = __ldcs(v4 + f);
@@ -90,104 +156,155 @@ __global__ void __launch_bounds__(W * 32) append_kernel(AppendArgs a) {
 #pragma unroll
   for (int j = 0; j < U; ++j) {
     const long long f = base + 32LL * j + lane;
-    if (f < n_chunks) {
-      const long long row = f / S::CPR;                 // token * n_kv + kvh
-      const int tok = (int)(row / a.n_kv);
-      const int kvh = (int)(row - (long long)tok * a.n_kv);
-      const int seq = __ldg(a.tok_seq + tok);
-      const int pos = __ldg(a.tok_pos + tok);
-      if (seq >= 0 && seq < a.n_seq && pos >= 0 && (pos >> a.bs_log2) < a.max_blocks) {
-        const int blk = __ldg(a.block_table + (size_t)seq * a.max_blocks + (pos >> a.bs_log2));
-        if (blk >= 0 && blk < a.n_blocks)  // precondition broken: write nothing
-          dst_row[j] = ((long long)blk * a.n_kv + kvh) * (1LL << a.bs_log2) +
-                       (pos & ((1 << a.bs_log2) - 1));
-      }
-    }
-  }
-
-#pragma unroll
-  for (int j = 0; j < U; ++j) {
-    const long long f = base + 32LL * j + lane;
-    const int d = (int)(f % S::CPR) * 4;                // first dim of this chunk
+    if (f >= n_chunks) continue;
+    const long long dr = dest_row(a, f / CPR, rows32);
+    if (dr < 0) continue;
+    const int d = (int)(f % CPR) * 4;  // first dim of this chunk
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const float4 x = which ? xv[j] : xk[j];
-      if constexpr (FMT == KVQ_F16) {
-        if (dst_row[j] >= 0) {
-          __half* dst = static_cast<__half*>(which ? a.v_dst : a.k_dst) + dst_row[j] * HD + d;
-          uint2 u;
-          u.x = (uint32_t)__half_as_ushort(__float2half_rn(x.x)) |
-                ((uint32_t)__half_as_ushort(__float2half_rn(x.y)) << 16);
-          u.y = (uint32_t)__half_as_ushort(__float2half_rn(x.z)) |
-                ((uint32_t)__half_as_ushort(__float2half_rn(x.w)) << 16);
-          *reinterpret_cast<uint2*>(dst) = u;
-        }
-      } else {
-        // every lane takes part in the butterfly (out-of-range half-warps
-        // carry zeros and store nothing)
-        float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-        amax = group_max<16>(amax);
-        const __half sh = __float2half_rn(amax / 127.0f);
-        const float sf = __half2float(sh);
-        const float rs = 1.0f / sf;
-        if (dst_row[j] >= 0) {
-          const uint32_t packed = ((uint32_t)(quantize_one(x.x, sf, rs) & 0xff)) |
-                                  ((uint32_t)(quantize_one(x.y, sf, rs) & 0xff) << 8) |
-                                  ((uint32_t)(quantize_one(x.z, sf, rs) & 0xff) << 16) |
-                                  ((uint32_t)(quantize_one(x.w, sf, rs) & 0xff) << 24);
-          int8_t* dst = static_cast<int8_t*>(which ? a.v_dst : a.k_dst) + dst_row[j] * HD + d;
-          *reinterpret_cast<uint32_t*>(dst) = packed;
-          if ((lane & 15) == 0)
-            (which ? a.vs_dst : a.ks_dst)[dst_row[j] * NG + d / kGroup] = sh;
-        }
-      }
+      __half* dst = static_cast<__half*>(which ? a.v_dst : a.k_dst) + dr * HD + d;
+      uint2 u;
+      u.x = (uint32_t)__half_as_ushort(__float2half_rn(x.x)) |
+            ((uint32_t)__half_as_ushort(__float2half_rn(x.y)) << 16);
+      u.y = (uint32_t)__half_as_ushort(__float2half_rn(x.z)) |
+            ((uint32_t)__half_as_ushort(__float2half_rn(x.w)) << 16);
+      *reinterpret_cast<uint2*>(dst) = u;
     }
   }
 }
 
-template <int FMT, int HD, int U, int W>
-cudaError_t launch_shape(const AppendArgs& a, cudaStream_t s) {
-  using S = AppendShape<HD, U, W>;
-  const long long chunks = (long long)a.n_tok * a.n_kv * S::CPR;
-  const long long blocks = (chunks + S::CHUNKS_PER_CTA - 1) / S::CHUNKS_PER_CTA;
+// int8 append.  A quad of 4 lanes owns one 64-dim group of one row: lane q
+// holds the 16-byte chunks q, q + 4, q + 8, q + 12 of the group (dims
+// 16 i + 4 q .. + 3), so every load instruction reads 64 contiguous bytes
+// per quad.  The group maximum is a 2-step butterfly inside the quad (on
+// the bit patterns of |x|, whose integer order is the numeric order with
+// inf and NaN on top); scale, reciprocal and 16 codes follow per lane.
+// Each thread handles U groups of K and the same groups of V; a warp covers
+// 8 U groups, W warps a CTA.  With KV_SPLIT (few tokens) even warps take K
+// and odd warps V, halving each thread's chain.
+template <int HD, int U, int W, bool KV_SPLIT>
+__global__ void __launch_bounds__(W * 32) append_q8_kernel(AppendArgs a) {
+  constexpr int NG = HD / kGroup;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, q = lane & 3, quad = lane >> 2;
+  const long long n_groups = (long long)a.n_tok * a.n_kv * NG;
+  const bool rows32 = n_groups / NG <= 0x7fffffffLL;
+  const long long wid = (long long)blockIdx.x * W + (threadIdx.x >> 5);
+  const int only = KV_SPLIT ? (int)(wid & 1) : -1;  // K (0) or V (1) only, or both (-1)
+  const long long gbase = (KV_SPLIT ? wid >> 1 : wid) * 8LL * U + quad;
+  const float4* k4 = reinterpret_cast<const float4*>(a.k);
+  const float4* v4 = reinterpret_cast<const float4*>(a.v);
+
+  float4 x[2][U][4];  // [K, V][group][chunk]
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long g = gbase + 8LL * u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[0][u][i] = x[1][u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < n_groups) {
+        if (only != 1) x[0][u][i] = __ldcs(k4 + g * 16 + 4 * i + q);
+        if (only != 0) x[1][u][i] = __ldcs(v4 + g * 16 + 4 * i + q);
+      }
+    }
+  }
+  long long dr[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long g = gbase + 8LL * u;
+    dr[u] = g < n_groups ? dest_row(a, g / NG, rows32) : -1;
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long g = gbase + 8LL * u;
+    const int gi = (int)(g % NG);
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      if (KV_SPLIT && which != only) continue;  // warp-uniform
+      uint32_t mb = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4& v = x[which][u][i];
+        mb = max(mb, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                         max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+      }
+      // every lane takes part (quads past the end carry zeros, store nothing)
+      mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      const float amax = __uint_as_float(mb);
+      const __half sh = group_scale(amax);
+      const float sf = __half2float(sh);
+      if (dr[u] < 0) continue;
+      int8_t* dst = static_cast<int8_t*>(which ? a.v_dst : a.k_dst) + dr[u] * HD + gi * kGroup + 4 * q;
+      if (amax <= 3.4028234663852886e38f) {  // finite group: packed fast path
+        const float rs = rcp_approx(sf);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint32_t*>(dst + 16 * i) = codes4(x[which][u][i], sf, rs);
+      } else {  // inf or NaN in the group: element by element from the quotients
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4& v = x[which][u][i];
+          *reinterpret_cast<uint32_t*>(dst + 16 * i) = exact_code(v.x, sf) | (exact_code(v.y, sf) << 8) |
+                                                        (exact_code(v.z, sf) << 16) |
+                                                        (exact_code(v.w, sf) << 24);
+        }
+      }
+      if (q == 0) (which ? a.vs_dst : a.ks_dst)[dr[u] * NG + gi] = sh;
+    }
+  }
+}
+
+template <typename Kernel>
+cudaError_t launch_grid(Kernel kern, long long blocks, int threads, const AppendArgs& a,
+                        cudaStream_t s) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(32 * S::WARPS);
+  cfg.blockDim = dim3(threads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, append_kernel<FMT, HD, U, W>, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Bulk appends (prefill, prompt chunks) keep 8 chunks of 16 bytes in flight
-// per thread; a few tokens (decode steps) take one chunk of K and one of V
-// per thread in small CTAs, so the work spreads over more SMs and no thread
-// runs a long serial chain of group maxima.
-template <int FMT, int HD>
-cudaError_t launch_hd(const AppendArgs& a, cudaStream_t s) {
+// Bulk appends (prefill, prompt chunks) keep several 16-byte loads in
+// flight per thread; a few tokens (decode steps) use small CTAs, so the work
+// spreads over more SMs and no thread runs a long serial chain.
+template <int HD>
+cudaError_t launch_f16(const AppendArgs& a, cudaStream_t s) {
   const long long chunks = (long long)a.n_tok * a.n_kv * (HD / 4);
-  if (chunks < (1LL << 16)) return launch_shape<FMT, HD, 1, 2>(a, s);
-  return launch_shape<FMT, HD, 4, 8>(a, s);
+  if (chunks < (1LL << 16)) return launch_grid(append_f16_kernel<HD, 1, 2>, (chunks + 63) / 64, 64, a, s);
+  return launch_grid(append_f16_kernel<HD, 4, 8>, (chunks + 1023) / 1024, 256, a, s);
 }
 
-template <int FMT>
-cudaError_t launch_fmt(int hd, const AppendArgs& a, cudaStream_t s) {
-  switch (hd) {
-    case 64: return launch_hd<FMT, 64>(a, s);
-    case 128: return launch_hd<FMT, 128>(a, s);
-    case 256: return launch_hd<FMT, 256>(a, s);
-    default: return cudaErrorInvalidValue;
-  }
+template <int HD>
+cudaError_t launch_q8(const AppendArgs& a, cudaStream_t s) {
+  const long long groups = (long long)a.n_tok * a.n_kv * (HD / kGroup);
+  if (groups < (1LL << 12))
+    return launch_grid(append_q8_kernel<HD, 1, 2, true>, (groups + 7) / 8, 64, a, s);
+  return launch_grid(append_q8_kernel<HD, 2, 8, false>, (groups + 127) / 128, 256, a, s);
+}
+
+template <int HD>
+cudaError_t launch_hd(int fmt, const AppendArgs& a, cudaStream_t s) {
+  return fmt == KVQ_F16 ? launch_f16<HD>(a, s) : launch_q8<HD>(a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_append(int fmt, int hd, const AppendArgs& a, cudaStream_t s) {
-  return fmt == KVQ_F16 ? launch_fmt<KVQ_F16>(hd, a, s) : launch_fmt<KVQ_Q8>(hd, a, s);
+  switch (hd) {
+    case 64: return launch_hd<64>(fmt, a, s);
+    case 128: return launch_hd<128>(fmt, a, s);
+    case 256: return launch_hd<256>(fmt, a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace kvq

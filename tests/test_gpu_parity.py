@@ -193,6 +193,36 @@ def test_quantization_ties_and_near_ties():
     p.assert_cache_equal()
 
 
+def test_scale_rounding_midpoints():
+    # Group maxima a with a / 127 on, or a few fp32 ulps from, a midpoint
+    # between two fp16 values (where fp16(a / 127) is decided by the last
+    # bits of the fp32 quotient), and maxima whose scale is an fp16
+    # subnormal or near the fp16 maximum.
+    rng = np.random.default_rng(12)
+    n, n_kv, hd = 64, 2, 128
+    x = rng.uniform(-1.0, 1.0, size=(n, n_kv, hd)).astype(np.float32)
+    ng = n * n_kv * (hd // 64)
+    h = rng.uniform(2.0 ** -13, 500.0, size=ng).astype(np.float16)
+    h_next = np.nextafter(h, np.float16(np.inf))
+    mid = (h.astype(np.float64) + h_next.astype(np.float64)) / 2.0
+    a = (mid * 127.0).astype(np.float32)
+    shift = rng.integers(-3, 4, size=ng)
+    for k in (1, 2, 3):
+        a[shift >= k] = np.nextafter(a[shift >= k], np.float32(np.inf))
+        a[shift <= -k] = np.nextafter(a[shift <= -k], np.float32(-np.inf))
+    a[:16] = rng.uniform(1e-7, 6e-3, size=16).astype(np.float32)        # fp16-subnormal scales
+    a[16:24] = np.float32(65504.0 * 127.0) * rng.uniform(0.999, 1.001, size=8).astype(np.float32)
+    groups = x.reshape(ng, 64)
+    groups *= (a / np.abs(groups).max(axis=1))[:, None]
+    groups[np.arange(ng), rng.integers(0, 64, size=ng)] = a * np.where(rng.random(ng) < 0.5, 1, -1)
+    x = groups.reshape(n, n_kv, hd).astype(np.float32)
+    v = x[::-1].copy()
+    table = np.arange(4, dtype=np.int32)[None]
+    p = Pair("q8", n_kv, hd, 16, 4, table)
+    p.append(x, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32))
+    p.assert_cache_equal()
+
+
 def test_paged_equals_contiguous_bitwise():
     lens = [700, 1500]
     for fmt in ("f16", "q8"):
