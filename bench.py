@@ -293,6 +293,27 @@ def run_kvq(args):
     torch.cuda.synchronize()
     append_step_us = a.elapsed_time(b) / chunk / 2 * 1e3
 
+    # FP16 compaction of a whole layer (32768 cells, both formats), layers in turn
+    compact_us = {}
+    ck = torch.empty((n_kv, L, hd), dtype=torch.float16, device="cuda")
+    cv = torch.empty_like(ck)
+    for name in ("f16", "q8"):
+        gc = torch.cuda.CUDAGraph()
+        for i in range(LAYERS):
+            layers[i][name][0].compact(bt[0], L, ck, cv)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gc):
+            for i in range(4 * LAYERS):
+                layers[i % LAYERS][name][0].compact(bt[0], L, ck, cv)
+        gc.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gc.replay()
+        b.record()
+        torch.cuda.synchronize()
+        compact_us[name] = a.elapsed_time(b) / (4 * LAYERS) * 1e3
+
     peak, peak_kind = _peaks()
     avg_bytes = {n: sum(v) / len(v) for n, v in bytes_per_step.items()}
     gbs = {n: avg_bytes[n] / (kernel_ms[n] * 1e-3) / 1e9 for n in kernel_ms}
@@ -327,6 +348,13 @@ def run_kvq(args):
                        for n in kernel_ms},
             "append": {"bulk_Mcells_per_s": {n: round(v, 1) for n, v in append_mcells.items()},
                        "one_cell_step_us": round(append_step_us, 3)},
+            "compact_f16": {n: {"us": round(compact_us[n], 3),
+                                "GB/s": round(L * n_kv * (_row_bytes(n == "q8", hd) + 4 * hd)
+                                              / (compact_us[n] * 1e-6) / 1e9, 1),
+                                "frac_of_measured_hbm": round(
+                                    L * n_kv * (_row_bytes(n == "q8", hd) + 4 * hd)
+                                    / (compact_us[n] * 1e-6) / 1e9 / peak, 4)}
+                            for n in compact_us},
             "clocks": clock_info,
             "e2e": e2e,
         }

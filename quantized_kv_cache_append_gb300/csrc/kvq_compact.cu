@@ -7,63 +7,92 @@
 // fp16(code * scale); the product of an 8-bit code and an fp16 scale is
 // exact in fp32, so the only rounding is __float2half_rn (nearest even).
 //
-// One thread moves 8 consecutive dims of one row: 8 int8 codes (8 bytes) or
-// 8 fp16 values (16 bytes) in, 16 bytes out.  Consecutive threads walk the
-// dims of a row, then the cells, so loads and stores are both coalesced.
+// Grid y = (K or V, KV head), so a thread's cell and dims come from shifts
+// alone.  FP16: one thread copies 8 dims (16 bytes).  int8: one thread
+// takes 16 codes (16 bytes) of one 64-dim group, widens each exactly to
+// fp16 (XOR 0x80, PRMT with the 0x64 exponent byte, minus 1152) and
+// multiplies pairs by the group's fp16 scale with mul.rn.f16x2: the product
+// of a code and an fp16 scale is exact, and the fp16 multiply rounds it once
+// to nearest even, with subnormals, which is fp16(code * scale).  Loads and
+// stores are coalesced along the dims of a row, then the cells.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 namespace {
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Codes in bytes 0, 1 (sel 0x4140) or 2, 3 (sel 0x4342) of w, times scale s2.
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t w, uint32_t sel, uint32_t s2) {
+  const uint32_t biased = w ^ 0x80808080u;  // c + 128 as unsigned bytes
+  const uint32_t h = hsub2(prmt(biased, 0x64646464u, sel), 0x64806480u);  // (1024 + u) - 1152 = c
+  return hmul2(h, s2);
+}
+
 template <int FMT, int HD>
 __global__ void __launch_bounds__(256) compact_kernel(CompactArgs a) {
-  constexpr int CPR = HD / 8;  // 8-dim chunks per row
+  constexpr int DPT = FMT == KVQ_F16 ? 8 : 16;  // dims per thread
+  constexpr int CPR = HD / DPT;                  // threads per row
   constexpr int NG = HD / kGroup;
-  const long long total = 2LL * a.pool.n_kv * a.n_cells * CPR;
+  const int kvh = blockIdx.y % a.pool.n_kv;
+  const int which = blockIdx.y / a.pool.n_kv;    // 0 = K, 1 = V
+  const long long total = (long long)a.n_cells * CPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const int bs = 1 << a.pool.bs_log2;
+  __half* out = which ? a.out_v : a.out_k;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int p = (int)(i / CPR);
     const int chunk = (int)(i % CPR);
-    const long long r = i / CPR;                 // (which, kvh, p)
-    const int p = (int)(r % a.n_cells);
-    const long long wk = r / a.n_cells;          // which * n_kv + kvh
-    const int kvh = (int)(wk % a.pool.n_kv);
-    const int which = (int)(wk / a.pool.n_kv);   // 0 = K, 1 = V
-
     const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
     if (blk < 0 || blk >= a.pool.n_blocks) continue;  // precondition broken: skip
     const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
-    __half* dst = (which ? a.out_v : a.out_k) + ((size_t)kvh * a.n_cells + p) * HD + chunk * 8;
-
+    __half* dst = out + ((size_t)kvh * a.n_cells + p) * HD + chunk * DPT;
     if constexpr (FMT == KVQ_F16) {
       const __half* src = static_cast<const __half*>(which ? a.pool.v : a.pool.k) + row * HD;
-      *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src + chunk * 8));
+      *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src + chunk * DPT));
     } else {
       const int8_t* src = static_cast<const int8_t*>(which ? a.pool.v : a.pool.k) + row * HD;
-      const __half* sc = (which ? a.pool.vs : a.pool.ks) + row * NG;
-      const uint2 codes = __ldg(reinterpret_cast<const uint2*>(src + chunk * 8));
-      const float sf = __half2float(sc[(chunk * 8) / kGroup]);
-      uint32_t outw[4];
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const uint32_t w = e < 4 ? codes.x : codes.y;
-        const int sh = (e & 3) * 8;
-        const float lo = (float)(int8_t)(w >> sh) * sf;
-        const float hi = (float)(int8_t)(w >> (sh + 8)) * sf;
-        outw[e / 2] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
-                      ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
-      }
-      *reinterpret_cast<uint4*>(dst) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(src + chunk * DPT));
+      const unsigned short sbits =
+          __half_as_ushort(((which ? a.pool.vs : a.pool.ks) + row * NG)[(chunk * DPT) / kGroup]);
+      const uint32_t s2 = (uint32_t)sbits * 0x10001u;
+      uint4 o0, o1;
+      o0.x = dequant_pair(c.x, 0x4140u, s2);
+      o0.y = dequant_pair(c.x, 0x4342u, s2);
+      o0.z = dequant_pair(c.y, 0x4140u, s2);
+      o0.w = dequant_pair(c.y, 0x4342u, s2);
+      o1.x = dequant_pair(c.z, 0x4140u, s2);
+      o1.y = dequant_pair(c.z, 0x4342u, s2);
+      o1.z = dequant_pair(c.w, 0x4140u, s2);
+      o1.w = dequant_pair(c.w, 0x4342u, s2);
+      reinterpret_cast<uint4*>(dst)[0] = o0;
+      reinterpret_cast<uint4*>(dst)[1] = o1;
     }
   }
 }
 
 template <int FMT>
-cudaError_t launch_fmt(int hd, const CompactArgs& a, cudaStream_t s, int blocks) {
+cudaError_t launch_fmt(int hd, const CompactArgs& a, cudaStream_t s, dim3 grid) {
   switch (hd) {
-    case 64: compact_kernel<FMT, 64><<<blocks, 256, 0, s>>>(a); break;
-    case 128: compact_kernel<FMT, 128><<<blocks, 256, 0, s>>>(a); break;
-    case 256: compact_kernel<FMT, 256><<<blocks, 256, 0, s>>>(a); break;
+    case 64: compact_kernel<FMT, 64><<<grid, 256, 0, s>>>(a); break;
+    case 128: compact_kernel<FMT, 128><<<grid, 256, 0, s>>>(a); break;
+    case 256: compact_kernel<FMT, 256><<<grid, 256, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -75,13 +104,17 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long total = 2LL * a.pool.n_kv * a.n_cells * (hd / 8);
-  long long blocks = (total + 255) / 256;
-  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;  // grid-stride beyond 8 CTAs/SM
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  return fmt == KVQ_F16 ? launch_fmt<KVQ_F16>(hd, a, s, (int)blocks)
-                        : launch_fmt<KVQ_Q8>(hd, a, s, (int)blocks);
+  if (sms <= 0) sms = 1;
+  const int dpt = fmt == KVQ_F16 ? 8 : 16;
+  const long long per_row = (long long)a.n_cells * (hd / dpt);  // threads per (K or V, KV head)
+  const int ys = 2 * a.pool.n_kv;
+  long long xs = (per_row + 255) / 256;
+  const long long cap = ((long long)sms * 8 + ys - 1) / ys;  // about 8 CTAs per SM in total
+  if (xs > cap) xs = cap;
+  if (xs < 1) xs = 1;
+  if (ys > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)xs, (unsigned)ys);
+  return fmt == KVQ_F16 ? launch_fmt<KVQ_F16>(hd, a, s, grid) : launch_fmt<KVQ_Q8>(hd, a, s, grid);
 }
 
 }  // namespace kvq
