@@ -65,6 +65,8 @@ def _bind(lib):
                                   ctypes.c_float, P]
     lib.kvo_compact_f16.restype = I
     lib.kvo_compact_f16.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, P]
+    lib.kvo_chunk_attention.restype = I
+    lib.kvo_chunk_attention.argtypes = [I, I, I, P, P, P, I, I, ctypes.c_float, P]
     return lib
 
 
@@ -237,3 +239,23 @@ def compact_f16(pool: PoolImage, block_table_row, n_cells: int):
     if rc != 0:
         raise RuntimeError(f"kvo_compact_f16 failed: {rc}")
     return out_k, out_v
+
+
+def chunk_attention(k16, v16, q, sm_scale: float) -> np.ndarray:
+    """float64 prompt-chunk attention over fp16 staging.
+
+    k16, v16: uint16 fp16 bits [n_kv][P][hd]; q float32 [T][n_q][hd] (the
+    chunk's tokens are the last T cells; token t sees cells [0, P - T + t]).
+    Returns float64 [T][n_q][hd]."""
+    k16 = _c(k16, np.uint16)
+    v16 = _c(v16, np.uint16)
+    q = _c(q, np.float32)
+    n_kv, P, hd = k16.shape
+    T, n_q, qhd = q.shape
+    assert qhd == hd and v16.shape == k16.shape
+    out = np.empty(q.shape, dtype=np.float64)
+    rc = _load().kvo_chunk_attention(n_kv, P, hd, _ptr(k16), _ptr(v16), _ptr(q), T, n_q,
+                                     float(sm_scale), _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"kvo_chunk_attention failed: {rc}")
+    return out

@@ -393,3 +393,57 @@ int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Prompt-chunk attention over the fp16 staging.                             */
+/*                                                                           */
+/* [kv-q8 PR, "Extra Notes"]: the prompt chunk's Q K^T and P V products read  */
+/* the contiguous [kvh][P][HD] fp16 halves k_kv_f16 writes.  The chunk's      */
+/* tokens are the sequence's last T cells (appended before the attention),   */
+/* each attending causally to every cell up to its own position.  Written    */
+/* out as the softmax definition, float64, like kvo_attention.                */
+/* ------------------------------------------------------------------------ */
+
+int kvo_chunk_attention(int n_kv, int P, int hd, const uint16_t *k16, const uint16_t *v16,
+                        const float *q, int T, int n_q, float sm_scale, double *out)
+{
+    if (n_kv <= 0 || P <= 0 || hd <= 0 || T <= 0 || T > P || n_q <= 0 || n_q % n_kv != 0)
+        return -1;
+    fp16_table_init();
+    const int G = n_q / n_kv;
+    double *z = (double *)malloc(sizeof(double) * (size_t)P);
+    if (z == NULL)
+        return -5;
+    for (int t = 0; t < T; ++t) {
+        const int last = P - T + t; /* last visible cell */
+        for (int h = 0; h < n_q; ++h) {
+            const int src_head = h / G; /* the KV head query head h reads */
+            const float *qv = q + ((size_t)t * n_q + h) * hd;
+            double *o = out + ((size_t)t * n_q + h) * hd;
+            double zmax = -INFINITY;
+            for (int c = 0; c <= last; ++c) {
+                const uint16_t *kr = k16 + ((size_t)src_head * P + c) * hd;
+                double dot = 0.0;
+                for (int d = 0; d < hd; ++d)
+                    dot += (double)qv[d] * (double)g_fp16_table[kr[d]];
+                z[c] = dot * (double)sm_scale;
+                if (z[c] > zmax)
+                    zmax = z[c];
+            }
+            for (int d = 0; d < hd; ++d)
+                o[d] = 0.0;
+            double den = 0.0;
+            for (int c = 0; c <= last; ++c) {
+                const double e = exp(z[c] - zmax);
+                const uint16_t *vr = v16 + ((size_t)src_head * P + c) * hd;
+                den += e;
+                for (int d = 0; d < hd; ++d)
+                    o[d] += e * (double)g_fp16_table[vr[d]];
+            }
+            for (int d = 0; d < hd; ++d)
+                o[d] = o[d] / den;
+        }
+    }
+    free(z);
+    return 0;
+}

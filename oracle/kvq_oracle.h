@@ -75,6 +75,14 @@ int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                     const int32_t *block_table_row, int n_cells,
                     uint16_t *out_k, uint16_t *out_v);
 
+/* Attention of a prompt chunk over contiguous fp16 staging, float64.  The
+ * staging k16/v16 [n_kv][P][hd] (fp16 bits) holds the sequence's P cells;
+ * the chunk's T query tokens are its last T cells, so token t sees cells
+ * [0, P - T + t].  q and out are [T][n_q][hd]; query head h reads KV head
+ * h / (n_q / n_kv). */
+int kvo_chunk_attention(int n_kv, int P, int hd, const uint16_t *k16, const uint16_t *v16,
+                        const float *q, int T, int n_q, float sm_scale, double *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_attention as att
+from tests import test_oracle_chunk as chk
 from tests import test_oracle_fp16 as f16
 from tests import test_oracle_quant as qt
 
@@ -40,6 +41,14 @@ MUTATIONS = {
     "no_normalisation": ("o[d] /= den;", "o[d] /= (den + 1.0);"),
     "compact_k_from_v": ("(float)dequant(fmt, hd, k_data, k_scales, row, d));",
                          "(float)dequant(fmt, hd, v_data, v_scales, row, d));"),
+    "chunk_causal_drop_diagonal": ("const int last = P - T + t; /* last visible cell */",
+                                   "const int last = P - T + t - 1;"),
+    "chunk_causal_from_start": ("const int last = P - T + t; /* last visible cell */",
+                                "const int last = t;"),
+    "chunk_gqa_modulo": ("const int src_head = h / G;", "const int src_head = h % n_kv;"),
+    "chunk_no_softmax_scale": ("z[c] = dot * (double)sm_scale;", "z[c] = dot;"),
+    "chunk_k_reads_v": ("const uint16_t *kr = k16 +", "const uint16_t *kr = v16 +"),
+    "chunk_no_normalisation": ("o[d] = o[d] / den;", "o[d] = o[d] / (den + 1.0);"),
 }
 
 
@@ -64,6 +73,11 @@ def _all_pins():
                  lambda fmt=fmt: att.test_compaction(fmt)]
     for args in [(F16, 4, 2, 64, 3), (Q8, 3, 4, 128, 4), (Q8, 2, 8, 256, 1)]:
         pins.append(lambda args=args: att.test_matches_torch_sdpa(*args))
+    pins += [lambda: chk.test_matches_torch_sdpa(1, 4, 128, 200, 37),
+             lambda: chk.test_matches_torch_sdpa(2, 2, 64, 96, 96),
+             chk.test_matches_paged_attention_over_an_fp16_pool,
+             chk.test_first_token_of_a_whole_prompt_sees_one_cell,
+             chk.test_equal_keys_give_the_running_mean_of_v]
     return pins
 
 
