@@ -9,6 +9,7 @@
  *   kvq_decode_attn  GQA attention of 1..W query tokens against the pool,
  *                    as split-K partials merged by a log-sum-exp combine
  *   kvq_compact_f16  the pool copied out to contiguous FP16 staging
+ *   kvq_chunk_attn   attention of a prompt chunk over that staging
  *
  * Sources (page title, section):
  *   [kv-q8 PR]  "#3084 qwen35: FP16 K/V cache by default, int8 with --kv-q8
@@ -197,6 +198,29 @@ kvq_status kvq_decode_attn(const kvq_cache *cache, const float *q, int n_seq, in
  */
 kvq_status kvq_compact_f16(const kvq_cache *cache, const int32_t *block_table_row, int n_cells,
                            void *out_k, void *out_v, void *stream);
+
+/*
+ * Attention of a prompt chunk over the FP16 staging ([kv-q8 PR], "Extra
+ * Notes": the prompt chunk's Q K^T and P V products read the contiguous
+ * [kvh][P][HD] fp16 halves that k_kv_f16 writes).
+ *
+ *   k16, v16   device fp16 [n_kv_heads][P][head_dim], 16-byte aligned: the
+ *              sequence's P cells as kvq_compact_f16 writes them
+ *   q          device fp32 [T][n_q][head_dim], 16-byte aligned: the chunk's
+ *              T query tokens, which are the sequence's last T cells
+ *   out        device fp32 [T][n_q][head_dim], 16-byte aligned
+ *
+ * Token t attends to cells [0, P - T + t] (causal); query head h reads KV
+ * head h / (n_q / n_kv_heads).  out = softmax(sm_scale * q . K^T) V with
+ * fp32 accumulation (q enters the tensor cores as an fp16 hi + lo pair, the
+ * softmax weights likewise).  head_dim in {64, 128, 256}; 1 <= T <= P;
+ * n_q a multiple of n_kv_heads; n_kv_heads * P < 2^31.  Invalid arguments
+ * return KVQ_ERR_ARG / KVQ_ERR_UNSUPPORTED before any launch.  Asynchronous
+ * on `stream`; the library allocates nothing.
+ */
+kvq_status kvq_chunk_attn(const void *k16, const void *v16, int n_kv_heads, int P, int head_dim,
+                          const float *q, int T, int n_q, float sm_scale, float *out,
+                          void *stream);
 
 /*
  * Bytes of device scratch that kvq_decode_attn_static keeps in the library

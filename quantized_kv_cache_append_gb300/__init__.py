@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = (
     "kvq_decode_workspace_bytes",
     "kvq_decode_attn",
     "kvq_compact_f16",
+    "kvq_chunk_attn",
     "kvq_decode_attn_static",
     "kvq_status_string",
 )
@@ -91,6 +92,8 @@ def load_library(path: Optional[str] = None):
     lib.kvq_decode_attn.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P, Z, P]
     lib.kvq_compact_f16.restype = I
     lib.kvq_compact_f16.argtypes = [CP, P, I, P, P, P]
+    lib.kvq_chunk_attn.restype = I
+    lib.kvq_chunk_attn.argtypes = [P, P, I, I, I, P, I, I, ctypes.c_float, P, P]
     lib.kvq_decode_attn_static.restype = I
     lib.kvq_decode_attn_static.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P]
     lib.kvq_status_string.restype = ctypes.c_char_p
@@ -158,6 +161,12 @@ def kvq_compact_f16(cache: kvq_cache, block_table_row, n_cells: int, out_k, out_
                     stream=None) -> int:
     return load_library().kvq_compact_f16(ctypes.byref(cache), _ptr(block_table_row), n_cells,
                                           _ptr(out_k), _ptr(out_v), _stream(stream))
+
+
+def kvq_chunk_attn(k16, v16, n_kv_heads: int, P: int, head_dim: int, q, T: int, n_q: int,
+                   sm_scale: float, out, stream=None) -> int:
+    return load_library().kvq_chunk_attn(_ptr(k16), _ptr(v16), n_kv_heads, P, head_dim, _ptr(q),
+                                         T, n_q, float(sm_scale), _ptr(out), _stream(stream))
 
 
 def kvq_decode_attn_static(cache: kvq_cache, q, n_seq: int, W: int, n_q: int, ctx_lens,

@@ -270,6 +270,34 @@ KVQ_API kvq_status kvq_compact_f16(const kvq_cache* cache, const int32_t* block_
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+KVQ_API kvq_status kvq_chunk_attn(const void* k16, const void* v16, int n_kv_heads, int P,
+                                  int head_dim, const float* q, int T, int n_q, float sm_scale,
+                                  float* out, void* stream) {
+  if (k16 == nullptr || v16 == nullptr || q == nullptr || out == nullptr) return KVQ_ERR_ARG;
+  if (!aligned(k16, 16) || !aligned(v16, 16) || !aligned(q, 16) || !aligned(out, 16))
+    return KVQ_ERR_ARG;
+  if (n_kv_heads <= 0 || P <= 0 || T <= 0 || T > P || n_q <= 0 || n_q % n_kv_heads != 0)
+    return KVQ_ERR_ARG;
+  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return KVQ_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if ((long long)n_kv_heads * P >= (1LL << 31) || (long long)T * n_q >= (1LL << 31) ||
+      n_kv_heads > 65535)
+    return KVQ_ERR_UNSUPPORTED;
+  ChunkArgs a;
+  a.k16 = static_cast<const __half*>(k16);
+  a.v16 = static_cast<const __half*>(v16);
+  a.q = q;
+  a.out = out;
+  a.n_kv = n_kv_heads;
+  a.P = P;
+  a.T = T;
+  a.n_q = n_q;
+  a.G = n_q / n_kv_heads;
+  a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
+  const cudaError_t e = launch_chunk_attn(head_dim, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 KVQ_API const char* kvq_status_string(int status) {
   switch (status) {
     case KVQ_OK: return "KVQ_OK";

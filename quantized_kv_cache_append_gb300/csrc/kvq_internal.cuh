@@ -89,4 +89,19 @@ int mma_ctas_per_sm(int fmt, int hd, int rows);
 cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, const DecodeArgs& a,
                                       cudaStream_t s);
 
+// The driver's cuTensorMapEncodeTiled (version 12000), looked up once; null
+// if the driver does not provide it.
+void* tensor_map_encoder();
+
+// Prompt-chunk attention over fp16 staging (kvq_chunk.cu).
+struct ChunkArgs {
+  const __half* k16;   // [n_kv][P][hd]
+  const __half* v16;
+  const float* q;      // [T][n_q][hd]
+  float* out;          // [T][n_q][hd]
+  int n_kv, P, T, n_q, G;
+  float qscale;        // sm_scale * log2(e)
+};
+cudaError_t launch_chunk_attn(int hd, const ChunkArgs& a, cudaStream_t s);
+
 }  // namespace kvq
