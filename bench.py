@@ -314,6 +314,8 @@ def run_kvq(args):
         torch.cuda.synchronize()
         compact_us[name] = a.elapsed_time(b) / (4 * LAYERS) * 1e3
 
+    chunk = _chunk_attn_bench(torch, kvq)
+
     peak, peak_kind = _peaks()
     avg_bytes = {n: sum(v) / len(v) for n, v in bytes_per_step.items()}
     gbs = {n: avg_bytes[n] / (kernel_ms[n] * 1e-3) / 1e9 for n in kernel_ms}
@@ -348,6 +350,7 @@ def run_kvq(args):
                        for n in kernel_ms},
             "append": {"bulk_Mcells_per_s": {n: round(v, 1) for n, v in append_mcells.items()},
                        "one_cell_step_us": round(append_step_us, 3)},
+            "chunk_attn": chunk,
             "compact_f16": {n: {"us": round(compact_us[n], 3),
                                 "GB/s": round(L * n_kv * (_row_bytes(n == "q8", hd) + 4 * hd)
                                               / (compact_us[n] * 1e-6) / 1e9, 1),
@@ -362,6 +365,49 @@ def run_kvq(args):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def _chunk_attn_bench(torch, kvq):
+    """Prompt-chunk attention at the chunk_verify sizes: a 4096-token chunk
+    at the end of 131072 cells, 32/8 heads, head_dim 128, over fp16 staging;
+    synthetic N(0, 1) staging and queries.  Tensor-bound: algorithmic flops
+    are 4 * head_dim per (query head, visible cell) -- q.k and p.v -- against
+    the measured dense bf16 peak (fp16 runs at the same nominal rate)."""
+    n_kv, n_q, hd, P, T = 8, 32, 128, 131072, 4096
+    g = torch.Generator(device="cuda").manual_seed(1005)
+    k16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
+    v16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
+    q = torch.randn(T, n_q, hd, device="cuda", generator=g)
+    out = torch.empty_like(q)
+    sm = float(1.0 / np.sqrt(hd))
+
+    def run():
+        st = kvq.kvq_chunk_attn(k16, v16, n_kv, P, hd, q, T, n_q, sm, out)
+        if st != kvq.KVQ_OK:
+            raise RuntimeError(kvq.kvq_status_string(st))
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    a.record()
+    for _ in range(reps):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    flops = 4.0 * hd * n_q * (T * (P - T) + T * (T + 1) / 2)
+    tflops = flops / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured bf16 dense"
+    except Exception:
+        peak, kind = 1900.0, "fallback bf16 dense"
+    return {"workload": "4096-token chunk over 131072 cells, 32/8 heads, head_dim 128",
+            "ms": round(ms, 3), "TFLOP/s": round(tflops, 1), "peak_TFLOP/s": peak,
+            "peak_kind": kind, "frac": round(tflops / peak, 4),
+            "note": "mma.sync m16n8k16 with fp16 hi+lo q and p: 2 MMAs per algorithmic one"}
 
 
 def _decode_sources_sha() -> str:
