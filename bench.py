@@ -47,6 +47,18 @@ def _dist():
     return rank, world, local
 
 
+def _max_over_ranks(x: float, dist, world: int, device) -> float:
+    """The largest x over all ranks (the timed region is as long as the
+    slowest rank's); x itself at world size 1."""
+    if world <= 1:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _row_bytes(fmt_q8: bool, hd: int) -> int:
     """Cache bytes per (cell, KV head): K and V codes (+ fp16 scale per 64 dims)."""
     return 2 * (hd + 2 * (hd // 64)) if fmt_q8 else 2 * 2 * hd
@@ -265,10 +277,7 @@ def run_kvq(args):
         dist.barrier()
     ms = e0.elapsed_time(e1)
     clock_info = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(ms, dist, world, "cuda")
     value = total_bytes * world / (ms * 1e-3) / 1e9
 
     # per-kernel durations: graphs of decode-only steps, one format at a time
@@ -482,10 +491,7 @@ def _e2e(step_fn, torch, layers, wl, bt, cap, L, n_kv, hd, K, W, world, dist):
         ctx = _step_ctx(s, L)
         total += ctx * n_kv * (_row_bytes(False, hd) + _row_bytes(True, hd))
     dt = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dt], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = _max_over_ranks(dt, dist, world, "cuda")
     return {"value": round(total * world / dt / 1e9, 2), "unit": "GB/s", "steps": K,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt / K * 1e3, 4)}
