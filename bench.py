@@ -570,6 +570,21 @@ def run_profile_case(args):
 
     kvq.build()
     kvq.load_library()
+    if args.profile_workload == "chunk":
+        # prompt-chunk attention: a 4096-token chunk over 32768 cells of fp16
+        # staging, 32/8 heads, head_dim 128 (134 MB of staging, above L2)
+        n_kv, n_q, hd, P, T = 8, 32, 128, 32768, 4096
+        g = torch.Generator(device="cuda").manual_seed(1005)
+        k16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
+        v16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
+        q = torch.randn(T, n_q, hd, device="cuda", generator=g)
+        out = torch.empty_like(q)
+        for _ in range(args.profile_reps):
+            st = kvq.kvq_chunk_attn(k16, v16, n_kv, P, hd, q, T, n_q, float(1 / np.sqrt(hd)), out)
+            assert st == kvq.KVQ_OK, kvq.kvq_status_string(st)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "chunk", "reps": args.profile_reps}))
+        return
     wl = workloads.make(args.profile_workload)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     bt = dev(wl.block_table)
