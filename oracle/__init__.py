@@ -65,6 +65,10 @@ def _bind(lib):
                                   ctypes.c_float, P]
     lib.kvo_compact_f16.restype = I
     lib.kvo_compact_f16.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, P]
+    lib.kvo_gather_cells.restype = I
+    lib.kvo_gather_cells.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, P, P, P]
+    lib.kvo_scatter_cells.restype = I
+    lib.kvo_scatter_cells.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, P, P, P]
     lib.kvo_chunk_attention.restype = I
     lib.kvo_chunk_attention.argtypes = [I, I, I, P, P, P, I, I, ctypes.c_float, P]
     return lib
@@ -259,3 +263,38 @@ def chunk_attention(k16, v16, q, sm_scale: float) -> np.ndarray:
     if rc != 0:
         raise RuntimeError(f"kvo_chunk_attention failed: {rc}")
     return out
+
+
+def gather_cells(pool: PoolImage, block_table_row, n_cells: int):
+    """Cells [0, n_cells) of one sequence, token-major: (codes_k, codes_v,
+    scales_k, scales_v) with codes [n_cells][n_kv][hd] (uint16 fp16 bits or
+    int8) and scales [n_cells][n_kv][hd/64] uint16 (None for fp16)."""
+    bt = _c(block_table_row, np.int32)
+    cdt = np.uint16 if pool.fmt == FMT_F16 else np.int8
+    ck = np.empty((n_cells, pool.n_kv, pool.head_dim), dtype=cdt)
+    cv = np.empty_like(ck)
+    sk = sv = None
+    if pool.fmt == FMT_Q8:
+        sk = np.empty((n_cells, pool.n_kv, pool.head_dim // 64), dtype=np.uint16)
+        sv = np.empty_like(sk)
+    rc = _load().kvo_gather_cells(*pool.geometry(), _ptr(pool.k), _ptr(pool.v), _ptr(pool.ks),
+                                  _ptr(pool.vs), _ptr(bt), n_cells, _ptr(ck), _ptr(cv),
+                                  _ptr(sk), _ptr(sv))
+    if rc != 0:
+        raise RuntimeError(f"kvo_gather_cells failed: {rc}")
+    return ck, cv, sk, sv
+
+
+def scatter_cells(pool: PoolImage, block_table_row, codes_k, codes_v, scales_k=None,
+                  scales_v=None) -> None:
+    """Write token-major cells back into the pool (the inverse of gather_cells)."""
+    bt = _c(block_table_row, np.int32)
+    cdt = np.uint16 if pool.fmt == FMT_F16 else np.int8
+    ck, cv = _c(codes_k, cdt), _c(codes_v, cdt)
+    sk = None if scales_k is None else _c(scales_k, np.uint16)
+    sv = None if scales_v is None else _c(scales_v, np.uint16)
+    rc = _load().kvo_scatter_cells(*pool.geometry(), _ptr(pool.k), _ptr(pool.v), _ptr(pool.ks),
+                                   _ptr(pool.vs), _ptr(bt), ck.shape[0], _ptr(ck), _ptr(cv),
+                                   _ptr(sk), _ptr(sv))
+    if rc != 0:
+        raise RuntimeError(f"kvo_scatter_cells failed: {rc}")

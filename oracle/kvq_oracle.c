@@ -447,3 +447,88 @@ int kvo_chunk_attention(int n_kv, int P, int hd, const uint16_t *k16, const uint
     free(z);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Persistence: gather a sequence's cells out of the pool and scatter them   */
+/* back ([Path F v3], "Scope": the saved body is the used cells' K/V bytes   */
+/* followed by their scales, token-major; [k8v4 PR, "How"]: a block's runs   */
+/* are its codes, then its scales).  Int8 codes never move without their     */
+/* scales ([Path F v3], "Why": int8 bytes without scales hydrate to garbage). */
+/* ------------------------------------------------------------------------ */
+
+static int64_t seq_row(const int32_t *block_table_row, int n_blocks, int n_kv, int block_size,
+                       int pos, int kvh)
+{
+    const int32_t blk = block_table_row[pos / block_size];
+    if (blk < 0 || blk >= n_blocks)
+        return -1;
+    return ((int64_t)blk * n_kv + kvh) * block_size + pos % block_size;
+}
+
+int kvo_gather_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                     const void *k_data, const void *v_data,
+                     const uint16_t *k_scales, const uint16_t *v_scales,
+                     const int32_t *block_table_row, int n_cells,
+                     void *codes_k, void *codes_v, uint16_t *scales_k, uint16_t *scales_v)
+{
+    if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0 || n_cells < 0)
+        return -1;
+    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL || scales_k == NULL ||
+                              scales_v == NULL))
+        return -2;
+    const size_t esz = fmt == KVO_FMT_F16 ? 2 : 1;
+    const int ng = hd / KVO_GROUP;
+    for (int p = 0; p < n_cells; ++p) {
+        for (int kvh = 0; kvh < n_kv; ++kvh) {
+            const int64_t row = seq_row(block_table_row, n_blocks, n_kv, block_size, p, kvh);
+            if (row < 0)
+                return -3;
+            const size_t dst = (size_t)p * n_kv + kvh;
+            memcpy((char *)codes_k + dst * hd * esz, (const char *)k_data + (size_t)row * hd * esz,
+                   hd * esz);
+            memcpy((char *)codes_v + dst * hd * esz, (const char *)v_data + (size_t)row * hd * esz,
+                   hd * esz);
+            if (fmt == KVO_FMT_Q8) {
+                for (int gi = 0; gi < ng; ++gi) {
+                    scales_k[dst * ng + gi] = k_scales[(size_t)row * ng + gi];
+                    scales_v[dst * ng + gi] = v_scales[(size_t)row * ng + gi];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+int kvo_scatter_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                      void *k_data, void *v_data, uint16_t *k_scales, uint16_t *v_scales,
+                      const int32_t *block_table_row, int n_cells,
+                      const void *codes_k, const void *codes_v,
+                      const uint16_t *scales_k, const uint16_t *scales_v)
+{
+    if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0 || n_cells < 0)
+        return -1;
+    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL || scales_k == NULL ||
+                              scales_v == NULL))
+        return -2;
+    const size_t esz = fmt == KVO_FMT_F16 ? 2 : 1;
+    const int ng = hd / KVO_GROUP;
+    for (int p = 0; p < n_cells; ++p) {
+        for (int kvh = 0; kvh < n_kv; ++kvh) {
+            const int64_t row = seq_row(block_table_row, n_blocks, n_kv, block_size, p, kvh);
+            if (row < 0)
+                return -3;
+            const size_t src = (size_t)p * n_kv + kvh;
+            memcpy((char *)k_data + (size_t)row * hd * esz, (const char *)codes_k + src * hd * esz,
+                   hd * esz);
+            memcpy((char *)v_data + (size_t)row * hd * esz, (const char *)codes_v + src * hd * esz,
+                   hd * esz);
+            if (fmt == KVO_FMT_Q8) {
+                for (int gi = 0; gi < ng; ++gi) {
+                    k_scales[(size_t)row * ng + gi] = scales_k[src * ng + gi];
+                    v_scales[(size_t)row * ng + gi] = scales_v[src * ng + gi];
+                }
+            }
+        }
+    }
+    return 0;
+}

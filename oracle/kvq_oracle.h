@@ -75,6 +75,22 @@ int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                     const int32_t *block_table_row, int n_cells,
                     uint16_t *out_k, uint16_t *out_v);
 
+/* Persistence: cells [0, n_cells) of one sequence gathered out of the pool
+ * into token-major runs, and scattered back.  codes_k / codes_v are
+ * [n_cells][n_kv][hd] elements of the pool's format (fp16 bits or int8);
+ * scales_k / scales_v [n_cells][n_kv][hd/64] fp16 bits, required for int8
+ * (-2 without them) and ignored for fp16. */
+int kvo_gather_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                     const void *k_data, const void *v_data,
+                     const uint16_t *k_scales, const uint16_t *v_scales,
+                     const int32_t *block_table_row, int n_cells,
+                     void *codes_k, void *codes_v, uint16_t *scales_k, uint16_t *scales_v);
+int kvo_scatter_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                      void *k_data, void *v_data, uint16_t *k_scales, uint16_t *v_scales,
+                      const int32_t *block_table_row, int n_cells,
+                      const void *codes_k, const void *codes_v,
+                      const uint16_t *scales_k, const uint16_t *scales_v);
+
 /* Attention of a prompt chunk over contiguous fp16 staging, float64.  The
  * staging k16/v16 [n_kv][P][hd] (fp16 bits) holds the sequence's P cells;
  * the chunk's T query tokens are its last T cells, so token t sees cells

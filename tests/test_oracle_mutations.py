@@ -14,6 +14,7 @@ import pytest
 import oracle
 from tests import test_oracle_attention as att
 from tests import test_oracle_chunk as chk
+from tests import test_oracle_persist as per
 from tests import test_oracle_fp16 as f16
 from tests import test_oracle_quant as qt
 
@@ -49,6 +50,14 @@ MUTATIONS = {
     "chunk_no_softmax_scale": ("z[c] = dot * (double)sm_scale;", "z[c] = dot;"),
     "chunk_k_reads_v": ("const uint16_t *kr = k16 +", "const uint16_t *kr = v16 +"),
     "chunk_no_normalisation": ("o[d] = o[d] / den;", "o[d] = o[d] / (den + 1.0);"),
+    "gather_v_from_k": ("memcpy((char *)codes_v + dst * hd * esz, (const char *)v_data +",
+                        "memcpy((char *)codes_v + dst * hd * esz, (const char *)k_data +"),
+    "gather_k_scales_from_v": ("scales_k[dst * ng + gi] = k_scales[(size_t)row * ng + gi];",
+                               "scales_k[dst * ng + gi] = v_scales[(size_t)row * ng + gi];"),
+    "persist_slot_off_by_one": ("return ((int64_t)blk * n_kv + kvh) * block_size + pos % block_size;",
+                                "return ((int64_t)blk * n_kv + kvh) * block_size + (pos + 1) % block_size;"),
+    "scatter_drops_v_scales": ("v_scales[(size_t)row * ng + gi] = scales_v[src * ng + gi];",
+                               "v_scales[(size_t)row * ng + gi] = scales_k[src * ng + gi];"),
 }
 
 
@@ -77,7 +86,11 @@ def _all_pins():
              lambda: chk.test_matches_torch_sdpa(2, 2, 64, 96, 96),
              chk.test_matches_paged_attention_over_an_fp16_pool,
              chk.test_first_token_of_a_whole_prompt_sees_one_cell,
-             chk.test_equal_keys_give_the_running_mean_of_v]
+             chk.test_equal_keys_give_the_running_mean_of_v,
+             per.test_int8_codes_without_scales_are_refused]
+    for fmt in (F16, Q8):
+        pins += [lambda fmt=fmt: per.test_gather_returns_the_stored_rows_in_order(fmt),
+                 lambda fmt=fmt: per.test_scatter_into_another_layout_then_gather_is_the_identity(fmt)]
     return pins
 
 
