@@ -10,6 +10,8 @@
  *                    as split-K partials merged by a log-sum-exp combine
  *   kvq_compact_f16  the pool copied out to contiguous FP16 staging
  *   kvq_chunk_attn   attention of a prompt chunk over that staging
+ *   kvq_gather_cells / kvq_scatter_cells
+ *                    a sequence's codes and scales out of / into the pool
  *
  * Sources (page title, section):
  *   [kv-q8 PR]  "#3084 qwen35: FP16 K/V cache by default, int8 with --kv-q8
@@ -221,6 +223,33 @@ kvq_status kvq_compact_f16(const kvq_cache *cache, const int32_t *block_table_ro
 kvq_status kvq_chunk_attn(const void *k16, const void *v16, int n_kv_heads, int P, int head_dim,
                           const float *q, int T, int n_q, float sm_scale, float *out,
                           void *stream);
+
+/*
+ * Persistence of one sequence: cells [0, n_cells) gathered out of the pool
+ * into token-major runs, and scattered back into a pool (Path F format v3:
+ * persist per-head INT8 KV scales for INT8 + persistent KV interop,
+ * "Scope": a saved turn is its used cells' K/V bytes followed by their
+ * scales; "Why": int8 bytes without the scales would hydrate to garbage).
+ *
+ *   block_table_row  device int32 [ceil(n_cells / block_size)]: the
+ *                    sequence's row of the block table
+ *   codes_k, codes_v device [n_cells][n_kv_heads][head_dim] elements of the
+ *                    pool's format (fp16 or int8), 16-byte aligned
+ *   scales_k, scales_v
+ *                    device fp16 [n_cells][n_kv_heads][head_dim / 64]; required
+ *                    for KVQ_Q8 (KVQ_ERR_ARG without them), ignored for KVQ_F16
+ *
+ * Both copy bits unchanged: a gather followed by a scatter into any pool
+ * of the same format and geometry, under any block table, restores the
+ * cells exactly.  Cells whose block id is out of range are skipped.
+ * n_cells == 0 is a no-op.  Asynchronous on `stream`.
+ */
+kvq_status kvq_gather_cells(const kvq_cache *cache, const int32_t *block_table_row, int n_cells,
+                            void *codes_k, void *codes_v, void *scales_k, void *scales_v,
+                            void *stream);
+kvq_status kvq_scatter_cells(const kvq_cache *cache, const int32_t *block_table_row, int n_cells,
+                             const void *codes_k, const void *codes_v, const void *scales_k,
+                             const void *scales_v, void *stream);
 
 /*
  * Bytes of device scratch that kvq_decode_attn_static keeps in the library

@@ -35,6 +35,8 @@ EXPORTED_SYMBOLS = (
     "kvq_decode_attn",
     "kvq_compact_f16",
     "kvq_chunk_attn",
+    "kvq_gather_cells",
+    "kvq_scatter_cells",
     "kvq_decode_attn_static",
     "kvq_status_string",
 )
@@ -94,6 +96,10 @@ def load_library(path: Optional[str] = None):
     lib.kvq_compact_f16.argtypes = [CP, P, I, P, P, P]
     lib.kvq_chunk_attn.restype = I
     lib.kvq_chunk_attn.argtypes = [P, P, I, I, I, P, I, I, ctypes.c_float, P, P]
+    lib.kvq_gather_cells.restype = I
+    lib.kvq_gather_cells.argtypes = [CP, P, I, P, P, P, P, P]
+    lib.kvq_scatter_cells.restype = I
+    lib.kvq_scatter_cells.argtypes = [CP, P, I, P, P, P, P, P]
     lib.kvq_decode_attn_static.restype = I
     lib.kvq_decode_attn_static.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P]
     lib.kvq_status_string.restype = ctypes.c_char_p
@@ -167,6 +173,20 @@ def kvq_chunk_attn(k16, v16, n_kv_heads: int, P: int, head_dim: int, q, T: int, 
                    sm_scale: float, out, stream=None) -> int:
     return load_library().kvq_chunk_attn(_ptr(k16), _ptr(v16), n_kv_heads, P, head_dim, _ptr(q),
                                          T, n_q, float(sm_scale), _ptr(out), _stream(stream))
+
+
+def kvq_gather_cells(cache: kvq_cache, block_table_row, n_cells: int, codes_k, codes_v,
+                     scales_k=None, scales_v=None, stream=None) -> int:
+    return load_library().kvq_gather_cells(ctypes.byref(cache), _ptr(block_table_row), n_cells,
+                                           _ptr(codes_k), _ptr(codes_v), _ptr(scales_k),
+                                           _ptr(scales_v), _stream(stream))
+
+
+def kvq_scatter_cells(cache: kvq_cache, block_table_row, n_cells: int, codes_k, codes_v,
+                      scales_k=None, scales_v=None, stream=None) -> int:
+    return load_library().kvq_scatter_cells(ctypes.byref(cache), _ptr(block_table_row), n_cells,
+                                            _ptr(codes_k), _ptr(codes_v), _ptr(scales_k),
+                                            _ptr(scales_v), _stream(stream))
 
 
 def kvq_decode_attn_static(cache: kvq_cache, q, n_seq: int, W: int, n_q: int, ctx_lens,

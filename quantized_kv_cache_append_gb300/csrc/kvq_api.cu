@@ -270,6 +270,57 @@ KVQ_API kvq_status kvq_compact_f16(const kvq_cache* cache, const int32_t* block_
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+namespace kvq {
+namespace {
+
+kvq_status persist_impl(const kvq_cache* cache, const int32_t* block_table_row, int n_cells,
+                        const void* codes_k, const void* codes_v, const void* scales_k,
+                        const void* scales_v, bool gather, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_cells < 0) return KVQ_ERR_ARG;
+  if (n_cells == 0) return KVQ_OK;
+  if (block_table_row == nullptr || codes_k == nullptr || codes_v == nullptr) return KVQ_ERR_ARG;
+  // int8 codes never move without their scales
+  if (cache->fmt == KVQ_Q8 && (scales_k == nullptr || scales_v == nullptr)) return KVQ_ERR_ARG;
+  if (!aligned(block_table_row, 4) || !aligned(codes_k, 16) || !aligned(codes_v, 16) ||
+      !aligned(scales_k, 2) || !aligned(scales_v, 2))
+    return KVQ_ERR_ARG;
+  if ((long long)n_cells * cache->n_kv_heads >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
+  PersistArgs a;
+  a.pool = make_pool(cache);
+  a.pool_k = cache->k_data;
+  a.pool_v = cache->v_data;
+  a.pool_ks = static_cast<__half*>(cache->k_scales);
+  a.pool_vs = static_cast<__half*>(cache->v_scales);
+  a.block_row = block_table_row;
+  a.n_cells = n_cells;
+  a.codes_k = const_cast<void*>(codes_k);
+  a.codes_v = const_cast<void*>(codes_v);
+  a.scales_k = static_cast<__half*>(const_cast<void*>(scales_k));
+  a.scales_v = static_cast<__half*>(const_cast<void*>(scales_v));
+  const cudaError_t e =
+      launch_persist(cache->fmt, cache->head_dim, gather, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace kvq
+
+KVQ_API kvq_status kvq_gather_cells(const kvq_cache* cache, const int32_t* block_table_row,
+                                    int n_cells, void* codes_k, void* codes_v, void* scales_k,
+                                    void* scales_v, void* stream) {
+  return kvq::persist_impl(cache, block_table_row, n_cells, codes_k, codes_v, scales_k, scales_v,
+                           true, stream);
+}
+
+KVQ_API kvq_status kvq_scatter_cells(const kvq_cache* cache, const int32_t* block_table_row,
+                                     int n_cells, const void* codes_k, const void* codes_v,
+                                     const void* scales_k, const void* scales_v, void* stream) {
+  return kvq::persist_impl(cache, block_table_row, n_cells, codes_k, codes_v, scales_k, scales_v,
+                           false, stream);
+}
+
 KVQ_API kvq_status kvq_chunk_attn(const void* k16, const void* v16, int n_kv_heads, int P,
                                   int head_dim, const float* q, int T, int n_q, float sm_scale,
                                   float* out, void* stream) {

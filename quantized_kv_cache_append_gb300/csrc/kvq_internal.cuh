@@ -70,10 +70,26 @@ struct CompactArgs {
   __half* out_v;
 };
 
+// A sequence's cells between the pool and token-major runs (kvq_persist.cu).
+struct PersistArgs {
+  Pool pool;               // the pool, read by the gather
+  void* pool_k;            // the same arrays, written by the scatter
+  void* pool_v;
+  __half* pool_ks;
+  __half* pool_vs;
+  const int32_t* block_row;
+  int n_cells;
+  void* codes_k;           // [n_cells][n_kv][hd]: written by gather, read by scatter
+  void* codes_v;
+  __half* scales_k;        // [n_cells][n_kv][hd/64] (int8 only)
+  __half* scales_v;
+};
+
 // Launchers (host side, one per translation unit).  They return the launch
 // status from the runtime.
 cudaError_t launch_append(int fmt, int hd, const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s);
+cudaError_t launch_persist(int fmt, int hd, bool gather, const PersistArgs& a, cudaStream_t s);
 bool decode_supported(int fmt, int hd, int rows);
 int decode_rows_pad(int hd, int rows);
 int decode_cell_tile();

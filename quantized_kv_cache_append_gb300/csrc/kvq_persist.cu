@@ -1,0 +1,99 @@
+// kvq_persist.cu -- a sequence's cells gathered out of the paged pool into
+// token-major runs, and scattered back.
+//
+// Path F format v3: persist per-head INT8 KV scales for INT8 + persistent
+// KV interop, "Scope": what a saved turn keeps is its used cells' K/V bytes
+// followed by their scales, token-major, and "Why": int8 bytes without the
+// scales would hydrate to garbage, so int8 codes never move without them.
+// #711 kv: --kv k8v4 streams with --kv-resident, "How": a block moves as its
+// byte runs (codes, then scales).
+//
+// Runs: codes [n_cells][n_kv][hd] in the pool's element type, scales
+// [n_cells][n_kv][hd/64] fp16 (int8 only).  One thread moves 16 bytes of a
+// row of K and the same 16 bytes of V; the thread that takes a row's first
+// chunk also moves its scales.  Loads and stores are coalesced along the
+// row, then the KV heads, then the cells.  A block id out of range skips
+// its cells (the gather leaves them unwritten, the scatter writes nothing).
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+template <int FMT, int HD, bool GATHER>
+__global__ void __launch_bounds__(256) persist_kernel(PersistArgs a) {
+  constexpr int ESZ = FMT == KVQ_F16 ? 2 : 1;
+  constexpr int CPR = HD * ESZ / 16;  // 16-byte chunks per row
+  constexpr int NG = HD / kGroup;
+  const long long rows = (long long)a.n_cells * a.pool.n_kv;
+  const long long total = rows * CPR;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const int bs = 1 << a.pool.bs_log2;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int chunk = (int)(i % CPR);
+    const long long r = i / CPR;  // p * n_kv + kvh (token-major)
+    const int p = (int)(r / a.pool.n_kv);
+    const int kvh = (int)(r - (long long)p * a.pool.n_kv);
+    const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
+    if (blk < 0 || blk >= a.pool.n_blocks) continue;
+    const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+    const size_t pool_off = row * HD * ESZ + (size_t)chunk * 16;
+    const size_t run_off = (size_t)r * HD * ESZ + (size_t)chunk * 16;
+    if constexpr (GATHER) {
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.codes_k) + run_off) =
+          __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.pool.k) + pool_off));
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.codes_v) + run_off) =
+          __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.pool.v) + pool_off));
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.pool_k) + pool_off) =
+          __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.codes_k) + run_off));
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.pool_v) + pool_off) =
+          __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.codes_v) + run_off));
+    }
+    if constexpr (FMT == KVQ_Q8) {
+      if (chunk == 0) {
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+          if constexpr (GATHER) {
+            a.scales_k[(size_t)r * NG + gi] = a.pool.ks[row * NG + gi];
+            a.scales_v[(size_t)r * NG + gi] = a.pool.vs[row * NG + gi];
+          } else {
+            a.pool_ks[row * NG + gi] = a.scales_k[(size_t)r * NG + gi];
+            a.pool_vs[row * NG + gi] = a.scales_v[(size_t)r * NG + gi];
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int FMT, bool GATHER>
+cudaError_t launch_fmt(int hd, const PersistArgs& a, cudaStream_t s, int blocks) {
+  switch (hd) {
+    case 64: persist_kernel<FMT, 64, GATHER><<<blocks, 256, 0, s>>>(a); break;
+    case 128: persist_kernel<FMT, 128, GATHER><<<blocks, 256, 0, s>>>(a); break;
+    case 256: persist_kernel<FMT, 256, GATHER><<<blocks, 256, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_persist(int fmt, int hd, bool gather, const PersistArgs& a, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int esz = fmt == KVQ_F16 ? 2 : 1;
+  const long long total = (long long)a.n_cells * a.pool.n_kv * (hd * esz / 16);
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;  // grid-stride beyond 8 CTAs/SM
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (fmt == KVQ_F16)
+    return gather ? launch_fmt<KVQ_F16, true>(hd, a, s, (int)blocks)
+                  : launch_fmt<KVQ_F16, false>(hd, a, s, (int)blocks);
+  return gather ? launch_fmt<KVQ_Q8, true>(hd, a, s, (int)blocks)
+                : launch_fmt<KVQ_Q8, false>(hd, a, s, (int)blocks);
+}
+
+}  // namespace kvq
