@@ -325,6 +325,31 @@ def run_kvq(args):
 
     chunk = _chunk_attn_bench(torch, kvq)
 
+    # gather / scatter of a whole layer's sequence (32768 cells), both formats
+    persist_us = {}
+    for name in ("f16", "q8"):
+        pool0 = layers[0][name][0]
+        cdt = torch.float16 if name == "f16" else torch.int8
+        ck = torch.empty((L, n_kv, hd), dtype=cdt, device="cuda")
+        cvv = torch.empty_like(ck)
+        sk = sv = None
+        if name == "q8":
+            sk = torch.empty((L, n_kv, hd // 64), dtype=torch.float16, device="cuda")
+            sv = torch.empty_like(sk)
+        times = {}
+        for op, fn in (("gather", kvq.kvq_gather_cells), ("scatter", kvq.kvq_scatter_cells)):
+            for _ in range(3):
+                fn(pool0.cache, bt[0], L, ck, cvv, sk, sv)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(10):
+                fn(pool0.cache, bt[0], L, ck, cvv, sk, sv)
+            b.record()
+            torch.cuda.synchronize()
+            times[op] = a.elapsed_time(b) / 10 * 1e3
+        persist_us[name] = times
+
     peak, peak_kind = _peaks()
     avg_bytes = {n: sum(v) / len(v) for n, v in bytes_per_step.items()}
     gbs = {n: avg_bytes[n] / (kernel_ms[n] * 1e-3) / 1e9 for n in kernel_ms}
@@ -360,6 +385,11 @@ def run_kvq(args):
             "append": {"bulk_Mcells_per_s": {n: round(v, 1) for n, v in append_mcells.items()},
                        "one_cell_step_us": round(append_step_us, 3)},
             "chunk_attn": chunk,
+            "persist": {n: {op: {"us": round(t, 3),
+                                 "GB/s": round(2 * L * n_kv * _row_bytes(n == "q8", hd)
+                                               / (t * 1e-6) / 1e9, 1)}
+                            for op, t in persist_us[n].items()}
+                        for n in persist_us},
             "compact_f16": {n: {"us": round(compact_us[n], 3),
                                 "GB/s": round(L * n_kv * (_row_bytes(n == "q8", hd) + 4 * hd)
                                               / (compact_us[n] * 1e-6) / 1e9, 1),
