@@ -23,7 +23,9 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "libkvq_oracle.so")
 
 FMT_F16 = 0
 FMT_Q8 = 1
+FMT_K8V4 = 2
 GROUP = 64
+Q4_BLOCK = 32
 
 # No FMA contraction and no fast-math: float division, fabsf and rintf keep
 # their IEEE meaning (round-to-nearest-even is the default mode).
@@ -58,6 +60,10 @@ def _bind(lib):
     lib.kvo_fp16_to_float_array.argtypes = [P, P, ctypes.c_int64]
     lib.kvo_quantize_row_q8.restype = I
     lib.kvo_quantize_row_q8.argtypes = [P, I, P, P]
+    lib.kvo_quantize_row_q4r.restype = I
+    lib.kvo_quantize_row_q4r.argtypes = [P, I, P, P]
+    lib.kvo_hadamard_f32.restype = None
+    lib.kvo_hadamard_f32.argtypes = [P, I]
     lib.kvo_append.restype = I
     lib.kvo_append.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, P, P, P, I]
     lib.kvo_attention.restype = I
@@ -173,6 +179,47 @@ def quantize_rows_q8(x):
     return codes.reshape(x.shape), scales.reshape(x.shape[:-1] + (hd // GROUP,))
 
 
+def hadamard_f32(x):
+    """Unnormalised Walsh-Hadamard transform of rows of x [..., n] in float32
+    (the oracle's butterfly order); n a power of two."""
+    x = _c(x, np.float32).copy()
+    n = x.shape[-1]
+    rows = x.reshape(-1, n)
+    lib = _load()
+    for i in range(rows.shape[0]):
+        lib.kvo_hadamard_f32(_ptr(rows[i]), n)
+    return rows.reshape(x.shape)
+
+
+def quantize_rows_q4r(x):
+    """K8V4's V rows: rotate, then Q4_0 per 32 rotated dims.  x [..., hd] ->
+    (codes uint8 [..., hd/2] packed nibbles, scales uint16 [..., hd/32])."""
+    x = _c(x, np.float32)
+    hd = x.shape[-1]
+    rows = x.reshape(-1, hd)
+    codes = np.empty((rows.shape[0], hd // 2), dtype=np.uint8)
+    scales = np.empty((rows.shape[0], hd // Q4_BLOCK), dtype=np.uint16)
+    lib = _load()
+    for i in range(rows.shape[0]):
+        rc = lib.kvo_quantize_row_q4r(_ptr(rows[i]), hd, _ptr(codes[i]), _ptr(scales[i]))
+        if rc != 0:
+            raise RuntimeError(f"kvo_quantize_row_q4r failed: {rc}")
+    return (codes.reshape(x.shape[:-1] + (hd // 2,)),
+            scales.reshape(x.shape[:-1] + (hd // Q4_BLOCK,)))
+
+
+def row_layout(fmt: int, head_dim: int):
+    """(K element dtype, K elements per row, V dtype, V elements per row, K
+    scales per row, V scales per row) of a pool row in each format."""
+    if fmt == FMT_F16:
+        return np.uint16, head_dim, np.uint16, head_dim, 0, 0
+    if fmt == FMT_Q8:
+        return np.int8, head_dim, np.int8, head_dim, head_dim // GROUP, head_dim // GROUP
+    if fmt == FMT_K8V4:
+        return np.int8, head_dim, np.uint8, head_dim // 2, head_dim // GROUP, head_dim // Q4_BLOCK
+    raise ValueError(f"unknown format {fmt}")
+
+
 # --------------------------------------------------------------------------
 # paged cache image
 # --------------------------------------------------------------------------
@@ -183,17 +230,12 @@ class PoolImage:
     def __init__(self, fmt: int, n_kv: int, head_dim: int, block_size: int, n_blocks: int):
         self.fmt, self.n_kv, self.head_dim = fmt, n_kv, head_dim
         self.block_size, self.n_blocks = block_size, n_blocks
-        shape = (n_blocks, n_kv, block_size, head_dim)
-        dt = np.uint16 if fmt == FMT_F16 else np.int8
-        self.k = np.zeros(shape, dtype=dt)
-        self.v = np.zeros(shape, dtype=dt)
-        if fmt == FMT_Q8:
-            sshape = (n_blocks, n_kv, block_size, head_dim // GROUP)
-            self.ks = np.zeros(sshape, dtype=np.uint16)
-            self.vs = np.zeros(sshape, dtype=np.uint16)
-        else:
-            self.ks = None
-            self.vs = None
+        kdt, kn, vdt, vn, kng, vng = row_layout(fmt, head_dim)
+        lead = (n_blocks, n_kv, block_size)
+        self.k = np.zeros(lead + (kn,), dtype=kdt)
+        self.v = np.zeros(lead + (vn,), dtype=vdt)
+        self.ks = np.zeros(lead + (kng,), dtype=np.uint16) if kng else None
+        self.vs = np.zeros(lead + (vng,), dtype=np.uint16) if vng else None
 
     def geometry(self):
         return (self.fmt, self.n_kv, self.head_dim, self.block_size, self.n_blocks)
@@ -268,15 +310,14 @@ def chunk_attention(k16, v16, q, sm_scale: float) -> np.ndarray:
 def gather_cells(pool: PoolImage, block_table_row, n_cells: int):
     """Cells [0, n_cells) of one sequence, token-major: (codes_k, codes_v,
     scales_k, scales_v) with codes [n_cells][n_kv][hd] (uint16 fp16 bits or
-    int8) and scales [n_cells][n_kv][hd/64] uint16 (None for fp16)."""
+    int8) and scales [n_cells][n_kv][hd/64] uint16 (None for fp16); K8V4's V
+    codes are uint8 [..][hd/2] and its V scales [..][hd/32]."""
     bt = _c(block_table_row, np.int32)
-    cdt = np.uint16 if pool.fmt == FMT_F16 else np.int8
-    ck = np.empty((n_cells, pool.n_kv, pool.head_dim), dtype=cdt)
-    cv = np.empty_like(ck)
-    sk = sv = None
-    if pool.fmt == FMT_Q8:
-        sk = np.empty((n_cells, pool.n_kv, pool.head_dim // 64), dtype=np.uint16)
-        sv = np.empty_like(sk)
+    kdt, kn, vdt, vn, kng, vng = row_layout(pool.fmt, pool.head_dim)
+    ck = np.empty((n_cells, pool.n_kv, kn), dtype=kdt)
+    cv = np.empty((n_cells, pool.n_kv, vn), dtype=vdt)
+    sk = np.empty((n_cells, pool.n_kv, kng), dtype=np.uint16) if kng else None
+    sv = np.empty((n_cells, pool.n_kv, vng), dtype=np.uint16) if vng else None
     rc = _load().kvo_gather_cells(*pool.geometry(), _ptr(pool.k), _ptr(pool.v), _ptr(pool.ks),
                                   _ptr(pool.vs), _ptr(bt), n_cells, _ptr(ck), _ptr(cv),
                                   _ptr(sk), _ptr(sv))
@@ -289,8 +330,8 @@ def scatter_cells(pool: PoolImage, block_table_row, codes_k, codes_v, scales_k=N
                   scales_v=None) -> None:
     """Write token-major cells back into the pool (the inverse of gather_cells)."""
     bt = _c(block_table_row, np.int32)
-    cdt = np.uint16 if pool.fmt == FMT_F16 else np.int8
-    ck, cv = _c(codes_k, cdt), _c(codes_v, cdt)
+    kdt, _, vdt, _, _, _ = row_layout(pool.fmt, pool.head_dim)
+    ck, cv = _c(codes_k, kdt), _c(codes_v, vdt)
     sk = None if scales_k is None else _c(scales_k, np.uint16)
     sv = None if scales_v is None else _c(scales_v, np.uint16)
     rc = _load().kvo_scatter_cells(*pool.geometry(), _ptr(pool.k), _ptr(pool.v), _ptr(pool.ks),

@@ -188,19 +188,79 @@ static int64_t cell_row(const int32_t *block_table, int max_blocks_per_seq,
 
 static int check_geometry(int fmt, int n_kv, int hd, int block_size, int n_blocks)
 {
-    if (fmt != KVO_FMT_F16 && fmt != KVO_FMT_Q8)
+    if (fmt != KVO_FMT_F16 && fmt != KVO_FMT_Q8 && fmt != KVO_FMT_K8V4)
         return -1;
     if (n_kv <= 0 || hd <= 0 || block_size <= 0 || n_blocks <= 0)
         return -1;
-    if (fmt == KVO_FMT_Q8 && hd % KVO_GROUP != 0)
+    if (fmt != KVO_FMT_F16 && hd % KVO_GROUP != 0)
         return -1;
+    if (fmt == KVO_FMT_K8V4 && (hd & (hd - 1)) != 0) /* the rotation needs a power of two */
+        return -1;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* K8V4: int8 K and rotated Q4_0 V ([k8v4 PR], "What": INT8 K + rotated Q4_0  */
+/* V, 816 B/cell).  The page names the rotation but not which one: here the  */
+/* Walsh-Hadamard transform (entries +-1, applied by butterflies in fp32),   */
+/* which spreads a row's outliers over all its dims before 4-bit codes, and  */
+/* whose inverse is itself divided by hd (a power of two, so exact).         */
+/* ------------------------------------------------------------------------ */
+
+void kvo_hadamard_f32(float *x, int n)
+{
+    for (int h = 1; h < n; h *= 2)
+        for (int i = 0; i < n; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                const float a = x[j], b = x[j + h];
+                x[j] = a + b;
+                x[j + h] = a - b;
+            }
+}
+
+int kvo_quantize_row_q4r(const float *x, int hd, uint8_t *codes, uint16_t *scales)
+{
+    if (hd <= 0 || hd % KVO_Q4_BLOCK != 0 || (hd & (hd - 1)) != 0 || hd > 4096)
+        return -1;
+    float y[4096];
+    memcpy(y, x, sizeof(float) * (size_t)hd);
+    kvo_hadamard_f32(y, hd);
+    for (int b0 = 0; b0 < hd; b0 += KVO_Q4_BLOCK) {
+        float m = 0.0f;
+        for (int i = b0; i < b0 + KVO_Q4_BLOCK; ++i)
+            if (fabsf(y[i]) > fabsf(m))
+                m = y[i];
+        const uint16_t d16 = kvo_fp16_from_float(m / -8.0f);
+        const float d = kvo_fp16_to_float(d16);
+        scales[b0 / KVO_Q4_BLOCK] = d16;
+        for (int i = b0; i < b0 + KVO_Q4_BLOCK; i += 2) {
+            int c[2];
+            for (int e = 0; e < 2; ++e) {
+                c[e] = 8;
+                if (d != 0.0f) {
+                    float r = rintf(y[i + e] / d);
+                    if (!(r == r))
+                        r = 0.0f;
+                    if (r < -8.0f)
+                        r = -8.0f;
+                    if (r > 7.0f)
+                        r = 7.0f;
+                    c[e] = (int)r + 8;
+                }
+            }
+            codes[i / 2] = (uint8_t)(c[0] | (c[1] << 4));
+        }
+    }
     return 0;
 }
 
 /* Store one row (one cell, one KV head) of K or V at pool row `row`. */
 static int store_row(int fmt, int hd, void *data, uint16_t *scales, int64_t row,
-                     const float *x)
+                     const float *x, int is_v)
 {
+    if (fmt == KVO_FMT_K8V4 && is_v)
+        return kvo_quantize_row_q4r(x, hd, (uint8_t *)data + (size_t)row * (hd / 2),
+                                    scales + (size_t)row * (hd / KVO_Q4_BLOCK));
     if (fmt == KVO_FMT_F16) {
         uint16_t *dst = (uint16_t *)data + (size_t)row * hd;
         for (int d = 0; d < hd; ++d)
@@ -220,7 +280,7 @@ int kvo_append(int fmt, int n_kv, int hd, int block_size, int n_blocks,
 {
     if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0)
         return -1;
-    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL))
+    if (fmt != KVO_FMT_F16 && (k_scales == NULL || v_scales == NULL))
         return -2;
     for (int t = 0; t < n_tok; ++t) {
         for (int kvh = 0; kvh < n_kv; ++kvh) {
@@ -229,9 +289,9 @@ int kvo_append(int fmt, int n_kv, int hd, int block_size, int n_blocks,
             if (row < 0)
                 return -3;
             const size_t src = ((size_t)t * n_kv + kvh) * hd;
-            if (store_row(fmt, hd, k_data, k_scales, row, k + src) != 0)
+            if (store_row(fmt, hd, k_data, k_scales, row, k + src, 0) != 0)
                 return -4;
-            if (store_row(fmt, hd, v_data, v_scales, row, v + src) != 0)
+            if (store_row(fmt, hd, v_data, v_scales, row, v + src, 1) != 0)
                 return -4;
         }
     }
@@ -246,12 +306,39 @@ int kvo_append(int fmt, int n_kv, int hd, int block_size, int n_blocks,
 
 static double dequant(int fmt, int hd, const void *data, const uint16_t *scales,
                       int64_t row, int d)
-{
+{   /* K of every format, V of FP16 and int8 */
     if (fmt == KVO_FMT_F16)
         return (double)g_fp16_table[((const uint16_t *)data)[(size_t)row * hd + d]];
     const int8_t c = ((const int8_t *)data)[(size_t)row * hd + d];
     const uint16_t s = scales[(size_t)row * (hd / KVO_GROUP) + d / KVO_GROUP];
     return (double)c * (double)g_fp16_table[s];
+}
+
+/* V of any format: K8V4's V is dequantized in the rotated basis, (code - 8)
+ * * d, exact in float and double; its attention output is rotated back. */
+static double dequant_v(int fmt, int hd, const void *data, const uint16_t *scales,
+                        int64_t row, int d)
+{
+    if (fmt != KVO_FMT_K8V4)
+        return dequant(fmt, hd, data, scales, row, d);
+    const uint8_t byte = ((const uint8_t *)data)[(size_t)row * (hd / 2) + d / 2];
+    const int c = (d & 1) ? (byte >> 4) : (byte & 15);
+    const uint16_t s = scales[(size_t)row * (hd / KVO_Q4_BLOCK) + d / KVO_Q4_BLOCK];
+    return (double)(c - 8) * (double)g_fp16_table[s];
+}
+
+/* The inverse rotation of a K8V4 attention output row, in float64. */
+static void unrotate_f64(double *o, int hd)
+{
+    for (int h = 1; h < hd; h *= 2)
+        for (int i = 0; i < hd; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                const double a = o[j], b = o[j + h];
+                o[j] = a + b;
+                o[j + h] = a - b;
+            }
+    for (int d = 0; d < hd; ++d)
+        o[d] /= (double)hd;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -279,7 +366,7 @@ int kvo_attention(int fmt, int n_kv, int hd, int block_size, int n_blocks,
         return -1;
     if (n_seq <= 0 || W <= 0 || n_q <= 0 || n_q % n_kv != 0)
         return -1;
-    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL))
+    if (fmt != KVO_FMT_F16 && (k_scales == NULL || v_scales == NULL))
         return -2;
     fp16_table_init();
     const int G = n_q / n_kv;
@@ -335,10 +422,12 @@ int kvo_attention(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                     const double e = exp(z[c] - zmax);
                     den += e;
                     for (int d = 0; d < hd; ++d)
-                        o[d] += e * dequant(fmt, hd, v_data, v_scales, rows[c], d);
+                        o[d] += e * dequant_v(fmt, hd, v_data, v_scales, rows[c], d);
                 }
                 for (int d = 0; d < hd; ++d)
                     o[d] /= den;
+                if (fmt == KVO_FMT_K8V4)
+                    unrotate_f64(o, hd);
             }
         }
     }
@@ -366,8 +455,10 @@ int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
         return -1;
     if (n_cells < 0)
         return -1;
-    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL))
+    if (fmt != KVO_FMT_F16 && (k_scales == NULL || v_scales == NULL))
         return -2;
+    if (hd > 4096)
+        return -1;
     fp16_table_init();
     const int max_blocks = (n_cells + block_size - 1) / block_size;
     for (int kvh = 0; kvh < n_kv; ++kvh) {
@@ -385,9 +476,20 @@ int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                 } else {
                     dk[d] = kvo_fp16_from_float(
                         (float)dequant(fmt, hd, k_data, k_scales, row, d));
-                    dv[d] = kvo_fp16_from_float(
-                        (float)dequant(fmt, hd, v_data, v_scales, row, d));
+                    if (fmt == KVO_FMT_Q8)
+                        dv[d] = kvo_fp16_from_float(
+                            (float)dequant(fmt, hd, v_data, v_scales, row, d));
                 }
+            }
+            if (fmt == KVO_FMT_K8V4) {
+                /* V rotated back in fp32 (the transform's butterflies, then
+                 * / hd, a power of two) and rounded to fp16 */
+                float w[4096];
+                for (int d = 0; d < hd; ++d)
+                    w[d] = (float)dequant_v(fmt, hd, v_data, v_scales, row, d);
+                kvo_hadamard_f32(w, hd);
+                for (int d = 0; d < hd; ++d)
+                    dv[d] = kvo_fp16_from_float(w[d] / (float)hd);
             }
         }
     }
@@ -465,6 +567,15 @@ static int64_t seq_row(const int32_t *block_table_row, int n_blocks, int n_kv, i
     return ((int64_t)blk * n_kv + kvh) * block_size + pos % block_size;
 }
 
+/* Bytes of one K or V row and fp16 scales per row, per format. */
+static void row_sizes(int fmt, int hd, size_t *k_b, size_t *v_b, int *k_ng, int *v_ng)
+{
+    *k_b = fmt == KVO_FMT_F16 ? (size_t)hd * 2 : (size_t)hd;
+    *v_b = fmt == KVO_FMT_F16 ? (size_t)hd * 2 : fmt == KVO_FMT_Q8 ? (size_t)hd : (size_t)hd / 2;
+    *k_ng = fmt == KVO_FMT_F16 ? 0 : hd / KVO_GROUP;
+    *v_ng = fmt == KVO_FMT_F16 ? 0 : fmt == KVO_FMT_Q8 ? hd / KVO_GROUP : hd / KVO_Q4_BLOCK;
+}
+
 int kvo_gather_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                      const void *k_data, const void *v_data,
                      const uint16_t *k_scales, const uint16_t *v_scales,
@@ -473,27 +584,24 @@ int kvo_gather_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
 {
     if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0 || n_cells < 0)
         return -1;
-    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL || scales_k == NULL ||
-                              scales_v == NULL))
+    if (fmt != KVO_FMT_F16 && (k_scales == NULL || v_scales == NULL || scales_k == NULL ||
+                               scales_v == NULL))
         return -2;
-    const size_t esz = fmt == KVO_FMT_F16 ? 2 : 1;
-    const int ng = hd / KVO_GROUP;
+    size_t kb, vb;
+    int kng, vng;
+    row_sizes(fmt, hd, &kb, &vb, &kng, &vng);
     for (int p = 0; p < n_cells; ++p) {
         for (int kvh = 0; kvh < n_kv; ++kvh) {
             const int64_t row = seq_row(block_table_row, n_blocks, n_kv, block_size, p, kvh);
             if (row < 0)
                 return -3;
             const size_t dst = (size_t)p * n_kv + kvh;
-            memcpy((char *)codes_k + dst * hd * esz, (const char *)k_data + (size_t)row * hd * esz,
-                   hd * esz);
-            memcpy((char *)codes_v + dst * hd * esz, (const char *)v_data + (size_t)row * hd * esz,
-                   hd * esz);
-            if (fmt == KVO_FMT_Q8) {
-                for (int gi = 0; gi < ng; ++gi) {
-                    scales_k[dst * ng + gi] = k_scales[(size_t)row * ng + gi];
-                    scales_v[dst * ng + gi] = v_scales[(size_t)row * ng + gi];
-                }
-            }
+            memcpy((char *)codes_k + dst * kb, (const char *)k_data + (size_t)row * kb, kb);
+            memcpy((char *)codes_v + dst * vb, (const char *)v_data + (size_t)row * vb, vb);
+            for (int gi = 0; gi < kng; ++gi)
+                scales_k[dst * kng + gi] = k_scales[(size_t)row * kng + gi];
+            for (int gi = 0; gi < vng; ++gi)
+                scales_v[dst * vng + gi] = v_scales[(size_t)row * vng + gi];
         }
     }
     return 0;
@@ -507,27 +615,24 @@ int kvo_scatter_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
 {
     if (check_geometry(fmt, n_kv, hd, block_size, n_blocks) != 0 || n_cells < 0)
         return -1;
-    if (fmt == KVO_FMT_Q8 && (k_scales == NULL || v_scales == NULL || scales_k == NULL ||
-                              scales_v == NULL))
+    if (fmt != KVO_FMT_F16 && (k_scales == NULL || v_scales == NULL || scales_k == NULL ||
+                               scales_v == NULL))
         return -2;
-    const size_t esz = fmt == KVO_FMT_F16 ? 2 : 1;
-    const int ng = hd / KVO_GROUP;
+    size_t kb, vb;
+    int kng, vng;
+    row_sizes(fmt, hd, &kb, &vb, &kng, &vng);
     for (int p = 0; p < n_cells; ++p) {
         for (int kvh = 0; kvh < n_kv; ++kvh) {
             const int64_t row = seq_row(block_table_row, n_blocks, n_kv, block_size, p, kvh);
             if (row < 0)
                 return -3;
             const size_t src = (size_t)p * n_kv + kvh;
-            memcpy((char *)k_data + (size_t)row * hd * esz, (const char *)codes_k + src * hd * esz,
-                   hd * esz);
-            memcpy((char *)v_data + (size_t)row * hd * esz, (const char *)codes_v + src * hd * esz,
-                   hd * esz);
-            if (fmt == KVO_FMT_Q8) {
-                for (int gi = 0; gi < ng; ++gi) {
-                    k_scales[(size_t)row * ng + gi] = scales_k[src * ng + gi];
-                    v_scales[(size_t)row * ng + gi] = scales_v[src * ng + gi];
-                }
-            }
+            memcpy((char *)k_data + (size_t)row * kb, (const char *)codes_k + src * kb, kb);
+            memcpy((char *)v_data + (size_t)row * vb, (const char *)codes_v + src * vb, vb);
+            for (int gi = 0; gi < kng; ++gi)
+                k_scales[(size_t)row * kng + gi] = scales_k[src * kng + gi];
+            for (int gi = 0; gi < vng; ++gi)
+                v_scales[(size_t)row * vng + gi] = scales_v[src * vng + gi];
         }
     }
     return 0;

@@ -37,7 +37,9 @@ extern "C" {
 
 #define KVO_FMT_F16 0
 #define KVO_FMT_Q8 1
+#define KVO_FMT_K8V4 2 /* int8 K (as KVO_FMT_Q8) + rotated Q4_0 V */
 #define KVO_GROUP 64
+#define KVO_Q4_BLOCK 32
 
 /* IEEE-754 binary16 conversion, round to nearest, ties to even, subnormals
  * kept, overflow to infinity. */
@@ -50,7 +52,23 @@ void kvo_fp16_to_float_array(const uint16_t *h, float *out, int64_t n);
  * s = fp16(max|x| / 127) and codes clamp(rint(x / s), -127, 127). */
 int kvo_quantize_row_q8(const float *x, int hd, int8_t *codes, uint16_t *scales);
 
-/* Write n_tok new cells (K and V) into the paged pool image. */
+/* In-place Walsh-Hadamard transform of n values (n a power of two), fp32:
+ * stages h = 1, 2, 4, ..., n/2; in each, every pair (j, j + h) with bit h of
+ * j clear becomes (x[j] + x[j+h], x[j] - x[j+h]).  No normalisation: applied
+ * twice it multiplies by n. */
+void kvo_hadamard_f32(float *x, int n);
+
+/* K8V4's V row: the row rotated by the Walsh-Hadamard transform, then
+ * Q4_0 per block of 32 rotated dims: d = fp16(m / -8) with m the block's
+ * element of largest magnitude (the first on ties), code = clamp(rint(y /
+ * d), -8, 7) + 8 (0..15; 8 when d is 0), value (code - 8) * d.  codes[j]
+ * holds dims 2j (low nibble) and 2j + 1 (high nibble); one fp16 d per 32
+ * dims. */
+int kvo_quantize_row_q4r(const float *x, int hd, uint8_t *codes, uint16_t *scales);
+
+/* Write n_tok new cells (K and V) into the paged pool image.  KVO_FMT_K8V4:
+ * v_data is [n_blocks][n_kv][block_size][hd/2] packed nibbles and v_scales
+ * [..][hd/32]. */
 int kvo_append(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                void *k_data, void *v_data, uint16_t *k_scales, uint16_t *v_scales,
                const float *k, const float *v, int n_tok,
@@ -79,7 +97,8 @@ int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,
  * into token-major runs, and scattered back.  codes_k / codes_v are
  * [n_cells][n_kv][hd] elements of the pool's format (fp16 bits or int8);
  * scales_k / scales_v [n_cells][n_kv][hd/64] fp16 bits, required for int8
- * (-2 without them) and ignored for fp16. */
+ * (-2 without them) and ignored for fp16.  K8V4: codes_v [..][hd/2] packed
+ * nibbles and scales_v [..][hd/32], both required. */
 int kvo_gather_cells(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                      const void *k_data, const void *v_data,
                      const uint16_t *k_scales, const uint16_t *v_scales,

@@ -14,6 +14,7 @@ import pytest
 import oracle
 from tests import test_oracle_attention as att
 from tests import test_oracle_chunk as chk
+from tests import test_oracle_k8v4 as k84
 from tests import test_oracle_persist as per
 from tests import test_oracle_fp16 as f16
 from tests import test_oracle_quant as qt
@@ -50,14 +51,34 @@ MUTATIONS = {
     "chunk_no_softmax_scale": ("z[c] = dot * (double)sm_scale;", "z[c] = dot;"),
     "chunk_k_reads_v": ("const uint16_t *kr = k16 +", "const uint16_t *kr = v16 +"),
     "chunk_no_normalisation": ("o[d] = o[d] / den;", "o[d] = o[d] / (den + 1.0);"),
-    "gather_v_from_k": ("memcpy((char *)codes_v + dst * hd * esz, (const char *)v_data +",
-                        "memcpy((char *)codes_v + dst * hd * esz, (const char *)k_data +"),
-    "gather_k_scales_from_v": ("scales_k[dst * ng + gi] = k_scales[(size_t)row * ng + gi];",
-                               "scales_k[dst * ng + gi] = v_scales[(size_t)row * ng + gi];"),
+    "gather_v_from_k": ("memcpy((char *)codes_v + dst * vb, (const char *)v_data +",
+                        "memcpy((char *)codes_v + dst * vb, (const char *)k_data +"),
+    "gather_k_scales_from_v": ("scales_k[dst * kng + gi] = k_scales[(size_t)row * kng + gi];",
+                               "scales_k[dst * kng + gi] = v_scales[(size_t)row * kng + gi];"),
     "persist_slot_off_by_one": ("return ((int64_t)blk * n_kv + kvh) * block_size + pos % block_size;",
                                 "return ((int64_t)blk * n_kv + kvh) * block_size + (pos + 1) % block_size;"),
-    "scatter_drops_v_scales": ("v_scales[(size_t)row * ng + gi] = scales_v[src * ng + gi];",
-                               "v_scales[(size_t)row * ng + gi] = scales_k[src * ng + gi];"),
+    "scatter_drops_v_scales": ("v_scales[(size_t)row * vng + gi] = scales_v[src * vng + gi];",
+                               "v_scales[(size_t)row * vng + gi] = scales_k[src * vng + gi];"),
+    # K8V4
+    "q4_max_last_on_ties": ("if (fabsf(y[i]) > fabsf(m))", "if (fabsf(y[i]) >= fabsf(m))"),
+    "q4_positive_scale": ("kvo_fp16_from_float(m / -8.0f)", "kvo_fp16_from_float(m / 8.0f)"),
+    "q4_scale_over_7": ("kvo_fp16_from_float(m / -8.0f)", "kvo_fp16_from_float(m / -7.0f)"),
+    "q4_round_half_away": ("float r = rintf(y[i + e] / d);", "float r = roundf(y[i + e] / d);"),
+    "q4_clamp_8": ("if (r > 7.0f)\n                        r = 7.0f;",
+                   "if (r > 8.0f)\n                        r = 8.0f;"),
+    "q4_nibble_swap": ("codes[i / 2] = (uint8_t)(c[0] | (c[1] << 4));",
+                       "codes[i / 2] = (uint8_t)(c[1] | (c[0] << 4));"),
+    "q4_offset_7": ("return (double)(c - 8) * (double)g_fp16_table[s];",
+                    "return (double)(c - 7) * (double)g_fp16_table[s];"),
+    "q4_scale_per_64_dims": ("+ d / KVO_Q4_BLOCK];", "+ d / KVO_GROUP];"),
+    "hadamard_difference_reversed": ("x[j + h] = a - b;", "x[j + h] = b - a;"),
+    "hadamard_skips_last_stage": ("for (int h = 1; h < n; h *= 2)", "for (int h = 1; h < n / 2; h *= 2)"),
+    "attention_no_unrotate": ("if (fmt == KVO_FMT_K8V4)\n                    unrotate_f64(o, hd);", ""),
+    "unrotate_not_divided": ("o[d] /= (double)hd;", "o[d] /= 1.0;"),
+    "unrotate_difference_reversed": ("o[j + h] = a - b;", "o[j + h] = b - a;"),
+    "compact_v_not_rotated_back": ("kvo_hadamard_f32(w, hd);", ""),
+    "compact_v_not_divided": ("dv[d] = kvo_fp16_from_float(w[d] / (float)hd);",
+                              "dv[d] = kvo_fp16_from_float(w[d]);"),
 }
 
 
@@ -88,7 +109,16 @@ def _all_pins():
              chk.test_first_token_of_a_whole_prompt_sees_one_cell,
              chk.test_equal_keys_give_the_running_mean_of_v,
              per.test_int8_codes_without_scales_are_refused]
-    for fmt in (F16, Q8):
+    pins += [lambda: k84.test_transform_is_sylvester_hadamard(64),
+             k84.test_designed_block_scale_codes_and_nibble_order,
+             k84.test_zero_block_gives_zero_scale_and_offset_codes,
+             k84.test_random_rows_within_half_a_step,
+             k84.test_stored_codes_are_the_row_quantizers,
+             k84.test_one_visible_cell_returns_its_derotated_value,
+             lambda: k84.test_matches_torch_sdpa(2, 4, 256, 3),
+             k84.test_compaction_derotates_v,
+             k84.test_compaction_exact_when_every_block_shares_its_scale]
+    for fmt in (F16, Q8, oracle.FMT_K8V4):
         pins += [lambda fmt=fmt: per.test_gather_returns_the_stored_rows_in_order(fmt),
                  lambda fmt=fmt: per.test_scatter_into_another_layout_then_gather_is_the_identity(fmt)]
     return pins

@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 
-F16, Q8 = oracle.FMT_F16, oracle.FMT_Q8
+F16, Q8, K8V4 = oracle.FMT_F16, oracle.FMT_Q8, oracle.FMT_K8V4
 
 
 def _pool(fmt, n_kv, hd, bs, nb, table_row, k, v):
@@ -25,7 +25,7 @@ def _pool(fmt, n_kv, hd, bs, nb, table_row, k, v):
     return pool
 
 
-@pytest.mark.parametrize("fmt", [F16, Q8])
+@pytest.mark.parametrize("fmt", [F16, Q8, K8V4])
 def test_gather_returns_the_stored_rows_in_order(fmt):
     rng = np.random.default_rng(21)
     n, n_kv, hd, bs = 45, 2, 128, 16
@@ -40,13 +40,15 @@ def test_gather_returns_the_stored_rows_in_order(fmt):
         np.testing.assert_array_equal(cv, v.astype(np.float16).view(np.uint16))
         assert sk is None and sv is None
     else:
-        for x, c, s in ((k, ck, sk), (v, cv, sv)):
-            codes, scales = oracle.quantize_rows_q8(x.reshape(-1, hd))
-            np.testing.assert_array_equal(c.reshape(-1, hd), codes)
-            np.testing.assert_array_equal(s.reshape(-1, hd // 64), scales)
+        v_rows = oracle.quantize_rows_q8 if fmt == Q8 else oracle.quantize_rows_q4r
+        for x, c, s, rows in ((k, ck, sk, oracle.quantize_rows_q8), (v, cv, sv, v_rows)):
+            codes, scales = rows(x.reshape(-1, hd))
+            np.testing.assert_array_equal(c.reshape(codes.shape), codes)
+            np.testing.assert_array_equal(s.reshape(scales.shape), scales)
+            assert c.shape[:2] == s.shape[:2] == (n, n_kv)
 
 
-@pytest.mark.parametrize("fmt", [F16, Q8])
+@pytest.mark.parametrize("fmt", [F16, Q8, K8V4])
 def test_scatter_into_another_layout_then_gather_is_the_identity(fmt):
     rng = np.random.default_rng(22)
     n, n_kv, hd, bs = 70, 3, 64, 32
