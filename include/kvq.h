@@ -1,9 +1,10 @@
 /*
  * kvq.h -- C ABI of the quantized K/V cache library (one GB300, sm_103a).
  *
- * The library keeps a transformer's K/V cache in a paged pool, as FP16 or as
- * int8 codes with one FP16 scale per 64 head dims, and runs the three calls
- * that touch it on the decode / verify / prompt paths:
+ * The library keeps a transformer's K/V cache in a paged pool, as FP16, as
+ * int8 codes with one FP16 scale per 64 head dims, or as K8V4 (int8 K and
+ * rotated 4-bit V), and runs the calls that touch it on the decode / verify
+ * / prompt paths:
  *
  *   kvq_append       quantize-on-write of new K/V rows into the pool
  *   kvq_decode_attn  GQA attention of 1..W query tokens against the pool,
@@ -26,7 +27,8 @@
  *               (a block is a list of byte runs -- codes, then scales; the
  *               decode, verify-window and prompt appends; a writer that
  *               tests one pointer and silently skips the other), "Tests"
- *               (the negative control that catches that skip).
+ *               (the negative control that catches that skip), "What"
+ *               (K8V4: INT8 K + rotated Q4_0 V, 816 B per cell).
  *   [Path F v3] "Path F format v3: persist per-head INT8 KV scales for
  *               INT8 + persistent KV interop": "Why", "Scope" (int8 bytes
  *               without their scales are refused, not used).
@@ -68,7 +70,9 @@ extern "C" {
 /* Cache formats ([kv-q8 PR], "Summary"). */
 typedef enum {
     KVQ_F16 = 0, /* K and V stored as IEEE fp16 (round to nearest even)      */
-    KVQ_Q8 = 1   /* int8 codes + one fp16 scale per 64 dims of a row         */
+    KVQ_Q8 = 1,  /* int8 codes + one fp16 scale per 64 dims of a row         */
+    KVQ_K8V4 = 2 /* K as KVQ_Q8; V rotated (Walsh-Hadamard), then 4-bit      */
+                 /* codes + one fp16 scale per 32 rotated dims ([k8v4 PR])  */
 } kvq_format;
 
 typedef enum {
@@ -79,8 +83,10 @@ typedef enum {
     KVQ_ERR_CUDA = 4         /* the CUDA runtime reported a launch error     */
 } kvq_status;
 
-/* Group of head dims sharing one fp16 scale in KVQ_Q8. */
+/* Group of head dims sharing one fp16 scale in KVQ_Q8 (and K8V4's K). */
 #define KVQ_GROUP 64
+/* Block of rotated V dims sharing one fp16 scale in KVQ_K8V4. */
+#define KVQ_Q4_BLOCK 32
 
 /*
  * One layer's paged K/V pool.  A physical block holds block_size consecutive
@@ -92,6 +98,20 @@ typedef enum {
  *   k_scales, v_scales [n_blocks][n_kv_heads][block_size][head_dim / 64]
  *                      fp16 bits; KVQ_Q8 only (must be NULL-free for Q8,
  *                      ignored for F16)
+ *
+ * KVQ_K8V4 keeps K as KVQ_Q8 does (k_data int8, k_scales per 64 dims) and V
+ * as two other runs:
+ *
+ *   v_data             [n_blocks][n_kv_heads][block_size][head_dim / 2]
+ *                      bytes: two 4-bit codes each, dim 2j in the low
+ *                      nibble of byte j, dim 2j + 1 in the high nibble
+ *   v_scales           [n_blocks][n_kv_heads][block_size][head_dim / 32]
+ *                      fp16 bits, one per 32 dims
+ *
+ * where the dims are those of the rotated row y = H v (H the Walsh-Hadamard
+ * matrix of order head_dim, Sylvester order, entries +-1), so a cell costs
+ * 2 * n_kv_heads * (head_dim + head_dim / 32) + n_kv_heads * head_dim * 18 /
+ * 32 bytes: 816 at 2 KV heads of 256 dims ([k8v4 PR], "What").
  *
  * Cell p of sequence b is block block_table[b * max_blocks_per_seq +
  * p / block_size], slot p % block_size; its row of KV head h starts at
@@ -118,7 +138,8 @@ typedef struct kvq_cache {
  * Bytes one physical block occupies in the pool: K and V codes plus, for
  * KVQ_Q8, their scales (2 bytes per 64 dims).  Per element that is 2 bytes
  * (F16) or 1 + 2/64 bytes (Q8) -- the 6.0 GiB and 3.1 GiB of a 262144-cell
- * cache in [kv-q8 PR], "Summary".  Returns 0 for an invalid geometry.
+ * cache in [kv-q8 PR], "Summary".  KVQ_K8V4: 1 + 2/64 bytes per K element
+ * and 18/32 per V element.  Returns 0 for an invalid geometry.
  */
 size_t kvq_block_bytes(int fmt, int n_kv_heads, int head_dim, int block_size);
 
@@ -138,7 +159,13 @@ size_t kvq_block_bytes(int fmt, int n_kv_heads, int head_dim, int block_size);
  * dims, s = fp16_rne(max|x| / 127) and codes clamp(rint(x / float(s)), -127,
  * 127): both divisions are IEEE fp32 divisions, rint rounds half to even; a
  * group whose scale is 0 gets zero codes.  The result is bit-identical to
- * that definition.  A cell written twice holds the last write; two tokens of
+ * that definition.  KVQ_K8V4 writes K that way; V is first rotated, y = H v,
+ * in fp32 by butterflies (stages h = 1, 2, ..., head_dim / 2; in each, dims
+ * j and j + h, bit h of j clear, become their sum and difference), then
+ * each block of 32 dims of y gets d = fp16_rne(m / -8), m the block's
+ * element of largest magnitude (the first one on ties), and codes
+ * clamp(rint(y / float(d)), -8, 7) + 8 (8 when d is 0), both divisions
+ * IEEE fp32.  A cell written twice holds the last write; two tokens of
  * one call must not name the same cell.  n_tok == 0 is a no-op returning
  * KVQ_OK.
  */
@@ -178,6 +205,8 @@ size_t kvq_decode_workspace_bytes(const kvq_cache *cache, int n_seq, int W, int 
  * ctx_lens[b] - W + w and attends to cells [0, ctx_lens[b] - W + w]
  * (causal inside the window).  out = softmax(sm_scale * q . K^T) V over the
  * dequantized cache, computed in fp32; a query with no visible cell gets 0.
+ * For KVQ_K8V4 the dequantized V is the rotated one, (code - 8) * d, and
+ * the result is rotated back, out = H o / head_dim.
  * W in [1, 16], n_q / n_kv_heads * W <= 32.
  */
 kvq_status kvq_decode_attn(const kvq_cache *cache, const float *q, int n_seq, int W, int n_q,
@@ -196,7 +225,10 @@ kvq_status kvq_decode_attn(const kvq_cache *cache, const float *q, int n_seq, in
  *                   aligned
  *
  * KVQ_F16 copies the stored bits; KVQ_Q8 writes fp16_rne(code * scale)
- * (the product is exact in fp32).  n_cells == 0 is a no-op.
+ * (the product is exact in fp32).  KVQ_K8V4 writes K that way and V as
+ * fp16_rne(w / head_dim), w the fp32 butterflies of kvq_append applied to
+ * the row of (code - 8) * d (the inverse rotation).  n_cells == 0 is a
+ * no-op.
  */
 kvq_status kvq_compact_f16(const kvq_cache *cache, const int32_t *block_table_row, int n_cells,
                            void *out_k, void *out_v, void *stream);
@@ -234,10 +266,13 @@ kvq_status kvq_chunk_attn(const void *k16, const void *v16, int n_kv_heads, int 
  *   block_table_row  device int32 [ceil(n_cells / block_size)]: the
  *                    sequence's row of the block table
  *   codes_k, codes_v device [n_cells][n_kv_heads][head_dim] elements of the
- *                    pool's format (fp16 or int8), 16-byte aligned
+ *                    pool's format (fp16 or int8), 16-byte aligned; K8V4's
+ *                    codes_v is [n_cells][n_kv_heads][head_dim / 2] bytes
  *   scales_k, scales_v
  *                    device fp16 [n_cells][n_kv_heads][head_dim / 64]; required
- *                    for KVQ_Q8 (KVQ_ERR_ARG without them), ignored for KVQ_F16
+ *                    for KVQ_Q8 (KVQ_ERR_ARG without them), ignored for
+ *                    KVQ_F16; K8V4 requires both, scales_v being
+ *                    [n_cells][n_kv_heads][head_dim / 32]
  *
  * Both copy bits unchanged: a gather followed by a scatter into any pool
  * of the same format and geometry, under any block table, restores the

@@ -19,7 +19,9 @@ from .build import LIB_PATH, build  # noqa: F401  (build() is the in-tree nvcc b
 
 KVQ_F16 = 0
 KVQ_Q8 = 1
+KVQ_K8V4 = 2
 KVQ_GROUP = 64
+KVQ_Q4_BLOCK = 32
 
 KVQ_OK = 0
 KVQ_ERR_ARG = 1

@@ -29,7 +29,7 @@ int log2_exact(int v) {
 // Geometry checks shared by every call.
 kvq_status check_cache(const kvq_cache* c) {
   if (c == nullptr) return KVQ_ERR_ARG;
-  if (c->fmt != KVQ_F16 && c->fmt != KVQ_Q8) return KVQ_ERR_ARG;
+  if (c->fmt != KVQ_F16 && c->fmt != KVQ_Q8 && c->fmt != KVQ_K8V4) return KVQ_ERR_ARG;
   if (c->reserved != 0) return KVQ_ERR_ARG;
   if (c->n_kv_heads <= 0 || c->n_blocks <= 0) return KVQ_ERR_ARG;
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_ARG;
@@ -38,8 +38,8 @@ kvq_status check_cache(const kvq_cache* c) {
   if ((long long)c->n_blocks * c->n_kv_heads * c->block_size >= (1LL << 31)) return KVQ_ERR_ARG;
   if (c->k_data == nullptr || c->v_data == nullptr) return KVQ_ERR_ARG;
   if (!aligned(c->k_data, 256) || !aligned(c->v_data, 256)) return KVQ_ERR_ARG;
-  if (c->fmt == KVQ_Q8) {
-    // int8 codes without their scales are refused, never half-written.
+  if (c->fmt != KVQ_F16) {
+    // int8 (or 4-bit) codes without their scales are refused, never half-written.
     if (c->k_scales == nullptr || c->v_scales == nullptr) return KVQ_ERR_ARG;
     if (!aligned(c->k_scales, 256) || !aligned(c->v_scales, 256)) return KVQ_ERR_ARG;
   }
@@ -138,6 +138,10 @@ KVQ_API size_t kvq_block_bytes(int fmt, int n_kv_heads, int head_dim, int block_
   if (fmt == KVQ_Q8) {
     if (head_dim % KVQ_GROUP != 0) return 0;
     return 2 * (elems + (elems / KVQ_GROUP) * 2);
+  }
+  if (fmt == KVQ_K8V4) {
+    if (head_dim % KVQ_GROUP != 0) return 0;
+    return elems + (elems / KVQ_GROUP) * 2 + elems / 2 + (elems / KVQ_Q4_BLOCK) * 2;
   }
   return 0;
 }
@@ -281,8 +285,8 @@ kvq_status persist_impl(const kvq_cache* cache, const int32_t* block_table_row, 
   if (n_cells < 0) return KVQ_ERR_ARG;
   if (n_cells == 0) return KVQ_OK;
   if (block_table_row == nullptr || codes_k == nullptr || codes_v == nullptr) return KVQ_ERR_ARG;
-  // int8 codes never move without their scales
-  if (cache->fmt == KVQ_Q8 && (scales_k == nullptr || scales_v == nullptr)) return KVQ_ERR_ARG;
+  // int8 (and 4-bit) codes never move without their scales
+  if (cache->fmt != KVQ_F16 && (scales_k == nullptr || scales_v == nullptr)) return KVQ_ERR_ARG;
   if (!aligned(block_table_row, 4) || !aligned(codes_k, 16) || !aligned(codes_v, 16) ||
       !aligned(scales_k, 2) || !aligned(scales_v, 2))
     return KVQ_ERR_ARG;

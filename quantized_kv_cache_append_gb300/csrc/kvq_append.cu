@@ -15,6 +15,12 @@
 // __float2half_rn rounds to nearest even with subnormals; rounding is to
 // nearest even, and clamping before rounding equals clamping after it for
 // the bound 127.
+//
+// #711 kv: --kv k8v4 streams with --kv-resident, "What": K8V4 keeps K as the
+// int8 format does and V rotated, as Q4_0 (one fp16 scale per 32 dims,
+// 4-bit codes with an offset of 8).  The rotation is the Walsh-Hadamard
+// transform in fp32 butterflies, stage by stage, and the codes follow the
+// same bit-exact discipline as the int8 ones.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -257,6 +263,146 @@ __global__ void __launch_bounds__(W * 32) append_q8_kernel(AppendArgs a) {
   }
 }
 
+// K8V4 V code of y in the block of scale d (d != 0, rs ~ 1 / d): the 4-bit
+// offset code clamp(rint(y / d), -8, 7) + 8.  |y / d| <= 8 (up to d's fp16
+// rounding), so y * rs is within 2e-6 of the quotient and decides the
+// integer wherever it lies more than 2.5e-4 from a half-integer; inside
+// that band, and for non-finite values, the IEEE quotient itself decides
+// (a NaN quotient gives 0).  Clamping to integer bounds commutes with
+// rounding.
+__device__ __forceinline__ uint32_t q4_code(float y, float d, float rs) {
+  const float qa = y * rs;
+  const float rq = rintf(qa);
+  float r;
+  if (fabsf(qa - rq) < 0.5f - 2.5e-4f) {
+    r = rq;
+  } else {
+    r = rintf(__fdiv_rn(y, d));
+    if (!(r == r)) r = 0.0f;
+  }
+  return (uint32_t)((int)fminf(fmaxf(r, -8.0f), 7.0f) + 8);
+}
+
+// K8V4 append: one warp per (token, KV head) row, K and V.  Lane l holds
+// units of U consecutive dims, dims U l + 32 U i (i < NI): the loads of a
+// unit are coalesced across the warp and the Walsh-Hadamard stages map onto
+// the layout (wht_warp).  K: int8 codes per 64-dim group, exactly as the
+// int8 format (group maximum over the 64 / U lanes of the group, then
+// group_scale and codes4).  V: rotated in fp32, then per block of 32
+// rotated dims (32 / U lanes) the element of largest magnitude, the first
+// one on ties (key: |y| bits above the complemented dim index; NaN counts
+// as 0 and a zero maximum gives m = +0, as the comparison-based definition
+// does), d = fp16(m / -8), and two codes a byte.
+template <int HD, int W>
+__global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
+  constexpr int U = HD >= 128 ? 4 : 2;
+  constexpr int NI = HD / (32 * U);
+  constexpr int LG = kGroup / U;     // lanes of a 64-dim K group
+  constexpr int LB = kQ4Block / U;   // lanes of a 32-dim V block
+  constexpr int NG = HD / kGroup, NB = HD / kQ4Block;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)a.n_tok * a.n_kv;
+  const bool rows32 = rows <= 0x7fffffffLL;
+  const long long row = (long long)blockIdx.x * W + (threadIdx.x >> 5);
+  if (row >= rows) return;  // warp-uniform; no block-level barrier follows
+
+  float xk[NI][U], xv[NI][U];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const size_t off = (size_t)row * HD + U * lane + 32 * U * i;
+    if constexpr (U == 4) {
+      const float4 k4 = __ldcs(reinterpret_cast<const float4*>(a.k + off));
+      const float4 v4 = __ldcs(reinterpret_cast<const float4*>(a.v + off));
+      xk[i][0] = k4.x; xk[i][1] = k4.y; xk[i][2] = k4.z; xk[i][3] = k4.w;
+      xv[i][0] = v4.x; xv[i][1] = v4.y; xv[i][2] = v4.z; xv[i][3] = v4.w;
+    } else {
+      const float2 k2 = __ldcs(reinterpret_cast<const float2*>(a.k + off));
+      const float2 v2 = __ldcs(reinterpret_cast<const float2*>(a.v + off));
+      xk[i][0] = k2.x; xk[i][1] = k2.y;
+      xv[i][0] = v2.x; xv[i][1] = v2.y;
+    }
+  }
+  const long long dr = dest_row(a, row, rows32);
+
+  // ---- K: int8, one fp16 scale per 64 dims
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    uint32_t mb = 0;
+#pragma unroll
+    for (int e = 0; e < U; ++e) mb = max(mb, __float_as_uint(xk[i][e]) & 0x7fffffffu);
+#pragma unroll
+    for (int off = 1; off < LG; off <<= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+    const float amax = __uint_as_float(mb);
+    const __half sh = group_scale(amax);
+    const float sf = __half2float(sh);
+    if (dr < 0) continue;
+    const float4 x4 = U == 4 ? make_float4(xk[i][0], xk[i][1], xk[i][U > 2 ? 2 : 0], xk[i][U > 3 ? 3 : 0])
+                             : make_float4(xk[i][0], xk[i][1], 0.f, 0.f);
+    uint32_t c;
+    if (amax <= 3.4028234663852886e38f) {
+      c = codes4(x4, sf, rcp_approx(sf));
+    } else {
+      c = exact_code(x4.x, sf) | (exact_code(x4.y, sf) << 8) | (exact_code(x4.z, sf) << 16) |
+          (exact_code(x4.w, sf) << 24);
+    }
+    const int d0 = U * lane + 32 * U * i;
+    int8_t* dst = static_cast<int8_t*>(a.k_dst) + dr * HD + d0;
+    if constexpr (U == 4) *reinterpret_cast<uint32_t*>(dst) = c;
+    else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)c;
+    if (lane % LG == 0) a.ks_dst[dr * NG + d0 / kGroup] = sh;
+  }
+
+  // ---- V: rotate, then 4-bit codes and one fp16 scale per 32 rotated dims
+  wht_warp<U, NI>(xv, lane);
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int d0 = U * lane + 32 * U * i;
+    unsigned long long key = 0;
+#pragma unroll
+    for (int e = 0; e < U; ++e) {
+      const float y = xv[i][e];
+      const uint32_t ab = y == y ? (__float_as_uint(y) & 0x7fffffffu) : 0u;
+      const unsigned long long ke = ((unsigned long long)ab << 32) | (0xffffffffu - (uint32_t)(d0 + e));
+      key = ke > key ? ke : key;
+    }
+#pragma unroll
+    for (int off = 1; off < LB; off <<= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+      key = o > key ? o : key;
+    }
+    // the value at the winning dim, from the lane that holds it
+    const int jwin = (int)(0xffffffffu - (uint32_t)key);
+    const int src = (jwin % (32 * U)) / U;   // lane of dim jwin
+    float mine = 0.f;
+#pragma unroll
+    for (int e = 0; e < U; ++e)
+      if (d0 + e == jwin) mine = xv[i][e];
+    float m = __shfl_sync(0xffffffffu, mine, src);
+    if ((key >> 32) == 0) m = 0.0f;
+    const __half dh = __float2half_rn(m / -8.0f);
+    const float d = __half2float(dh);
+    if (dr < 0) continue;
+    uint32_t c[U];
+    if (d == 0.0f) {
+#pragma unroll
+      for (int e = 0; e < U; ++e) c[e] = 8;
+    } else {
+      const float rs = rcp_approx(d);
+#pragma unroll
+      for (int e = 0; e < U; ++e) c[e] = q4_code(xv[i][e], d, rs);
+    }
+    uint8_t* dst = static_cast<uint8_t*>(a.v_dst) + dr * (HD / 2) + d0 / 2;
+    if constexpr (U == 4)
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(c[0] | (c[1] << 4) | (c[U > 2 ? 2 : 0] << 8) |
+                                                     (c[U > 3 ? 3 : 0] << 12));
+    else
+      *dst = (uint8_t)(c[0] | (c[1] << 4));
+    if (lane % LB == 0) a.vs_dst[dr * NB + d0 / kQ4Block] = dh;
+  }
+}
+
 template <typename Kernel>
 cudaError_t launch_grid(Kernel kern, long long blocks, int threads, const AppendArgs& a,
                         cudaStream_t s) {
@@ -292,8 +438,18 @@ cudaError_t launch_q8(const AppendArgs& a, cudaStream_t s) {
 }
 
 template <int HD>
+cudaError_t launch_k8v4(const AppendArgs& a, cudaStream_t s) {
+  const long long rows = (long long)a.n_tok * a.n_kv;
+  constexpr int W = 4;
+  return launch_grid(append_k8v4_kernel<HD, W>, (rows + W - 1) / W, W * 32, a, s);
+}
+
+template <int HD>
 cudaError_t launch_hd(int fmt, const AppendArgs& a, cudaStream_t s) {
-  return fmt == KVQ_F16 ? launch_f16<HD>(a, s) : launch_q8<HD>(a, s);
+  if (fmt == KVQ_F16) return launch_f16<HD>(a, s);
+  if (fmt == KVQ_Q8) return launch_q8<HD>(a, s);
+  if (fmt == KVQ_K8V4) return launch_k8v4<HD>(a, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace

@@ -15,6 +15,12 @@
 // of a code and an fp16 scale is exact, and the fp16 multiply rounds it once
 // to nearest even, with subnormals, which is fp16(code * scale).  Loads and
 // stores are coalesced along the dims of a row, then the cells.
+//
+// K8V4 (#711 kv: --kv k8v4 streams with --kv-resident, "What": INT8 K +
+// rotated Q4_0 V): K as the int8 format; V is decoded in the rotated basis,
+// (code - 8) * d (exact in fp32), rotated back by the same fp32 butterflies
+// as the append's rotation (wht_warp), divided by head_dim (a power of
+// two, exact) and rounded to fp16.  One warp per V row.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -45,6 +51,49 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, uint32_t sel, uint3
   return hmul2(h, s2);
 }
 
+// K8V4 V rows of KV head kvh, one warp per cell (grid-stride over warps).
+template <int HD>
+__device__ __forceinline__ void compact_v4_rows(const CompactArgs& a, int kvh) {
+  constexpr int U = HD >= 128 ? 4 : 2;
+  constexpr int NI = HD / (32 * U);
+  constexpr int NB = HD / kQ4Block;
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int bs = 1 << a.pool.bs_log2;
+  for (int p = blockIdx.x * wpb + (threadIdx.x >> 5); p < a.n_cells; p += gridDim.x * wpb) {
+    const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
+    if (blk < 0 || blk >= a.pool.n_blocks) continue;  // warp-uniform skip
+    const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+    const uint8_t* src = static_cast<const uint8_t*>(a.pool.v) + row * (HD / 2);
+    const __half* sc = a.pool.vs + row * NB;
+    float x[NI][U];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int d0 = U * lane + 32 * U * i;
+      const float d = __half2float(__ldg(sc + d0 / kQ4Block));
+      uint32_t bits;
+      if constexpr (U == 4) bits = __ldg(reinterpret_cast<const unsigned short*>(src + d0 / 2));
+      else bits = __ldg(src + d0 / 2);
+#pragma unroll
+      for (int e = 0; e < U; ++e) x[i][e] = __fmul_rn((float)((int)((bits >> (4 * e)) & 15u) - 8), d);
+    }
+    wht_warp<U, NI>(x, lane);
+    __half* dst = a.out_v + ((size_t)kvh * a.n_cells + p) * HD;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int d0 = U * lane + 32 * U * i;
+      uint32_t h[U];
+#pragma unroll
+      for (int e = 0; e < U; ++e)
+        h[e] = __half_as_ushort(__float2half_rn(__fmul_rn(x[i][e], 1.0f / HD)));
+      if constexpr (U == 4)
+        *reinterpret_cast<uint2*>(dst + d0) = make_uint2(h[0] | (h[1] << 16), h[U > 2 ? 2 : 0] | (h[U > 3 ? 3 : 0] << 16));
+      else
+        *reinterpret_cast<uint32_t*>(dst + d0) = h[0] | (h[1] << 16);
+    }
+  }
+}
+
 template <int FMT, int HD>
 __global__ void __launch_bounds__(256) compact_kernel(CompactArgs a) {
   constexpr int DPT = FMT == KVQ_F16 ? 8 : 16;  // dims per thread
@@ -52,6 +101,12 @@ __global__ void __launch_bounds__(256) compact_kernel(CompactArgs a) {
   constexpr int NG = HD / kGroup;
   const int kvh = blockIdx.y % a.pool.n_kv;
   const int which = blockIdx.y / a.pool.n_kv;    // 0 = K, 1 = V
+  if constexpr (FMT == KVQ_K8V4) {
+    if (which == 1) {
+      compact_v4_rows<HD>(a, kvh);
+      return;
+    }
+  }
   const long long total = (long long)a.n_cells * CPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const int bs = 1 << a.pool.bs_log2;
@@ -105,7 +160,7 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int dpt = fmt == KVQ_F16 ? 8 : 16;
+  const int dpt = fmt == KVQ_F16 ? 8 : 16;  // K8V4: sized by its K rows
   const long long per_row = (long long)a.n_cells * (hd / dpt);  // threads per (K or V, KV head)
   const int ys = 2 * a.pool.n_kv;
   long long xs = (per_row + 255) / 256;
@@ -114,7 +169,10 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   if (xs < 1) xs = 1;
   if (ys > 65535) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)xs, (unsigned)ys);
-  return fmt == KVQ_F16 ? launch_fmt<KVQ_F16>(hd, a, s, grid) : launch_fmt<KVQ_Q8>(hd, a, s, grid);
+  if (fmt == KVQ_F16) return launch_fmt<KVQ_F16>(hd, a, s, grid);
+  if (fmt == KVQ_Q8) return launch_fmt<KVQ_Q8>(hd, a, s, grid);
+  if (fmt == KVQ_K8V4) return launch_fmt<KVQ_K8V4>(hd, a, s, grid);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvq

@@ -19,6 +19,11 @@
 //
 // Rows r = w * G + g: query token w of the window, head kvh * G + g.  Token
 // w sees cells [0, L - W + w].  A row with no visible cell outputs zeros.
+//
+// K8V4 (#711 kv: --kv k8v4 streams with --kv-resident, "What"): K is read
+// as int8; V as (nibble - 8) * d in the rotated basis, the CTA's merged
+// partial is rotated back (Walsh-Hadamard, divided by HD) before it is
+// written, and the combine, being linear in the partials, is unchanged.
 #include <math.h>
 
 #include "kvq_internal.cuh"
@@ -64,8 +69,9 @@ template <int FMT, int HD, int RP>
 __global__ void __launch_bounds__(kWarps * 32) decode_partial(DecodeArgs a) {
   constexpr int E = HD / 32;                // dims per lane in the P.V phase
   constexpr int NG = HD / kGroup;
-  constexpr int ESZ = FMT == KVQ_F16 ? 2 : 1;
+  constexpr int ESZ = FMT == KVQ_F16 ? 2 : 1;  // K (and F16 / int8 V) element bytes
   constexpr int EPW = 4 / ESZ;              // elements per 32-bit word
+  constexpr bool V4 = FMT == KVQ_K8V4;
   constexpr float kNegInf = -INFINITY;
 
   __shared__ __align__(16) float s_q[HD][RP];           // q * sm_scale * log2(e), [d][r]
@@ -120,7 +126,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_partial(DecodeArgs a) {
     if (row >= 0) {
       const uint8_t* kp = static_cast<const uint8_t*>(a.pool.k) + (size_t)row * HD * ESZ;
       uint32_t sc_bits[NG];
-      if constexpr (FMT == KVQ_Q8) {
+      if constexpr (FMT != KVQ_F16) {
         const unsigned short* ks =
             reinterpret_cast<const unsigned short*>(a.pool.ks) + (size_t)row * NG;
 #pragma unroll
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_partial(DecodeArgs a) {
 #pragma unroll
             for (int e = 0; e < EPW; ++e) {
               const int d = g * kGroup + ch * (16 / ESZ) + wi * EPW + e;
-              const float x = FMT == KVQ_Q8 ? code_i8(words[wi], e) : code_f16(words[wi], e);
+              const float x = FMT != KVQ_F16 ? code_i8(words[wi], e) : code_f16(words[wi], e);
 #pragma unroll
               for (int r4 = 0; r4 < RP / 4; ++r4) {
                 const float4 qv = *reinterpret_cast<const float4*>(&s_q[d][r4 * 4]);
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_partial(DecodeArgs a) {
             }
           }
         }
-        if constexpr (FMT == KVQ_Q8) {
+        if constexpr (FMT != KVQ_F16) {
           const float sf = __half2float(__ushort_as_half((unsigned short)sc_bits[g]));
 #pragma unroll
           for (int r = 0; r < RP; ++r) z[r] = fmaf(part[r], sf, z[r]);
@@ -192,6 +198,24 @@ __global__ void __launch_bounds__(kWarps * 32) decode_partial(DecodeArgs a) {
         pr[r4 * 4 + 1] = pv.y;
         pr[r4 * 4 + 2] = pv.z;
         pr[r4 * 4 + 3] = pv.w;
+      }
+      if constexpr (V4) {
+        // lane's E dims: E / 2 bytes of nibbles, one scale (E <= 32)
+        const uint8_t* vp = static_cast<const uint8_t*>(a.pool.v) + (size_t)rowc * (HD / 2) + lane * E / 2;
+        const float sv = __half2float(__ldg(a.pool.vs + (size_t)rowc * (HD / kQ4Block) + (lane * E) / kQ4Block));
+#pragma unroll
+        for (int r = 0; r < RP; ++r) pr[r] *= sv;
+        uint32_t bits;
+        if constexpr (E == 2) bits = __ldg(vp);
+        else if constexpr (E == 4) bits = __ldg(reinterpret_cast<const unsigned short*>(vp));
+        else bits = __ldg(reinterpret_cast<const uint32_t*>(vp));
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float x = (float)((int)((bits >> (4 * e)) & 15u) - 8);
+#pragma unroll
+          for (int r = 0; r < RP; ++r) o[r][e] = fmaf(pr[r], x, o[r][e]);
+        }
+        continue;
       }
       const uint8_t* vp =
           static_cast<const uint8_t*>(a.pool.v) + ((size_t)rowc * HD + lane * E) * ESZ;
@@ -264,9 +288,27 @@ __global__ void __launch_bounds__(kWarps * 32) decode_partial(DecodeArgs a) {
   }
 
   const size_t base = (((size_t)b * a.pool.n_kv + kvh) * a.nsplit + split) * a.R;
-  for (int i = threadIdx.x; i < a.R * HD; i += blockDim.x) {
-    const int r = i / HD, d = i - r * HD;
-    a.ws_o[(base + r) * HD + d] = s_o[r][d];
+  if constexpr (V4) {
+    // rotate each merged row back: one warp per row
+    constexpr int U = HD >= 128 ? 4 : 2, NI = HD / (32 * U);
+    for (int r = warp; r < a.R; r += kWarps) {
+      float x[NI][U];
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+#pragma unroll
+        for (int e = 0; e < U; ++e) x[i][e] = s_o[r][e + U * lane + 32 * U * i];
+      wht_warp<U, NI>(x, lane);
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+#pragma unroll
+        for (int e = 0; e < U; ++e)
+          a.ws_o[(base + r) * HD + e + U * lane + 32 * U * i] = x[i][e] * (1.0f / HD);
+    }
+  } else {
+    for (int i = threadIdx.x; i < a.R * HD; i += blockDim.x) {
+      const int r = i / HD, d = i - r * HD;
+      a.ws_o[(base + r) * HD + d] = s_o[r][d];
+    }
   }
   if (threadIdx.x < a.R) {
     const int r = threadIdx.x;
@@ -421,7 +463,7 @@ int decode_rows_pad(int hd, int rows) {
 }
 
 bool decode_supported(int fmt, int hd, int rows) {
-  if (fmt != KVQ_F16 && fmt != KVQ_Q8) return false;
+  if (fmt != KVQ_F16 && fmt != KVQ_Q8 && fmt != KVQ_K8V4) return false;
   if (hd != 64 && hd != 128 && hd != 256) return false;
   if (mma_decode_supported(fmt, hd, rows)) return true;
   const int rp = decode_rows_pad(hd, rows);
@@ -438,10 +480,14 @@ cudaError_t launch_decode(int fmt, int hd, const DecodePlan& plan, const DecodeA
     if (hd == 64) e = launch_rows<KVQ_F16, 64>(plan, a, s);
     else if (hd == 128) e = launch_rows<KVQ_F16, 128>(plan, a, s);
     else if (hd == 256) e = launch_rows<KVQ_F16, 256>(plan, a, s);
-  } else {
+  } else if (fmt == KVQ_Q8) {
     if (hd == 64) e = launch_rows<KVQ_Q8, 64>(plan, a, s);
     else if (hd == 128) e = launch_rows<KVQ_Q8, 128>(plan, a, s);
     else if (hd == 256) e = launch_rows<KVQ_Q8, 256>(plan, a, s);
+  } else if (fmt == KVQ_K8V4) {
+    if (hd == 64) e = launch_rows<KVQ_K8V4, 64>(plan, a, s);
+    else if (hd == 128) e = launch_rows<KVQ_K8V4, 128>(plan, a, s);
+    else if (hd == 256) e = launch_rows<KVQ_K8V4, 256>(plan, a, s);
   }
   if (e != cudaSuccess) return e;
   if (hd == 64) return launch_combine<64>(a, s);

@@ -61,17 +61,26 @@ constexpr unsigned kFull = 0xffffffffu;
 
 template <int FMT, int HD, int NT>
 struct Cfg {
+  static constexpr bool KI8 = FMT != KVQ_F16;            // K as int8 codes + scales
+  static constexpr bool V4 = FMT == KVQ_K8V4;            // V as rotated 4-bit codes
   static constexpr int ESZ = FMT == KVQ_F16 ? 2 : 1;
-  static constexpr int ROWB = HD * ESZ;                  // code bytes per cell row
+  static constexpr int ROWB = HD * ESZ;                  // K code bytes per cell row
   static constexpr int SWB = ROWB < 128 ? ROWB : 128;    // swizzle span (64 or 128 B)
   static constexpr int NCH = ROWB / SWB;                 // swizzle spans per row
   static constexpr int NG = HD / kGroup;
-  static constexpr int TILE_B = kTC * ROWB;              // K (or V) codes of a stage
-  static constexpr int SCALE_B = FMT == KVQ_Q8 ? kTC * NG * 2 : 0;
+  static constexpr int VROWB = V4 ? HD / 2 : ROWB;       // V code bytes per cell row
+  static constexpr int VSWB = VROWB < 128 ? VROWB : 128; // (32, 64 or 128 B)
+  static constexpr int VNCH = VROWB / VSWB;
+  static constexpr int VNS = V4 ? HD / kQ4Block : NG;    // V scales per cell row
+  static constexpr int TILE_B = kTC * ROWB;              // K codes of a stage
+  static constexpr int VTILE_B = kTC * VROWB;            // V codes of a stage
+  static constexpr int KSCALE_B = KI8 ? kTC * NG * 2 : 0;
+  static constexpr int VSCALE_B = KI8 ? kTC * VNS * 2 : 0;
+  static constexpr int SC_STAGE_B = KSCALE_B + VSCALE_B;
   // A stage holds the K and V code tiles (each a whole number of 1 KB
-  // swizzle atoms); the int8 scales of all stages live in a region of their
+  // swizzle atoms); the scales of all stages live in a region of their
   // own so no stage is padded.
-  static constexpr int STAGE_B = 2 * TILE_B;
+  static constexpr int STAGE_B = TILE_B + VTILE_B;
   // Three stages per CTA (one landing while two are read) and as many
   // 4-warp CTAs per SM as the 227 KB allow keep about 100 KB or more of
   // copies in flight per SM.
@@ -80,14 +89,14 @@ struct Cfg {
   static constexpr int SLAB_B = kConsumerWarps * NT * 8 * HD * 4;
   static constexpr int STAGES = (SLAB_B + STAGE_B - 1) / STAGE_B > 3 ? (SLAB_B + STAGE_B - 1) / STAGE_B : 3;
   static constexpr int OFF_V = TILE_B;
-  static constexpr int SMEM_SC = STAGES * STAGE_B;           // [STAGES][K, V][64 cells][NG] fp16
+  static constexpr int SMEM_SC = STAGES * STAGE_B;  // [STAGES]{K [64][NG], V [64][VNS]} fp16
   // q as fp16 hi / lo rows, padded by 16 bytes so ldmatrix rows hit distinct banks
   static constexpr int QROW = HD * 2 + 16;
   static constexpr int QBYTES_MAX = 2 * NT * 8 * QROW;   // hi and lo, NT*8 padded rows
-  static constexpr int SMEM_Q = SMEM_SC + STAGES * 2 * SCALE_B;
+  static constexpr int SMEM_Q = SMEM_SC + STAGES * SC_STAGE_B;
   // int8: per (padded row, 64-dim group, 32-dim half) 1152 * sum of q (hi + lo)
   static constexpr int SMEM_QC = SMEM_Q + (QBYTES_MAX + 15) / 16 * 16;
-  static constexpr int QC_BYTES = FMT == KVQ_Q8 ? (NT * 8 * NG * 2 * 4 + 15) / 16 * 16 : 0;
+  static constexpr int QC_BYTES = KI8 ? (NT * 8 * NG * 2 * 4 + 15) / 16 * 16 : 0;
   // per-warp row maxima and sums for the merge at the end: [4][RP][2] fp32
   static constexpr int SMEM_WML = SMEM_QC + QC_BYTES;
   static constexpr int SMEM_BAR = SMEM_WML + kConsumerWarps * NT * 8 * 2 * 4;
@@ -99,7 +108,8 @@ struct Cfg {
   static constexpr int FIT = (228 * 1024) / (SMEM + 1024);  // 1 KB reserved per CTA
   // 32-row tiles (NT 4) hold 4x the accumulators: at most 3 CTAs (168
   // registers a thread) so they do not spill
-  static constexpr int FIT_R = NT >= 4 ? (FIT < 3 ? FIT : 3) : FIT;
+  // (K8V4's 16-row tiles, whose smaller stages would fit 4, likewise)
+  static constexpr int FIT_R = (NT >= 4 || (V4 && NT >= 2)) ? (FIT < 3 ? FIT : 3) : FIT;
   static constexpr int MIN_CTAS = FIT_R >= 4 ? 4 : (FIT_R >= 3 ? 3 : (FIT_R >= 2 ? 2 : 1));
   static_assert(STAGES * STAGE_B >= SLAB_B, "merge slabs fit in the stages");
   // the SM's 228 KB hold MIN_CTAS of these CTAs (1 KB of each is reserved)
@@ -123,12 +133,16 @@ constexpr uint32_t kBias = 0x64806480u;  // fp16 1152 in both halves
 // cells, one span) is placed at its [span][first cell] slot, so the layout
 // and the swizzle (XOR of the 16-byte chunk with the line index mod 8 or 4)
 // do not depend on the block size.
+__device__ __forceinline__ uint32_t swz_off(int c, int b, int sw) {
+  const uint32_t off = ((uint32_t)(b / sw) * kTC + (uint32_t)c) * sw + (uint32_t)(b % sw);
+  // 128-byte swizzle: chunk bits [4:6] ^= address bits [7:9]; 64-byte:
+  // [4:5] ^= [7:8]; 32-byte: [4] ^= [7]
+  return off ^ (((off >> 7) & (uint32_t)(sw / 16 - 1)) << 4);
+}
+
 template <int FMT, int HD>
 __device__ __forceinline__ uint32_t tile_off(int c, int b) {
-  using C = Cfg<FMT, HD, 1>;
-  const uint32_t off = ((uint32_t)(b / C::SWB) * kTC + (uint32_t)c) * C::SWB + (uint32_t)(b % C::SWB);
-  // 128-byte swizzle: chunk bits [4:6] ^= address bits [7:9]; 64-byte: [4:5] ^= [7:8]
-  return off ^ (((off >> 7) & (C::SWB == 128 ? 7u : 3u)) << 4);
+  return swz_off(c, b, Cfg<FMT, HD, 1>::SWB);
 }
 
 __device__ __forceinline__ int clamp_len_mma(int L, const DecodeArgs& a) {
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       rows[p] = (p < n_pieces && blk >= 0 && blk < a.pool.n_blocks)
                     ? (blk * a.pool.n_kv + kvh) * bsz + (c & (bsz - 1))
                     : -1;
-      if (rows[p] >= 0) bytes += 2u * pc * C::ROWB + (FMT == KVQ_Q8 ? 2u * pc * C::NG * 2 : 0u);
+      if (rows[p] >= 0) bytes += (uint32_t)pc * (C::ROWB + C::VROWB + (C::KI8 ? (C::NG + C::VNS) * 2 : 0));
     }
     const uint32_t full = bar_full + 8 * s;
     mbar_expect_tx(full, bytes);
@@ -277,14 +291,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       for (int sp = 0; sp < C::NCH; ++sp) {
         const uint32_t so = (uint32_t)(sp * kTC + (p << pc_log2)) * C::SWB;
         tma_load_2d(st + so, &maps.k[sp], 0, row, full);
+      }
+#pragma unroll
+      for (int sp = 0; sp < C::VNCH; ++sp) {
+        const uint32_t so = (uint32_t)(sp * kTC + (p << pc_log2)) * C::VSWB;
         tma_load_2d(st + C::OFF_V + so, &maps.v[sp], 0, row, full);
       }
-      if constexpr (FMT == KVQ_Q8) {
-        const uint32_t sb = (uint32_t)pc * C::NG * 2;
-        const uint32_t soff = (uint32_t)p * sb;
-        const uint32_t sc = sbase + C::SMEM_SC + (uint32_t)s * 2 * C::SCALE_B;
-        bulk_load(sc + soff, a.pool.ks + (size_t)row * C::NG, sb, full);
-        bulk_load(sc + C::SCALE_B + soff, a.pool.vs + (size_t)row * C::NG, sb, full);
+      if constexpr (C::KI8) {
+        const uint32_t sbk = (uint32_t)pc * C::NG * 2, sbv = (uint32_t)pc * C::VNS * 2;
+        const uint32_t sc = sbase + C::SMEM_SC + (uint32_t)s * C::SC_STAGE_B;
+        bulk_load(sc + (uint32_t)p * sbk, a.pool.ks + (size_t)row * C::NG, sbk, full);
+        bulk_load(sc + C::KSCALE_B + (uint32_t)p * sbv, a.pool.vs + (size_t)row * C::VNS, sbv, full);
       }
     }
   };
@@ -309,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     if (i < RP * HD) {
       const int r = i / HD, k = i - r * HD;
       int dim = k;
-      if constexpr (FMT == KVQ_Q8) {
+      if constexpr (C::KI8) {
         const int ks = k >> 4, kq = k & 15;
         const int tt = (kq & 7) >> 1, e = kq & 1, hi8 = kq >> 3;
         dim = 16 * ks + 4 * tt + 2 * hi8 + e;
@@ -356,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         const __half lo = __float2half_rn(x - __half2float(h));
         *reinterpret_cast<__half*>(qs + r * C::QROW + k * 2) = h;
         *reinterpret_cast<__half*>(qs + (RP + r) * C::QROW + k * 2) = lo;
-        if constexpr (FMT == KVQ_Q8) {
+        if constexpr (C::KI8) {
           // The 32 lanes of a warp hold 32 consecutive k of one row and one
           // 64-dim group (RP * HD is a multiple of 128): their sum of q,
           // times 1152, fills the (row, group, half) slot of the int8 bias.
@@ -383,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // int8 K enters the MMA as fp16 (1152 + code) (no subtraction per
   // element); the 1152 * sum(q) of each (row, 64-dim group) is taken off
   // once, as the starting value of that group's hi accumulator.
-  float qcorr[C::NG > 0 ? (FMT == KVQ_Q8 ? C::NG : 1) : 1][NT][2];
-  if constexpr (FMT == KVQ_Q8) {
+  float qcorr[C::KI8 ? C::NG : 1][NT][2];
+  if constexpr (C::KI8) {
     const float* s_qc = reinterpret_cast<const float*>(smem + C::SMEM_QC);
 #pragma unroll
     for (int gq = 0; gq < C::NG; ++gq)
@@ -472,6 +489,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       }
     }
   }
+  // K8V4 V: the same matrix order over 16-byte chunks of the nibble rows
+  // (chunk = one 32-dim block), in the V tile's own swizzle span.
+  uint32_t vq[C::V4 ? C::VROWB / 32 : 1];
+  if constexpr (C::V4) {
+    const int mi = lane >> 3, rr = lane & 7;
+    const int ck = cl + ((mi & 1) << 3) + rr;
+#pragma unroll
+    for (int k = 0; k < C::VROWB / 32; ++k) vq[k] = C::OFF_V + swz_off(ck, 32 * k + 16 * (mi >> 1), C::VSWB);
+  }
   // shared-memory offset of the k-th 32-byte step of the kx row set
   auto kstep = [&](int k) -> uint32_t {
     if constexpr (C::SWB == 128) return kx[k & 3] + (uint32_t)(k >> 2) * kSpanB;
@@ -509,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   } else {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) z[nt][0] = z[nt][1] = z[nt][2] = z[nt][3] = 0.f;
-    const unsigned short* ksc = reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * 2 * C::SCALE_B);
+    const unsigned short* ksc = reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * C::SC_STAGE_B);
 #pragma unroll
     for (int gq = 0; gq < C::NG; ++gq) {
       // words: [k-step kk][cells +0 | +8], each the 4 code bytes of dims
@@ -634,9 +660,96 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         mma16816(o[mt][nt], af, bl[nt][0], bl[nt][1]);
       }
     }
+  } else if constexpr (C::V4) {
+    // P^T as the F16 path builds it; V carries its own scales
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint32_t h01, l01, h23, l23;
+      split_pair(p[nt][0], p[nt][1], h01, l01);
+      split_pair(p[nt][2], p[nt][3], h23, l23);
+      bh[nt][0] = movmatrix_t(h01);
+      bh[nt][1] = movmatrix_t(h23);
+      bl[nt][0] = movmatrix_t(l01);
+      bl[nt][1] = movmatrix_t(l23);
+    }
+    const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
+    const uint32_t mhi =
+        (2 * t + 8 < nvalid ? 0xffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
+    // the fp16 scales of this thread's cells 2t, 2t + 1, 2t + 8, 2t + 9
+    // (one 32-bit word per two blocks)
+    constexpr int SWD = C::VNS / 2;
+    const unsigned char* vsc = smem + C::SMEM_SC + s * C::SC_STAGE_B + C::KSCALE_B;
+    uint32_t sw[4][SWD];
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+      const unsigned char* src = vsc + (cl + 2 * t + (ci & 1) + 8 * (ci >> 1)) * (C::VNS * 2);
+      if constexpr (SWD == 4) {
+        const uint4 u = *reinterpret_cast<const uint4*>(src);
+        sw[ci][0] = u.x;
+        sw[ci][SWD > 1 ? 1 : 0] = u.y;
+        sw[ci][SWD > 2 ? 2 : 0] = u.z;
+        sw[ci][SWD > 3 ? 3 : 0] = u.w;
+      } else if constexpr (SWD == 2) {
+        const uint2 u = *reinterpret_cast<const uint2*>(src);
+        sw[ci][0] = u.x;
+        sw[ci][SWD > 1 ? 1 : 0] = u.y;
+      } else {
+        sw[ci][0] = *reinterpret_cast<const uint32_t*>(src);
+      }
+    }
+    // One ldmatrix.trans x4 per two 32-dim blocks, on 16-bit units of 4
+    // nibbles: register (cells 2t, 2t + 1; unit g) holds dims 4g .. 4g + 3
+    // of the block for both cells.  Nibble e of both halves becomes the
+    // fp16 pair (code - 8) exactly (OR into 1024's exponent, then minus
+    // 1032; for the upper nibble of a byte 1024 + 16 code, times 1/16,
+    // minus 72).  Its product with the cell's scale has up to 15
+    // significant bits, so it enters as hi = fp16(v) and lo = v - hi (exact,
+    // one fused multiply-add), and p.v takes hi.p_hi + hi.p_lo + lo.p_hi.
+    // M-tile 2 blk + h: row g is dim 32 blk + 4g + 2h, row g + 8 the dim
+    // after it.
+#pragma unroll
+    for (int kq = 0; kq < C::VROWB / 32; ++kq) {
+      uint32_t r[4];
+      ldsm_x4_t(r, st + vq[kq]);
+#pragma unroll
+      for (int jb = 0; jb < 2; ++jb) {
+        const int blk = 2 * kq + jb;
+        const uint32_t sel = (blk & 1) ? 0x7632u : 0x5410u;
+        const uint32_t slo = prmt(sw[0][blk >> 1], sw[1][blk >> 1], sel);
+        const uint32_t shi = prmt(sw[2][blk >> 1], sw[3][blk >> 1], sel);
+        const uint32_t wl = r[2 * jb], wh = r[2 * jb + 1];
+        const uint32_t wl8 = wl >> 8, wh8 = wh >> 8;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t xl = h ? wl8 : wl, xh = h ? wh8 : wh;
+          const uint32_t n4[4] = {nib_lo(xl), nib_hi(xl), nib_lo(xh), nib_hi(xh)};
+          const uint32_t s4[4] = {slo, slo, shi, shi};
+          uint32_t af[4], al[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            af[i] = hmul2(n4[i], s4[i]);
+            al[i] = hfma2(n4[i], s4[i], hneg2(af[i]));
+          }
+          if (nvalid < kCellsPerWarp) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              af[i] &= i < 2 ? mlo : mhi;
+              al[i] &= i < 2 ? mlo : mhi;
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(o[2 * blk + h][nt], af, bh[nt][0], bh[nt][1]);
+            mma16816(o[2 * blk + h][nt], af, bl[nt][0], bl[nt][1]);
+            mma16816(o[2 * blk + h][nt], al, bh[nt][0], bh[nt][1]);
+          }
+        }
+      }
+    }
   } else {
     const unsigned short* vsc =
-        reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * 2 * C::SCALE_B + C::SCALE_B);
+        reinterpret_cast<const unsigned short*>(smem + C::SMEM_SC + s * C::SC_STAGE_B + C::KSCALE_B);
 #pragma unroll
     for (int gv = 0; gv < C::NG; ++gv) {
       // p = 0 exactly for masked cells, whose scale bits may be anything
@@ -804,6 +917,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
           if constexpr (FMT == KVQ_F16) {  // m-tile rows g, g + 8 are dims 16 mt + g, + 8
             orow[mt * 16 + g] = wgt * o[mt][nt][j];
             orow[mt * 16 + g + 8] = wgt * o[mt][nt][2 + j];
+          } else if constexpr (C::V4) {   // K8V4: dims 32 (mt / 2) + 4g + 2 (mt % 2), + 1
+            *reinterpret_cast<float2*>(orow + (mt >> 1) * 32 + 4 * g + 2 * (mt & 1)) =
+                make_float2(wgt * o[mt][nt][j], wgt * o[mt][nt][2 + j]);
           } else {                        // int8: dims 16 mt + 2g, + 1
             *reinterpret_cast<float2*>(orow + mt * 16 + 2 * g) =
                 make_float2(wgt * o[mt][nt][j], wgt * o[mt][nt][2 + j]);
@@ -813,6 +929,37 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     }
   __syncthreads();
   const size_t slot0 = (((size_t)b * a.pool.n_kv + kvh) * a.nsplit + split) * a.R;
+  if constexpr (C::V4) {
+    // K8V4: the merged rows are in the rotated basis; one warp per row sums
+    // the slabs, rotates the row back (Walsh-Hadamard, divided by HD) and
+    // writes it.  The combine is linear in the partials, so it needs no
+    // change.
+    constexpr int U = HD >= 128 ? 4 : 2, NI = HD / (32 * U);
+    for (int r = warp; r < a.R; r += kConsumerWarps) {
+      float x[NI][U];
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int d0 = U * lane + 32 * U * i;
+#pragma unroll
+        for (int e = 0; e < U; ++e) {
+          const float* col = s_slab + r * HD + d0 + e;
+          x[i][e] = (col[0] + col[a.R * HD]) + (col[2 * a.R * HD] + col[3 * a.R * HD]);
+        }
+      }
+      wht_warp<U, NI>(x, lane);
+      float* dst = a.ws_o + (slot0 + r) * HD;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int d0 = U * lane + 32 * U * i;
+        if constexpr (U == 4)
+          *reinterpret_cast<float4*>(dst + d0) =
+              make_float4(x[i][0] * (1.0f / HD), x[i][1] * (1.0f / HD), x[i][U > 2 ? 2 : 0] * (1.0f / HD),
+                          x[i][U > 3 ? 3 : 0] * (1.0f / HD));
+        else
+          *reinterpret_cast<float2*>(dst + d0) = make_float2(x[i][0] * (1.0f / HD), x[i][1] * (1.0f / HD));
+      }
+    }
+  } else
   for (int i4 = threadIdx.x; i4 < a.R * HD / 4; i4 += kThreads) {
     const float4 v0 = reinterpret_cast<const float4*>(s_slab)[i4];
     const float4 v1 = reinterpret_cast<const float4*>(s_slab + a.R * HD)[i4];
@@ -1014,22 +1161,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
 }
 
-// Span sp of one codes array: [total rows][SWB bytes] starting at byte
-// sp * SWB of each row, box = one piece of cells.
-template <int FMT, int HD>
-bool make_map(CUtensorMap* map, const void* base, int sp, long long rows, int piece_cells) {
-  using C = Cfg<FMT, HD, 1>;
+// Span sp of one codes array: [total rows][span bytes] starting at byte
+// sp * span of each row (rows of row_bytes), box = one piece of cells, the
+// swizzle as wide as the span (32, 64 or 128 bytes).
+bool make_map(CUtensorMap* map, const void* base, int span, int row_bytes, int sp, long long rows,
+              int piece_cells) {
   auto enc = encoder();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)C::SWB, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)C::ROWB};
-  const cuuint32_t box[2] = {(cuuint32_t)C::SWB, (cuuint32_t)piece_cells};
+  const cuuint64_t dims[2] = {(cuuint64_t)span, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)span, (cuuint32_t)piece_cells};
   const cuuint32_t estr[2] = {1, 1};
-  void* span_base = static_cast<char*>(const_cast<void*>(base)) + (size_t)sp * C::SWB;
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, span_base, dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         C::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  void* span_base = static_cast<char*>(const_cast<void*>(base)) + (size_t)sp * span;
+  const CUtensorMapSwizzle sw = span == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, span_base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -1066,11 +1215,10 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
   const int piece = 1 << (a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6);
   TmaMaps maps;
   memset(&maps, 0, sizeof(maps));
-  for (int sp = 0; sp < C::NCH; ++sp) {
-    if (!make_map<FMT, HD>(&maps.k[sp], a.pool.k, sp, rows, piece) ||
-        !make_map<FMT, HD>(&maps.v[sp], a.pool.v, sp, rows, piece))
-      return cudaErrorInvalidValue;
-  }
+  for (int sp = 0; sp < C::NCH; ++sp)
+    if (!make_map(&maps.k[sp], a.pool.k, C::SWB, C::ROWB, sp, rows, piece)) return cudaErrorInvalidValue;
+  for (int sp = 0; sp < C::VNCH; ++sp)
+    if (!make_map(&maps.v[sp], a.pool.v, C::VSWB, C::VROWB, sp, rows, piece)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   const long long items = (long long)p.nsplit * a.pool.n_kv * a.n_seq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -1130,7 +1278,7 @@ bool mma_decode_supported(int fmt, int hd, int rows) {
   const int nt = n_tiles_for(rows);
   if (nt == 0 || rows < 1) return false;
   if (hd != 64 && hd != 128 && hd != 256) return false;
-  if (fmt != KVQ_F16 && fmt != KVQ_Q8) return false;
+  if (fmt != KVQ_F16 && fmt != KVQ_Q8 && fmt != KVQ_K8V4) return false;
   return nt * hd <= 256;
 }
 
@@ -1143,9 +1291,14 @@ int mma_ctas_per_sm(int fmt, int hd, int rows) {
     if (hd == 128) return ctas_per_sm_hd<KVQ_F16, 128>(nt);
     return ctas_per_sm_hd<KVQ_F16, 256>(nt);
   }
-  if (hd == 64) return ctas_per_sm_hd<KVQ_Q8, 64>(nt);
-  if (hd == 128) return ctas_per_sm_hd<KVQ_Q8, 128>(nt);
-  return ctas_per_sm_hd<KVQ_Q8, 256>(nt);
+  if (fmt == KVQ_Q8) {
+    if (hd == 64) return ctas_per_sm_hd<KVQ_Q8, 64>(nt);
+    if (hd == 128) return ctas_per_sm_hd<KVQ_Q8, 128>(nt);
+    return ctas_per_sm_hd<KVQ_Q8, 256>(nt);
+  }
+  if (hd == 64) return ctas_per_sm_hd<KVQ_K8V4, 64>(nt);
+  if (hd == 128) return ctas_per_sm_hd<KVQ_K8V4, 128>(nt);
+  return ctas_per_sm_hd<KVQ_K8V4, 256>(nt);
 }
 
 cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, const DecodeArgs& a,
@@ -1156,9 +1309,14 @@ cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, cons
     if (hd == 128) return launch_hd<KVQ_F16, 128>(nt, p, a, s);
     return launch_hd<KVQ_F16, 256>(nt, p, a, s);
   }
-  if (hd == 64) return launch_hd<KVQ_Q8, 64>(nt, p, a, s);
-  if (hd == 128) return launch_hd<KVQ_Q8, 128>(nt, p, a, s);
-  return launch_hd<KVQ_Q8, 256>(nt, p, a, s);
+  if (fmt == KVQ_Q8) {
+    if (hd == 64) return launch_hd<KVQ_Q8, 64>(nt, p, a, s);
+    if (hd == 128) return launch_hd<KVQ_Q8, 128>(nt, p, a, s);
+    return launch_hd<KVQ_Q8, 256>(nt, p, a, s);
+  }
+  if (hd == 64) return launch_hd<KVQ_K8V4, 64>(nt, p, a, s);
+  if (hd == 128) return launch_hd<KVQ_K8V4, 128>(nt, p, a, s);
+  return launch_hd<KVQ_K8V4, 256>(nt, p, a, s);
 }
 
 }  // namespace kvq

@@ -11,15 +11,61 @@
 namespace kvq {
 
 constexpr int kGroup = KVQ_GROUP;  // dims per fp16 scale in the int8 format
+constexpr int kQ4Block = KVQ_Q4_BLOCK;  // rotated V dims per fp16 scale in K8V4
+
+// Walsh-Hadamard transform (Sylvester order, no normalisation) of a row of
+// 32 * U * NI values held by one warp: lane l holds x[i][e] = dim e + U l +
+// 32 U i (units of U consecutive dims, the lanes' units side by side, NI
+// such runs).  The stages run h = 1, 2, ..., 16 U NI: those below U inside
+// a unit, those up to 16 U between lanes l and l ^ (h / U), the rest
+// between a lane's units.  Each stage turns dims (j, j + h), bit h of j
+// clear, into (x_j + x_{j+h}, x_j - x_{j+h}), so every fp32 sum and
+// difference is the one the stage-by-stage definition rounds.
+template <int U, int NI>
+__device__ __forceinline__ void wht_warp(float (&x)[NI][U], int lane) {
+#pragma unroll
+  for (int h = 1; h < U; h *= 2)
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+#pragma unroll
+      for (int e = 0; e < U; ++e)
+        if (!(e & h)) {
+          const float a = x[i][e], b = x[i][e + h];
+          x[i][e] = __fadd_rn(a, b);
+          x[i][e + h] = __fsub_rn(a, b);
+        }
+#pragma unroll
+  for (int hl = 1; hl < 32; hl *= 2) {
+    const bool upper = (lane & hl) != 0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+#pragma unroll
+      for (int e = 0; e < U; ++e) {
+        const float y = __shfl_xor_sync(0xffffffffu, x[i][e], hl);
+        x[i][e] = upper ? __fsub_rn(y, x[i][e]) : __fadd_rn(x[i][e], y);
+      }
+  }
+#pragma unroll
+  for (int hi = 1; hi < NI; hi *= 2)
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if (!(i & hi))
+#pragma unroll
+        for (int e = 0; e < U; ++e) {
+          const float a = x[i][e], b = x[i + hi][e];
+          x[i][e] = __fadd_rn(a, b);
+          x[i + hi][e] = __fsub_rn(a, b);
+        }
+}
 
 // ---------------------------------------------------------------------------
 // Pool geometry as the kernels see it.
 // ---------------------------------------------------------------------------
 struct Pool {
   const void* k;       // codes: fp16 or int8 [n_blocks][n_kv][bs][hd]
-  const void* v;
+  const void* v;       // (K8V4: V nibbles [n_blocks][n_kv][bs][hd/2])
   const __half* ks;    // scales: fp16 [n_blocks][n_kv][bs][hd/64] (int8 only)
-  const __half* vs;
+  const __half* vs;    // (K8V4: V scales [n_blocks][n_kv][bs][hd/32])
   int n_kv;
   int bs_log2;         // block size = 1 << bs_log2
   int n_blocks;
@@ -80,9 +126,9 @@ struct PersistArgs {
   const int32_t* block_row;
   int n_cells;
   void* codes_k;           // [n_cells][n_kv][hd]: written by gather, read by scatter
-  void* codes_v;
-  __half* scales_k;        // [n_cells][n_kv][hd/64] (int8 only)
-  __half* scales_v;
+  void* codes_v;           // (K8V4: [n_cells][n_kv][hd/2] nibbles)
+  __half* scales_k;        // [n_cells][n_kv][hd/64] (int8 and K8V4)
+  __half* scales_v;        // (K8V4: [n_cells][n_kv][hd/32])
 };
 
 // Launchers (host side, one per translation unit).  They return the launch

@@ -9,9 +9,11 @@
 // byte runs (codes, then scales).
 //
 // Runs: codes [n_cells][n_kv][hd] in the pool's element type, scales
-// [n_cells][n_kv][hd/64] fp16 (int8 only).  One thread moves 16 bytes of a
-// row of K and the same 16 bytes of V; the thread that takes a row's first
-// chunk also moves its scales.  Loads and stores are coalesced along the
+// [n_cells][n_kv][hd/64] fp16 (int8 only); K8V4's V runs are its nibbles
+// [n_cells][n_kv][hd/2] and scales [n_cells][n_kv][hd/32].  One thread
+// moves 16 bytes of a row of K and the same 16 bytes of V (while the V row
+// has them); the thread that takes a row's first chunk also moves its
+// scales.  Loads and stores are coalesced along the
 // row, then the KV heads, then the cells.  A block id out of range skips
 // its cells (the gather leaves them unwritten, the scatter writes nothing).
 #include "kvq_internal.cuh"
@@ -22,8 +24,11 @@ namespace {
 template <int FMT, int HD, bool GATHER>
 __global__ void __launch_bounds__(256) persist_kernel(PersistArgs a) {
   constexpr int ESZ = FMT == KVQ_F16 ? 2 : 1;
-  constexpr int CPR = HD * ESZ / 16;  // 16-byte chunks per row
+  constexpr int KROWB = HD * ESZ;                             // K row bytes
+  constexpr int VROWB = FMT == KVQ_K8V4 ? HD / 2 : KROWB;     // V row bytes
+  constexpr int CPR = KROWB / 16;  // 16-byte chunks per row (K, the longer one)
   constexpr int NG = HD / kGroup;
+  constexpr int NVS = FMT == KVQ_K8V4 ? HD / kQ4Block : NG;  // V scales per row
   const long long rows = (long long)a.n_cells * a.pool.n_kv;
   const long long total = rows * CPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -36,30 +41,35 @@ __global__ void __launch_bounds__(256) persist_kernel(PersistArgs a) {
     const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
     if (blk < 0 || blk >= a.pool.n_blocks) continue;
     const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
-    const size_t pool_off = row * HD * ESZ + (size_t)chunk * 16;
-    const size_t run_off = (size_t)r * HD * ESZ + (size_t)chunk * 16;
+    const size_t pool_off = row * KROWB + (size_t)chunk * 16;
+    const size_t run_off = (size_t)r * KROWB + (size_t)chunk * 16;
+    const size_t vpool_off = row * VROWB + (size_t)chunk * 16;
+    const size_t vrun_off = (size_t)r * VROWB + (size_t)chunk * 16;
+    const bool v_here = chunk * 16 < VROWB;
     if constexpr (GATHER) {
       *reinterpret_cast<uint4*>(static_cast<char*>(a.codes_k) + run_off) =
           __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.pool.k) + pool_off));
-      *reinterpret_cast<uint4*>(static_cast<char*>(a.codes_v) + run_off) =
-          __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.pool.v) + pool_off));
+      if (v_here)
+        *reinterpret_cast<uint4*>(static_cast<char*>(a.codes_v) + vrun_off) =
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.pool.v) + vpool_off));
     } else {
       *reinterpret_cast<uint4*>(static_cast<char*>(a.pool_k) + pool_off) =
           __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.codes_k) + run_off));
-      *reinterpret_cast<uint4*>(static_cast<char*>(a.pool_v) + pool_off) =
-          __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.codes_v) + run_off));
+      if (v_here)
+        *reinterpret_cast<uint4*>(static_cast<char*>(a.pool_v) + vpool_off) =
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.codes_v) + vrun_off));
     }
-    if constexpr (FMT == KVQ_Q8) {
+    if constexpr (FMT != KVQ_F16) {
       if (chunk == 0) {
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
-          if constexpr (GATHER) {
-            a.scales_k[(size_t)r * NG + gi] = a.pool.ks[row * NG + gi];
-            a.scales_v[(size_t)r * NG + gi] = a.pool.vs[row * NG + gi];
-          } else {
-            a.pool_ks[row * NG + gi] = a.scales_k[(size_t)r * NG + gi];
-            a.pool_vs[row * NG + gi] = a.scales_v[(size_t)r * NG + gi];
-          }
+          if constexpr (GATHER) a.scales_k[(size_t)r * NG + gi] = a.pool.ks[row * NG + gi];
+          else a.pool_ks[row * NG + gi] = a.scales_k[(size_t)r * NG + gi];
+        }
+#pragma unroll
+        for (int gi = 0; gi < NVS; ++gi) {
+          if constexpr (GATHER) a.scales_v[(size_t)r * NVS + gi] = a.pool.vs[row * NVS + gi];
+          else a.pool_vs[row * NVS + gi] = a.scales_v[(size_t)r * NVS + gi];
         }
       }
     }
@@ -92,8 +102,13 @@ cudaError_t launch_persist(int fmt, int hd, bool gather, const PersistArgs& a, c
   if (fmt == KVQ_F16)
     return gather ? launch_fmt<KVQ_F16, true>(hd, a, s, (int)blocks)
                   : launch_fmt<KVQ_F16, false>(hd, a, s, (int)blocks);
-  return gather ? launch_fmt<KVQ_Q8, true>(hd, a, s, (int)blocks)
-                : launch_fmt<KVQ_Q8, false>(hd, a, s, (int)blocks);
+  if (fmt == KVQ_Q8)
+    return gather ? launch_fmt<KVQ_Q8, true>(hd, a, s, (int)blocks)
+                  : launch_fmt<KVQ_Q8, false>(hd, a, s, (int)blocks);
+  if (fmt == KVQ_K8V4)
+    return gather ? launch_fmt<KVQ_K8V4, true>(hd, a, s, (int)blocks)
+                  : launch_fmt<KVQ_K8V4, false>(hd, a, s, (int)blocks);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvq

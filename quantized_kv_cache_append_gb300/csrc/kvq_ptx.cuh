@@ -107,6 +107,41 @@ static __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
   return d;
 }
 
+static __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+static __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+static __device__ __forceinline__ uint32_t hneg2(uint32_t a) {
+  uint32_t d;
+  asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// (a & b) | c in one instruction
+static __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 4-bit codes n (bits 0-3 of each 16-bit half) -> the fp16 pair n - 8,
+// exactly: 0x6400 | n is 1024 + n.
+static __device__ __forceinline__ uint32_t nib_lo(uint32_t w) {
+  return hsub2(and_or(w, 0x000f000fu, 0x64006400u), 0x64086408u);  // - 1032
+}
+// bits 4-7 of each half: 0x6400 | 16 n is 1024 + 16 n; / 16 - 72 = n - 8.
+static __device__ __forceinline__ uint32_t nib_hi(uint32_t w) {
+  return hfma2(and_or(w, 0x00f000f0u, 0x64006400u), 0x2c002c00u, 0xd480d480u);
+}
+
 static __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));

@@ -8,28 +8,39 @@ from __future__ import annotations
 
 import torch
 
-from . import (KVQ_F16, KVQ_GROUP, KVQ_Q8, check, kvq_append, kvq_compact_f16,
-               kvq_decode_attn, kvq_decode_workspace_bytes, make_cache)
+from . import (KVQ_F16, KVQ_GROUP, KVQ_K8V4, KVQ_Q4_BLOCK, KVQ_Q8, check, kvq_append,
+               kvq_compact_f16, kvq_decode_attn, kvq_decode_workspace_bytes, make_cache)
+
+
+def row_layout(fmt: int, head_dim: int):
+    """(K dtype, K elements per row, V dtype, V elements per row, K scales
+    per row, V scales per row) of one pool row in the given format."""
+    if fmt == KVQ_F16:
+        return torch.float16, head_dim, torch.float16, head_dim, 0, 0
+    if fmt == KVQ_Q8:
+        return torch.int8, head_dim, torch.int8, head_dim, head_dim // KVQ_GROUP, head_dim // KVQ_GROUP
+    if fmt == KVQ_K8V4:   # V: two 4-bit codes a byte, one scale per 32 rotated dims
+        return (torch.int8, head_dim, torch.uint8, head_dim // 2, head_dim // KVQ_GROUP,
+                head_dim // KVQ_Q4_BLOCK)
+    raise ValueError(f"unknown cache format {fmt}")
 
 
 class PagedPool:
-    """One layer's pool: codes [n_blocks][n_kv][bs][hd] (+ fp16 scales for int8)."""
+    """One layer's pool: codes [n_blocks][n_kv][bs][hd] (+ fp16 scales for int8;
+    K8V4: int8 K, V nibbles [..][hd/2], V scales [..][hd/32])."""
 
     def __init__(self, fmt: int, n_kv: int, head_dim: int, block_size: int, n_blocks: int,
                  device="cuda", fill: int = 0):
         self.fmt, self.n_kv, self.head_dim = fmt, n_kv, head_dim
         self.block_size, self.n_blocks = block_size, n_blocks
-        shape = (n_blocks, n_kv, block_size, head_dim)
-        dt = torch.float16 if fmt == KVQ_F16 else torch.int8
-        self.k = torch.full(shape, fill, dtype=dt, device=device) if fill else \
-            torch.zeros(shape, dtype=dt, device=device)
-        self.v = torch.zeros_like(self.k) if not fill else torch.full_like(self.k, fill)
-        if fmt == KVQ_Q8:
-            sshape = (n_blocks, n_kv, block_size, head_dim // KVQ_GROUP)
-            self.ks = torch.zeros(sshape, dtype=torch.float16, device=device)
-            self.vs = torch.zeros_like(self.ks)
-        else:
-            self.ks = self.vs = None
+        kdt, kn, vdt, vn, kng, vng = row_layout(fmt, head_dim)
+        lead = (n_blocks, n_kv, block_size)
+        make = lambda n, dt: torch.full(lead + (n,), fill, dtype=dt, device=device) if fill else \
+            torch.zeros(lead + (n,), dtype=dt, device=device)
+        self.k = make(kn, kdt)
+        self.v = make(vn, vdt)
+        self.ks = torch.zeros(lead + (kng,), dtype=torch.float16, device=device) if kng else None
+        self.vs = torch.zeros(lead + (vng,), dtype=torch.float16, device=device) if vng else None
         self.cache = make_cache(fmt, n_kv, head_dim, block_size, n_blocks,
                                 self.k, self.v, self.ks, self.vs)
 

@@ -17,7 +17,8 @@ from quantized_kv_cache_append_gb300.pool import PagedPool
 MAX_ABS = 2e-3
 REL_L2 = 1e-3
 
-FORMATS = {"f16": (kvq.KVQ_F16, oracle.FMT_F16), "q8": (kvq.KVQ_Q8, oracle.FMT_Q8)}
+FORMATS = {"f16": (kvq.KVQ_F16, oracle.FMT_F16), "q8": (kvq.KVQ_Q8, oracle.FMT_Q8),
+           "k8v4": (kvq.KVQ_K8V4, oracle.FMT_K8V4)}
 
 
 def dev(a):
@@ -52,7 +53,7 @@ class Pair:
         torch.cuda.synchronize()
         assert np.array_equal(host_bits(self.gpu.k), self.img.k), "K codes differ"
         assert np.array_equal(host_bits(self.gpu.v), self.img.v), "V codes differ"
-        if self.fmt_name == "q8":
+        if self.fmt_name != "f16":
             assert np.array_equal(host_bits(self.gpu.ks), self.img.ks), "K scales differ"
             assert np.array_equal(host_bits(self.gpu.vs), self.img.vs), "V scales differ"
 

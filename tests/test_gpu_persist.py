@@ -16,7 +16,7 @@ import torch
 import oracle
 import quantized_kv_cache_append_gb300 as kvq
 from quantized_kv_cache_append_gb300 import persist
-from quantized_kv_cache_append_gb300.pool import PagedPool
+from quantized_kv_cache_append_gb300.pool import PagedPool, row_layout
 from tests.gpu_pairs import Pair, dev, host_bits
 
 pytestmark = pytest.mark.gpu
@@ -42,20 +42,21 @@ def _case(fmt, n, n_kv, hd, bs, seed):
 
 
 def _gather_gpu(pool, row, n):
-    cdt = torch.float16 if pool.fmt == kvq.KVQ_F16 else torch.int8
-    ck = torch.empty((n, pool.n_kv, pool.head_dim), dtype=cdt, device="cuda")
-    cv = torch.empty_like(ck)
+    kdt, kn, vdt, vn, kng, vng = row_layout(pool.fmt, pool.head_dim)
+    ck = torch.empty((n, pool.n_kv, kn), dtype=kdt, device="cuda")
+    cv = torch.empty((n, pool.n_kv, vn), dtype=vdt, device="cuda")
     sk = sv = None
-    if pool.fmt == kvq.KVQ_Q8:
-        sk = torch.empty((n, pool.n_kv, pool.head_dim // 64), dtype=torch.float16, device="cuda")
-        sv = torch.empty_like(sk)
+    if kng:
+        sk = torch.empty((n, pool.n_kv, kng), dtype=torch.float16, device="cuda")
+        sv = torch.empty((n, pool.n_kv, vng), dtype=torch.float16, device="cuda")
     assert kvq.kvq_gather_cells(pool.cache, row, n, ck, cv, sk, sv) == kvq.KVQ_OK
     torch.cuda.synchronize()
     return ck, cv, sk, sv
 
 
 @pytest.mark.parametrize("fmt,hd,bs", [("f16", 128, 16), ("q8", 128, 256), ("q8", 256, 32),
-                                        ("f16", 64, 64)])
+                                        ("f16", 64, 64), ("k8v4", 256, 16), ("k8v4", 128, 64),
+                                        ("k8v4", 64, 32)])
 def test_gather_matches_oracle_and_scatter_restores(fmt, hd, bs):
     n, n_kv = 300, 2
     p, table = _case(fmt, n, n_kv, hd, bs, 40 + hd + bs)
@@ -86,7 +87,7 @@ def test_gather_matches_oracle_and_scatter_restores(fmt, hd, bs):
     assert torch.equal(o1, o2)
 
 
-@pytest.mark.parametrize("fmt", ["f16", "q8"])
+@pytest.mark.parametrize("fmt", ["f16", "q8", "k8v4"])
 def test_file_round_trip(tmp_path, fmt):
     n, n_kv, hd, bs = 200, 4, 128, 64
     p, table = _case(fmt, n, n_kv, hd, bs, 50)

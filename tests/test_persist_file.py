@@ -9,7 +9,7 @@ import struct
 import numpy as np
 import pytest
 
-from quantized_kv_cache_append_gb300 import KVQ_F16, KVQ_Q8
+from quantized_kv_cache_append_gb300 import KVQ_F16, KVQ_K8V4, KVQ_Q8
 from quantized_kv_cache_append_gb300 import persist
 
 
@@ -20,13 +20,17 @@ def _arrays(fmt, n, n_kv, hd, seed):
         cv = rng.standard_normal((n, n_kv, hd)).astype(np.float16).view(np.uint16)
         return ck, cv, None, None
     ck = rng.integers(-127, 128, (n, n_kv, hd)).astype(np.int8)
-    cv = rng.integers(-127, 128, (n, n_kv, hd)).astype(np.int8)
     sk = rng.random((n, n_kv, hd // 64)).astype(np.float16).view(np.uint16)
+    if fmt == KVQ_K8V4:   # V: nibble bytes and one scale per 32 dims
+        cv = rng.integers(0, 256, (n, n_kv, hd // 2)).astype(np.uint8)
+        sv = rng.random((n, n_kv, hd // 32)).astype(np.float16).view(np.uint16)
+        return ck, cv, sk, sv
+    cv = rng.integers(-127, 128, (n, n_kv, hd)).astype(np.int8)
     sv = rng.random((n, n_kv, hd // 64)).astype(np.float16).view(np.uint16)
     return ck, cv, sk, sv
 
 
-@pytest.mark.parametrize("fmt", [KVQ_F16, KVQ_Q8])
+@pytest.mark.parametrize("fmt", [KVQ_F16, KVQ_Q8, KVQ_K8V4])
 def test_round_trip(tmp_path, fmt):
     ck, cv, sk, sv = _arrays(fmt, 37, 3, 128, 1)
     tokens = np.arange(100, 137, dtype=np.int32)
@@ -36,7 +40,7 @@ def test_round_trip(tmp_path, fmt):
     np.testing.assert_array_equal(t, tokens)
     np.testing.assert_array_equal(ck2, ck)
     np.testing.assert_array_equal(cv2, cv)
-    if fmt == KVQ_Q8:
+    if fmt != KVQ_F16:
         np.testing.assert_array_equal(sk2, sk)
         np.testing.assert_array_equal(sv2, sv)
     else:
@@ -79,7 +83,8 @@ def test_fp16_pool_reads_a_version2_file(tmp_path):
     np.testing.assert_array_equal(cv2, cv)
 
 
-@pytest.mark.parametrize("how", ["geometry", "format", "truncated", "magic", "version"])
+@pytest.mark.parametrize("how", ["geometry", "format", "format_k8v4", "truncated", "magic",
+                                 "version"])
 def test_mismatched_or_damaged_files_are_refused(tmp_path, how):
     path = tmp_path / "c.kvq"
     persist.write_cells(path, KVQ_Q8, 2, 128, None, *_arrays(KVQ_Q8, 5, 2, 128, 5))
@@ -88,6 +93,8 @@ def test_mismatched_or_damaged_files_are_refused(tmp_path, how):
         n_kv = 4
     elif how == "format":
         fmt = KVQ_F16
+    elif how == "format_k8v4":
+        fmt = KVQ_K8V4
     elif how == "truncated":
         path.write_bytes(path.read_bytes()[:-7])
     elif how == "magic":
