@@ -14,6 +14,11 @@ entry points, called through the binding while capturing); `e2e` repeats
 the measurement through the same public calls without graphs, with the
 step's inputs copied from pinned host memory and the outputs read back every
 step.  `--impl reference` times the CPU oracle on the same workload.
+
+Beside the step (not in `value`): the K8V4 format (int8 K, rotated 4-bit V)
+on the same workload -- decode, one-cell and bulk append, compaction and
+gather / scatter -- under the "decode", "append", "compact_f16" and
+"persist" keys.
 """
 from __future__ import annotations
 
@@ -59,9 +64,15 @@ def _max_over_ranks(x: float, dist, world: int, device) -> float:
     return float(t.item())
 
 
-def _row_bytes(fmt_q8: bool, hd: int) -> int:
-    """Cache bytes per (cell, KV head): K and V codes (+ fp16 scale per 64 dims)."""
-    return 2 * (hd + 2 * (hd // 64)) if fmt_q8 else 2 * 2 * hd
+def _row_bytes(fmt, hd: int) -> int:
+    """Cache bytes per (cell, KV head): K and V codes (+ fp16 scale per 64
+    dims; K8V4: int8 K + scales, V nibbles + one fp16 scale per 32 dims).
+    fmt: "f16", "q8", "k8v4" (or a bool, True meaning "q8")."""
+    if fmt is True or fmt == "q8":
+        return 2 * (hd + 2 * (hd // 64))
+    if fmt == "k8v4":
+        return hd + 2 * (hd // 64) + hd // 2 + 2 * (hd // 32)
+    return 2 * 2 * hd
 
 
 def _step_ctx(s: int, L: int) -> int:
@@ -158,7 +169,7 @@ def run_kvq(args):
 
     import quantized_kv_cache_append_gb300 as kvq
     import workloads
-    from quantized_kv_cache_append_gb300.pool import PagedPool
+    from quantized_kv_cache_append_gb300.pool import PagedPool, row_layout
 
     rank, world, local = _dist()
     torch.cuda.set_device(local)
@@ -179,7 +190,8 @@ def run_kvq(args):
     layers = []
     for _ in range(LAYERS):
         pair = {}
-        for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8)):
+        # (K8V4, timed beside the step, not in it)
+        for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8), ("k8v4", kvq.KVQ_K8V4)):
             pool = PagedPool(fmt, n_kv, hd, bs, wl.n_blocks)
             pool.append(k_pre, v_pre, seq_pre, pos_pre, bt)
             ws_bytes = pool.workspace_bytes(1, 1, n_q, cap)
@@ -190,7 +202,7 @@ def run_kvq(args):
 
     # append throughput (bulk: the 32768-cell prefill), outside the timed steps
     append_mcells = {}
-    for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8)):
+    for name in ("f16", "q8", "k8v4"):
         pool = layers[0][name][0]
         for _ in range(3):
             pool.append(k_pre, v_pre, seq_pre, pos_pre, bt)
@@ -249,11 +261,11 @@ def run_kvq(args):
                 for i in range(n % chunk):
                     step(i)
 
-    bytes_per_step = {"f16": [], "q8": []}
+    bytes_per_step = {"f16": [], "q8": [], "k8v4": []}
     for s in range(chunk):
         ctx = _step_ctx(s, L)
-        bytes_per_step["f16"].append(ctx * n_kv * _row_bytes(False, hd))
-        bytes_per_step["q8"].append(ctx * n_kv * _row_bytes(True, hd))
+        for name in bytes_per_step:
+            bytes_per_step[name].append(ctx * n_kv * _row_bytes(name, hd))
     total_bytes = sum(bytes_per_step["f16"][s % chunk] + bytes_per_step["q8"][s % chunk]
                       for s in range(K))
 
@@ -282,7 +294,7 @@ def run_kvq(args):
 
     # per-kernel durations: graphs of decode-only steps, one format at a time
     kernel_ms = {}
-    for name in ("f16", "q8"):
+    for name in ("f16", "q8", "k8v4"):
         g = capture(chunk, formats=(name,), do_append=False)
         g.replay()
         torch.cuda.synchronize()
@@ -301,12 +313,21 @@ def run_kvq(args):
     b.record()
     torch.cuda.synchronize()
     append_step_us = a.elapsed_time(b) / chunk / 2 * 1e3
+    g = capture(chunk, formats=("k8v4",), do_decode=False)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    append_step_us_k8v4 = a.elapsed_time(b) / chunk * 1e3
 
     # FP16 compaction of a whole layer (32768 cells, both formats), layers in turn
     compact_us = {}
     ck = torch.empty((n_kv, L, hd), dtype=torch.float16, device="cuda")
     cv = torch.empty_like(ck)
-    for name in ("f16", "q8"):
+    for name in ("f16", "q8", "k8v4"):
         gc = torch.cuda.CUDAGraph()
         for i in range(LAYERS):
             layers[i][name][0].compact(bt[0], L, ck, cv)
@@ -327,15 +348,15 @@ def run_kvq(args):
 
     # gather / scatter of a whole layer's sequence (32768 cells), both formats
     persist_us = {}
-    for name in ("f16", "q8"):
+    for name in ("f16", "q8", "k8v4"):
         pool0 = layers[0][name][0]
-        cdt = torch.float16 if name == "f16" else torch.int8
-        ck = torch.empty((L, n_kv, hd), dtype=cdt, device="cuda")
-        cvv = torch.empty_like(ck)
+        kdt, kn, vdt, vn, kng, vng = row_layout(pool0.fmt, hd)
+        ck = torch.empty((L, n_kv, kn), dtype=kdt, device="cuda")
+        cvv = torch.empty((L, n_kv, vn), dtype=vdt, device="cuda")
         sk = sv = None
-        if name == "q8":
-            sk = torch.empty((L, n_kv, hd // 64), dtype=torch.float16, device="cuda")
-            sv = torch.empty_like(sk)
+        if kng:
+            sk = torch.empty((L, n_kv, kng), dtype=torch.float16, device="cuda")
+            sv = torch.empty((L, n_kv, vng), dtype=torch.float16, device="cuda")
         times = {}
         for op, fn in (("gather", kvq.kvq_gather_cells), ("scatter", kvq.kvq_scatter_cells)):
             for _ in range(3):
@@ -353,7 +374,7 @@ def run_kvq(args):
     peak, peak_kind = _peaks()
     avg_bytes = {n: sum(v) / len(v) for n, v in bytes_per_step.items()}
     gbs = {n: avg_bytes[n] / (kernel_ms[n] * 1e-3) / 1e9 for n in kernel_ms}
-    dominant = max(kernel_ms, key=kernel_ms.get)
+    dominant = max(("f16", "q8"), key=kernel_ms.get)   # of the step's two formats
     traffic = _ncu_traffic(dominant)
 
     # end to end through the public calls, host buffers, no graphs
@@ -383,18 +404,19 @@ def run_kvq(args):
                            "frac_of_nominal_8TBs": round(gbs[n] / 8000.0, 4)}
                        for n in kernel_ms},
             "append": {"bulk_Mcells_per_s": {n: round(v, 1) for n, v in append_mcells.items()},
-                       "one_cell_step_us": round(append_step_us, 3)},
+                       "one_cell_step_us": round(append_step_us, 3),
+                       "one_cell_step_us_k8v4": round(append_step_us_k8v4, 3)},
             "chunk_attn": chunk,
             "persist": {n: {op: {"us": round(t, 3),
-                                 "GB/s": round(2 * L * n_kv * _row_bytes(n == "q8", hd)
+                                 "GB/s": round(2 * L * n_kv * _row_bytes(n, hd)
                                                / (t * 1e-6) / 1e9, 1)}
                             for op, t in persist_us[n].items()}
                         for n in persist_us},
             "compact_f16": {n: {"us": round(compact_us[n], 3),
-                                "GB/s": round(L * n_kv * (_row_bytes(n == "q8", hd) + 4 * hd)
+                                "GB/s": round(L * n_kv * (_row_bytes(n, hd) + 4 * hd)
                                               / (compact_us[n] * 1e-6) / 1e9, 1),
                                 "frac_of_measured_hbm": round(
-                                    L * n_kv * (_row_bytes(n == "q8", hd) + 4 * hd)
+                                    L * n_kv * (_row_bytes(n, hd) + 4 * hd)
                                     / (compact_us[n] * 1e-6) / 1e9 / peak, 4)}
                             for n in compact_us},
             "clocks": clock_info,
@@ -621,8 +643,9 @@ def run_profile_case(args):
     L = int(wl.ctx_lens[0])
     k, v, seq, pos = dev(wl.k), dev(wl.v), dev(wl.tok_seq), dev(wl.tok_pos)
     q, ctx = dev(wl.q), dev(wl.ctx_lens)
-    for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8)):
-        if name not in wl.formats:
+    formats = args.profile_formats.split(",") if args.profile_formats else wl.formats
+    for name, fmt in (("f16", kvq.KVQ_F16), ("q8", kvq.KVQ_Q8), ("k8v4", kvq.KVQ_K8V4)):
+        if name not in formats:
             continue
         pool = PagedPool(fmt, wl.n_kv, wl.head_dim, wl.block_size, wl.n_blocks)
         for _ in range(args.profile_reps):
@@ -641,6 +664,8 @@ def main():
                     help="run a few launches of every kernel on one layer (for ncu)")
     ap.add_argument("--profile-workload", default="gqa32k")
     ap.add_argument("--profile-reps", type=int, default=3)
+    ap.add_argument("--profile-formats", default="",
+                    help="comma-separated cache formats for --profile-case (f16, q8, k8v4)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=8192)
     ap.add_argument("--warmup", type=int, default=512)

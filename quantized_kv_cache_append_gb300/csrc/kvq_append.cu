@@ -283,49 +283,19 @@ __device__ __forceinline__ uint32_t q4_code(float y, float d, float rs) {
   return (uint32_t)((int)fminf(fmaxf(r, -8.0f), 7.0f) + 8);
 }
 
-// K8V4 append: one warp per (token, KV head) row, K and V.  Lane l holds
-// units of U consecutive dims, dims U l + 32 U i (i < NI): the loads of a
-// unit are coalesced across the warp and the Walsh-Hadamard stages map onto
-// the layout (wht_warp).  K: int8 codes per 64-dim group, exactly as the
-// int8 format (group maximum over the 64 / U lanes of the group, then
-// group_scale and codes4).  V: rotated in fp32, then per block of 32
-// rotated dims (32 / U lanes) the element of largest magnitude, the first
-// one on ties (key: |y| bits above the complemented dim index; NaN counts
-// as 0 and a zero maximum gives m = +0, as the comparison-based definition
-// does), d = fp16(m / -8), and two codes a byte.
-template <int HD, int W>
-__global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
+// One K8V4 row (K and V of one token and KV head) held by a warp in the
+// lane layout described below; dr < 0 (a broken precondition, or a row
+// past the end) computes but stores nothing.  Every lane executes every
+// shuffle.
+template <int HD>
+__device__ __forceinline__ void k8v4_row(const AppendArgs& a, float (&xk)[HD / (32 * (HD >= 128 ? 4 : 2))][HD >= 128 ? 4 : 2],
+                                         float (&xv)[HD / (32 * (HD >= 128 ? 4 : 2))][HD >= 128 ? 4 : 2],
+                                         long long dr, int lane) {
   constexpr int U = HD >= 128 ? 4 : 2;
   constexpr int NI = HD / (32 * U);
   constexpr int LG = kGroup / U;     // lanes of a 64-dim K group
   constexpr int LB = kQ4Block / U;   // lanes of a 32-dim V block
   constexpr int NG = HD / kGroup, NB = HD / kQ4Block;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const long long rows = (long long)a.n_tok * a.n_kv;
-  const bool rows32 = rows <= 0x7fffffffLL;
-  const long long row = (long long)blockIdx.x * W + (threadIdx.x >> 5);
-  if (row >= rows) return;  // warp-uniform; no block-level barrier follows
-
-  float xk[NI][U], xv[NI][U];
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const size_t off = (size_t)row * HD + U * lane + 32 * U * i;
-    if constexpr (U == 4) {
-      const float4 k4 = __ldcs(reinterpret_cast<const float4*>(a.k + off));
-      const float4 v4 = __ldcs(reinterpret_cast<const float4*>(a.v + off));
-      xk[i][0] = k4.x; xk[i][1] = k4.y; xk[i][2] = k4.z; xk[i][3] = k4.w;
-      xv[i][0] = v4.x; xv[i][1] = v4.y; xv[i][2] = v4.z; xv[i][3] = v4.w;
-    } else {
-      const float2 k2 = __ldcs(reinterpret_cast<const float2*>(a.k + off));
-      const float2 v2 = __ldcs(reinterpret_cast<const float2*>(a.v + off));
-      xk[i][0] = k2.x; xk[i][1] = k2.y;
-      xv[i][0] = v2.x; xv[i][1] = v2.y;
-    }
-  }
-  const long long dr = dest_row(a, row, rows32);
-
   // ---- K: int8, one fp16 scale per 64 dims
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
@@ -359,28 +329,31 @@ __global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int d0 = U * lane + 32 * U * i;
-    unsigned long long key = 0;
+    // the block's largest |y| (NaN counts as 0) ...
+    uint32_t ab[U], amax = 0;
 #pragma unroll
     for (int e = 0; e < U; ++e) {
       const float y = xv[i][e];
-      const uint32_t ab = y == y ? (__float_as_uint(y) & 0x7fffffffu) : 0u;
-      const unsigned long long ke = ((unsigned long long)ab << 32) | (0xffffffffu - (uint32_t)(d0 + e));
-      key = ke > key ? ke : key;
+      ab[e] = y == y ? (__float_as_uint(y) & 0x7fffffffu) : 0u;
+      amax = max(amax, ab[e]);
     }
 #pragma unroll
-    for (int off = 1; off < LB; off <<= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-      key = o > key ? o : key;
-    }
-    // the value at the winning dim, from the lane that holds it
-    const int jwin = (int)(0xffffffffu - (uint32_t)key);
-    const int src = (jwin % (32 * U)) / U;   // lane of dim jwin
+    for (int off = 1; off < LB; off <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    // ... and the first dim holding it: the lowest lane of the block with a
+    // match (lanes hold ascending dims), its lowest unit element
+    int ef = U;
+#pragma unroll
+    for (int e = U - 1; e >= 0; --e)
+      if (ab[e] == amax) ef = e;
+    const unsigned hit = __ballot_sync(0xffffffffu, ef < U);
+    const unsigned blk_lanes = (LB == 32 ? 0xffffffffu : ((1u << LB) - 1u)) << ((lane / LB) * LB);
+    const int src = __ffs(hit & blk_lanes) - 1;
     float mine = 0.f;
 #pragma unroll
     for (int e = 0; e < U; ++e)
-      if (d0 + e == jwin) mine = xv[i][e];
+      if (e == ef) mine = xv[i][e];
     float m = __shfl_sync(0xffffffffu, mine, src);
-    if ((key >> 32) == 0) m = 0.0f;
+    if (amax == 0) m = 0.0f;  // no nonzero element: m stays +0
     const __half dh = __float2half_rn(m / -8.0f);
     const float d = __half2float(dh);
     if (dr < 0) continue;
@@ -401,6 +374,57 @@ __global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
       *dst = (uint8_t)(c[0] | (c[1] << 4));
     if (lane % LB == 0) a.vs_dst[dr * NB + d0 / kQ4Block] = dh;
   }
+}
+
+// K8V4 append: one warp per (token, KV head) row, K and V.  Lane l holds
+// units of U consecutive dims, dims U l + 32 U i (i < NI): the loads of a
+// unit are coalesced across the warp and the Walsh-Hadamard stages map onto
+// the layout (wht_warp).  K: int8 codes per 64-dim group, exactly as the
+// int8 format (group maximum over the 64 / U lanes of the group, then
+// group_scale and codes4).  V: rotated in fp32, then per block of 32
+// rotated dims (32 / U lanes) the element of largest magnitude, the first
+// one on ties (the block maximum of |y|, then the lowest dim holding it;
+// NaN counts as 0 and a zero maximum gives m = +0, as the comparison-based
+// definition does), d = fp16(m / -8), and two codes a byte.  A warp takes RPW
+// consecutive rows, all their loads issued before the first row's work.
+template <int HD, int W, int RPW>
+__global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
+  constexpr int U = HD >= 128 ? 4 : 2;
+  constexpr int NI = HD / (32 * U);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)a.n_tok * a.n_kv;
+  const bool rows32 = rows <= 0x7fffffffLL;
+  const long long row0 = ((long long)blockIdx.x * W + (threadIdx.x >> 5)) * RPW;
+  if (row0 >= rows) return;  // warp-uniform; no block-level barrier follows
+
+  float xk[RPW][NI][U], xv[RPW][NI][U];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r)
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+#pragma unroll
+      for (int e = 0; e < U; ++e) xk[r][i][e] = xv[r][i][e] = 0.f;
+      if (row0 + r >= rows) continue;
+      const size_t off = (size_t)(row0 + r) * HD + U * lane + 32 * U * i;
+      if constexpr (U == 4) {
+        const float4 k4 = __ldcs(reinterpret_cast<const float4*>(a.k + off));
+        const float4 v4 = __ldcs(reinterpret_cast<const float4*>(a.v + off));
+        xk[r][i][0] = k4.x; xk[r][i][1] = k4.y; xk[r][i][U > 2 ? 2 : 0] = k4.z; xk[r][i][U > 3 ? 3 : 0] = k4.w;
+        xv[r][i][0] = v4.x; xv[r][i][1] = v4.y; xv[r][i][U > 2 ? 2 : 0] = v4.z; xv[r][i][U > 3 ? 3 : 0] = v4.w;
+      } else {
+        const float2 k2 = __ldcs(reinterpret_cast<const float2*>(a.k + off));
+        const float2 v2 = __ldcs(reinterpret_cast<const float2*>(a.v + off));
+        xk[r][i][0] = k2.x; xk[r][i][1] = k2.y;
+        xv[r][i][0] = v2.x; xv[r][i][1] = v2.y;
+      }
+    }
+  long long dr[RPW];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) dr[r] = row0 + r < rows ? dest_row(a, row0 + r, rows32) : -1;
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) k8v4_row<HD>(a, xk[r], xv[r], dr[r], lane);
 }
 
 template <typename Kernel>
@@ -437,11 +461,14 @@ cudaError_t launch_q8(const AppendArgs& a, cudaStream_t s) {
   return launch_grid(append_q8_kernel<HD, 2, 8, false>, (groups + 127) / 128, 256, a, s);
 }
 
+// Few rows (decode steps): one row per warp, small CTAs; bulk: 8 warps of
+// 32 / (U NI) rows each (32 row values a lane in flight).
 template <int HD>
 cudaError_t launch_k8v4(const AppendArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.n_tok * a.n_kv;
-  constexpr int W = 4;
-  return launch_grid(append_k8v4_kernel<HD, W>, (rows + W - 1) / W, W * 32, a, s);
+  constexpr int RPW = HD == 256 ? 2 : 4;
+  if (rows < 4096) return launch_grid(append_k8v4_kernel<HD, 4, 1>, (rows + 3) / 4, 128, a, s);
+  return launch_grid(append_k8v4_kernel<HD, 8, RPW>, (rows + 8 * RPW - 1) / (8 * RPW), 256, a, s);
 }
 
 template <int HD>

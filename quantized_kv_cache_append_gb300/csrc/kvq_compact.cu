@@ -20,7 +20,9 @@
 // rotated Q4_0 V): K as the int8 format; V is decoded in the rotated basis,
 // (code - 8) * d (exact in fp32), rotated back by the same fp32 butterflies
 // as the append's rotation (wht_warp), divided by head_dim (a power of
-// two, exact) and rounded to fp16.  One warp per V row.
+// two, exact; applied to d first, which gives the same bits since scaling
+// by a power of two commutes with every rounded sum) and rounded to fp16.  One warp per V row, in a launch of its
+// own (after the K launch on the same stream).
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -44,6 +46,13 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// (fp16_rne(lo), fp16_rne(hi)) packed, one conversion
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 // Codes in bytes 0, 1 (sel 0x4140) or 2, 3 (sel 0x4342) of w, times scale s2.
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, uint32_t sel, uint32_t s2) {
   const uint32_t biased = w ^ 0x80808080u;  // c + 128 as unsigned bytes
@@ -51,45 +60,70 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, uint32_t sel, uint3
   return hmul2(h, s2);
 }
 
-// K8V4 V rows of KV head kvh, one warp per cell (grid-stride over warps).
+// K8V4 V rows: grid (cell groups, KV head), one warp per cell, RPW cells a
+// warp (their loads first); the grid covers every cell (the loop runs once
+// unless the x dimension was capped).
+constexpr int kV4RowsPerWarp = 2;
+
 template <int HD>
-__device__ __forceinline__ void compact_v4_rows(const CompactArgs& a, int kvh) {
+__global__ void __launch_bounds__(256) compact_v4_kernel(CompactArgs a) {
   constexpr int U = HD >= 128 ? 4 : 2;
   constexpr int NI = HD / (32 * U);
   constexpr int NB = HD / kQ4Block;
+  constexpr int RPW = kV4RowsPerWarp;
+  const int kvh = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int bs = 1 << a.pool.bs_log2;
-  for (int p = blockIdx.x * wpb + (threadIdx.x >> 5); p < a.n_cells; p += gridDim.x * wpb) {
-    const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
-    if (blk < 0 || blk >= a.pool.n_blocks) continue;  // warp-uniform skip
-    const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
-    const uint8_t* src = static_cast<const uint8_t*>(a.pool.v) + row * (HD / 2);
-    const __half* sc = a.pool.vs + row * NB;
-    float x[NI][U];
+  for (int p0 = (blockIdx.x * wpb + (threadIdx.x >> 5)) * RPW; p0 < a.n_cells;
+       p0 += gridDim.x * wpb * RPW) {
+    uint32_t bits[RPW][NI];
+    float d[RPW][NI];
+    bool ok[RPW];
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int d0 = U * lane + 32 * U * i;
-      const float d = __half2float(__ldg(sc + d0 / kQ4Block));
-      uint32_t bits;
-      if constexpr (U == 4) bits = __ldg(reinterpret_cast<const unsigned short*>(src + d0 / 2));
-      else bits = __ldg(src + d0 / 2);
+    for (int r = 0; r < RPW; ++r) {
+      const int p = p0 + r;
+      const int blk = p < a.n_cells ? __ldg(a.block_row + (p >> a.pool.bs_log2)) : -1;
+      ok[r] = blk >= 0 && blk < a.pool.n_blocks;  // warp-uniform
+      const size_t row = ok[r] ? ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1)) : 0;
+      const uint8_t* src = static_cast<const uint8_t*>(a.pool.v) + row * (HD / 2);
+      const __half* sc = a.pool.vs + row * NB;
 #pragma unroll
-      for (int e = 0; e < U; ++e) x[i][e] = __fmul_rn((float)((int)((bits >> (4 * e)) & 15u) - 8), d);
+      for (int i = 0; i < NI; ++i) {
+        const int d0 = U * lane + 32 * U * i;
+        bits[r][i] = 0;
+        d[r][i] = 0.f;
+        if (!ok[r]) continue;
+        // d / HD: the power-of-two factor of the inverse rotation, taken
+        // before the butterflies (exact, and it commutes with every sum)
+        d[r][i] = __half2float(__ldg(sc + d0 / kQ4Block)) * (1.0f / HD);
+        if constexpr (U == 4) bits[r][i] = __ldg(reinterpret_cast<const unsigned short*>(src + d0 / 2));
+        else bits[r][i] = __ldg(src + d0 / 2);
+      }
     }
-    wht_warp<U, NI>(x, lane);
-    __half* dst = a.out_v + ((size_t)kvh * a.n_cells + p) * HD;
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int d0 = U * lane + 32 * U * i;
-      uint32_t h[U];
+    for (int r = 0; r < RPW; ++r) {
+      if (!ok[r]) continue;  // out-of-range block or past the end: skip
+      float x[NI][U];
 #pragma unroll
-      for (int e = 0; e < U; ++e)
-        h[e] = __half_as_ushort(__float2half_rn(__fmul_rn(x[i][e], 1.0f / HD)));
-      if constexpr (U == 4)
-        *reinterpret_cast<uint2*>(dst + d0) = make_uint2(h[0] | (h[1] << 16), h[U > 2 ? 2 : 0] | (h[U > 3 ? 3 : 0] << 16));
-      else
-        *reinterpret_cast<uint32_t*>(dst + d0) = h[0] | (h[1] << 16);
+      for (int i = 0; i < NI; ++i)
+#pragma unroll
+        for (int e = 0; e < U; ++e) {
+          // 2^23 + code as float bits, minus 2^23 + 8: code - 8, exactly
+          const float c = __uint_as_float(0x4b000000u | ((bits[r][i] >> (4 * e)) & 15u)) - 8388616.0f;
+          x[i][e] = __fmul_rn(c, d[r][i]);
+        }
+      wht_warp<U, NI>(x, lane);
+      __half* dst = a.out_v + ((size_t)kvh * a.n_cells + p0 + r) * HD;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int d0 = U * lane + 32 * U * i;
+        if constexpr (U == 4)
+          *reinterpret_cast<uint2*>(dst + d0) =
+              make_uint2(f16x2_rn(x[i][0], x[i][1]), f16x2_rn(x[i][U > 2 ? 2 : 0], x[i][U > 3 ? 3 : 0]));
+        else
+          *reinterpret_cast<uint32_t*>(dst + d0) = f16x2_rn(x[i][0], x[i][1]);
+      }
     }
   }
 }
@@ -101,12 +135,6 @@ __global__ void __launch_bounds__(256) compact_kernel(CompactArgs a) {
   constexpr int NG = HD / kGroup;
   const int kvh = blockIdx.y % a.pool.n_kv;
   const int which = blockIdx.y / a.pool.n_kv;    // 0 = K, 1 = V
-  if constexpr (FMT == KVQ_K8V4) {
-    if (which == 1) {
-      compact_v4_rows<HD>(a, kvh);
-      return;
-    }
-  }
   const long long total = (long long)a.n_cells * CPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const int bs = 1 << a.pool.bs_log2;
@@ -160,9 +188,9 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int dpt = fmt == KVQ_F16 ? 8 : 16;  // K8V4: sized by its K rows
+  const int dpt = fmt == KVQ_F16 ? 8 : 16;
   const long long per_row = (long long)a.n_cells * (hd / dpt);  // threads per (K or V, KV head)
-  const int ys = 2 * a.pool.n_kv;
+  const int ys = (fmt == KVQ_K8V4 ? 1 : 2) * a.pool.n_kv;     // K8V4: K here, V below
   long long xs = (per_row + 255) / 256;
   const long long cap = ((long long)sms * 8 + ys - 1) / ys;  // about 8 CTAs per SM in total
   if (xs > cap) xs = cap;
@@ -171,8 +199,19 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   const dim3 grid((unsigned)xs, (unsigned)ys);
   if (fmt == KVQ_F16) return launch_fmt<KVQ_F16>(hd, a, s, grid);
   if (fmt == KVQ_Q8) return launch_fmt<KVQ_Q8>(hd, a, s, grid);
-  if (fmt == KVQ_K8V4) return launch_fmt<KVQ_K8V4>(hd, a, s, grid);
-  return cudaErrorInvalidValue;
+  if (fmt != KVQ_K8V4) return cudaErrorInvalidValue;
+  cudaError_t e = launch_fmt<KVQ_K8V4>(hd, a, s, grid);
+  if (e != cudaSuccess) return e;
+  long long vx = (a.n_cells + 8 * kV4RowsPerWarp - 1) / (8 * kV4RowsPerWarp);
+  if (vx > 0x7fffffffLL) vx = 0x7fffffffLL;
+  const dim3 vgrid((unsigned)vx, (unsigned)a.pool.n_kv);
+  switch (hd) {
+    case 64: compact_v4_kernel<64><<<vgrid, 256, 0, s>>>(a); break;
+    case 128: compact_v4_kernel<128><<<vgrid, 256, 0, s>>>(a); break;
+    case 256: compact_v4_kernel<256><<<vgrid, 256, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace kvq

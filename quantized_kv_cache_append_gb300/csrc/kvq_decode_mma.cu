@@ -673,6 +673,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       bl[nt][0] = movmatrix_t(l01);
       bl[nt][1] = movmatrix_t(l23);
     }
+    uint32_t bhn[NT][2];  // -p_hi, for the -lo halves of V
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      bhn[nt][0] = bh[nt][0] ^ 0x80008000u;
+      bhn[nt][1] = bh[nt][1] ^ 0x80008000u;
+    }
     const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
     const uint32_t mhi =
         (2 * t + 8 < nvalid ? 0xffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
@@ -705,7 +711,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     // 1032; for the upper nibble of a byte 1024 + 16 code, times 1/16,
     // minus 72).  Its product with the cell's scale has up to 15
     // significant bits, so it enters as hi = fp16(v) and lo = v - hi (exact,
-    // one fused multiply-add), and p.v takes hi.p_hi + hi.p_lo + lo.p_hi.
+    // one fused multiply-add, computed as hi - v with the negated scale),
+    // and p.v takes hi.p_hi + hi.p_lo + (-lo).(-p_hi).
     // M-tile 2 blk + h: row g is dim 32 blk + 4g + 2h, row g + 8 the dim
     // after it.
 #pragma unroll
@@ -718,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         const uint32_t sel = (blk & 1) ? 0x7632u : 0x5410u;
         const uint32_t slo = prmt(sw[0][blk >> 1], sw[1][blk >> 1], sel);
         const uint32_t shi = prmt(sw[2][blk >> 1], sw[3][blk >> 1], sel);
+        const uint32_t slo_n = slo ^ 0x80008000u, shi_n = shi ^ 0x80008000u;  // -scale
         const uint32_t wl = r[2 * jb], wh = r[2 * jb + 1];
         const uint32_t wl8 = wl >> 8, wh8 = wh >> 8;
 #pragma unroll
@@ -725,11 +733,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
           const uint32_t xl = h ? wl8 : wl, xh = h ? wh8 : wh;
           const uint32_t n4[4] = {nib_lo(xl), nib_hi(xl), nib_lo(xh), nib_hi(xh)};
           const uint32_t s4[4] = {slo, slo, shi, shi};
-          uint32_t af[4], al[4];
+          const uint32_t n4s[4] = {slo_n, slo_n, shi_n, shi_n};
+          uint32_t af[4], al[4];  // hi = fp16(v); al = hi - v = -lo (exact)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             af[i] = hmul2(n4[i], s4[i]);
-            al[i] = hfma2(n4[i], s4[i], hneg2(af[i]));
+            al[i] = hfma2(n4[i], n4s[i], af[i]);
           }
           if (nvalid < kCellsPerWarp) {
 #pragma unroll
@@ -742,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(o[2 * blk + h][nt], af, bh[nt][0], bh[nt][1]);
             mma16816(o[2 * blk + h][nt], af, bl[nt][0], bl[nt][1]);
-            mma16816(o[2 * blk + h][nt], al, bh[nt][0], bh[nt][1]);
+            mma16816(o[2 * blk + h][nt], al, bhn[nt][0], bhn[nt][1]);  // (-lo)(-p_hi)
           }
         }
       }

@@ -36,13 +36,15 @@ __device__ __forceinline__ void wht_warp(float (&x)[NI][U], int lane) {
         }
 #pragma unroll
   for (int hl = 1; hl < 32; hl *= 2) {
-    const bool upper = (lane & hl) != 0;
+    // the lower lane keeps x + y, the upper y - x: fma(x, +-1, y), whose
+    // product is exact, rounds the same sum or difference once
+    const float sgn = (lane & hl) ? -1.0f : 1.0f;
 #pragma unroll
     for (int i = 0; i < NI; ++i)
 #pragma unroll
       for (int e = 0; e < U; ++e) {
         const float y = __shfl_xor_sync(0xffffffffu, x[i][e], hl);
-        x[i][e] = upper ? __fsub_rn(y, x[i][e]) : __fadd_rn(x[i][e], y);
+        x[i][e] = __fmaf_rn(x[i][e], sgn, y);
       }
   }
 #pragma unroll
