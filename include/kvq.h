@@ -13,6 +13,8 @@
  *   kvq_chunk_attn   attention of a prompt chunk over that staging
  *   kvq_gather_cells / kvq_scatter_cells
  *                    a sequence's codes and scales out of / into the pool
+ *   kvq_stream_plan / kvq_stream_fetch
+ *                    a resident window of device blocks over a host copy
  *
  * Sources (page title, section):
  *   [kv-q8 PR]  "#3084 qwen35: FP16 K/V cache by default, int8 with --kv-q8
@@ -285,6 +287,84 @@ kvq_status kvq_gather_cells(const kvq_cache *cache, const int32_t *block_table_r
 kvq_status kvq_scatter_cells(const kvq_cache *cache, const int32_t *block_table_row, int n_cells,
                              const void *codes_k, const void *codes_v, const void *scales_k,
                              const void *scales_v, void *stream);
+
+/*
+ * Block streaming with a resident window ([k8v4 PR], "What" and "How": the
+ * cache's authoritative copy lives in pinned host memory and a window of
+ * N cells' worth of device blocks holds what the GPU reads; a block moves
+ * as its list of byte runs, so every format streams the same way; "Tests":
+ * attention over the streamed state is bitwise equal to attention over a
+ * fully resident pool).
+ *
+ * The host copy is a kvq_cache whose four arrays are pinned host memory
+ * the device can address (cudaHostAlloc'd or registered, mapped; on a
+ * Grace-Blackwell node the kernels reach it over NVLink-C2C), n_blocks of
+ * them; the window is an ordinary device kvq_cache of n_slots blocks with
+ * the same format and geometry.  Appends go to both (the host copy under
+ * the sequences' block table, the window under the slot table, where
+ * non-resident blocks are -1 and therefore skipped); attention and
+ * compaction read the window under the slot table.  One step:
+ *
+ *   kvq_append(host copy, block_table)        authoritative write
+ *   kvq_stream_plan(..., block_table, ctx)    slots, fetch list (host)
+ *   kvq_stream_fetch(host copy, window, list) missing blocks -> slots
+ *   kvq_append(window, slot_table)            resident blocks' new cells
+ *   kvq_decode_attn(window, slot_table)
+ */
+
+/*
+ * Residency plan for one call, host only (no device access, nothing
+ * launched).  The residency state is three caller-owned host arrays and a
+ * counter, initialised by the caller to -1 / -1 / 0 / 0:
+ *
+ *   slot_of_block [n_host_blocks]  int32: window slot of a host block, -1
+ *   block_of_slot [n_slots]        int32: host block in a slot, -1 if free
+ *   last_use      [n_slots]        int64: the counter value of the slot's
+ *                                  last plan
+ *   clock                          int64: advanced by one per plan
+ *
+ * Inputs (host int32): block_table [n_seq][max_blocks_per_seq] of host
+ * block ids, ctx_lens [n_seq] (cells each sequence's call reads, its new
+ * cells included), block_size.  The call reads blocks [0, ceil(ctx_lens[b]
+ * / block_size)) of each row; ids outside [0, n_host_blocks) are ignored.
+ * Every distinct block read gets a slot: a resident one keeps its slot (a
+ * hit); the others take, in order of first use, free slots in index
+ * order, then the slots this call does not read, least recently used first
+ * (ties: lower index).  Outputs (host): slot_table [n_seq][max_blocks_per_seq]
+ * (the slot of each entry's block, -1 where it is not resident),
+ * fetch_src / fetch_dst [capacity n_slots] the (host block, slot) pairs
+ * to fetch, *n_fetch their count, *n_hits (may be NULL) the hits.  A call
+ * that reads more distinct blocks than n_slots returns KVQ_ERR_UNSUPPORTED
+ * and changes nothing; invalid sizes or NULL arrays return KVQ_ERR_ARG.
+ * The function uses temporary host memory and keeps no state of its own.
+ */
+kvq_status kvq_stream_plan(int n_host_blocks, int n_slots, int32_t *slot_of_block,
+                           int32_t *block_of_slot, int64_t *last_use, int64_t *clock,
+                           const int32_t *block_table, int n_seq, int max_blocks_per_seq,
+                           const int32_t *ctx_lens, int block_size, int32_t *slot_table,
+                           int32_t *fetch_src, int32_t *fetch_dst, int *n_fetch, int *n_hits);
+
+/*
+ * Copy n_fetch blocks from the host copy into window slots: block
+ * fetch_src[i] of every run of host_copy goes to block fetch_dst[i] of the
+ * same run of window, bits unchanged (two runs for KVQ_F16, four
+ * otherwise).  One kernel reads the host memory directly (16-byte loads,
+ * several in flight per thread) and writes the window; no copy engine is
+ * involved.  fetch_src / fetch_dst: int32 [n_fetch] that the device can
+ * read (device memory or mapped pinned host memory, e.g. the plan's
+ * outputs in pinned memory).  Both caches must pass the kvq_append checks
+ * and agree in format, n_kv_heads, head_dim and block_size (else
+ * KVQ_ERR_ARG); every array of the host copy must be device-addressable
+ * at its own address (the runtime's pointer attributes give it that device
+ * address: pinned memory under unified addressing, device or managed
+ * memory), so that kvq_append can write it too, else KVQ_ERR_ARG -- checked
+ * even when n_fetch is 0, so a call with n_fetch 0 validates a host copy
+ * before anything writes to it.  Ids out of range skip their fetch.  Two
+ * fetches must not name the same slot.  Asynchronous on `stream`.
+ */
+kvq_status kvq_stream_fetch(const kvq_cache *host_copy, const kvq_cache *window,
+                            const int32_t *fetch_src, const int32_t *fetch_dst, int n_fetch,
+                            void *stream);
 
 /*
  * Bytes of device scratch that kvq_decode_attn_static keeps in the library

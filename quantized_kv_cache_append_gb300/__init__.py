@@ -39,6 +39,8 @@ EXPORTED_SYMBOLS = (
     "kvq_chunk_attn",
     "kvq_gather_cells",
     "kvq_scatter_cells",
+    "kvq_stream_plan",
+    "kvq_stream_fetch",
     "kvq_decode_attn_static",
     "kvq_status_string",
 )
@@ -102,6 +104,10 @@ def load_library(path: Optional[str] = None):
     lib.kvq_gather_cells.argtypes = [CP, P, I, P, P, P, P, P]
     lib.kvq_scatter_cells.restype = I
     lib.kvq_scatter_cells.argtypes = [CP, P, I, P, P, P, P, P]
+    lib.kvq_stream_plan.restype = I
+    lib.kvq_stream_plan.argtypes = [I, I, P, P, P, P, P, I, I, P, I, P, P, P, P, P]
+    lib.kvq_stream_fetch.restype = I
+    lib.kvq_stream_fetch.argtypes = [CP, CP, P, P, I, P]
     lib.kvq_decode_attn_static.restype = I
     lib.kvq_decode_attn_static.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P]
     lib.kvq_status_string.restype = ctypes.c_char_p
@@ -119,6 +125,8 @@ def _ptr(x):
         return x
     if hasattr(x, "data_ptr"):
         return x.data_ptr()
+    if hasattr(x, "ctypes") and hasattr(x, "dtype"):   # numpy (host) array
+        return x.ctypes.data
     raise TypeError(f"cannot take the address of {type(x)}")
 
 
@@ -200,6 +208,24 @@ def kvq_decode_attn_static(cache: kvq_cache, q, n_seq: int, W: int, n_q: int, ct
                                                  _ptr(ctx_lens), max_ctx, _ptr(block_table),
                                                  max_blocks_per_seq, float(sm_scale), _ptr(out),
                                                  _stream(stream))
+
+
+def kvq_stream_plan(n_host_blocks: int, n_slots: int, slot_of_block, block_of_slot, last_use,
+                    clock, block_table, n_seq: int, max_blocks_per_seq: int, ctx_lens,
+                    block_size: int, slot_table, fetch_src, fetch_dst, n_fetch, n_hits=None) -> int:
+    """Host-only residency plan; every array argument is host memory (numpy
+    arrays or CPU tensors); n_fetch / n_hits are 1-element int32 arrays."""
+    return load_library().kvq_stream_plan(
+        n_host_blocks, n_slots, _ptr(slot_of_block), _ptr(block_of_slot), _ptr(last_use),
+        _ptr(clock), _ptr(block_table), n_seq, max_blocks_per_seq, _ptr(ctx_lens), block_size,
+        _ptr(slot_table), _ptr(fetch_src), _ptr(fetch_dst), _ptr(n_fetch), _ptr(n_hits))
+
+
+def kvq_stream_fetch(host_copy: kvq_cache, window: kvq_cache, fetch_src, fetch_dst,
+                     n_fetch: int, stream=None) -> int:
+    return load_library().kvq_stream_fetch(ctypes.byref(host_copy), ctypes.byref(window),
+                                           _ptr(fetch_src), _ptr(fetch_dst), n_fetch,
+                                           _stream(stream))
 
 
 def kvq_status_string(status: int) -> str:

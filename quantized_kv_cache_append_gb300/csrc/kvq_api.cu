@@ -353,6 +353,60 @@ KVQ_API kvq_status kvq_chunk_attn(const void* k16, const void* v16, int n_kv_hea
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+KVQ_API kvq_status kvq_stream_plan(int n_host_blocks, int n_slots, int32_t* slot_of_block,
+                                   int32_t* block_of_slot, int64_t* last_use, int64_t* clock,
+                                   const int32_t* block_table, int n_seq, int max_blocks_per_seq,
+                                   const int32_t* ctx_lens, int block_size, int32_t* slot_table,
+                                   int32_t* fetch_src, int32_t* fetch_dst, int* n_fetch,
+                                   int* n_hits) {
+  if (n_host_blocks <= 0 || n_slots <= 0 || n_seq < 0 || max_blocks_per_seq <= 0 || block_size <= 0)
+    return KVQ_ERR_ARG;
+  if (slot_of_block == nullptr || block_of_slot == nullptr || last_use == nullptr ||
+      clock == nullptr || fetch_src == nullptr || fetch_dst == nullptr || n_fetch == nullptr)
+    return KVQ_ERR_ARG;
+  if (n_seq > 0 && (block_table == nullptr || ctx_lens == nullptr || slot_table == nullptr))
+    return KVQ_ERR_ARG;
+  return kvq::stream_plan(n_host_blocks, n_slots, slot_of_block, block_of_slot, last_use, clock,
+                          block_table, n_seq, max_blocks_per_seq, ctx_lens, block_size, slot_table,
+                          fetch_src, fetch_dst, n_fetch, n_hits);
+}
+
+KVQ_API kvq_status kvq_stream_fetch(const kvq_cache* host_copy, const kvq_cache* window,
+                                    const int32_t* fetch_src, const int32_t* fetch_dst, int n_fetch,
+                                    void* stream) {
+  kvq_status st = check_cache(host_copy);
+  if (st != KVQ_OK) return st;
+  st = check_cache(window);
+  if (st != KVQ_OK) return st;
+  if (host_copy->fmt != window->fmt || host_copy->n_kv_heads != window->n_kv_heads ||
+      host_copy->head_dim != window->head_dim || host_copy->block_size != window->block_size)
+    return KVQ_ERR_ARG;
+  if (n_fetch < 0) return KVQ_ERR_ARG;
+  // Every run of the host copy must be memory the device can address at
+  // the same address (pinned and mapped under unified addressing, or device
+  // / managed memory).  Anything else is refused here rather than faulting
+  // in a kernel.
+  kvq_cache h = *host_copy;
+  void** runs[4] = {&h.k_data, &h.v_data, &h.k_scales, &h.v_scales};
+  const int n_runs = h.fmt == KVQ_F16 ? 2 : 4;
+  for (int r = 0; r < n_runs; ++r) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, *runs[r]) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return KVQ_ERR_ARG;
+    }
+    // the same address on both sides (unified addressing), so the appends
+    // that write the host copy through this descriptor reach it too
+    if (at.devicePointer == nullptr || at.devicePointer != *runs[r]) return KVQ_ERR_ARG;
+  }
+  if (n_fetch == 0) return KVQ_OK;
+  if (fetch_src == nullptr || fetch_dst == nullptr || !aligned(fetch_src, 4) || !aligned(fetch_dst, 4))
+    return KVQ_ERR_ARG;
+  const cudaError_t e = launch_fetch(window->fmt, window->head_dim, &h, window, fetch_src,
+                                     fetch_dst, n_fetch, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 KVQ_API const char* kvq_status_string(int status) {
   switch (status) {
     case KVQ_OK: return "KVQ_OK";

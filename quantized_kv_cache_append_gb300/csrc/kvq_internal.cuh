@@ -157,6 +157,16 @@ cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, cons
 // if the driver does not provide it.
 void* tensor_map_encoder();
 
+// Block streaming (kvq_stream.cu): the residency plan (host only) and the
+// fetch of blocks from the host copy into window slots.
+kvq_status stream_plan(int n_host_blocks, int n_slots, int32_t* slot_of_block, int32_t* block_of_slot,
+                       int64_t* last_use, int64_t* clock, const int32_t* block_table, int n_seq,
+                       int max_blocks, const int32_t* ctx_lens, int block_size, int32_t* slot_table,
+                       int32_t* fetch_src, int32_t* fetch_dst, int* n_fetch, int* n_hits);
+cudaError_t launch_fetch(int fmt, int hd, const kvq_cache* host, const kvq_cache* win,
+                         const int32_t* fetch_src, const int32_t* fetch_dst, int n_fetch,
+                         cudaStream_t s);
+
 // Prompt-chunk attention over fp16 staging (kvq_chunk.cu).
 struct ChunkArgs {
   const __half* k16;   // [n_kv][P][hd]

@@ -30,17 +30,25 @@ class PagedPool:
     K8V4: int8 K, V nibbles [..][hd/2], V scales [..][hd/32])."""
 
     def __init__(self, fmt: int, n_kv: int, head_dim: int, block_size: int, n_blocks: int,
-                 device="cuda", fill: int = 0):
+                 device="cuda", fill: int = 0, pinned: bool = False):
+        """pinned: hold the arrays in pinned host memory (a streaming host
+        copy, which the kernels address directly) instead of on `device`."""
         self.fmt, self.n_kv, self.head_dim = fmt, n_kv, head_dim
         self.block_size, self.n_blocks = block_size, n_blocks
         kdt, kn, vdt, vn, kng, vng = row_layout(fmt, head_dim)
         lead = (n_blocks, n_kv, block_size)
-        make = lambda n, dt: torch.full(lead + (n,), fill, dtype=dt, device=device) if fill else \
-            torch.zeros(lead + (n,), dtype=dt, device=device)
+        where = dict(device="cpu", pin_memory=True) if pinned else dict(device=device)
+
+        def make(n, dt):
+            t = torch.zeros(lead + (n,), dtype=dt, **where)
+            if fill:
+                t.fill_(fill)
+            return t
+
         self.k = make(kn, kdt)
         self.v = make(vn, vdt)
-        self.ks = torch.zeros(lead + (kng,), dtype=torch.float16, device=device) if kng else None
-        self.vs = torch.zeros(lead + (vng,), dtype=torch.float16, device=device) if vng else None
+        self.ks = make(kng, torch.float16) if kng else None
+        self.vs = make(vng, torch.float16) if vng else None
         self.cache = make_cache(fmt, n_kv, head_dim, block_size, n_blocks,
                                 self.k, self.v, self.ks, self.vs)
 

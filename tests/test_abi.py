@@ -146,3 +146,15 @@ def test_workspace_size_grows_with_context(lib):
     b = kvq.kvq_decode_workspace_bytes(c, 1, 1, 32, 32768)
     assert 0 < a <= b
     assert kvq.kvq_decode_workspace_bytes(c, 1, 1, 30, 1024) == 0
+
+
+@no_gpu_only
+def test_stream_fetch_refuses_mismatched_or_bad_arguments(lib):
+    win = _cache(n_blocks=2)
+    for bad in (dict(head_dim=256), dict(block_size=128), dict(n_kv_heads=4),
+                dict(fmt=kvq.KVQ_F16), dict(k_scales=None), dict(k_data=FAKE + 16)):
+        host = _cache(**bad)
+        assert kvq.kvq_stream_fetch(host, win, FAKE, FAKE, 1, 0) == kvq.KVQ_ERR_ARG
+    assert kvq.kvq_stream_fetch(_cache(), win, FAKE, FAKE, -1, 0) == kvq.KVQ_ERR_ARG
+    # without a GPU no address is device-addressable: refused before any launch
+    assert kvq.kvq_stream_fetch(_cache(), win, FAKE, FAKE, 1, 0) == kvq.KVQ_ERR_ARG
