@@ -371,6 +371,8 @@ def run_kvq(args):
             times[op] = a.elapsed_time(b) / 10 * 1e3
         persist_us[name] = times
 
+    stream = _stream_bench(torch, kvq, layers, n_kv, hd, bs, wl.n_blocks)
+
     peak, peak_kind = _peaks()
     avg_bytes = {n: sum(v) / len(v) for n, v in bytes_per_step.items()}
     gbs = {n: avg_bytes[n] / (kernel_ms[n] * 1e-3) / 1e9 for n in kernel_ms}
@@ -407,6 +409,7 @@ def run_kvq(args):
                        "one_cell_step_us": round(append_step_us, 3),
                        "one_cell_step_us_k8v4": round(append_step_us_k8v4, 3)},
             "chunk_attn": chunk,
+            "stream": stream,
             "persist": {n: {op: {"us": round(t, 3),
                                  "GB/s": round(2 * L * n_kv * _row_bytes(n, hd)
                                                / (t * 1e-6) / 1e9, 1)}
@@ -426,6 +429,52 @@ def run_kvq(args):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def _stream_bench(torch, kvq, layers, n_kv, hd, bs, n_blocks):
+    """Block streaming: a whole gqa32k layer (all its blocks) fetched from a
+    pinned host copy into an empty window by kvq_stream_fetch, per format,
+    against the pinned host-to-device copy of the same runs by the copy
+    engine (cudaMemcpyAsync through torch), the link's measured rate."""
+    from quantized_kv_cache_append_gb300.pool import PagedPool
+
+    out = {}
+    src = torch.arange(n_blocks, dtype=torch.int32, device="cuda")
+    for name in ("f16", "q8", "k8v4"):
+        dpool = layers[0][name][0]
+        host = PagedPool(dpool.fmt, n_kv, hd, bs, n_blocks, pinned=True)
+        win = PagedPool(dpool.fmt, n_kv, hd, bs, n_blocks)
+        runs = [(h, d) for h, d in ((host.k, dpool.k), (host.v, dpool.v), (host.ks, dpool.ks),
+                                    (host.vs, dpool.vs)) if h is not None]
+        for h, d in runs:
+            h.copy_(d)
+        torch.cuda.synchronize()
+        nbytes = sum(h.numel() * h.element_size() for h, _ in runs)
+
+        def timed(fn, reps=10):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps * 1e3
+
+        fetch_us = timed(lambda: kvq.check(
+            kvq.kvq_stream_fetch(host.cache, win.cache, src, src, n_blocks), "kvq_stream_fetch"))
+        wins = [(w, h) for w, h in ((win.k, host.k), (win.v, host.v), (win.ks, host.ks),
+                                    (win.vs, host.vs)) if h is not None]
+        copy_us = timed(lambda: [w.copy_(h, non_blocking=True) for w, h in wins])
+        ok = all(torch.equal(w, d) for (w, _), (_, d) in zip(wins, runs))
+        out[name] = {"bytes": nbytes, "fetch_us": round(fetch_us, 2),
+                     "fetch_GB/s": round(nbytes / (fetch_us * 1e-6) / 1e9, 1),
+                     "h2d_copy_GB/s": round(nbytes / (copy_us * 1e-6) / 1e9, 1),
+                     "frac_of_h2d_copy": round(copy_us / fetch_us, 4), "bits_equal": ok}
+        del host, win
+    return out
 
 
 def _chunk_attn_bench(torch, kvq):
