@@ -18,7 +18,9 @@ step.  `--impl reference` times the CPU oracle on the same workload.
 Beside the step (not in `value`): the K8V4 format (int8 K, rotated 4-bit V)
 on the same workload -- decode, one-cell and bulk append, compaction and
 gather / scatter -- under the "decode", "append", "compact_f16" and
-"persist" keys.
+"persist" keys; and block streaming ("stream"): a whole layer fetched from a
+pinned host copy into a device window, against the pinned host-to-device
+copy rate.
 """
 from __future__ import annotations
 
