@@ -661,35 +661,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       }
     }
   } else if constexpr (C::V4) {
-    // P^T as the F16 path builds it; V carries its own scales
-    uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      uint32_t h01, l01, h23, l23;
-      split_pair(p[nt][0], p[nt][1], h01, l01);
-      split_pair(p[nt][2], p[nt][3], h23, l23);
-      bh[nt][0] = movmatrix_t(h01);
-      bh[nt][1] = movmatrix_t(h23);
-      bl[nt][0] = movmatrix_t(l01);
-      bl[nt][1] = movmatrix_t(l23);
-    }
-    uint32_t bhn[NT][2];  // -p_hi, for the -lo halves of V
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      bhn[nt][0] = bh[nt][0] ^ 0x80008000u;
-      bhn[nt][1] = bh[nt][1] ^ 0x80008000u;
-    }
-    const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
-    const uint32_t mhi =
-        (2 * t + 8 < nvalid ? 0xffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
-    // the fp16 scales of this thread's cells 2t, 2t + 1, 2t + 8, 2t + 9
-    // (one 32-bit word per two blocks)
+    // The fp16 scales of this thread's cells g and g + 8 (the rows of its
+    // p fragments), every 32-dim block: one vector load per cell.
     constexpr int SWD = C::VNS / 2;
     const unsigned char* vsc = smem + C::SMEM_SC + s * C::SC_STAGE_B + C::KSCALE_B;
-    uint32_t sw[4][SWD];
+    uint32_t sw[2][SWD];
 #pragma unroll
-    for (int ci = 0; ci < 4; ++ci) {
-      const unsigned char* src = vsc + (cl + 2 * t + (ci & 1) + 8 * (ci >> 1)) * (C::VNS * 2);
+    for (int ci = 0; ci < 2; ++ci) {
+      const unsigned char* src = vsc + (cl + g + 8 * ci) * (C::VNS * 2);
       if constexpr (SWD == 4) {
         const uint4 u = *reinterpret_cast<const uint4*>(src);
         sw[ci][0] = u.x;
@@ -709,10 +688,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     // of the block for both cells.  Nibble e of both halves becomes the
     // fp16 pair (code - 8) exactly (OR into 1024's exponent, then minus
     // 1032; for the upper nibble of a byte 1024 + 16 code, times 1/16,
-    // minus 72).  Its product with the cell's scale has up to 15
-    // significant bits, so it enters as hi = fp16(v) and lo = v - hi (exact,
-    // one fused multiply-add, computed as hi - v with the negated scale),
-    // and p.v takes hi.p_hi + hi.p_lo + (-lo).(-p_hi).
+    // minus 72), and the block's scales are folded into P (fp32, then the
+    // hi + lo split), as the int8 path does per 64-dim group.  Nibbles are
+    // always finite and masked cells have p = 0, so no V mask is needed;
+    // a masked cell's scale bits may be anything, and clamping them to
+    // +-65504 keeps 0 * s == 0 (finite scales pass unchanged).
     // M-tile 2 blk + h: row g is dim 32 blk + 4g + 2h, row g + 8 the dim
     // after it.
 #pragma unroll
@@ -722,36 +702,32 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
       for (int jb = 0; jb < 2; ++jb) {
         const int blk = 2 * kq + jb;
-        const uint32_t sel = (blk & 1) ? 0x7632u : 0x5410u;
-        const uint32_t slo = prmt(sw[0][blk >> 1], sw[1][blk >> 1], sel);
-        const uint32_t shi = prmt(sw[2][blk >> 1], sw[3][blk >> 1], sel);
-        const uint32_t slo_n = slo ^ 0x80008000u, shi_n = shi ^ 0x80008000u;  // -scale
+        const int sh = 16 * (blk & 1);
+        const float s0 = fmaxf(fminf(__half2float(__ushort_as_half((unsigned short)(sw[0][blk >> 1] >> sh))),
+                                     65504.f), -65504.f);
+        const float s8 = fmaxf(fminf(__half2float(__ushort_as_half((unsigned short)(sw[1][blk >> 1] >> sh))),
+                                     65504.f), -65504.f);
+        uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t h01, l01, h23, l23;
+          split_pair(p[nt][0] * s0, p[nt][1] * s0, h01, l01);
+          split_pair(p[nt][2] * s8, p[nt][3] * s8, h23, l23);
+          bh[nt][0] = movmatrix_t(h01);
+          bh[nt][1] = movmatrix_t(h23);
+          bl[nt][0] = movmatrix_t(l01);
+          bl[nt][1] = movmatrix_t(l23);
+        }
         const uint32_t wl = r[2 * jb], wh = r[2 * jb + 1];
         const uint32_t wl8 = wl >> 8, wh8 = wh >> 8;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t xl = h ? wl8 : wl, xh = h ? wh8 : wh;
-          const uint32_t n4[4] = {nib_lo(xl), nib_hi(xl), nib_lo(xh), nib_hi(xh)};
-          const uint32_t s4[4] = {slo, slo, shi, shi};
-          const uint32_t n4s[4] = {slo_n, slo_n, shi_n, shi_n};
-          uint32_t af[4], al[4];  // hi = fp16(v); al = hi - v = -lo (exact)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            af[i] = hmul2(n4[i], s4[i]);
-            al[i] = hfma2(n4[i], n4s[i], af[i]);
-          }
-          if (nvalid < kCellsPerWarp) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              af[i] &= i < 2 ? mlo : mhi;
-              al[i] &= i < 2 ? mlo : mhi;
-            }
-          }
+          const uint32_t af[4] = {nib_lo(xl), nib_hi(xl), nib_lo(xh), nib_hi(xh)};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(o[2 * blk + h][nt], af, bh[nt][0], bh[nt][1]);
             mma16816(o[2 * blk + h][nt], af, bl[nt][0], bl[nt][1]);
-            mma16816(o[2 * blk + h][nt], al, bhn[nt][0], bhn[nt][1]);  // (-lo)(-p_hi)
           }
         }
       }
@@ -762,10 +738,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
     for (int gv = 0; gv < C::NG; ++gv) {
       // p = 0 exactly for masked cells, whose scale bits may be anything
-      // (even inf / NaN): clamping keeps 0 * s == 0.  Finite fp16
-      // scales are below 65504 and pass unchanged.
-      const float s0 = fminf(__half2float(__ushort_as_half(vsc[(cl + g) * C::NG + gv])), 65504.f);
-      const float s8 = fminf(__half2float(__ushort_as_half(vsc[(cl + g + 8) * C::NG + gv])), 65504.f);
+      // (even +-inf / NaN): clamping to +-65504 keeps 0 * s == 0.  Finite
+      // fp16 scales pass unchanged.
+      const float s0 = fmaxf(fminf(__half2float(__ushort_as_half(vsc[(cl + g) * C::NG + gv])), 65504.f), -65504.f);
+      const float s8 = fmaxf(fminf(__half2float(__ushort_as_half(vsc[(cl + g + 8) * C::NG + gv])), 65504.f), -65504.f);
       uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
