@@ -79,20 +79,32 @@ kvq_status stream_plan(int n_host_blocks, int n_slots, int32_t* slot_of_block, i
                        int64_t* last_use, int64_t* clock, const int32_t* block_table, int n_seq,
                        int max_blocks, const int32_t* ctx_lens, int block_size, int32_t* slot_table,
                        int32_t* fetch_src, int32_t* fetch_dst, int* n_fetch, int* n_hits) {
-  // the distinct host blocks this call reads, in first-use order
-  std::vector<int32_t> need;
-  std::vector<char> seen((size_t)n_host_blocks, 0);
+  // the distinct host blocks this call reads, in first-use order (sorted
+  // by id to drop repeats, then back into the order of first use: the cost
+  // follows the blocks read, not the size of the host copy)
+  std::vector<std::pair<int32_t, int32_t>> uses;  // (block, first use)
   for (int b = 0; b < n_seq; ++b) {
     const long long L = ctx_lens[b];
     if (L < 0 || L > (long long)max_blocks * block_size) return KVQ_ERR_ARG;
     const int nb = (int)((L + block_size - 1) / block_size);
     for (int j = 0; j < nb; ++j) {
       const int32_t blk = block_table[(size_t)b * max_blocks + j];
-      if (blk < 0 || blk >= n_host_blocks || seen[blk]) continue;
-      seen[blk] = 1;
-      need.push_back(blk);
+      if (blk >= 0 && blk < n_host_blocks) uses.emplace_back(blk, (int32_t)uses.size());
     }
   }
+  std::sort(uses.begin(), uses.end());
+  uses.erase(std::unique(uses.begin(), uses.end(),
+                         [](const std::pair<int32_t, int32_t>& x, const std::pair<int32_t, int32_t>& y) {
+                           return x.first == y.first;
+                         }),
+             uses.end());
+  std::sort(uses.begin(), uses.end(),
+            [](const std::pair<int32_t, int32_t>& x, const std::pair<int32_t, int32_t>& y) {
+              return x.second < y.second;
+            });
+  std::vector<int32_t> need;
+  need.reserve(uses.size());
+  for (const auto& u : uses) need.push_back(u.first);
   if ((long long)need.size() > n_slots) return KVQ_ERR_UNSUPPORTED;  // nothing changed yet
   const int64_t now = ++*clock;
   int hits = 0;
