@@ -688,6 +688,22 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile_case": "chunk", "reps": args.profile_reps}))
         return
+    if args.profile_workload == "stream":
+        # block streaming: one gqa32k int8 layer (128 blocks, 70 MB) in a
+        # pinned host copy, fetched whole into an empty device window
+        from quantized_kv_cache_append_gb300.pool import PagedPool
+        wl = workloads.make("gqa32k")
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        host = PagedPool(kvq.KVQ_Q8, wl.n_kv, wl.head_dim, wl.block_size, wl.n_blocks, pinned=True)
+        win = PagedPool(kvq.KVQ_Q8, wl.n_kv, wl.head_dim, wl.block_size, wl.n_blocks)
+        host.append(dev(wl.k), dev(wl.v), dev(wl.tok_seq), dev(wl.tok_pos), dev(wl.block_table))
+        ids = torch.arange(wl.n_blocks, dtype=torch.int32, device="cuda")
+        for _ in range(args.profile_reps):
+            st = kvq.kvq_stream_fetch(host.cache, win.cache, ids, ids, wl.n_blocks)
+            assert st == kvq.KVQ_OK, kvq.kvq_status_string(st)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "stream", "reps": args.profile_reps}))
+        return
     wl = workloads.make(args.profile_workload)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     bt = dev(wl.block_table)
