@@ -68,6 +68,7 @@ def _gpu_chunk(k16, v16, q, sm):
     (oracle.FMT_F16, 4, 1, 128, 64, 1),        # one token, one key tile
     (oracle.FMT_Q8, 1, 4, 128, 2048, 256),
     (oracle.FMT_F16, 3, 3, 64, 777, 40),       # G = 3: rows of a tile span tokens unevenly
+    (oracle.FMT_K8V4, 2, 4, 128, 1000, 128),   # staging of a K8V4 cache (V rotated back)
 ])
 def test_chunk_matches_oracle(fmt, n_kv, G, hd, P, T):
     k16, v16 = _staging_from_oracle_pool(fmt, n_kv, hd, P, 31 + hd + T)

@@ -59,9 +59,10 @@ def test_gqa32k_append_decode_steps(fmt):
     p.assert_cache_equal()
 
 
-def test_ragged_paged_batch():
+@pytest.mark.parametrize("fmt", ["q8", "k8v4"])
+def test_ragged_paged_batch(fmt):
     wl = workloads.make("ragged")
-    p = _prefilled(wl, "q8")
+    p = _prefilled(wl, fmt)
     p.assert_cache_equal()
     p.check_decode(wl.q, wl.ctx_lens, wl.sm_scale)
 
@@ -74,9 +75,10 @@ def test_long256k(fmt):
     p.check_decode(wl.q, wl.ctx_lens, wl.sm_scale)
 
 
-def test_chunk_compact_verify():
+@pytest.mark.parametrize("fmt", ["q8", "k8v4"])
+def test_chunk_compact_verify(fmt):
     wl = workloads.make("chunk_verify")
-    p = _prefilled(wl, "q8")
+    p = _prefilled(wl, fmt)
     c = wl.chunk
     p.append(c["k"], c["v"], c["tok_seq"], c["tok_pos"])
     p.assert_cache_equal()
