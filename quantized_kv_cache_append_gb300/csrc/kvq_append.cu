@@ -263,168 +263,209 @@ __global__ void __launch_bounds__(W * 32) append_q8_kernel(AppendArgs a) {
   }
 }
 
-// K8V4 V code of y in the block of scale d (d != 0, rs ~ 1 / d): the 4-bit
-// offset code clamp(rint(y / d), -8, 7) + 8.  |y / d| <= 8 (up to d's fp16
-// rounding), so y * rs is within 2e-6 of the quotient and decides the
-// integer wherever it lies more than 2.5e-4 from a half-integer; inside
-// that band, and for non-finite values, the IEEE quotient itself decides
-// (a NaN quotient gives 0).  Clamping to integer bounds commutes with
-// rounding.
-__device__ __forceinline__ uint32_t q4_code(float y, float d, float rs) {
-  const float qa = y * rs;
-  const float rq = rintf(qa);
-  float r;
-  if (fabsf(qa - rq) < 0.5f - 2.5e-4f) {
-    r = rq;
-  } else {
-    r = rintf(__fdiv_rn(y, d));
-    if (!(r == r)) r = 0.0f;
+// K8V4 V codes of U values y of one block of scale d: the 4-bit offset
+// codes clamp(rint(y / d), -8, 7) + 8, packed 4 bits each (value e in bits
+// 4e..4e+3).  |y / d| <= 8 (up to d's fp16 rounding), so y * rs (rs ~ 1/d)
+// is within 2e-6 of the quotient and decides the integer wherever it lies
+// more than 2.5e-4 from a half-integer; adding and taking off 1.5 * 2^23
+// rounds it (to nearest even) in packed pairs.  If any of the U values
+// lies inside that band, or is not finite, the IEEE quotients decide all
+// U (a NaN quotient gives 0).  Clamping to integer bounds commutes with
+// rounding; the clamped integer k plus 1.5 * 2^23 + 8 has k + 8 in its
+// low mantissa bits.  d == 0 gives code 8 throughout.
+template <int U>
+__device__ __forceinline__ uint32_t q4_codes(const float (&y)[U], float d) {
+  if (d == 0.0f) return U == 4 ? 0x8888u : 0x88u;
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kBand = 0.5f - 2.5e-4f;
+  const float rs = rcp_approx(d);
+  const unsigned long long r2 = pack2(rs, rs), m2 = pack2(kMagic, kMagic);
+  float k[U];
+  bool near = false;
+#pragma unroll
+  for (int e = 0; e < U; e += 2) {
+    const unsigned long long qa = mul2(pack2(y[e], y[e + 1]), r2);
+    const unsigned long long r = sub2(add2(qa, m2), m2);
+    const unsigned long long df = sub2(qa, r);
+    near |= !(fabsf(lo2(df)) < kBand) || !(fabsf(hi2(df)) < kBand);
+    k[e] = lo2(r);
+    k[e + 1] = hi2(r);
   }
-  return (uint32_t)((int)fminf(fmaxf(r, -8.0f), 7.0f) + 8);
+  if (near) {  // rare: the quotients themselves
+#pragma unroll
+    for (int e = 0; e < U; ++e) {
+      const float r = rintf(__fdiv_rn(y[e], d));
+      k[e] = r == r ? r : 0.0f;
+    }
+  }
+  uint32_t out = 0;
+#pragma unroll
+  for (int e = 0; e < U; ++e)
+    out |= (__float_as_uint(fminf(fmaxf(k[e], -8.0f), 7.0f) + (kMagic + 8.0f)) & 15u) << (4 * e);
+  return out;
 }
 
-// One K8V4 row (K and V of one token and KV head) held by a warp in the
-// lane layout described below; dr < 0 (a broken precondition, or a row
-// past the end) computes but stores nothing.  Every lane executes every
-// shuffle.
-template <int HD>
-__device__ __forceinline__ void k8v4_row(const AppendArgs& a, float (&xk)[HD / (32 * (HD >= 128 ? 4 : 2))][HD >= 128 ? 4 : 2],
-                                         float (&xv)[HD / (32 * (HD >= 128 ? 4 : 2))][HD >= 128 ? 4 : 2],
-                                         long long dr, int lane) {
-  constexpr int U = HD >= 128 ? 4 : 2;
-  constexpr int NI = HD / (32 * U);
-  constexpr int LG = kGroup / U;     // lanes of a 64-dim K group
-  constexpr int LB = kQ4Block / U;   // lanes of a 32-dim V block
-  constexpr int NG = HD / kGroup, NB = HD / kQ4Block;
-  // ---- K: int8, one fp16 scale per 64 dims
+// Row shape of the K8V4 append: a row (one token and KV head, K and V) is
+// held by a group of LPR consecutive lanes, lane j of the group holding the
+// VPL consecutive dims j VPL .. j VPL + VPL - 1, so a warp carries 32 / LPR
+// rows at once.  Bulk appends take VPL = 16 (8 at HD 64): few shuffles per
+// row; a few rows (decode steps) take VPL = 4 (8 at HD 256): short chains.
+template <int HD, int VPL_>
+struct K8V4Rows {
+  static constexpr int VPL = VPL_;                // values a lane holds (4, 8 or 16)
+  static constexpr int LPR = HD / VPL;            // lanes of a row
+  static constexpr int RPW = 32 / LPR;            // rows a warp holds
+  static_assert(VPL % 4 == 0 && LPR <= 32 && LPR * VPL == HD, "K8V4 row shape");
+};
+
+// Walsh-Hadamard transform of a row held by LPR lanes of VPL consecutive
+// dims each: stages h = 1 .. VPL/2 inside a lane, then h = VPL .. HD/2
+// between lanes j and j ^ (h / VPL) of the group (its lanes are an aligned
+// run, so the partner stays inside it).  Each stage turns dims (i, i + h),
+// bit h of i clear, into (x_i + x_{i+h}, x_i - x_{i+h}), every sum and
+// difference rounded once in fp32, as the stage-by-stage definition does
+// (the upper lane's y - x as fma(x, -1, y), an exact product).
+template <int VPL, int LPR>
+__device__ __forceinline__ void wht_group(float (&x)[VPL], int lane) {
 #pragma unroll
-  for (int i = 0; i < NI; ++i) {
+  for (int h = 1; h < VPL; h *= 2)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (!(i & h)) {
+        const float p = x[i], q = x[i + h];
+        x[i] = __fadd_rn(p, q);
+        x[i + h] = __fsub_rn(p, q);
+      }
+#pragma unroll
+  for (int hl = 1; hl < LPR; hl *= 2) {
+    const float sgn = (lane & hl) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const float y = __shfl_xor_sync(0xffffffffu, x[i], hl);
+      x[i] = __fmaf_rn(x[i], sgn, y);
+    }
+  }
+}
+
+// K8V4 append (K8V4Rows layout; W warps a CTA).  K: int8 codes per 64-dim
+// group, the int8 format's arithmetic (group maximum over the group's
+// lanes, group_scale, codes4).  V: rotated (wht_group), then per block of
+// 32 rotated dims the element of largest magnitude, the first one on ties
+// (the block maximum of |y|, then the lowest dim holding it; NaN counts as
+// 0 and a zero maximum gives m = +0, as the comparison-based definition
+// does), d = fp16(m / -8), and two codes a byte.  Rows past the end carry
+// zeros through every shuffle and store nothing.
+template <int HD, int VPL_, int W>
+__global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
+  using R = K8V4Rows<HD, VPL_>;
+  constexpr int VPL = R::VPL, LPR = R::LPR, RPW = R::RPW;
+  constexpr int NG = HD / kGroup, NB = HD / kQ4Block;
+  constexpr int LG = kGroup / VPL;    // lanes of a 64-dim K group
+  constexpr int LB = kQ4Block / VPL;  // lanes of a 32-dim V block
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, j = lane & (LPR - 1);
+  const long long rows = (long long)a.n_tok * a.n_kv;
+  const bool rows32 = rows <= 0x7fffffffLL;
+  const long long row0 = ((long long)blockIdx.x * W + (threadIdx.x >> 5)) * RPW;
+  if (row0 >= rows) return;  // warp-uniform; no block-level barrier follows
+  const long long row = row0 + lane / LPR;
+  const bool live = row < rows;
+
+  float xk[VPL], xv[VPL];
+#pragma unroll
+  for (int q = 0; q < VPL / 4; ++q) {
+    float4 k4 = make_float4(0.f, 0.f, 0.f, 0.f), v4 = k4;
+    if (live) {
+      const size_t off = (size_t)row * HD + (size_t)j * VPL + 4 * q;
+      k4 = __ldcs(reinterpret_cast<const float4*>(a.k + off));
+      v4 = __ldcs(reinterpret_cast<const float4*>(a.v + off));
+    }
+    xk[4 * q] = k4.x; xk[4 * q + 1] = k4.y; xk[4 * q + 2] = k4.z; xk[4 * q + 3] = k4.w;
+    xv[4 * q] = v4.x; xv[4 * q + 1] = v4.y; xv[4 * q + 2] = v4.z; xv[4 * q + 3] = v4.w;
+  }
+  const long long dr = live ? dest_row(a, row, rows32) : -1;
+
+  // ---- K: int8, one fp16 scale per 64 dims
+  {
     uint32_t mb = 0;
 #pragma unroll
-    for (int e = 0; e < U; ++e) mb = max(mb, __float_as_uint(xk[i][e]) & 0x7fffffffu);
+    for (int e = 0; e < VPL; ++e) mb = max(mb, __float_as_uint(xk[e]) & 0x7fffffffu);
 #pragma unroll
     for (int off = 1; off < LG; off <<= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, off));
     const float amax = __uint_as_float(mb);
     const __half sh = group_scale(amax);
     const float sf = __half2float(sh);
-    if (dr < 0) continue;
-    const float4 x4 = U == 4 ? make_float4(xk[i][0], xk[i][1], xk[i][U > 2 ? 2 : 0], xk[i][U > 3 ? 3 : 0])
-                             : make_float4(xk[i][0], xk[i][1], 0.f, 0.f);
-    uint32_t c;
+    uint32_t c[VPL / 4];
     if (amax <= 3.4028234663852886e38f) {
-      c = codes4(x4, sf, rcp_approx(sf));
+      const float rs = rcp_approx(sf);
+#pragma unroll
+      for (int q = 0; q < VPL / 4; ++q)
+        c[q] = codes4(make_float4(xk[4 * q], xk[4 * q + 1], xk[4 * q + 2], xk[4 * q + 3]), sf, rs);
     } else {
-      c = exact_code(x4.x, sf) | (exact_code(x4.y, sf) << 8) | (exact_code(x4.z, sf) << 16) |
-          (exact_code(x4.w, sf) << 24);
+#pragma unroll
+      for (int q = 0; q < VPL / 4; ++q)
+        c[q] = exact_code(xk[4 * q], sf) | (exact_code(xk[4 * q + 1], sf) << 8) |
+               (exact_code(xk[4 * q + 2], sf) << 16) | (exact_code(xk[4 * q + 3], sf) << 24);
     }
-    const int d0 = U * lane + 32 * U * i;
-    int8_t* dst = static_cast<int8_t*>(a.k_dst) + dr * HD + d0;
-    if constexpr (U == 4) *reinterpret_cast<uint32_t*>(dst) = c;
-    else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)c;
-    if (lane % LG == 0) a.ks_dst[dr * NG + d0 / kGroup] = sh;
+    if (dr >= 0) {
+      int8_t* dst = static_cast<int8_t*>(a.k_dst) + dr * HD + j * VPL;
+      if constexpr (VPL == 16)
+        *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[VPL > 8 ? 2 : 0], c[VPL > 8 ? 3 : 0]);
+      else if constexpr (VPL == 8)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[VPL > 4 ? 1 : 0]);
+      else
+        *reinterpret_cast<uint32_t*>(dst) = c[0];
+      if (j % LG == 0) a.ks_dst[dr * NG + (j * VPL) / kGroup] = sh;
+    }
   }
 
   // ---- V: rotate, then 4-bit codes and one fp16 scale per 32 rotated dims
-  wht_warp<U, NI>(xv, lane);
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int d0 = U * lane + 32 * U * i;
+  wht_group<VPL, LPR>(xv, lane);
+  {
     // the block's largest |y| (NaN counts as 0) ...
-    uint32_t ab[U], amax = 0;
+    uint32_t ab[VPL], amax = 0;
 #pragma unroll
-    for (int e = 0; e < U; ++e) {
-      const float y = xv[i][e];
-      ab[e] = y == y ? (__float_as_uint(y) & 0x7fffffffu) : 0u;
+    for (int e = 0; e < VPL; ++e) {
+      ab[e] = xv[e] == xv[e] ? (__float_as_uint(xv[e]) & 0x7fffffffu) : 0u;
       amax = max(amax, ab[e]);
     }
 #pragma unroll
     for (int off = 1; off < LB; off <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     // ... and the first dim holding it: the lowest lane of the block with a
-    // match (lanes hold ascending dims), its lowest unit element
-    int ef = U;
+    // match (lanes hold ascending dims), then its lowest element
+    int ef = VPL;
 #pragma unroll
-    for (int e = U - 1; e >= 0; --e)
+    for (int e = VPL - 1; e >= 0; --e)
       if (ab[e] == amax) ef = e;
-    const unsigned hit = __ballot_sync(0xffffffffu, ef < U);
-    const unsigned blk_lanes = (LB == 32 ? 0xffffffffu : ((1u << LB) - 1u)) << ((lane / LB) * LB);
+    const unsigned hit = __ballot_sync(0xffffffffu, ef < VPL);
+    const unsigned blk_lanes = ((1u << LB) - 1u) << (lane & ~(LB - 1));
     const int src = __ffs(hit & blk_lanes) - 1;
     float mine = 0.f;
 #pragma unroll
-    for (int e = 0; e < U; ++e)
-      if (e == ef) mine = xv[i][e];
+    for (int e = 0; e < VPL; ++e)
+      if (e == ef) mine = xv[e];
     float m = __shfl_sync(0xffffffffu, mine, src);
     if (amax == 0) m = 0.0f;  // no nonzero element: m stays +0
-    const __half dh = __float2half_rn(m / -8.0f);
+    const __half dh = __float2half_rn(m * -0.125f);  // = m / -8, both correctly rounded
     const float d = __half2float(dh);
-    if (dr < 0) continue;
-    uint32_t c[U];
-    if (d == 0.0f) {
+    uint32_t c[VPL / 4];  // 4 codes (16 bits) each; dims 2i low nibble, 2i + 1 high
 #pragma unroll
-      for (int e = 0; e < U; ++e) c[e] = 8;
-    } else {
-      const float rs = rcp_approx(d);
-#pragma unroll
-      for (int e = 0; e < U; ++e) c[e] = q4_code(xv[i][e], d, rs);
+    for (int q = 0; q < VPL / 4; ++q) {
+      const float y4[4] = {xv[4 * q], xv[4 * q + 1], xv[4 * q + 2], xv[4 * q + 3]};
+      c[q] = q4_codes<4>(y4, d);
     }
-    uint8_t* dst = static_cast<uint8_t*>(a.v_dst) + dr * (HD / 2) + d0 / 2;
-    if constexpr (U == 4)
-      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(c[0] | (c[1] << 4) | (c[U > 2 ? 2 : 0] << 8) |
-                                                     (c[U > 3 ? 3 : 0] << 12));
-    else
-      *dst = (uint8_t)(c[0] | (c[1] << 4));
-    if (lane % LB == 0) a.vs_dst[dr * NB + d0 / kQ4Block] = dh;
+    if (dr >= 0) {
+      uint8_t* dst = static_cast<uint8_t*>(a.v_dst) + dr * (HD / 2) + j * (VPL / 2);
+      if constexpr (VPL == 16)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(c[0] | (c[1] << 16), c[VPL > 8 ? 2 : 0] | (c[VPL > 8 ? 3 : 0] << 16));
+      else if constexpr (VPL == 8)
+        *reinterpret_cast<uint32_t*>(dst) = c[0] | (c[VPL > 4 ? 1 : 0] << 16);
+      else
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)c[0];
+      if (j % LB == 0) a.vs_dst[dr * NB + (j * VPL) / kQ4Block] = dh;
+    }
   }
-}
-
-// K8V4 append: one warp per (token, KV head) row, K and V.  Lane l holds
-// units of U consecutive dims, dims U l + 32 U i (i < NI): the loads of a
-// unit are coalesced across the warp and the Walsh-Hadamard stages map onto
-// the layout (wht_warp).  K: int8 codes per 64-dim group, exactly as the
-// int8 format (group maximum over the 64 / U lanes of the group, then
-// group_scale and codes4).  V: rotated in fp32, then per block of 32
-// rotated dims (32 / U lanes) the element of largest magnitude, the first
-// one on ties (the block maximum of |y|, then the lowest dim holding it;
-// NaN counts as 0 and a zero maximum gives m = +0, as the comparison-based
-// definition does), d = fp16(m / -8), and two codes a byte.  A warp takes RPW
-// consecutive rows, all their loads issued before the first row's work.
-template <int HD, int W, int RPW>
-__global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
-  constexpr int U = HD >= 128 ? 4 : 2;
-  constexpr int NI = HD / (32 * U);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const long long rows = (long long)a.n_tok * a.n_kv;
-  const bool rows32 = rows <= 0x7fffffffLL;
-  const long long row0 = ((long long)blockIdx.x * W + (threadIdx.x >> 5)) * RPW;
-  if (row0 >= rows) return;  // warp-uniform; no block-level barrier follows
-
-  float xk[RPW][NI][U], xv[RPW][NI][U];
-#pragma unroll
-  for (int r = 0; r < RPW; ++r)
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-#pragma unroll
-      for (int e = 0; e < U; ++e) xk[r][i][e] = xv[r][i][e] = 0.f;
-      if (row0 + r >= rows) continue;
-      const size_t off = (size_t)(row0 + r) * HD + U * lane + 32 * U * i;
-      if constexpr (U == 4) {
-        const float4 k4 = __ldcs(reinterpret_cast<const float4*>(a.k + off));
-        const float4 v4 = __ldcs(reinterpret_cast<const float4*>(a.v + off));
-        xk[r][i][0] = k4.x; xk[r][i][1] = k4.y; xk[r][i][U > 2 ? 2 : 0] = k4.z; xk[r][i][U > 3 ? 3 : 0] = k4.w;
-        xv[r][i][0] = v4.x; xv[r][i][1] = v4.y; xv[r][i][U > 2 ? 2 : 0] = v4.z; xv[r][i][U > 3 ? 3 : 0] = v4.w;
-      } else {
-        const float2 k2 = __ldcs(reinterpret_cast<const float2*>(a.k + off));
-        const float2 v2 = __ldcs(reinterpret_cast<const float2*>(a.v + off));
-        xk[r][i][0] = k2.x; xk[r][i][1] = k2.y;
-        xv[r][i][0] = v2.x; xv[r][i][1] = v2.y;
-      }
-    }
-  long long dr[RPW];
-#pragma unroll
-  for (int r = 0; r < RPW; ++r) dr[r] = row0 + r < rows ? dest_row(a, row0 + r, rows32) : -1;
-#pragma unroll
-  for (int r = 0; r < RPW; ++r) k8v4_row<HD>(a, xk[r], xv[r], dr[r], lane);
 }
 
 template <typename Kernel>
@@ -461,14 +502,16 @@ cudaError_t launch_q8(const AppendArgs& a, cudaStream_t s) {
   return launch_grid(append_q8_kernel<HD, 2, 8, false>, (groups + 127) / 128, 256, a, s);
 }
 
-// Few rows (decode steps): one row per warp, small CTAs; bulk: 8 warps of
-// 32 / (U NI) rows each (32 row values a lane in flight).
+// Few rows (decode steps): short per-lane chains (VPL 4, 8 at HD 256) in
+// CTAs of 4 warps; bulk: VPL 16 (8 at HD 64) in CTAs of 8 warps.
 template <int HD>
 cudaError_t launch_k8v4(const AppendArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.n_tok * a.n_kv;
-  constexpr int RPW = HD == 256 ? 2 : 4;
-  if (rows < 4096) return launch_grid(append_k8v4_kernel<HD, 4, 1>, (rows + 3) / 4, 128, a, s);
-  return launch_grid(append_k8v4_kernel<HD, 8, RPW>, (rows + 8 * RPW - 1) / (8 * RPW), 256, a, s);
+  constexpr int VS = HD == 256 ? 8 : 4, VB = HD >= 128 ? 16 : 8;
+  constexpr int RS = K8V4Rows<HD, VS>::RPW, RB = K8V4Rows<HD, VB>::RPW;
+  if (rows < 4096)
+    return launch_grid(append_k8v4_kernel<HD, VS, 4>, (rows + 4 * RS - 1) / (4 * RS), 128, a, s);
+  return launch_grid(append_k8v4_kernel<HD, VB, 8>, (rows + 8 * RB - 1) / (8 * RB), 256, a, s);
 }
 
 template <int HD>

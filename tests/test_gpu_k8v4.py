@@ -58,9 +58,10 @@ def _designed_rows(n, hd, rng):
 
 
 @pytest.mark.parametrize("hd", [64, 128, 256])
-def test_append_bit_exact_on_designed_rows(hd):
-    rng = np.random.default_rng(hd)
-    n, n_kv, bs = 96, 2, 16
+@pytest.mark.parametrize("n", [96, 2100])       # a few rows, and the bulk kernel shape
+def test_append_bit_exact_on_designed_rows(hd, n):
+    rng = np.random.default_rng(hd + n)
+    n_kv, bs = 2, 16
     v = _designed_rows(n * n_kv, hd, rng).reshape(n, n_kv, hd)
     # near-ties: nudge some values 1-3 fp32 ulps (the rotation of x is then
     # inexact, so the quotient lands a few ulps off the half-integer)
@@ -70,8 +71,9 @@ def test_append_bit_exact_on_designed_rows(hd):
     for s in (1, 2, 3):
         nudged[steps >= s] = np.nextafter(nudged[steps >= s], np.float32(np.inf))
         nudged[steps <= -s] = np.nextafter(nudged[steps <= -s], np.float32(-np.inf))
-    table = np.arange(2 * n // bs, dtype=np.int32)[None]
-    p = Pair("k8v4", n_kv, hd, bs, 2 * n // bs, table)
+    nb = -(-2 * n // bs)
+    table = np.arange(nb, dtype=np.int32)[None]
+    p = Pair("k8v4", n_kv, hd, bs, nb, table)
     p.append(k, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32))
     p.append(k, nudged, np.zeros(n, np.int32), np.arange(n, 2 * n, dtype=np.int32))
     p.assert_cache_equal()
