@@ -60,70 +60,63 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, uint32_t sel, uint3
   return hmul2(h, s2);
 }
 
-// K8V4 V rows: grid (cell groups, KV head), one warp per cell, RPW cells a
-// warp (their loads first); the grid covers every cell (the loop runs once
-// unless the x dimension was capped).
-constexpr int kV4RowsPerWarp = 2;
+// K8V4 V rows: grid (cell groups, KV head); a cell's row is held by a
+// group of LPR = HD / VPL lanes (VPL consecutive dims each, within one
+// 32-dim block), so a warp de-rotates 32 / LPR cells at once; the grid
+// covers every cell (the loop runs once unless the x dimension was capped).
+template <int HD>
+struct V4Rows {
+  static constexpr int VPL = HD >= 128 ? 16 : 8;
+  static constexpr int LPR = HD / VPL;
+  static constexpr int RPW = 32 / LPR;
+};
 
 template <int HD>
 __global__ void __launch_bounds__(256) compact_v4_kernel(CompactArgs a) {
-  constexpr int U = HD >= 128 ? 4 : 2;
-  constexpr int NI = HD / (32 * U);
+  constexpr int VPL = V4Rows<HD>::VPL, LPR = V4Rows<HD>::LPR, RPW = V4Rows<HD>::RPW;
   constexpr int NB = HD / kQ4Block;
-  constexpr int RPW = kV4RowsPerWarp;
   const int kvh = blockIdx.y;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, j = lane & (LPR - 1);
   const int wpb = blockDim.x >> 5;
   const int bs = 1 << a.pool.bs_log2;
   for (int p0 = (blockIdx.x * wpb + (threadIdx.x >> 5)) * RPW; p0 < a.n_cells;
        p0 += gridDim.x * wpb * RPW) {
-    uint32_t bits[RPW][NI];
-    float d[RPW][NI];
-    bool ok[RPW];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      const int p = p0 + r;
-      const int blk = p < a.n_cells ? __ldg(a.block_row + (p >> a.pool.bs_log2)) : -1;
-      ok[r] = blk >= 0 && blk < a.pool.n_blocks;  // warp-uniform
-      const size_t row = ok[r] ? ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1)) : 0;
-      const uint8_t* src = static_cast<const uint8_t*>(a.pool.v) + row * (HD / 2);
-      const __half* sc = a.pool.vs + row * NB;
-#pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int d0 = U * lane + 32 * U * i;
-        bits[r][i] = 0;
-        d[r][i] = 0.f;
-        if (!ok[r]) continue;
-        // d / HD: the power-of-two factor of the inverse rotation, taken
-        // before the butterflies (exact, and it commutes with every sum)
-        d[r][i] = __half2float(__ldg(sc + d0 / kQ4Block)) * (1.0f / HD);
-        if constexpr (U == 4) bits[r][i] = __ldg(reinterpret_cast<const unsigned short*>(src + d0 / 2));
-        else bits[r][i] = __ldg(src + d0 / 2);
+    const int p = p0 + lane / LPR;
+    const int blk = p < a.n_cells ? __ldg(a.block_row + (p >> a.pool.bs_log2)) : -1;
+    const bool ok = blk >= 0 && blk < a.pool.n_blocks;  // else skip the cell
+    float x[VPL];
+    if (ok) {
+      const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+      const unsigned char* src = static_cast<const unsigned char*>(a.pool.v) + row * (HD / 2) + j * (VPL / 2);
+      // d / HD: the power-of-two factor of the inverse rotation, taken
+      // before the butterflies (exact, and it commutes with every sum)
+      const float d = __half2float(__ldg(a.pool.vs + row * NB + (j * VPL) / kQ4Block)) * (1.0f / HD);
+      uint32_t w[VPL / 8];
+      if constexpr (VPL == 16) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+        w[0] = u.x;
+        w[VPL / 8 > 1 ? 1 : 0] = u.y;
+      } else {
+        w[0] = __ldg(reinterpret_cast<const uint32_t*>(src));
       }
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) {
+        // 2^23 + code as float bits, minus 2^23 + 8: code - 8, exactly
+        const float c = __uint_as_float(0x4b000000u | ((w[e / 8] >> (4 * (e % 8))) & 15u)) - 8388616.0f;
+        x[e] = __fmul_rn(c, d);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) x[e] = 0.f;
     }
+    wht_group<VPL, LPR>(x, lane);  // every lane takes part
+    if (ok) {
+      __half* dst = a.out_v + ((size_t)kvh * a.n_cells + p) * HD + j * VPL;
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      if (!ok[r]) continue;  // out-of-range block or past the end: skip
-      float x[NI][U];
-#pragma unroll
-      for (int i = 0; i < NI; ++i)
-#pragma unroll
-        for (int e = 0; e < U; ++e) {
-          // 2^23 + code as float bits, minus 2^23 + 8: code - 8, exactly
-          const float c = __uint_as_float(0x4b000000u | ((bits[r][i] >> (4 * e)) & 15u)) - 8388616.0f;
-          x[i][e] = __fmul_rn(c, d[r][i]);
-        }
-      wht_warp<U, NI>(x, lane);
-      __half* dst = a.out_v + ((size_t)kvh * a.n_cells + p0 + r) * HD;
-#pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int d0 = U * lane + 32 * U * i;
-        if constexpr (U == 4)
-          *reinterpret_cast<uint2*>(dst + d0) =
-              make_uint2(f16x2_rn(x[i][0], x[i][1]), f16x2_rn(x[i][U > 2 ? 2 : 0], x[i][U > 3 ? 3 : 0]));
-        else
-          *reinterpret_cast<uint32_t*>(dst + d0) = f16x2_rn(x[i][0], x[i][1]);
-      }
+      for (int q = 0; q < VPL / 8; ++q)
+        reinterpret_cast<uint4*>(dst)[q] =
+            make_uint4(f16x2_rn(x[8 * q], x[8 * q + 1]), f16x2_rn(x[8 * q + 2], x[8 * q + 3]),
+                       f16x2_rn(x[8 * q + 4], x[8 * q + 5]), f16x2_rn(x[8 * q + 6], x[8 * q + 7]));
     }
   }
 }
@@ -202,7 +195,8 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   if (fmt != KVQ_K8V4) return cudaErrorInvalidValue;
   cudaError_t e = launch_fmt<KVQ_K8V4>(hd, a, s, grid);
   if (e != cudaSuccess) return e;
-  long long vx = (a.n_cells + 8 * kV4RowsPerWarp - 1) / (8 * kV4RowsPerWarp);
+  const int rpc = 8 * (hd == 64 ? V4Rows<64>::RPW : hd == 128 ? V4Rows<128>::RPW : V4Rows<256>::RPW);
+  long long vx = (a.n_cells + rpc - 1) / rpc;  // cells per CTA of 8 warps
   if (vx > 0x7fffffffLL) vx = 0x7fffffffLL;
   const dim3 vgrid((unsigned)vx, (unsigned)a.pool.n_kv);
   switch (hd) {

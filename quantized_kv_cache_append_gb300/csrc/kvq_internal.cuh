@@ -60,6 +60,35 @@ __device__ __forceinline__ void wht_warp(float (&x)[NI][U], int lane) {
         }
 }
 
+// Walsh-Hadamard transform of a row held by LPR lanes of VPL consecutive
+// dims each: stages h = 1 .. VPL/2 inside a lane, then h = VPL .. HD/2
+// between lanes j and j ^ (h / VPL) of the group (its lanes are an aligned
+// run, so the partner stays inside it).  Each stage turns dims (i, i + h),
+// bit h of i clear, into (x_i + x_{i+h}, x_i - x_{i+h}), every sum and
+// difference rounded once in fp32, as the stage-by-stage definition does
+// (the upper lane's y - x as fma(x, -1, y), an exact product).
+template <int VPL, int LPR>
+__device__ __forceinline__ void wht_group(float (&x)[VPL], int lane) {
+#pragma unroll
+  for (int h = 1; h < VPL; h *= 2)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (!(i & h)) {
+        const float p = x[i], q = x[i + h];
+        x[i] = __fadd_rn(p, q);
+        x[i + h] = __fsub_rn(p, q);
+      }
+#pragma unroll
+  for (int hl = 1; hl < LPR; hl *= 2) {
+    const float sgn = (lane & hl) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const float y = __shfl_xor_sync(0xffffffffu, x[i], hl);
+      x[i] = __fmaf_rn(x[i], sgn, y);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Pool geometry as the kernels see it.
 // ---------------------------------------------------------------------------
