@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(W * 32) append_f16_kernel(AppendArgs a) {
   }
 }
 
-// int8 append.  A quad of 4 lanes owns one 64-dim group of one row: lane q
+// int8 append for a few tokens (decode steps; bulk appends use
+// append_q8_rows_kernel).  A quad of 4 lanes owns one 64-dim group of one row: lane q
 // holds the 16-byte chunks q, q + 4, q + 8, q + 12 of the group (dims
 // 16 i + 4 q .. + 3), so every load instruction reads 64 contiguous bytes
 // per quad.  The group maximum is a 2-step butterfly inside the quad (on
@@ -305,20 +306,102 @@ __device__ __forceinline__ uint32_t q4_codes(const float (&y)[U], float d) {
   return out;
 }
 
-// Row shape of the K8V4 append: a row (one token and KV head, K and V) is
-// held by a group of LPR consecutive lanes, lane j of the group holding the
-// VPL consecutive dims j VPL .. j VPL + VPL - 1, so a warp carries 32 / LPR
-// rows at once.  Bulk appends take VPL = 16 (8 at HD 64): few shuffles per
-// row; a few rows (decode steps) take VPL = 4 (8 at HD 256): short chains.
+// Lane-group row shape of the bulk int8 and K8V4 appends: a row (one token
+// and KV head, K and V) is held by a group of LPR consecutive lanes, lane j
+// of the group holding the VPL consecutive dims j VPL .. j VPL + VPL - 1
+// (64 contiguous bytes of fp32 at VPL 16), so a warp carries 32 / LPR rows
+// at once.  Bulk appends take VPL = 16 (8 at HD 64): few shuffles per row;
+// a few K8V4 rows (decode steps) take VPL = 4 (8 at HD 256): short chains.
 template <int HD, int VPL_>
-struct K8V4Rows {
+struct LaneRows {
   static constexpr int VPL = VPL_;                // values a lane holds (4, 8 or 16)
   static constexpr int LPR = HD / VPL;            // lanes of a row
   static constexpr int RPW = 32 / LPR;            // rows a warp holds
   static_assert(VPL % 4 == 0 && LPR <= 32 && LPR * VPL == HD, "K8V4 row shape");
 };
 
-// K8V4 append (K8V4Rows layout; W warps a CTA).  K: int8 codes per 64-dim
+// int8 codes of one row held by a lane group (LaneRows layout): the group
+// maximum over the 64 / VPL lanes of each 64-dim group (bit patterns of |x|,
+// as the int8 kernel), group_scale, codes4 (or the quotients for a
+// non-finite group); dr < 0 stores nothing.
+template <int HD, int VPL, int LPR>
+__device__ __forceinline__ void q8_lanes(const float (&x)[VPL], long long dr, int j, int8_t* codes,
+                                         __half* scales) {
+  constexpr int NG = HD / kGroup;
+  constexpr int LG = kGroup / VPL;  // lanes of a 64-dim group
+  uint32_t mb = 0;
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) mb = max(mb, __float_as_uint(x[e]) & 0x7fffffffu);
+#pragma unroll
+  for (int off = 1; off < LG; off <<= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+  const float amax = __uint_as_float(mb);
+  const __half sh = group_scale(amax);
+  const float sf = __half2float(sh);
+  uint32_t c[VPL / 4];
+  if (amax <= 3.4028234663852886e38f) {
+    const float rs = rcp_approx(sf);
+#pragma unroll
+    for (int q = 0; q < VPL / 4; ++q)
+      c[q] = codes4(make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]), sf, rs);
+  } else {
+#pragma unroll
+    for (int q = 0; q < VPL / 4; ++q)
+      c[q] = exact_code(x[4 * q], sf) | (exact_code(x[4 * q + 1], sf) << 8) |
+             (exact_code(x[4 * q + 2], sf) << 16) | (exact_code(x[4 * q + 3], sf) << 24);
+  }
+  if (dr >= 0) {
+    int8_t* dst = codes + dr * HD + j * VPL;
+    if constexpr (VPL == 16)
+      *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[VPL > 8 ? 2 : 0], c[VPL > 8 ? 3 : 0]);
+    else if constexpr (VPL == 8)
+      *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[VPL > 4 ? 1 : 0]);
+    else
+      *reinterpret_cast<uint32_t*>(dst) = c[0];
+    if (j % LG == 0) scales[dr * NG + (j * VPL) / kGroup] = sh;
+  }
+}
+
+// Loads of one row into a lane group (zeros for rows past the end).
+template <int HD, int VPL>
+__device__ __forceinline__ void load_row_lanes(const float* src, long long row, bool live, int j,
+                                               float (&x)[VPL]) {
+#pragma unroll
+  for (int q = 0; q < VPL / 4; ++q) {
+    float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) v4 = __ldcs(reinterpret_cast<const float4*>(src + (size_t)row * HD + (size_t)j * VPL + 4 * q));
+    x[4 * q] = v4.x;
+    x[4 * q + 1] = v4.y;
+    x[4 * q + 2] = v4.z;
+    x[4 * q + 3] = v4.w;
+  }
+}
+
+// int8 append of bulk batches (prefill, prompt chunks) with the lane-group
+// row layout: K and V of a row each through q8_lanes.  Same arithmetic,
+// hence the same bytes, as append_q8_kernel; about 1.3x its rate, since
+// every lane keeps 128 contiguous bytes of K and V in flight.
+template <int HD, int VPL_, int W>
+__global__ void __launch_bounds__(W * 32) append_q8_rows_kernel(AppendArgs a) {
+  using R = LaneRows<HD, VPL_>;
+  constexpr int VPL = R::VPL, LPR = R::LPR, RPW = R::RPW;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, j = lane & (LPR - 1);
+  const long long rows = (long long)a.n_tok * a.n_kv;
+  const bool rows32 = rows <= 0x7fffffffLL;
+  const long long row0 = ((long long)blockIdx.x * W + (threadIdx.x >> 5)) * RPW;
+  if (row0 >= rows) return;  // warp-uniform
+  const long long row = row0 + lane / LPR;
+  const bool live = row < rows;
+  float xk[VPL], xv[VPL];
+  load_row_lanes<HD, VPL>(a.k, row, live, j, xk);
+  load_row_lanes<HD, VPL>(a.v, row, live, j, xv);
+  const long long dr = live ? dest_row(a, row, rows32) : -1;
+  q8_lanes<HD, VPL, LPR>(xk, dr, j, static_cast<int8_t*>(a.k_dst), a.ks_dst);
+  q8_lanes<HD, VPL, LPR>(xv, dr, j, static_cast<int8_t*>(a.v_dst), a.vs_dst);
+}
+
+// K8V4 append (LaneRows layout; W warps a CTA).  K: int8 codes per 64-dim
 // group, the int8 format's arithmetic (group maximum over the group's
 // lanes, group_scale, codes4).  V: rotated (wht_group), then per block of
 // 32 rotated dims the element of largest magnitude, the first one on ties
@@ -328,10 +411,9 @@ struct K8V4Rows {
 // zeros through every shuffle and store nothing.
 template <int HD, int VPL_, int W>
 __global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
-  using R = K8V4Rows<HD, VPL_>;
+  using R = LaneRows<HD, VPL_>;
   constexpr int VPL = R::VPL, LPR = R::LPR, RPW = R::RPW;
-  constexpr int NG = HD / kGroup, NB = HD / kQ4Block;
-  constexpr int LG = kGroup / VPL;    // lanes of a 64-dim K group
+  constexpr int NB = HD / kQ4Block;
   constexpr int LB = kQ4Block / VPL;  // lanes of a 32-dim V block
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -344,52 +426,12 @@ __global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
   const bool live = row < rows;
 
   float xk[VPL], xv[VPL];
-#pragma unroll
-  for (int q = 0; q < VPL / 4; ++q) {
-    float4 k4 = make_float4(0.f, 0.f, 0.f, 0.f), v4 = k4;
-    if (live) {
-      const size_t off = (size_t)row * HD + (size_t)j * VPL + 4 * q;
-      k4 = __ldcs(reinterpret_cast<const float4*>(a.k + off));
-      v4 = __ldcs(reinterpret_cast<const float4*>(a.v + off));
-    }
-    xk[4 * q] = k4.x; xk[4 * q + 1] = k4.y; xk[4 * q + 2] = k4.z; xk[4 * q + 3] = k4.w;
-    xv[4 * q] = v4.x; xv[4 * q + 1] = v4.y; xv[4 * q + 2] = v4.z; xv[4 * q + 3] = v4.w;
-  }
+  load_row_lanes<HD, VPL>(a.k, row, live, j, xk);
+  load_row_lanes<HD, VPL>(a.v, row, live, j, xv);
   const long long dr = live ? dest_row(a, row, rows32) : -1;
 
   // ---- K: int8, one fp16 scale per 64 dims
-  {
-    uint32_t mb = 0;
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) mb = max(mb, __float_as_uint(xk[e]) & 0x7fffffffu);
-#pragma unroll
-    for (int off = 1; off < LG; off <<= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-    const float amax = __uint_as_float(mb);
-    const __half sh = group_scale(amax);
-    const float sf = __half2float(sh);
-    uint32_t c[VPL / 4];
-    if (amax <= 3.4028234663852886e38f) {
-      const float rs = rcp_approx(sf);
-#pragma unroll
-      for (int q = 0; q < VPL / 4; ++q)
-        c[q] = codes4(make_float4(xk[4 * q], xk[4 * q + 1], xk[4 * q + 2], xk[4 * q + 3]), sf, rs);
-    } else {
-#pragma unroll
-      for (int q = 0; q < VPL / 4; ++q)
-        c[q] = exact_code(xk[4 * q], sf) | (exact_code(xk[4 * q + 1], sf) << 8) |
-               (exact_code(xk[4 * q + 2], sf) << 16) | (exact_code(xk[4 * q + 3], sf) << 24);
-    }
-    if (dr >= 0) {
-      int8_t* dst = static_cast<int8_t*>(a.k_dst) + dr * HD + j * VPL;
-      if constexpr (VPL == 16)
-        *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[VPL > 8 ? 2 : 0], c[VPL > 8 ? 3 : 0]);
-      else if constexpr (VPL == 8)
-        *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[VPL > 4 ? 1 : 0]);
-      else
-        *reinterpret_cast<uint32_t*>(dst) = c[0];
-      if (j % LG == 0) a.ks_dst[dr * NG + (j * VPL) / kGroup] = sh;
-    }
-  }
+  q8_lanes<HD, VPL, LPR>(xk, dr, j, static_cast<int8_t*>(a.k_dst), a.ks_dst);
 
   // ---- V: rotate, then 4-bit codes and one fp16 scale per 32 rotated dims
   wht_group<VPL, LPR>(xv, lane);
@@ -470,7 +512,10 @@ cudaError_t launch_q8(const AppendArgs& a, cudaStream_t s) {
   const long long groups = (long long)a.n_tok * a.n_kv * (HD / kGroup);
   if (groups < (1LL << 12))
     return launch_grid(append_q8_kernel<HD, 1, 2, true>, (groups + 7) / 8, 64, a, s);
-  return launch_grid(append_q8_kernel<HD, 2, 8, false>, (groups + 127) / 128, 256, a, s);
+  constexpr int VB = HD >= 128 ? 16 : 8;
+  constexpr int RB = LaneRows<HD, VB>::RPW;
+  const long long rows = (long long)a.n_tok * a.n_kv;
+  return launch_grid(append_q8_rows_kernel<HD, VB, 8>, (rows + 8 * RB - 1) / (8 * RB), 256, a, s);
 }
 
 // Few rows (decode steps): short per-lane chains (VPL 4, 8 at HD 256) in
@@ -479,7 +524,7 @@ template <int HD>
 cudaError_t launch_k8v4(const AppendArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.n_tok * a.n_kv;
   constexpr int VS = HD == 256 ? 8 : 4, VB = HD >= 128 ? 16 : 8;
-  constexpr int RS = K8V4Rows<HD, VS>::RPW, RB = K8V4Rows<HD, VB>::RPW;
+  constexpr int RS = LaneRows<HD, VS>::RPW, RB = LaneRows<HD, VB>::RPW;
   if (rows < 4096)
     return launch_grid(append_k8v4_kernel<HD, VS, 4>, (rows + 4 * RS - 1) / (4 * RS), 128, a, s);
   return launch_grid(append_k8v4_kernel<HD, VB, 8>, (rows + 8 * RB - 1) / (8 * RB), 256, a, s);

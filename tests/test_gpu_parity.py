@@ -151,7 +151,8 @@ def test_empty_sequences_give_zero_output():
     assert not got[0].any() and not got[2].any()
 
 
-def test_degenerate_quantization_groups():
+@pytest.mark.parametrize("reps", [1, 24])   # a few tokens, and the bulk kernel shape
+def test_degenerate_quantization_groups(reps):
     # zero rows, tiny rows (fp16-subnormal or underflowing scales), huge rows
     # (scale overflows to +inf: zero codes), exact ties, fp32 subnormal inputs
     rng = np.random.default_rng(5)
@@ -167,14 +168,17 @@ def test_degenerate_quantization_groups():
     k[6, 0, :64] = np.float32(260223.0 / 2048.0)
     k[6, 0, 1] = np.float32(65.51)
     v = k[::-1].copy()
-    table = np.arange(4, dtype=np.int32)[None]
+    k, v = np.tile(k, (reps, 1, 1)), np.tile(v, (reps, 1, 1))
+    n *= reps
+    table = np.arange(-(-n // 16), dtype=np.int32)[None]
     for fmt in ("f16", "q8", "k8v4"):
-        p = Pair(fmt, n_kv, hd, 16, 4, table)
+        p = Pair(fmt, n_kv, hd, 16, table.shape[1], table)
         p.append(k, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32))
         p.assert_cache_equal()
 
 
-def test_quantization_ties_and_near_ties():
+@pytest.mark.parametrize("reps", [1, 12])
+def test_quantization_ties_and_near_ties(reps):
     # Groups whose maximum is exactly 127 s (s an fp16 value, so the stored
     # scale is s itself) and whose other elements are (k + 1/2) s exactly or
     # 1-3 fp32 ulps away: x / s is an exact half-integer (round half to even)
@@ -192,13 +196,16 @@ def test_quantization_ties_and_near_ties():
         x[dn] = np.nextafter(x[dn], np.float32(-np.inf))
     x[..., ::64] = (np.float32(127.0) * s).astype(np.float32)   # the group maxima
     v = -x[::-1].copy()
-    table = np.arange(6, dtype=np.int32)[None]
-    p = Pair("q8", n_kv, hd, 16, 6, table)
+    x, v = np.tile(x, (reps, 1, 1)), np.tile(v, (reps, 1, 1))
+    n *= reps
+    table = np.arange(-(-n // 16), dtype=np.int32)[None]
+    p = Pair("q8", n_kv, hd, 16, table.shape[1], table)
     p.append(x, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32))
     p.assert_cache_equal()
 
 
-def test_scale_rounding_midpoints():
+@pytest.mark.parametrize("reps", [1, 16])
+def test_scale_rounding_midpoints(reps):
     # Group maxima a with a / 127 on, or a few fp32 ulps from, a midpoint
     # between two fp16 values (where fp16(a / 127) is decided by the last
     # bits of the fp32 quotient), and maxima whose scale is an fp16
@@ -222,8 +229,10 @@ def test_scale_rounding_midpoints():
     groups[np.arange(ng), rng.integers(0, 64, size=ng)] = a * np.where(rng.random(ng) < 0.5, 1, -1)
     x = groups.reshape(n, n_kv, hd).astype(np.float32)
     v = x[::-1].copy()
-    table = np.arange(4, dtype=np.int32)[None]
-    p = Pair("q8", n_kv, hd, 16, 4, table)
+    x, v = np.tile(x, (reps, 1, 1)), np.tile(v, (reps, 1, 1))
+    n *= reps
+    table = np.arange(-(-n // 16), dtype=np.int32)[None]
+    p = Pair("q8", n_kv, hd, 16, table.shape[1], table)
     p.append(x, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32))
     p.assert_cache_equal()
 
