@@ -66,8 +66,8 @@ class PagedPool:
         n_seq, W, n_q, hd = q.shape
         if out is None:
             out = torch.empty_like(q)
-        need = self.workspace_bytes(n_seq, W, n_q, max_ctx)
-        if workspace is None:   # needs no initial contents
+        if workspace is None:   # needs no initial contents; a given one is checked by the call
+            need = self.workspace_bytes(n_seq, W, n_q, max_ctx)
             workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
         check(kvq_decode_attn(self.cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
                               int(block_table.shape[1]), sm_scale, out, workspace,
