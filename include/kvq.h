@@ -217,6 +217,28 @@ kvq_status kvq_decode_attn(const kvq_cache *cache, const float *q, int n_seq, in
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kvq_decode_attn with the failure path of its copy waits exercised, for
+ * tests of that path only.  Every wait of the tensor-core decode for a
+ * copy into shared memory is bounded; a wait that runs out marks the
+ * split's partial as lost, the combine writes NaN for the affected output
+ * rows, and the kernel still waits (bounded) for its own copies before it
+ * exits, so the context stays usable.  This call adds extra_tx_bytes
+ * (a multiple of 16 in [16, 4096]) to the byte count every copy stage
+ * expects, bytes no copy ever delivers, and bounds each wait by
+ * wait_limit polls (1 .. 2^25; kvq_decode_attn uses 2^25): every wait runs
+ * out, and a correct failure path returns KVQ_OK with NaN in every output
+ * row of a sequence with cells.  No fault, trap or unbounded wait is
+ * involved.  Other arguments, checks and errors as kvq_decode_attn; shapes
+ * that the tensor-core kernel does not serve return KVQ_ERR_UNSUPPORTED.
+ */
+kvq_status kvq_decode_attn_lost_wait_test(const kvq_cache *cache, const float *q, int n_seq,
+                                          int W, int n_q, const int32_t *ctx_lens, int max_ctx,
+                                          const int32_t *block_table, int max_blocks_per_seq,
+                                          float sm_scale, float *out, void *workspace,
+                                          size_t workspace_bytes, uint32_t wait_limit,
+                                          uint32_t extra_tx_bytes, void *stream);
+
+/*
  * FP16 compaction of cells [0, n_cells) of one sequence ([kv-q8 PR],
  * "Extra Notes": k_kv_f16 compacts [kvh][ctx][HD] into [kvh][P][HD]
  * halves; on the FP16 cache it is a pure copy).

@@ -35,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "kvq_append",
     "kvq_decode_workspace_bytes",
     "kvq_decode_attn",
+    "kvq_decode_attn_lost_wait_test",
     "kvq_compact_f16",
     "kvq_chunk_attn",
     "kvq_gather_cells",
@@ -96,6 +97,9 @@ def load_library(path: Optional[str] = None):
     lib.kvq_decode_workspace_bytes.argtypes = [CP, I, I, I, I]
     lib.kvq_decode_attn.restype = I
     lib.kvq_decode_attn.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P, Z, P]
+    lib.kvq_decode_attn_lost_wait_test.restype = I
+    lib.kvq_decode_attn_lost_wait_test.argtypes = [CP, P, I, I, I, P, I, P, I, ctypes.c_float, P, P,
+                                                   Z, ctypes.c_uint32, ctypes.c_uint32, P]
     lib.kvq_compact_f16.restype = I
     lib.kvq_compact_f16.argtypes = [CP, P, I, P, P, P]
     lib.kvq_chunk_attn.restype = I
@@ -226,6 +230,16 @@ def kvq_stream_fetch(host_copy: kvq_cache, window: kvq_cache, fetch_src, fetch_d
     return load_library().kvq_stream_fetch(ctypes.byref(host_copy), ctypes.byref(window),
                                            _ptr(fetch_src), _ptr(fetch_dst), n_fetch,
                                            _stream(stream))
+
+
+def kvq_decode_attn_lost_wait_test(cache: kvq_cache, q, n_seq: int, W: int, n_q: int, ctx_lens,
+                                   max_ctx: int, block_table, max_blocks_per_seq: int,
+                                   sm_scale: float, out, workspace, workspace_bytes: int,
+                                   wait_limit: int, extra_tx_bytes: int, stream=None) -> int:
+    return load_library().kvq_decode_attn_lost_wait_test(
+        ctypes.byref(cache), _ptr(q), n_seq, W, n_q, _ptr(ctx_lens), max_ctx, _ptr(block_table),
+        max_blocks_per_seq, float(sm_scale), _ptr(out), _ptr(workspace), workspace_bytes,
+        wait_limit, extra_tx_bytes, _stream(stream))
 
 
 def kvq_status_string(status: int) -> str:

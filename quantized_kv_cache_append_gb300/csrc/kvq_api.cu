@@ -204,7 +204,8 @@ namespace {
 kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W, int n_q,
                        const int32_t* ctx_lens, int max_ctx, const int32_t* block_table,
                        int max_blocks_per_seq, float sm_scale, float* out, void* workspace,
-                       size_t workspace_bytes, void* stream, bool fit_plan) {
+                       size_t workspace_bytes, void* stream, bool fit_plan,
+                       uint32_t wait_limit = kDefaultWaitLimit, uint32_t extra_tx = 0) {
   kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
   st = check_decode_shape(cache, n_seq, W, n_q, max_ctx, max_blocks_per_seq);
@@ -219,6 +220,7 @@ kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W,
   if (!plan_decode(cache, n_seq, W, n_q, max_ctx, &plan, fit_plan ? workspace_bytes : SIZE_MAX))
     return fit_plan ? KVQ_ERR_WORKSPACE : KVQ_ERR_ARG;
   if (workspace_bytes < plan.bytes) return KVQ_ERR_WORKSPACE;
+  if (extra_tx != 0 && !plan.use_mma) return KVQ_ERR_UNSUPPORTED;  // no copy waits to run out
   DecodeArgs a;
   a.pool = make_pool(cache);
   a.q = q;
@@ -236,6 +238,8 @@ kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W,
   a.split_cells = plan.split_cells;
   a.nsplit = plan.nsplit;
   a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
+  a.wait_limit = wait_limit;
+  a.extra_tx = extra_tx;
   const cudaError_t e =
       launch_decode(cache->fmt, cache->head_dim, plan, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
@@ -252,6 +256,20 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache* cache, const float* q, int n
   return kvq::decode_impl(cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
                           max_blocks_per_seq, sm_scale, out, workspace, workspace_bytes, stream,
                           false);
+}
+
+KVQ_API kvq_status kvq_decode_attn_lost_wait_test(const kvq_cache* cache, const float* q, int n_seq,
+                                                  int W, int n_q, const int32_t* ctx_lens,
+                                                  int max_ctx, const int32_t* block_table,
+                                                  int max_blocks_per_seq, float sm_scale, float* out,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  uint32_t wait_limit, uint32_t extra_tx_bytes,
+                                                  void* stream) {
+  if (wait_limit == 0 || wait_limit > kDefaultWaitLimit) return KVQ_ERR_ARG;
+  if (extra_tx_bytes == 0 || extra_tx_bytes > 4096 || extra_tx_bytes % 16 != 0) return KVQ_ERR_ARG;
+  return kvq::decode_impl(cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
+                          max_blocks_per_seq, sm_scale, out, workspace, workspace_bytes, stream,
+                          false, wait_limit, extra_tx_bytes);
 }
 
 KVQ_API kvq_status kvq_compact_f16(const kvq_cache* cache, const int32_t* block_table_row,

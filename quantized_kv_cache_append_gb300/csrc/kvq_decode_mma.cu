@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       if (rows[p] >= 0) bytes += (uint32_t)pc * (C::ROWB + C::VROWB + (C::KI8 ? (C::NG + C::VNS) * 2 : 0));
     }
     const uint32_t full = bar_full + 8 * s;
-    mbar_expect_tx(full, bytes);
+    mbar_expect_tx(full, bytes + a.extra_tx);
     const uint32_t st = sbase + s * C::STAGE_B;
     for (int p = 0; p < n_pieces; ++p) {
       const int row = rows[p];
@@ -819,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   int nv_cur = 0;
   float p_cur[NT][4];
   if (n_tiles > 0) {
-    if (!mbar_wait(bar_full, 0)) {
+    if (!mbar_wait(bar_full, 0, a.wait_limit)) {
       lost = true;
     } else {
       nv_cur = slice_nvalid(0, blk_n);
@@ -832,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   int it = 0;
   for (; it + 1 < n_tiles && !lost; ++it) {
     const int sn = (it + 1) % C::STAGES;
-    if (!mbar_wait(bar_full + 8 * sn, ((it + 1) / C::STAGES) & 1)) {
+    if (!mbar_wait(bar_full + 8 * sn, ((it + 1) / C::STAGES) & 1, a.wait_limit)) {
       lost = true;
       break;
     }
@@ -853,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     // Every copy this CTA issued has landed before the CTA can exit (waits
     // return at once in normal runs; they are bounded after a lost wait).
     for (int it = n_tiles > C::STAGES ? n_tiles - C::STAGES : 0; it < n_tiles; ++it)
-      (void)mbar_wait(bar_full + 8 * (it % C::STAGES), (it / C::STAGES) & 1);
+      (void)mbar_wait(bar_full + 8 * (it % C::STAGES), (it / C::STAGES) & 1, a.wait_limit);
   }
 
   // ---------------- merge the 4 warps, write the split's partial ----------------

@@ -12,6 +12,7 @@ namespace kvq {
 
 constexpr int kGroup = KVQ_GROUP;  // dims per fp16 scale in the int8 format
 constexpr int kQ4Block = KVQ_Q4_BLOCK;  // rotated V dims per fp16 scale in K8V4
+constexpr uint32_t kDefaultWaitLimit = 1u << 25;  // polls of a copy wait before it is lost
 
 // Walsh-Hadamard transform (Sylvester order, no normalisation) of a row of
 // 32 * U * NI values held by one warp: lane l holds x[i][e] = dim e + U l +
@@ -137,6 +138,9 @@ struct DecodeArgs {
   float* ws_ml;        // [n_seq][n_kv][nsplit][R][2]    (running max, sum), log2 domain
   int n_seq, W, n_q, G, R, max_blocks, split_cells, nsplit;
   float qscale;        // sm_scale * log2(e): logits come out in the log2 domain
+  uint32_t wait_limit; // polls of a copy wait before it is declared lost
+  uint32_t extra_tx;   // bytes added to each stage's expected count (0; >0 only
+                       // in the failure-path test, where no copy delivers them)
 };
 
 struct CompactArgs {

@@ -4,13 +4,15 @@
 // permutes and fp16 pair arithmetic.  Each is one or two PTX instructions.
 #pragma once
 
+#include "kvq_internal.cuh"
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace kvq {
 
-constexpr uint32_t kWaitLimit = 1u << 25;  // polls before a wait is declared lost
+constexpr uint32_t kWaitLimit = kDefaultWaitLimit;  // polls before a wait is declared lost
 
 static __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -26,8 +28,9 @@ static __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // Bounded wait for the phase with the given parity; false if it never came.
-static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                                 uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
