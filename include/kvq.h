@@ -50,7 +50,8 @@
  *   - Device-side preconditions (not checked on the host, since the values
  *     live on the device): block ids in the block table lie in
  *     [0, n_blocks) for every cell that is read or written; token positions
- *     are < max_blocks_per_seq * block_size; W <= ctx_lens[b] <= max_ctx.
+ *     are < max_blocks_per_seq * block_size; 0 <= ctx_lens[b] <= max_ctx (a
+ *     query token with no visible cell, as when ctx_lens[b] < W, gets 0).
  *     Breaking them gives unspecified values for the cells involved but no
  *     out-of-bounds access: every kernel checks each block id it reads
  *     against [0, n_blocks) and skips (append, compaction) or reads as
