@@ -294,7 +294,8 @@ kvq_status kvq_chunk_attn(const void *k16, const void *v16, int n_kv_heads, int 
  *                    pool's format (fp16 or int8), 16-byte aligned; K8V4's
  *                    codes_v is [n_cells][n_kv_heads][head_dim / 2] bytes
  *   scales_k, scales_v
- *                    device fp16 [n_cells][n_kv_heads][head_dim / 64]; required
+ *                    device fp16 [n_cells][n_kv_heads][head_dim / 64], 16-byte
+ *                    aligned; required
  *                    for KVQ_Q8 (KVQ_ERR_ARG without them), ignored for
  *                    KVQ_F16; K8V4 requires both, scales_v being
  *                    [n_cells][n_kv_heads][head_dim / 32]

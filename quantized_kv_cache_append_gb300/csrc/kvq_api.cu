@@ -306,7 +306,7 @@ kvq_status persist_impl(const kvq_cache* cache, const int32_t* block_table_row, 
   // int8 (and 4-bit) codes never move without their scales
   if (cache->fmt != KVQ_F16 && (scales_k == nullptr || scales_v == nullptr)) return KVQ_ERR_ARG;
   if (!aligned(block_table_row, 4) || !aligned(codes_k, 16) || !aligned(codes_v, 16) ||
-      !aligned(scales_k, 2) || !aligned(scales_v, 2))
+      !aligned(scales_k, 16) || !aligned(scales_v, 16))
     return KVQ_ERR_ARG;
   if ((long long)n_cells * cache->n_kv_heads >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
   PersistArgs a;

@@ -21,6 +21,17 @@
 namespace kvq {
 namespace {
 
+// B bytes (2 .. 16, a power of two) from src to dst, both B-byte aligned
+// (a row's scales: B = 2 per 64 or 32 dims, and rows start at multiples of
+// B), as one access.
+template <int B>
+__device__ __forceinline__ void copy_run(void* dst, const void* src) {
+  if constexpr (B == 16) *static_cast<uint4*>(dst) = __ldg(static_cast<const uint4*>(src));
+  else if constexpr (B == 8) *static_cast<uint2*>(dst) = __ldg(static_cast<const uint2*>(src));
+  else if constexpr (B == 4) *static_cast<uint32_t*>(dst) = __ldg(static_cast<const uint32_t*>(src));
+  else *static_cast<unsigned short*>(dst) = __ldg(static_cast<const unsigned short*>(src));
+}
+
 template <int FMT, int HD, bool GATHER>
 __global__ void __launch_bounds__(256) persist_kernel(PersistArgs a) {
   constexpr int ESZ = FMT == KVQ_F16 ? 2 : 1;
@@ -60,16 +71,13 @@ __global__ void __launch_bounds__(256) persist_kernel(PersistArgs a) {
             __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.codes_v) + vrun_off));
     }
     if constexpr (FMT != KVQ_F16) {
-      if (chunk == 0) {
-#pragma unroll
-        for (int gi = 0; gi < NG; ++gi) {
-          if constexpr (GATHER) a.scales_k[(size_t)r * NG + gi] = a.pool.ks[row * NG + gi];
-          else a.pool_ks[row * NG + gi] = a.scales_k[(size_t)r * NG + gi];
-        }
-#pragma unroll
-        for (int gi = 0; gi < NVS; ++gi) {
-          if constexpr (GATHER) a.scales_v[(size_t)r * NVS + gi] = a.pool.vs[row * NVS + gi];
-          else a.pool_vs[row * NVS + gi] = a.scales_v[(size_t)r * NVS + gi];
+      if (chunk == 0) {  // a row's scales, each run as one aligned vector
+        if constexpr (GATHER) {
+          copy_run<NG * 2>(a.scales_k + (size_t)r * NG, a.pool.ks + row * NG);
+          copy_run<NVS * 2>(a.scales_v + (size_t)r * NVS, a.pool.vs + row * NVS);
+        } else {
+          copy_run<NG * 2>(a.pool_ks + row * NG, a.scales_k + (size_t)r * NG);
+          copy_run<NVS * 2>(a.pool_vs + row * NVS, a.scales_v + (size_t)r * NVS);
         }
       }
     }
