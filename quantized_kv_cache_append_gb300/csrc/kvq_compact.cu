@@ -60,10 +60,38 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, uint32_t sel, uint3
   return hmul2(h, s2);
 }
 
-// K8V4 V rows: grid (cell groups, KV head); a cell's row is held by a
-// group of LPR = HD / VPL lanes (VPL consecutive dims each, within one
-// 32-dim block), so a warp de-rotates 32 / LPR cells at once; the grid
-// covers every cell (the loop runs once unless the x dimension was capped).
+// int8 codes of chunk `chunk` (16 dims) of cell p of KV head kvh, K (which
+// 0) or V (1), widened and scaled to fp16 into the staging; a block id out
+// of range skips the cell.
+template <int HD>
+__device__ __forceinline__ void q8_chunk(const CompactArgs& a, int kvh, int which, int p, int chunk) {
+  constexpr int DPT = 16, NG = HD / kGroup;
+  const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
+  if (blk < 0 || blk >= a.pool.n_blocks) return;  // precondition broken: skip
+  const int bs = 1 << a.pool.bs_log2;
+  const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+  __half* dst = (which ? a.out_v : a.out_k) + ((size_t)kvh * a.n_cells + p) * HD + chunk * DPT;
+  const int8_t* src = static_cast<const int8_t*>(which ? a.pool.v : a.pool.k) + row * HD;
+  const uint4 c = __ldg(reinterpret_cast<const uint4*>(src + chunk * DPT));
+  const unsigned short sbits =
+      __half_as_ushort(((which ? a.pool.vs : a.pool.ks) + row * NG)[(chunk * DPT) / kGroup]);
+  const uint32_t s2 = (uint32_t)sbits * 0x10001u;
+  uint4 o0, o1;
+  o0.x = dequant_pair(c.x, 0x4140u, s2);
+  o0.y = dequant_pair(c.x, 0x4342u, s2);
+  o0.z = dequant_pair(c.y, 0x4140u, s2);
+  o0.w = dequant_pair(c.y, 0x4342u, s2);
+  o1.x = dequant_pair(c.z, 0x4140u, s2);
+  o1.y = dequant_pair(c.z, 0x4342u, s2);
+  o1.z = dequant_pair(c.w, 0x4140u, s2);
+  o1.w = dequant_pair(c.w, 0x4342u, s2);
+  reinterpret_cast<uint4*>(dst)[0] = o0;
+  reinterpret_cast<uint4*>(dst)[1] = o1;
+}
+
+// K8V4 V rows: a cell's row is held by a group of LPR = HD / VPL lanes
+// (VPL consecutive dims each, within one 32-dim block), so a warp
+// de-rotates RPW = 32 / LPR cells at once.
 template <int HD>
 struct V4Rows {
   static constexpr int VPL = HD >= 128 ? 16 : 8;
@@ -71,53 +99,72 @@ struct V4Rows {
   static constexpr int RPW = 32 / LPR;
 };
 
+// The warp's RPW cells from p_base (lane group g takes cell p_base + g);
+// cells past the end or in an out-of-range block are skipped, every lane
+// still taking part in the shuffles.
 template <int HD>
-__global__ void __launch_bounds__(256) compact_v4_kernel(CompactArgs a) {
-  constexpr int VPL = V4Rows<HD>::VPL, LPR = V4Rows<HD>::LPR, RPW = V4Rows<HD>::RPW;
+__device__ __forceinline__ void v4_rows(const CompactArgs& a, int kvh, int p_base, int lane) {
+  constexpr int VPL = V4Rows<HD>::VPL, LPR = V4Rows<HD>::LPR;
   constexpr int NB = HD / kQ4Block;
-  const int kvh = blockIdx.y;
-  const int lane = threadIdx.x & 31, j = lane & (LPR - 1);
-  const int wpb = blockDim.x >> 5;
+  const int j = lane & (LPR - 1);
   const int bs = 1 << a.pool.bs_log2;
-  for (int p0 = (blockIdx.x * wpb + (threadIdx.x >> 5)) * RPW; p0 < a.n_cells;
-       p0 += gridDim.x * wpb * RPW) {
-    const int p = p0 + lane / LPR;
-    const int blk = p < a.n_cells ? __ldg(a.block_row + (p >> a.pool.bs_log2)) : -1;
-    const bool ok = blk >= 0 && blk < a.pool.n_blocks;  // else skip the cell
-    float x[VPL];
-    if (ok) {
-      const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
-      const unsigned char* src = static_cast<const unsigned char*>(a.pool.v) + row * (HD / 2) + j * (VPL / 2);
-      // d / HD: the power-of-two factor of the inverse rotation, taken
-      // before the butterflies (exact, and it commutes with every sum)
-      const float d = __half2float(__ldg(a.pool.vs + row * NB + (j * VPL) / kQ4Block)) * (1.0f / HD);
-      uint32_t w[VPL / 8];
-      if constexpr (VPL == 16) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
-        w[0] = u.x;
-        w[VPL / 8 > 1 ? 1 : 0] = u.y;
-      } else {
-        w[0] = __ldg(reinterpret_cast<const uint32_t*>(src));
-      }
-#pragma unroll
-      for (int e = 0; e < VPL; ++e) {
-        // 2^23 + code as float bits, minus 2^23 + 8: code - 8, exactly
-        const float c = __uint_as_float(0x4b000000u | ((w[e / 8] >> (4 * (e % 8))) & 15u)) - 8388616.0f;
-        x[e] = __fmul_rn(c, d);
-      }
+  const int p = p_base + lane / LPR;
+  const int blk = p < a.n_cells ? __ldg(a.block_row + (p >> a.pool.bs_log2)) : -1;
+  const bool ok = blk >= 0 && blk < a.pool.n_blocks;
+  float x[VPL];
+  if (ok) {
+    const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+    const unsigned char* src = static_cast<const unsigned char*>(a.pool.v) + row * (HD / 2) + j * (VPL / 2);
+    // d / HD: the power-of-two factor of the inverse rotation, taken
+    // before the butterflies (exact, and it commutes with every sum)
+    const float d = __half2float(__ldg(a.pool.vs + row * NB + (j * VPL) / kQ4Block)) * (1.0f / HD);
+    uint32_t w[VPL / 8];
+    if constexpr (VPL == 16) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+      w[0] = u.x;
+      w[VPL / 8 > 1 ? 1 : 0] = u.y;
     } else {
-#pragma unroll
-      for (int e = 0; e < VPL; ++e) x[e] = 0.f;
+      w[0] = __ldg(reinterpret_cast<const uint32_t*>(src));
     }
-    wht_group<VPL, LPR>(x, lane);  // every lane takes part
-    if (ok) {
-      __half* dst = a.out_v + ((size_t)kvh * a.n_cells + p) * HD + j * VPL;
 #pragma unroll
-      for (int q = 0; q < VPL / 8; ++q)
-        reinterpret_cast<uint4*>(dst)[q] =
-            make_uint4(f16x2_rn(x[8 * q], x[8 * q + 1]), f16x2_rn(x[8 * q + 2], x[8 * q + 3]),
-                       f16x2_rn(x[8 * q + 4], x[8 * q + 5]), f16x2_rn(x[8 * q + 6], x[8 * q + 7]));
+    for (int e = 0; e < VPL; ++e) {
+      // 2^23 + code as float bits, minus 2^23 + 8: code - 8, exactly
+      const float c = __uint_as_float(0x4b000000u | ((w[e / 8] >> (4 * (e % 8))) & 15u)) - 8388616.0f;
+      x[e] = __fmul_rn(c, d);
     }
+  } else {
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) x[e] = 0.f;
+  }
+  wht_group<VPL, LPR>(x, lane);
+  if (ok) {
+    __half* dst = a.out_v + ((size_t)kvh * a.n_cells + p) * HD + j * VPL;
+#pragma unroll
+    for (int q = 0; q < VPL / 8; ++q)
+      reinterpret_cast<uint4*>(dst)[q] =
+          make_uint4(f16x2_rn(x[8 * q], x[8 * q + 1]), f16x2_rn(x[8 * q + 2], x[8 * q + 3]),
+                     f16x2_rn(x[8 * q + 4], x[8 * q + 5]), f16x2_rn(x[8 * q + 6], x[8 * q + 7]));
+  }
+}
+
+// K8V4 compaction in one launch: CTA x of KV head y takes cells
+// [x C, x C + C) with C = 256 / (HD / 16): first every thread one 16-code
+// chunk of K (memory-bound), then the warps the V rows in lane groups
+// (ALU-bound), so the two kinds of work of different CTAs overlap on an SM.
+template <int HD>
+__global__ void __launch_bounds__(256) compact_k8v4_kernel(CompactArgs a) {
+  constexpr int CPR = HD / 16;              // K chunks per cell
+  constexpr int C = 256 / CPR;              // cells per CTA
+  constexpr int RPW = V4Rows<HD>::RPW;
+  const int kvh = blockIdx.y;
+  const int c0 = blockIdx.x * C;
+  const int pk = c0 + threadIdx.x / CPR;
+  if (pk < a.n_cells) q8_chunk<HD>(a, kvh, 0, pk, threadIdx.x % CPR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int it = 0; it < C / (8 * RPW); ++it) {
+    const int p_base = c0 + (it * 8 + warp) * RPW;
+    if (p_base < a.n_cells) v4_rows<HD>(a, kvh, p_base, lane);  // warp-uniform
   }
 }
 
@@ -125,7 +172,6 @@ template <int FMT, int HD>
 __global__ void __launch_bounds__(256) compact_kernel(CompactArgs a) {
   constexpr int DPT = FMT == KVQ_F16 ? 8 : 16;  // dims per thread
   constexpr int CPR = HD / DPT;                  // threads per row
-  constexpr int NG = HD / kGroup;
   const int kvh = blockIdx.y % a.pool.n_kv;
   const int which = blockIdx.y / a.pool.n_kv;    // 0 = K, 1 = V
   const long long total = (long long)a.n_cells * CPR;
@@ -135,30 +181,15 @@ __global__ void __launch_bounds__(256) compact_kernel(CompactArgs a) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int p = (int)(i / CPR);
     const int chunk = (int)(i % CPR);
-    const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
-    if (blk < 0 || blk >= a.pool.n_blocks) continue;  // precondition broken: skip
-    const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
-    __half* dst = out + ((size_t)kvh * a.n_cells + p) * HD + chunk * DPT;
     if constexpr (FMT == KVQ_F16) {
+      const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
+      if (blk < 0 || blk >= a.pool.n_blocks) continue;  // precondition broken: skip
+      const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+      __half* dst = out + ((size_t)kvh * a.n_cells + p) * HD + chunk * DPT;
       const __half* src = static_cast<const __half*>(which ? a.pool.v : a.pool.k) + row * HD;
       *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src + chunk * DPT));
     } else {
-      const int8_t* src = static_cast<const int8_t*>(which ? a.pool.v : a.pool.k) + row * HD;
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(src + chunk * DPT));
-      const unsigned short sbits =
-          __half_as_ushort(((which ? a.pool.vs : a.pool.ks) + row * NG)[(chunk * DPT) / kGroup]);
-      const uint32_t s2 = (uint32_t)sbits * 0x10001u;
-      uint4 o0, o1;
-      o0.x = dequant_pair(c.x, 0x4140u, s2);
-      o0.y = dequant_pair(c.x, 0x4342u, s2);
-      o0.z = dequant_pair(c.y, 0x4140u, s2);
-      o0.w = dequant_pair(c.y, 0x4342u, s2);
-      o1.x = dequant_pair(c.z, 0x4140u, s2);
-      o1.y = dequant_pair(c.z, 0x4342u, s2);
-      o1.z = dequant_pair(c.w, 0x4140u, s2);
-      o1.w = dequant_pair(c.w, 0x4342u, s2);
-      reinterpret_cast<uint4*>(dst)[0] = o0;
-      reinterpret_cast<uint4*>(dst)[1] = o1;
+      q8_chunk<HD>(a, kvh, which, p, chunk);
     }
   }
 }
@@ -181,9 +212,22 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
+  if (fmt == KVQ_K8V4) {  // one launch: CTAs of 256 / (HD / 16) cells per KV head
+    const int cells = 256 / (hd / 16);
+    long long xs = (a.n_cells + cells - 1) / cells;
+    if (xs > 0x7fffffffLL || a.pool.n_kv > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)xs, (unsigned)a.pool.n_kv);
+    switch (hd) {
+      case 64: compact_k8v4_kernel<64><<<grid, 256, 0, s>>>(a); break;
+      case 128: compact_k8v4_kernel<128><<<grid, 256, 0, s>>>(a); break;
+      case 256: compact_k8v4_kernel<256><<<grid, 256, 0, s>>>(a); break;
+      default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
   const int dpt = fmt == KVQ_F16 ? 8 : 16;
   const long long per_row = (long long)a.n_cells * (hd / dpt);  // threads per (K or V, KV head)
-  const int ys = (fmt == KVQ_K8V4 ? 1 : 2) * a.pool.n_kv;     // K8V4: K here, V below
+  const int ys = 2 * a.pool.n_kv;
   long long xs = (per_row + 255) / 256;
   const long long cap = ((long long)sms * 8 + ys - 1) / ys;  // about 8 CTAs per SM in total
   if (xs > cap) xs = cap;
@@ -192,20 +236,7 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   const dim3 grid((unsigned)xs, (unsigned)ys);
   if (fmt == KVQ_F16) return launch_fmt<KVQ_F16>(hd, a, s, grid);
   if (fmt == KVQ_Q8) return launch_fmt<KVQ_Q8>(hd, a, s, grid);
-  if (fmt != KVQ_K8V4) return cudaErrorInvalidValue;
-  cudaError_t e = launch_fmt<KVQ_K8V4>(hd, a, s, grid);
-  if (e != cudaSuccess) return e;
-  const int rpc = 8 * (hd == 64 ? V4Rows<64>::RPW : hd == 128 ? V4Rows<128>::RPW : V4Rows<256>::RPW);
-  long long vx = (a.n_cells + rpc - 1) / rpc;  // cells per CTA of 8 warps
-  if (vx > 0x7fffffffLL) vx = 0x7fffffffLL;
-  const dim3 vgrid((unsigned)vx, (unsigned)a.pool.n_kv);
-  switch (hd) {
-    case 64: compact_v4_kernel<64><<<vgrid, 256, 0, s>>>(a); break;
-    case 128: compact_v4_kernel<128><<<vgrid, 256, 0, s>>>(a); break;
-    case 256: compact_v4_kernel<256><<<vgrid, 256, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvq
