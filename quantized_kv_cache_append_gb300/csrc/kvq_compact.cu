@@ -7,22 +7,25 @@
 // fp16(code * scale); the product of an 8-bit code and an fp16 scale is
 // exact in fp32, so the only rounding is __float2half_rn (nearest even).
 //
-// Grid y = (K or V, KV head), so a thread's cell and dims come from shifts
-// alone.  FP16: one thread copies 8 dims (16 bytes).  int8: one thread
-// takes 16 codes (16 bytes) of one 64-dim group, widens each exactly to
-// fp16 (XOR 0x80, PRMT with the 0x64 exponent byte, minus 1152) and
-// multiplies pairs by the group's fp16 scale with mul.rn.f16x2: the product
-// of a code and an fp16 scale is exact, and the fp16 multiply rounds it once
-// to nearest even, with subnormals, which is fp16(code * scale).  Loads and
-// stores are coalesced along the dims of a row, then the cells.
+// FP16: grid y = (K or V, KV head), grid-stride, one thread copies 8 dims
+// (16 bytes).  int8: CTA x of KV head y takes the cells [x C, x C + C),
+// C = 256 / (HD / 16), one thread one 16-code chunk of K and the same chunk
+// of V (both loads issued first); it widens each code exactly to fp16 (XOR
+// 0x80, PRMT with the 0x64 exponent byte, minus 1152) and multiplies pairs
+// by the group's fp16 scale with mul.rn.f16x2: the product of a code and an
+// fp16 scale is exact, and the fp16 multiply rounds it once to nearest
+// even, with subnormals, which is fp16(code * scale).  Loads and stores are
+// coalesced along the dims of a row, then the cells.
 //
 // K8V4 (#711 kv: --kv k8v4 streams with --kv-resident, "What": INT8 K +
-// rotated Q4_0 V): K as the int8 format; V is decoded in the rotated basis,
-// (code - 8) * d (exact in fp32), rotated back by the same fp32 butterflies
-// as the append's rotation (wht_warp), divided by head_dim (a power of
-// two, exact; applied to d first, which gives the same bits since scaling
-// by a power of two commutes with every rounded sum) and rounded to fp16.  One warp per V row, in a launch of its
-// own (after the K launch on the same stream).
+// rotated Q4_0 V): the same CTAs take K as the int8 format, then V rows:
+// decoded in the rotated basis, (code - 8) * d (exact in fp32), rotated
+// back by the same fp32 butterflies as the append's rotation (wht_group),
+// divided by head_dim (a power of two, exact; applied to d first, which
+// gives the same bits since scaling by a power of two commutes with every
+// rounded sum) and rounded to fp16.  A V row is held by a group of lanes;
+// the K chunks (memory-bound) and the V rows (ALU-bound) of different CTAs
+// overlap on an SM.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -87,6 +90,44 @@ __device__ __forceinline__ void q8_chunk(const CompactArgs& a, int kvh, int whic
   o1.w = dequant_pair(c.w, 0x4342u, s2);
   reinterpret_cast<uint4*>(dst)[0] = o0;
   reinterpret_cast<uint4*>(dst)[1] = o1;
+}
+
+// int8 compaction: CTA x of KV head y takes cells [x C, x C + C) with
+// C = 256 / (HD / 16); each thread widens one 16-code chunk of K and the
+// same chunk of V, both loads issued before either conversion.
+template <int HD>
+__global__ void __launch_bounds__(256) compact_q8_kernel(CompactArgs a) {
+  constexpr int CPR = HD / 16, C = 256 / CPR, NG = HD / kGroup;
+  const int kvh = blockIdx.y;
+  const int p = blockIdx.x * C + threadIdx.x / CPR, chunk = threadIdx.x % CPR;
+  if (p >= a.n_cells) return;  // no barrier in this kernel
+  const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
+  if (blk < 0 || blk >= a.pool.n_blocks) return;  // precondition broken: skip
+  const int bs = 1 << a.pool.bs_log2;
+  const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+  const size_t co = row * HD + chunk * 16, so = row * NG + (chunk * 16) / kGroup;
+  const uint4 ck = __ldg(reinterpret_cast<const uint4*>(static_cast<const int8_t*>(a.pool.k) + co));
+  const uint4 cv = __ldg(reinterpret_cast<const uint4*>(static_cast<const int8_t*>(a.pool.v) + co));
+  const uint32_t sk = (uint32_t)__half_as_ushort(a.pool.ks[so]) * 0x10001u;
+  const uint32_t sv = (uint32_t)__half_as_ushort(a.pool.vs[so]) * 0x10001u;
+  const size_t out = ((size_t)kvh * a.n_cells + p) * HD + chunk * 16;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint4 c = which ? cv : ck;
+    const uint32_t s2 = which ? sv : sk;
+    uint4 o0, o1;
+    o0.x = dequant_pair(c.x, 0x4140u, s2);
+    o0.y = dequant_pair(c.x, 0x4342u, s2);
+    o0.z = dequant_pair(c.y, 0x4140u, s2);
+    o0.w = dequant_pair(c.y, 0x4342u, s2);
+    o1.x = dequant_pair(c.z, 0x4140u, s2);
+    o1.y = dequant_pair(c.z, 0x4342u, s2);
+    o1.z = dequant_pair(c.w, 0x4140u, s2);
+    o1.w = dequant_pair(c.w, 0x4342u, s2);
+    uint4* dst = reinterpret_cast<uint4*>((which ? a.out_v : a.out_k) + out);
+    dst[0] = o0;
+    dst[1] = o1;
+  }
 }
 
 // K8V4 V rows: a cell's row is held by a group of LPR = HD / VPL lanes
@@ -212,15 +253,16 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  if (fmt == KVQ_K8V4) {  // one launch: CTAs of 256 / (HD / 16) cells per KV head
+  if (fmt != KVQ_F16) {  // one thread a 16-code chunk: CTAs of 256 / (HD / 16) cells per KV head
     const int cells = 256 / (hd / 16);
     long long xs = (a.n_cells + cells - 1) / cells;
     if (xs > 0x7fffffffLL || a.pool.n_kv > 65535) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)xs, (unsigned)a.pool.n_kv);
+    const bool q8 = fmt == KVQ_Q8;
     switch (hd) {
-      case 64: compact_k8v4_kernel<64><<<grid, 256, 0, s>>>(a); break;
-      case 128: compact_k8v4_kernel<128><<<grid, 256, 0, s>>>(a); break;
-      case 256: compact_k8v4_kernel<256><<<grid, 256, 0, s>>>(a); break;
+      case 64: q8 ? compact_q8_kernel<64><<<grid, 256, 0, s>>>(a) : compact_k8v4_kernel<64><<<grid, 256, 0, s>>>(a); break;
+      case 128: q8 ? compact_q8_kernel<128><<<grid, 256, 0, s>>>(a) : compact_k8v4_kernel<128><<<grid, 256, 0, s>>>(a); break;
+      case 256: q8 ? compact_q8_kernel<256><<<grid, 256, 0, s>>>(a) : compact_k8v4_kernel<256><<<grid, 256, 0, s>>>(a); break;
       default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -234,9 +276,7 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   if (xs < 1) xs = 1;
   if (ys > 65535) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)xs, (unsigned)ys);
-  if (fmt == KVQ_F16) return launch_fmt<KVQ_F16>(hd, a, s, grid);
-  if (fmt == KVQ_Q8) return launch_fmt<KVQ_Q8>(hd, a, s, grid);
-  return cudaErrorInvalidValue;
+  return launch_fmt<KVQ_F16>(hd, a, s, grid);
 }
 
 }  // namespace kvq
