@@ -209,41 +209,28 @@ __global__ void __launch_bounds__(256) compact_k8v4_kernel(CompactArgs a) {
   }
 }
 
-template <int FMT, int HD>
-__global__ void __launch_bounds__(256) compact_kernel(CompactArgs a) {
-  constexpr int DPT = FMT == KVQ_F16 ? 8 : 16;  // dims per thread
-  constexpr int CPR = HD / DPT;                  // threads per row
+// FP16 compaction: a pure copy, grid-stride over (cell, 16-byte chunk),
+// grid y = (K or V, KV head).
+template <int HD>
+__global__ void __launch_bounds__(256) compact_f16_kernel(CompactArgs a) {
+  constexpr int DPT = 8;          // dims per thread (16 bytes)
+  constexpr int CPR = HD / DPT;   // threads per row
   const int kvh = blockIdx.y % a.pool.n_kv;
   const int which = blockIdx.y / a.pool.n_kv;    // 0 = K, 1 = V
   const long long total = (long long)a.n_cells * CPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const int bs = 1 << a.pool.bs_log2;
   __half* out = which ? a.out_v : a.out_k;
+  const __half* pool = static_cast<const __half*>(which ? a.pool.v : a.pool.k);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int p = (int)(i / CPR);
     const int chunk = (int)(i % CPR);
-    if constexpr (FMT == KVQ_F16) {
-      const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
-      if (blk < 0 || blk >= a.pool.n_blocks) continue;  // precondition broken: skip
-      const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
-      __half* dst = out + ((size_t)kvh * a.n_cells + p) * HD + chunk * DPT;
-      const __half* src = static_cast<const __half*>(which ? a.pool.v : a.pool.k) + row * HD;
-      *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src + chunk * DPT));
-    } else {
-      q8_chunk<HD>(a, kvh, which, p, chunk);
-    }
+    const int blk = __ldg(a.block_row + (p >> a.pool.bs_log2));
+    if (blk < 0 || blk >= a.pool.n_blocks) continue;  // precondition broken: skip
+    const size_t row = ((size_t)blk * a.pool.n_kv + kvh) * bs + (p & (bs - 1));
+    __half* dst = out + ((size_t)kvh * a.n_cells + p) * HD + chunk * DPT;
+    *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(pool + row * HD + chunk * DPT));
   }
-}
-
-template <int FMT>
-cudaError_t launch_fmt(int hd, const CompactArgs& a, cudaStream_t s, dim3 grid) {
-  switch (hd) {
-    case 64: compact_kernel<FMT, 64><<<grid, 256, 0, s>>>(a); break;
-    case 128: compact_kernel<FMT, 128><<<grid, 256, 0, s>>>(a); break;
-    case 256: compact_kernel<FMT, 256><<<grid, 256, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -267,8 +254,7 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
     }
     return cudaGetLastError();
   }
-  const int dpt = fmt == KVQ_F16 ? 8 : 16;
-  const long long per_row = (long long)a.n_cells * (hd / dpt);  // threads per (K or V, KV head)
+  const long long per_row = (long long)a.n_cells * (hd / 8);  // threads per (K or V, KV head)
   const int ys = 2 * a.pool.n_kv;
   long long xs = (per_row + 255) / 256;
   const long long cap = ((long long)sms * 8 + ys - 1) / ys;  // about 8 CTAs per SM in total
@@ -276,7 +262,13 @@ cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s
   if (xs < 1) xs = 1;
   if (ys > 65535) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)xs, (unsigned)ys);
-  return launch_fmt<KVQ_F16>(hd, a, s, grid);
+  switch (hd) {
+    case 64: compact_f16_kernel<64><<<grid, 256, 0, s>>>(a); break;
+    case 128: compact_f16_kernel<128><<<grid, 256, 0, s>>>(a); break;
+    case 256: compact_f16_kernel<256><<<grid, 256, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace kvq
