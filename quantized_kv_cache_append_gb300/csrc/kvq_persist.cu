@@ -104,7 +104,10 @@ cudaError_t launch_persist(int fmt, int hd, bool gather, const PersistArgs& a, c
   const int esz = fmt == KVQ_F16 ? 2 : 1;
   const long long total = (long long)a.n_cells * a.pool.n_kv * (hd * esz / 16);
   long long blocks = (total + 255) / 256;
-  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;  // grid-stride beyond 8 CTAs/SM
+  // FP16 rows: one 16-byte chunk a thread over a grid that holds them all
+  // (measured 8 % faster); int8 and K8V4 rows, whose first chunk also moves
+  // the scales: grid-stride beyond 8 CTAs an SM (measured 5-12 % faster)
+  const long long cap = fmt == KVQ_F16 ? 0x7fffffffLL : (long long)(sms > 0 ? sms : 1) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (fmt == KVQ_F16)
