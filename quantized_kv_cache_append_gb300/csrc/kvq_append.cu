@@ -4,14 +4,15 @@
 // under --kv-q8 a row is written as scale = fp16(max|x| / 127) per 64 dims and
 // code = clamp(rint(x / scale), -127, 127); the FP16 cache stores fp16(x).
 // The same section notes that the group maximum needs every thread to reach
-// a barrier before the stores.  Here a quad of lanes owns one 64-dim group,
-// so the group maximum is a warp-shuffle butterfly that every lane executes:
-// no __syncthreads exists in these kernels and no early return can skip one.
+// a barrier before the stores.  Here the lanes of a 64-dim group (a quad
+// for a few tokens; 4 lanes of 16 dims each for bulk appends) take the
+// group maximum by a warp-shuffle butterfly that every lane executes: no
+// __syncthreads exists in these kernels and no early return can skip one.
 //
 // Bit-exactness: max|x| is exact; a / 127 and x / s are the IEEE fp32
 // quotients the pages define (the library is built without fast-math, so
 // '/' is div.rn.f32), replaced by multiplies only where those provably give
-// the same fp16 scale (group_scale) or the same integer code (code_byte);
+// the same fp16 scale (group_scale) or the same integer code (codes4);
 // __float2half_rn rounds to nearest even with subnormals; rounding is to
 // nearest even, and clamping before rounding equals clamping after it for
 // the bound 127.
