@@ -9,7 +9,7 @@
 //               shared-memory stages of 64 cells: K and V codes by TMA
 //               tensor copies (cp.async.bulk.tensor, 128-byte swizzle,
 //               straight from the paged pool through the block table), the
-//               int8 scales by bulk copies; an mbarrier per stage counts the
+//               scales by bulk copies; an mbarrier per stage counts the
 //               bytes in.  Thread 0 issues the first stages; after that the
 //               warp that releases a stage last (a shared-memory counter)
 //               issues its refill.
@@ -23,14 +23,18 @@
 //               maximum.
 //   p.v         O^T += V^T . P^T, another m16n8k16 per 16 dims; int8 V is
 //               widened to fp16 exactly in registers and the V scales are
-//               folded into P per group.
+//               folded into P per group.  K8V4 (#711 kv: --kv k8v4 streams
+//               with --kv-resident, "What"): K as int8; V's 4-bit codes
+//               widen exactly to code - 8, its per-32 scales fold into P,
+//               and each split's merged partial is rotated back
+//               (Walsh-Hadamard, / HD) before it is written.
 //
 // q and p enter the tensor cores as fp16 hi + lo pairs (about 22 significant
 // bits), K and V as exact fp16 values.
 //
-// Each warp writes its partial state, one (o, m, l) per row, straight from
-// registers; the combine kernel below merges the partials of every warp of
-// every split.  Masked cells (beyond the context, beyond the causal limit of a
+// The CTA's 4 warps merge their states through shared memory into one
+// partial (o, m, l) per row of the split; the combine kernel below merges
+// the partials of every split.  Masked cells (beyond the context, beyond the causal limit of a
 // verify-window row, or in a block whose id is out of range) get logit -inf
 // and contribute exact zeros.  Every mbarrier wait is bounded: a wait that
 // runs out marks the partial as NaN (the combine passes NaN to the output)
