@@ -135,8 +135,14 @@ def _ptr(x):
 
 
 def _stream(stream):
+    """cudaStream_t of a torch stream, an int handle, or (None) torch's
+    current stream on the current device (read without building a Stream
+    object, which costs a few microseconds a call)."""
     if stream is None:
         import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
