@@ -12,8 +12,8 @@ Printed: one JSON line.  `value` = cache bytes the two decodes read per step
 The timed region replays CUDA graphs of the captured steps (the library's C
 entry points, called through the binding while capturing); `e2e` repeats
 the measurement through the same public calls without graphs, with the
-step's inputs copied from pinned host memory and the outputs read back every
-step.  `--impl reference` times the CPU oracle on the same workload.
+step's inputs copied from pinned host memory (one packed copy) and both
+outputs read back (one copy) every step.  `--impl reference` times the CPU oracle on the same workload.
 
 Beside the step (not in `value`): the K8V4 format (int8 K, rotated 4-bit V)
 on the same workload -- decode, one-cell and bulk append, compaction and
@@ -550,37 +550,52 @@ def _ncu_traffic(fmt: str):
 
 
 def _e2e(step_fn, torch, layers, wl, bt, cap, L, n_kv, hd, K, W, world, dist):
-    """Per step: pinned host -> device copies of the new cell and the query,
-    append + decode on both formats through the public calls, device -> host
-    copy of both outputs, synchronize."""
+    """Per step: one pinned host -> device copy of the step's inputs (the new
+    cell's K and V, the query, its position and the context length, packed
+    back to back in one staging buffer), append + decode on both formats
+    through the public calls, one device -> host copy of both outputs,
+    synchronize."""
     n_q = wl.n_q
-    hk = torch.from_numpy(np.stack([st["k"] for st in wl.steps])).pin_memory()
-    hv = torch.from_numpy(np.stack([st["v"] for st in wl.steps])).pin_memory()
-    hq = torch.from_numpy(np.stack([st["q"] for st in wl.steps])).pin_memory()
-    hpos = torch.from_numpy(np.stack([st["tok_pos"] for st in wl.steps])).pin_memory()
-    hctx = torch.from_numpy(np.stack([st["ctx_lens"] for st in wl.steps])).pin_memory()
-    hout = torch.empty((2, 1, 1, n_q, hd), dtype=torch.float32).pin_memory()
-    dk = torch.empty_like(hk[0], device="cuda")
-    dv = torch.empty_like(hv[0], device="cuda")
-    dq = torch.empty_like(hq[0], device="cuda")
-    dpos = torch.empty_like(hpos[0], device="cuda")
-    dctx = torch.empty_like(hctx[0], device="cuda")
+    segs = [("k", np.float32), ("v", np.float32), ("q", np.float32),
+            ("tok_pos", np.int32), ("ctx_lens", np.int32)]
+    offs, words = {}, 0
+    for name, _ in segs:   # each input starts on a 256-byte boundary
+        n = int(np.asarray(wl.steps[0][name]).size)
+        offs[name] = (words, n)
+        words += -(-n // 64) * 64
+    pack = np.zeros((STEPS_PER_LAYER, words), np.float32)
+    for j, st in enumerate(wl.steps[:STEPS_PER_LAYER]):
+        for name, dt in segs:
+            o, n = offs[name]
+            pack[j, o:o + n] = np.ascontiguousarray(st[name], dt).reshape(-1).view(np.float32)
+    hin = torch.from_numpy(pack).pin_memory()
+    din = torch.empty(words, dtype=torch.float32, device="cuda")
+
+    def view(name, dtype, shape):
+        o, n = offs[name]
+        t = din[o:o + n]
+        return (t.view(torch.int32) if dtype is np.int32 else t).view(shape)
+
+    st0 = wl.steps[0]
+    dk = view("k", np.float32, st0["k"].shape)
+    dv = view("v", np.float32, st0["v"].shape)
+    dq = view("q", np.float32, st0["q"].shape)
+    dpos = view("tok_pos", np.int32, st0["tok_pos"].shape)
+    dctx = view("ctx_lens", np.int32, st0["ctx_lens"].shape)
+    dout = torch.empty((2,) + tuple(st0["q"].shape), dtype=torch.float32, device="cuda")
+    hout = torch.empty_like(dout, device="cpu").pin_memory()
     seq0 = torch.zeros(1, dtype=torch.int32, device="cuda")
-    h2d = (hk[0].numel() + hv[0].numel() + hq[0].numel()) * 4 + 2 * 4
+    h2d = words * 4
     d2h = hout.numel() * 4
 
     def one(s):
         j = (s // LAYERS) % STEPS_PER_LAYER
-        dk.copy_(hk[j], non_blocking=True)
-        dv.copy_(hv[j], non_blocking=True)
-        dq.copy_(hq[j], non_blocking=True)
-        dpos.copy_(hpos[j], non_blocking=True)
-        dctx.copy_(hctx[j], non_blocking=True)
+        din.copy_(hin[j], non_blocking=True)
         for i, name in enumerate(("f16", "q8")):
-            pool, ws, out = layers[s % LAYERS][name]
+            pool, ws, _ = layers[s % LAYERS][name]
             pool.append(dk, dv, seq0, dpos, bt)
-            pool.decode(dq, dctx, cap, bt, wl.sm_scale, out=out, workspace=ws)
-            hout[i].copy_(out, non_blocking=True)
+            pool.decode(dq, dctx, cap, bt, wl.sm_scale, out=dout[i], workspace=ws)
+        hout.copy_(dout, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for s in range(W):
