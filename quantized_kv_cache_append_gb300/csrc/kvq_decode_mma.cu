@@ -596,6 +596,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     // limit inside it needs masks
     const bool need_mask = nvalid < kCellsPerWarp || row_last_min - cw0 < kCellsPerWarp - 1;
   // ---------------- masks and online softmax ----------------
+  // A row's maximum over the slice (8 lanes) is needed only when the
+  // reference maximum must rise; that happens only if some lane's own
+  // maximum lies above it by more than kTau, so one warp vote decides
+  // whether the shuffles run at all (the outcome is the same either way).
+  float lmax[NT][2];
+  bool rise = false;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -605,20 +611,36 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         if (g > vis) z[nt][j] = kNegInf;
         if (g + 8 > vis) z[nt][2 + j] = kNegInf;
       }
-      float tmax = fmaxf(z[nt][j], z[nt][2 + j]);
-      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
-      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
-      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-      if (tmax > m[nt][j] + kTau) {  // also true for the first finite maximum
-        const float alpha = m[nt][j] == kNegInf ? 0.f : fast_exp2(m[nt][j] - tmax);
-        m[nt][j] = tmax;
-        l[nt][j] *= alpha;
+      lmax[nt][j] = fmaxf(z[nt][j], z[nt][2 + j]);
+      rise |= lmax[nt][j] > m[nt][j] + kTau;  // also true for the first finite maximum
+    }
+  }
+  if (__any_sync(kFull, rise)) {
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          o[mt][nt][j] *= alpha;
-          o[mt][nt][2 + j] *= alpha;
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float tmax = lmax[nt][j];
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+        if (tmax > m[nt][j] + kTau) {
+          const float alpha = m[nt][j] == kNegInf ? 0.f : fast_exp2(m[nt][j] - tmax);
+          m[nt][j] = tmax;
+          l[nt][j] *= alpha;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            o[mt][nt][j] *= alpha;
+            o[mt][nt][2 + j] *= alpha;
+          }
         }
       }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
       const bool none = m[nt][j] == kNegInf;
       p[nt][j] = none ? 0.f : fast_exp2(z[nt][j] - m[nt][j]);
       p[nt][2 + j] = none ? 0.f : fast_exp2(z[nt][2 + j] - m[nt][j]);
