@@ -600,6 +600,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // reference maximum must rise; that happens only if some lane's own
   // maximum lies above it by more than kTau, so one warp vote decides
   // whether the shuffles run at all (the outcome is the same either way).
+  // p is first computed against the current reference maximum, ahead of
+  // the vote, so its exponentials need not wait for the branch; the rare
+  // tile that raises the maximum computes p again.
+  auto probs = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const bool none = m[nt][j] == kNegInf;
+        p[nt][j] = none ? 0.f : fast_exp2(z[nt][j] - m[nt][j]);
+        p[nt][2 + j] = none ? 0.f : fast_exp2(z[nt][2 + j] - m[nt][j]);
+      }
+  };
   float lmax[NT][2];
   bool rise = false;
 #pragma unroll
@@ -615,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       rise |= lmax[nt][j] > m[nt][j] + kTau;  // also true for the first finite maximum
     }
   }
+  probs();
   if (__any_sync(kFull, rise)) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -636,17 +650,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         }
       }
     }
+    probs();
   }
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const bool none = m[nt][j] == kNegInf;
-      p[nt][j] = none ? 0.f : fast_exp2(z[nt][j] - m[nt][j]);
-      p[nt][2 + j] = none ? 0.f : fast_exp2(z[nt][2 + j] - m[nt][j]);
-      l[nt][j] += p[nt][j] + p[nt][2 + j];
-    }
-  }
+    for (int j = 0; j < 2; ++j) l[nt][j] += p[nt][j] + p[nt][2 + j];
 
   };
 
