@@ -717,6 +717,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       } else {
         sw[ci][0] = *reinterpret_cast<const uint32_t*>(src);
       }
+#pragma unroll
+      for (int i = 0; i < SWD; ++i) sw[ci][i] = clamp_finite_h2(sw[ci][i]);
     }
     // One ldmatrix.trans x4 per two 32-dim blocks, on 16-bit units of 4
     // nibbles: register (cells 2t, 2t + 1; unit g) holds dims 4g .. 4g + 3
@@ -738,10 +740,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       for (int jb = 0; jb < 2; ++jb) {
         const int blk = 2 * kq + jb;
         const int sh = 16 * (blk & 1);
-        const float s0 = fmaxf(fminf(__half2float(__ushort_as_half((unsigned short)(sw[0][blk >> 1] >> sh))),
-                                     65504.f), -65504.f);
-        const float s8 = fmaxf(fminf(__half2float(__ushort_as_half((unsigned short)(sw[1][blk >> 1] >> sh))),
-                                     65504.f), -65504.f);
+        const float s0 = __half2float(__ushort_as_half((unsigned short)(sw[0][blk >> 1] >> sh)));
+        const float s8 = __half2float(__ushort_as_half((unsigned short)(sw[1][blk >> 1] >> sh)));
         uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {

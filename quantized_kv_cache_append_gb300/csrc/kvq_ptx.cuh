@@ -151,6 +151,15 @@ static __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return d;
 }
 
+// Both fp16 halves clamped to [-65504, 65504]: infinities become the largest
+// finite value and NaN becomes 65504 (min/max return the non-NaN operand).
+static __device__ __forceinline__ uint32_t clamp_finite_h2(uint32_t a) {
+  uint32_t d;
+  asm("min.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(0x7bff7bffu));
+  asm("max.f16x2 %0, %0, %1;" : "+r"(d) : "r"(0xfbfffbffu));
+  return d;
+}
+
 static __device__ __forceinline__ float half_lo(uint32_t h) {
   return __half2float(__ushort_as_half((unsigned short)(h & 0xffff)));
 }
