@@ -158,3 +158,15 @@ def test_stream_fetch_refuses_mismatched_or_bad_arguments(lib):
     assert kvq.kvq_stream_fetch(_cache(), win, FAKE, FAKE, -1, 0) == kvq.KVQ_ERR_ARG
     # without a GPU no address is device-addressable: refused before any launch
     assert kvq.kvq_stream_fetch(_cache(), win, FAKE, FAKE, 1, 0) == kvq.KVQ_ERR_ARG
+
+
+def test_missing_library_raises_instead_of_falling_back(tmp_path):
+    # There is no CPU or library fallback: a missing libkvq.so is an error.
+    with pytest.raises(RuntimeError, match="not built"):
+        kvq.load_library(str(tmp_path / "libkvq.so"))
+
+
+def test_failed_status_raises_with_its_name(lib):
+    with pytest.raises(RuntimeError, match="kvq_append"):
+        kvq.check(kvq.KVQ_ERR_ARG, "kvq_append")
+    kvq.check(kvq.KVQ_OK, "kvq_append")   # success passes silently
