@@ -437,30 +437,28 @@ __global__ void __launch_bounds__(W * 32) append_k8v4_kernel(AppendArgs a) {
   // ---- V: rotate, then 4-bit codes and one fp16 scale per 32 rotated dims
   wht_group<VPL, LPR>(xv, lane);
   {
-    // the block's largest |y| (NaN counts as 0) ...
-    uint32_t ab[VPL], amax = 0;
+    // the block's largest |y| (fmaxf drops NaN, so NaN counts as 0) ...
+    float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-      ab[e] = xv[e] == xv[e] ? (__float_as_uint(xv[e]) & 0x7fffffffu) : 0u;
-      amax = max(amax, ab[e]);
-    }
+    for (int e = 0; e < VPL; ++e) amax = fmaxf(amax, fabsf(xv[e]));
 #pragma unroll
-    for (int off = 1; off < LB; off <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    for (int off = 1; off < LB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     // ... and the first dim holding it: the lowest lane of the block with a
-    // match (lanes hold ascending dims), then its lowest element
-    int ef = VPL;
+    // match (lanes hold ascending dims), then its lowest element (the
+    // backward scan keeps the lowest)
+    float mine = 0.f;
+    bool found = false;
 #pragma unroll
     for (int e = VPL - 1; e >= 0; --e)
-      if (ab[e] == amax) ef = e;
-    const unsigned hit = __ballot_sync(0xffffffffu, ef < VPL);
+      if (fabsf(xv[e]) == amax) {
+        mine = xv[e];
+        found = true;
+      }
     const unsigned blk_lanes = ((1u << LB) - 1u) << (lane & ~(LB - 1));
-    const int src = __ffs(hit & blk_lanes) - 1;
-    float mine = 0.f;
-#pragma unroll
-    for (int e = 0; e < VPL; ++e)
-      if (e == ef) mine = xv[e];
+    const unsigned hit = __ballot_sync(0xffffffffu, found) & blk_lanes;
+    const int src = hit ? __ffs(hit) - 1 : lane;  // no match only if amax is 0 (all NaN)
     float m = __shfl_sync(0xffffffffu, mine, src);
-    if (amax == 0) m = 0.0f;  // no nonzero element: m stays +0
+    if (amax == 0.f) m = 0.0f;  // no nonzero element: m stays +0
     const __half dh = __float2half_rn(m * -0.125f);  // = m / -8, both correctly rounded
     const float d = __half2float(dh);
     uint32_t c[VPL / 4];  // 4 codes (16 bits) each; dims 2i low nibble, 2i + 1 high
