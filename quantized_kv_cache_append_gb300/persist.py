@@ -136,18 +136,19 @@ def save_sequence(path, pool, block_table_row, n_cells: int, tokens=None, stream
     write them to `path`."""
     import torch
 
-    from .pool import row_layout
+    from .pool import on_stream, row_layout
 
     dev = pool.k.device
     kdt, kn, vdt, vn, kng, vng = row_layout(pool.fmt, pool.head_dim)
-    ck = torch.empty((n_cells, pool.n_kv, kn), dtype=kdt, device=dev)
-    cv = torch.empty((n_cells, pool.n_kv, vn), dtype=vdt, device=dev)
-    sk = sv = None
-    if kng:
-        sk = torch.empty((n_cells, pool.n_kv, kng), dtype=torch.float16, device=dev)
-        sv = torch.empty((n_cells, pool.n_kv, vng), dtype=torch.float16, device=dev)
-    check(kvq_gather_cells(pool.cache, block_table_row, n_cells, ck, cv, sk, sv, stream),
-          "kvq_gather_cells")
+    with on_stream(stream):
+        ck = torch.empty((n_cells, pool.n_kv, kn), dtype=kdt, device=dev)
+        cv = torch.empty((n_cells, pool.n_kv, vn), dtype=vdt, device=dev)
+        sk = sv = None
+        if kng:
+            sk = torch.empty((n_cells, pool.n_kv, kng), dtype=torch.float16, device=dev)
+            sv = torch.empty((n_cells, pool.n_kv, vng), dtype=torch.float16, device=dev)
+        check(kvq_gather_cells(pool.cache, block_table_row, n_cells, ck, cv, sk, sv, stream),
+              "kvq_gather_cells")
     torch.cuda.synchronize(dev)  # the gather may run on a stream of the caller's
     host = lambda t: None if t is None else t.cpu().numpy()
     bits = lambda a: None if a is None else (a.view(np.uint16) if a.dtype == np.float16 else a)
@@ -160,14 +161,17 @@ def load_sequence(path, pool, block_table_row, stream=None):
     given block-table row; returns (n_cells, tokens)."""
     import torch
 
+    from .pool import on_stream
+
     tokens, ck, cv, sk, sv = read_cells(path, pool.fmt, pool.n_kv, pool.head_dim)
     dev = pool.k.device
     to_dev = lambda a, dt: None if a is None else torch.from_numpy(a.view(dt)).to(dev)
     cdt = np.float16 if pool.fmt == KVQ_F16 else np.int8
-    dk, dv = to_dev(ck, cdt), to_dev(cv, cdt if pool.fmt != KVQ_K8V4 else np.uint8)
-    dsk, dsv = to_dev(sk, np.float16), to_dev(sv, np.float16)
     n_cells = ck.shape[0]
-    check(kvq_scatter_cells(pool.cache, block_table_row, n_cells, dk, dv, dsk, dsv, stream),
-          "kvq_scatter_cells")
+    with on_stream(stream):   # the staging copies run on the scatter's stream, ahead of it
+        dk, dv = to_dev(ck, cdt), to_dev(cv, cdt if pool.fmt != KVQ_K8V4 else np.uint8)
+        dsk, dsv = to_dev(sk, np.float16), to_dev(sv, np.float16)
+        check(kvq_scatter_cells(pool.cache, block_table_row, n_cells, dk, dv, dsk, dsv, stream),
+              "kvq_scatter_cells")
     torch.cuda.synchronize(dev)  # the staging tensors live until the scatter has run
     return n_cells, tokens

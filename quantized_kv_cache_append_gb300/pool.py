@@ -6,10 +6,24 @@ argument marshalling over the entry points of the same names.
 """
 from __future__ import annotations
 
+import contextlib
+
 import torch
 
 from . import (KVQ_F16, KVQ_GROUP, KVQ_K8V4, KVQ_Q4_BLOCK, KVQ_Q8, check, kvq_append,
                kvq_compact_f16, kvq_decode_attn, kvq_decode_workspace_bytes, make_cache)
+
+
+def on_stream(stream):
+    """Context under which tensors allocated for a call belong to the stream
+    the call runs on (torch's allocator then never hands their memory to
+    other work before that stream reaches it).  None: torch's current
+    stream, which allocations use already."""
+    if stream is None:
+        return contextlib.nullcontext()
+    if isinstance(stream, int):
+        stream = torch.cuda.ExternalStream(stream)
+    return torch.cuda.stream(stream)
 
 
 def row_layout(fmt: int, head_dim: int):
@@ -64,22 +78,24 @@ class PagedPool:
     def decode(self, q, ctx_lens, max_ctx: int, block_table, sm_scale: float, out=None,
                workspace=None, stream=None):
         n_seq, W, n_q, hd = q.shape
-        if out is None:
-            out = torch.empty_like(q)
-        if workspace is None:   # needs no initial contents; a given one is checked by the call
-            need = self.workspace_bytes(n_seq, W, n_q, max_ctx)
-            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-        check(kvq_decode_attn(self.cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
-                              int(block_table.shape[1]), sm_scale, out, workspace,
-                              workspace.numel(), stream), "kvq_decode_attn")
+        with on_stream(stream):
+            if out is None:
+                out = torch.empty_like(q)
+            if workspace is None:   # needs no initial contents; a given one is checked by the call
+                need = self.workspace_bytes(n_seq, W, n_q, max_ctx)
+                workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+            check(kvq_decode_attn(self.cache, q, n_seq, W, n_q, ctx_lens, max_ctx, block_table,
+                                  int(block_table.shape[1]), sm_scale, out, workspace,
+                                  workspace.numel(), stream), "kvq_decode_attn")
         return out
 
     def compact(self, block_table_row, n_cells: int, out_k=None, out_v=None, stream=None):
         shape = (self.n_kv, n_cells, self.head_dim)
-        if out_k is None:
-            out_k = torch.empty(shape, dtype=torch.float16, device=self.k.device)
-        if out_v is None:
-            out_v = torch.empty(shape, dtype=torch.float16, device=self.k.device)
-        check(kvq_compact_f16(self.cache, block_table_row, n_cells, out_k, out_v, stream),
-              "kvq_compact_f16")
+        with on_stream(stream):
+            if out_k is None:
+                out_k = torch.empty(shape, dtype=torch.float16, device=self.k.device)
+            if out_v is None:
+                out_v = torch.empty(shape, dtype=torch.float16, device=self.k.device)
+            check(kvq_compact_f16(self.cache, block_table_row, n_cells, out_k, out_v, stream),
+                  "kvq_compact_f16")
         return out_k, out_v

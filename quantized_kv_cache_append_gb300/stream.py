@@ -14,7 +14,7 @@ import numpy as np
 import torch
 
 from . import check, kvq_stream_fetch, kvq_stream_plan
-from .pool import PagedPool
+from .pool import PagedPool, on_stream
 
 
 class StreamedPool:
@@ -58,8 +58,9 @@ class StreamedPool:
         """Copy the planned blocks from the host copy into their slots."""
         if len(src) == 0:
             return
-        d_src = torch.from_numpy(np.ascontiguousarray(src, np.int32)).to(self.device)
-        d_dst = torch.from_numpy(np.ascontiguousarray(dst, np.int32)).to(self.device)
-        check(kvq_stream_fetch(self.host.cache, self.window.cache, d_src, d_dst, len(src), stream),
-              "kvq_stream_fetch")
+        with on_stream(stream):   # the id copies run on the fetch's own stream, ahead of it
+            d_src = torch.from_numpy(np.ascontiguousarray(src, np.int32)).to(self.device)
+            d_dst = torch.from_numpy(np.ascontiguousarray(dst, np.int32)).to(self.device)
+            check(kvq_stream_fetch(self.host.cache, self.window.cache, d_src, d_dst, len(src),
+                                   stream), "kvq_stream_fetch")
         self._keep = (d_src, d_dst)   # alive until the next fetch is queued behind this one
