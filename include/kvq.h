@@ -37,7 +37,10 @@
  *
  * Conventions for every call
  *   - All device arrays are owned and allocated by the caller; the library
- *     allocates nothing and keeps no state between calls.  Pointers marked
+ *     allocates nothing and keeps no state between calls beyond one-time
+ *     kernel setup (each kernel configuration's shared-memory limit and
+ *     occupancy, taken on the first device it runs on: use one device per
+ *     process) and kvq_decode_attn_static's scratch.  Pointers marked
  *     "device" must be device (or managed) memory of the current device.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  No call reads device memory on the host or
