@@ -47,6 +47,13 @@ WORKLOAD_DESC = ("gqa32k: batch 1, n_q 32, n_kv 8, head_dim 128, 32768-cell cont
                  "each step = append + decode on an FP16 cache and on an int8 cache")
 
 
+def _config(world: int) -> dict:
+    """The workload description both arms print (same keys, same values)."""
+    return {"workload": WORKLOAD_DESC, "layers": LAYERS,
+            "l2": "inputs larger than L2: 8 layer caches rotated, 1.6 GB",
+            "graph": "CUDA graphs of 512 captured steps", "parallelism": f"replicas x{world}"}
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -376,6 +383,7 @@ def run_kvq(args):
     stream = _stream_bench(torch, kvq, layers, n_kv, hd, bs, wl.n_blocks)
 
     peak, peak_kind = _peaks()
+    by_workload = _decode_workloads(torch, kvq, peak)
     avg_bytes = {n: sum(v) / len(v) for n, v in bytes_per_step.items()}
     gbs = {n: avg_bytes[n] / (kernel_ms[n] * 1e-3) / 1e9 for n in kernel_ms}
     dominant = max(("f16", "q8"), key=kernel_ms.get)   # of the step's two formats
@@ -392,10 +400,7 @@ def run_kvq(args):
             "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "storage": ["f16", "int8+fp16 scale/64"], "data": "synthetic (seeded N(0,1))",
-            "config": {"workload": WORKLOAD_DESC, "layers": LAYERS,
-                       "l2": "inputs larger than L2: 8 layer caches rotated, 1.6 GB",
-                       "graph": "CUDA graphs of 512 captured steps", "parallelism":
-                       f"replicas x{world}"},
+            "config": _config(world),
             "gpu_launches": 6 * K,
             "roofline": {"kernel": f"decode partial+combine ({dominant})", "bound": "hbm",
                          "achieved": round(gbs[dominant], 1), "peak": peak,
@@ -403,10 +408,11 @@ def run_kvq(args):
                          "frac": round(gbs[dominant] / peak, 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": int(avg_bytes[dominant]),
                          "launch_us": round(kernel_ms[dominant] * 1e3, 3)},
-            "decode": {n: {"us": round(kernel_ms[n] * 1e3, 3), "GB/s": round(gbs[n], 1),
-                           "frac_of_measured_hbm": round(gbs[n] / peak, 4),
-                           "frac_of_nominal_8TBs": round(gbs[n] / 8000.0, 4)}
-                       for n in kernel_ms},
+            "decode": {**{n: {"us": round(kernel_ms[n] * 1e3, 3), "GB/s": round(gbs[n], 1),
+                              "frac_of_measured_hbm": round(gbs[n] / peak, 4),
+                              "frac_of_nominal_8TBs": round(gbs[n] / 8000.0, 4)}
+                          for n in kernel_ms},
+                       **by_workload},
             "append": {"bulk_Mcells_per_s": {n: round(v, 1) for n, v in append_mcells.items()},
                        "one_cell_step_us": round(append_step_us, 3),
                        "one_cell_step_us_k8v4": round(append_step_us_k8v4, 3)},
@@ -431,6 +437,69 @@ def run_kvq(args):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def _decode_workloads(torch, kvq, peak):
+    """Decode time of every other workload and cache format, timed like the
+    step's decodes: a CUDA graph of decode calls over layer caches rotated
+    past L2 (at least 4x its size), the partial and combine kernels of each
+    call, bytes = the cache rows read (cells x KV heads x row bytes)."""
+    import workloads
+    from quantized_kv_cache_append_gb300.pool import PagedPool
+
+    fmts = {"f16": kvq.KVQ_F16, "q8": kvq.KVQ_Q8, "k8v4": kvq.KVQ_K8V4}
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    res = {}
+    for name in ("tiny", "ragged", "long256k", "chunk_verify"):
+        wl = workloads.make(name)
+        ctx = wl.chunk["ctx_lens"] if wl.chunk is not None else wl.ctx_lens
+        bt, q, dctx = dev(wl.block_table), dev(wl.q), dev(ctx)
+        k, v, seq, pos = dev(wl.k), dev(wl.v), dev(wl.tok_seq), dev(wl.tok_pos)
+        res[name] = {}
+        for fn in list(wl.formats) + ["k8v4"]:
+            nbytes = int(ctx.sum()) * wl.n_kv * _row_bytes(fn, wl.head_dim)
+            nl = max(2, min(8, -(-4 * 129_000_000 // nbytes)))
+            pools = []
+            for _ in range(nl):
+                p = PagedPool(fmts[fn], wl.n_kv, wl.head_dim, wl.block_size, wl.n_blocks)
+                p.append(k, v, seq, pos, bt)
+                if wl.chunk is not None:
+                    c = wl.chunk
+                    p.append(dev(c["k"]), dev(c["v"]), dev(c["tok_seq"]), dev(c["tok_pos"]), bt)
+                ws = torch.empty(max(256, p.workspace_bytes(wl.n_seq, wl.W, wl.n_q, int(ctx.max()))),
+                                 dtype=torch.uint8, device="cuda")
+                pools.append((p, ws, torch.empty_like(q)))
+
+            def one(i):
+                p, ws, out = pools[i % nl]
+                p.decode(q, dctx, int(ctx.max()), bt, wl.sm_scale, out=out, workspace=ws)
+
+            for i in range(2 * nl):
+                one(i)
+            torch.cuda.synchronize()
+            n = 8 * nl
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    one(i)
+            g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) / n * 1e3)
+            us = statistics.median(ts)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            res[name][fn] = {"us": round(us, 3), "GB/s": round(gbs, 1),
+                             "frac_of_measured_hbm": round(gbs / peak, 4),
+                             "bytes": nbytes, "layers": nl}
+            del pools, g
+            torch.cuda.empty_cache()
+    return res
 
 
 def _stream_bench(torch, kvq, layers, n_kv, hd, bs, n_blocks):
@@ -619,9 +688,12 @@ def _e2e(step_fn, torch, layers, wl, bt, cap, L, n_kv, hd, K, W, world, dist):
 # the reference arm: the CPU oracle on the same workload
 # --------------------------------------------------------------------------
 
-def _oracle_steps(n_steps: int, budget_s: float = None):
+def _oracle_steps(n_steps: int, budget_s: float = None, lib_path: str = None):
     """Prefill both oracle caches, then run oracle steps (append one cell +
-    float64 decode, FP16 and int8).  Returns (bytes, seconds, steps)."""
+    float64 decode, FP16 and int8).  Returns (bytes, seconds, steps).
+    lib_path: another build of the oracle (its OpenMP build) to time."""
+    import contextlib
+
     import oracle
     import workloads
 
@@ -632,29 +704,62 @@ def _oracle_steps(n_steps: int, budget_s: float = None):
         img = oracle.PoolImage(fmt, n_kv, hd, wl.block_size, wl.n_blocks)
         oracle.append(img, wl.k, wl.v, wl.tok_seq, wl.tok_pos, wl.block_table)
         imgs[name] = img
-    t0 = time.perf_counter()
-    total = 0
-    done = 0
-    for s in range(n_steps):
-        j = s % STEPS_PER_LAYER
-        st = wl.steps[j]
-        for name in ("f16", "q8"):
-            oracle.append(imgs[name], st["k"], st["v"], st["tok_seq"], st["tok_pos"],
-                          wl.block_table)
-            oracle.attention(imgs[name], st["q"], st["ctx_lens"], wl.block_table, wl.sm_scale)
-        total += int(st["ctx_lens"][0]) * n_kv * (_row_bytes(False, hd) + _row_bytes(True, hd))
-        done += 1
-        if budget_s is not None and time.perf_counter() - t0 > budget_s:
-            break
-    return total, time.perf_counter() - t0, done
+    ctx = oracle.use_library(lib_path) if lib_path else contextlib.nullcontext()
+    with ctx:
+        t0 = time.perf_counter()
+        total = 0
+        done = 0
+        for s in range(n_steps):
+            j = s % STEPS_PER_LAYER
+            st = wl.steps[j]
+            for name in ("f16", "q8"):
+                oracle.append(imgs[name], st["k"], st["v"], st["tok_seq"], st["tok_pos"],
+                              wl.block_table)
+                oracle.attention(imgs[name], st["q"], st["ctx_lens"], wl.block_table,
+                                 wl.sm_scale)
+            total += int(st["ctx_lens"][0]) * n_kv * (_row_bytes(False, hd) + _row_bytes(True, hd))
+            done += 1
+            if budget_s is not None and time.perf_counter() - t0 > budget_s:
+                break
+        return total, time.perf_counter() - t0, done
 
 
-def cpu_baseline(budget_s: float = 12.0):
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _parallel_oracle():
+    """(path, threads) of the oracle's OpenMP build on every host core, or
+    (None, 1) when it cannot be built."""
+    import oracle
+
+    cores = _host_cores()
+    path = oracle.parallel_library(cores)
+    return (path, cores) if path is not None else (None, 1)
+
+
+def cpu_baseline(budget_s: float = 10.0):
+    """The oracle on the host cores: single-threaded, and its OpenMP build
+    over the (sequence, token, head) rows on every core.  The line's value is
+    the multi-core leg (the single-threaded one when OpenMP is missing)."""
+    legs = []
     total, dt, done = _oracle_steps(10_000, budget_s)
-    return {"value": round(total / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{done} steps of the same workload (append 1 cell + float64 decode over "
-                      f"32769+ cells, FP16 and int8), single-threaded C oracle"}
+    legs.append({"value": round(total / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                 "steps": done})
+    path, cores = _parallel_oracle()
+    if path is not None:
+        total, dt, done = _oracle_steps(10_000, budget_s, lib_path=path)
+        legs.append({"value": round(total / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+                     "steps": done})
+    top = legs[-1]
+    return {"value": top["value"], "unit": "GB/s", "cores": top["cores"], "kind": "oracle",
+            "sample": f"{top['steps']} steps of the same workload (append 1 cell + float64 "
+                      f"decode over 32769+ cells, FP16 and int8), C oracle on "
+                      f"{top['cores']} host core(s)",
+            "legs": legs}
 
 
 def run_reference(args):
@@ -663,16 +768,17 @@ def run_reference(args):
         return None
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; its prefill is untimed
-    total, dt, done = _oracle_steps(args.steps)
+    path, cores = _parallel_oracle()
+    total, dt, done = _oracle_steps(args.steps, lib_path=path)
     value = total / dt / 1e9
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": done, "warmup": args.warmup,
             "ms_per_step": dt / done * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
-            "config": {"workload": WORKLOAD_DESC},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+            "config": _config(world),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                              "kind": "oracle",
-                             "sample": f"{done} steps, single-threaded C oracle"},
+                             "sample": f"{done} steps, C oracle on {cores} host core(s)"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

@@ -39,9 +39,10 @@
  *   - All device arrays are owned and allocated by the caller; the library
  *     allocates nothing and keeps no state between calls beyond one-time
  *     kernel setup (each kernel configuration's shared-memory limit and
- *     occupancy, taken on the first device it runs on: use one device per
- *     process) and kvq_decode_attn_static's scratch.  Pointers marked
- *     "device" must be device (or managed) memory of the current device.
+ *     occupancy, kept per device and redone when that device's context
+ *     changes, so one process may drive several devices) and
+ *     kvq_decode_attn_static's scratch.  Pointers marked "device" must be
+ *     device (or managed) memory of the current device.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  No call reads device memory on the host or
  *     synchronizes.
@@ -413,8 +414,10 @@ kvq_status kvq_stream_fetch(const kvq_cache *host_copy, const kvq_cache *window,
  * library; when the split plan kvq_decode_workspace_bytes describes needs
  * more, the context is cut into fewer splits until it fits, and a request
  * that does not fit even with one split per (sequence, KV head) returns
- * KVQ_ERR_WORKSPACE and launches nothing.  The first call on a device looks up the array's
- * address and caches it: make that first call before any stream capture.
+ * KVQ_ERR_WORKSPACE and launches nothing.  The first call on a device
+ * looks up the array's address and caches it for that device's context
+ * (looked up again after the context changes, e.g. after cudaDeviceReset):
+ * make that first call before any stream capture.
  * Every call uses the same array, so calls whose kernels may overlap on
  * the GPU (unordered streams) race on it; order them.  The array needs no
  * clearing between calls.

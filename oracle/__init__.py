@@ -47,6 +47,39 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+_OMP_LIB_PATH = os.path.join(_BUILD_DIR, "libkvq_oracle_omp.so")
+
+
+def build_parallel(force: bool = False):
+    """The same source compiled with -fopenmp: kvo_attention then runs its
+    independent (sequence, token, head) rows on OpenMP threads, each row with
+    the same arithmetic as the single-threaded build.  Returns the library's
+    path, or None when the compiler has no OpenMP support."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    newest_src = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if (not force and os.path.exists(_OMP_LIB_PATH)
+            and os.path.getmtime(_OMP_LIB_PATH) >= newest_src):
+        return _OMP_LIB_PATH
+    tmp = _OMP_LIB_PATH + f".tmp{os.getpid()}"
+    r = subprocess.run(["gcc", *CFLAGS, "-fopenmp", "-o", tmp, _SRC, "-lm"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        return None
+    os.replace(tmp, _OMP_LIB_PATH)
+    return _OMP_LIB_PATH
+
+
+def parallel_library(threads: int):
+    """Path of the OpenMP build, set to use `threads` threads (None if it
+    cannot be built).  Route attention() to it with use_library(path)."""
+    path = build_parallel()
+    if path is None:
+        return None
+    lib = _bind(ctypes.CDLL(path))
+    lib.kvo_set_threads(int(threads))
+    return path
+
+
 def _bind(lib):
     P = ctypes.c_void_p
     I = ctypes.c_int
@@ -75,6 +108,10 @@ def _bind(lib):
     lib.kvo_gather_cells.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, P, P, P]
     lib.kvo_scatter_cells.restype = I
     lib.kvo_scatter_cells.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, P, P, P]
+    lib.kvo_threads.restype = I
+    lib.kvo_threads.argtypes = []
+    lib.kvo_set_threads.restype = None
+    lib.kvo_set_threads.argtypes = [I]
     lib.kvo_chunk_attention.restype = I
     lib.kvo_chunk_attention.argtypes = [I, I, I, P, P, P, I, I, ctypes.c_float, P]
     return lib

@@ -1,8 +1,10 @@
 /*
  * kvq_oracle.c -- plain CPU oracle for the quantized K/V cache path.
  *
- * TEST INFRASTRUCTURE ONLY (see kvq_oracle.h).  Scalar, single-threaded,
- * no blocking, no reordering beyond the definitions it restates.
+ * TEST INFRASTRUCTURE ONLY (see kvq_oracle.h).  Scalar, no blocking, no
+ * reordering beyond the definitions it restates.  Single-threaded, except
+ * that a second build with -fopenmp runs the independent rows of the
+ * decode attention on several threads (same arithmetic per row).
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -fno-fast-math
  *        (no FMA contraction, IEEE float division and rint in the default
@@ -13,6 +15,10 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ------------------------------------------------------------------------ */
 /* IEEE-754 binary16 (fp16) from its definition.                             */
@@ -355,6 +361,61 @@ static void unrotate_f64(double *o, int hd)
 /* w sees cells [0, L - W + w].                                              */
 /* ------------------------------------------------------------------------ */
 
+/* One output row: sequence b, query token w, query head h.  z and rows are
+ * scratch of at least L_b entries.  Returns 0, or -3 for a cell whose block
+ * id is out of range. */
+static int attend_row(int fmt, int n_kv, int hd, int block_size, int n_blocks,
+                      const void *k_data, const void *v_data,
+                      const uint16_t *k_scales, const uint16_t *v_scales,
+                      const float *q, int W, int n_q, int G,
+                      const int32_t *ctx_lens, const int32_t *block_table,
+                      int max_blocks_per_seq, float sm_scale, int b, int w, int h,
+                      double *out, double *z, int64_t *rows)
+{
+    const int L = ctx_lens[b];
+    const int last = L - W + w; /* last visible cell */
+    double *o = out + (((size_t)b * W + w) * n_q + h) * hd;
+    const float *qv = q + (((size_t)b * W + w) * n_q + h) * hd;
+    for (int d = 0; d < hd; ++d)
+        o[d] = 0.0;
+    if (last < 0)
+        return 0;
+    const int kvh = h / G;
+    const int n_vis = last + 1;
+
+    double zmax = -INFINITY;
+    for (int c = 0; c < n_vis; ++c) {
+        const int64_t row = cell_row(block_table, max_blocks_per_seq, n_blocks,
+                                     n_kv, block_size, b, c, kvh);
+        if (row < 0)
+            return -3;
+        rows[c] = row;
+        double dot = 0.0;
+        for (int d = 0; d < hd; ++d)
+            dot += (double)qv[d] * dequant(fmt, hd, k_data, k_scales, row, d);
+        z[c] = (double)sm_scale * dot;
+        if (z[c] > zmax)
+            zmax = z[c];
+    }
+
+    double den = 0.0;
+    for (int c = 0; c < n_vis; ++c) {
+        const double e = exp(z[c] - zmax);
+        den += e;
+        for (int d = 0; d < hd; ++d)
+            o[d] += e * dequant_v(fmt, hd, v_data, v_scales, rows[c], d);
+    }
+    for (int d = 0; d < hd; ++d)
+        o[d] /= den;
+    if (fmt == KVO_FMT_K8V4)
+        unrotate_f64(o, hd);
+    return 0;
+}
+
+/* The rows are independent: a build with -fopenmp (the multi-core CPU
+ * baseline) spreads them over threads; without it the pragmas are ignored
+ * and the rows run in order on one thread.  Each row's arithmetic is the
+ * same either way. */
 int kvo_attention(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                   const void *k_data, const void *v_data,
                   const uint16_t *k_scales, const uint16_t *v_scales,
@@ -375,65 +436,55 @@ int kvo_attention(int fmt, int n_kv, int hd, int block_size, int n_blocks,
     for (int b = 0; b < n_seq; ++b)
         if (ctx_lens[b] > max_len)
             max_len = ctx_lens[b];
-    double *z = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
-    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_len > 0 ? max_len : 1));
-    if (z == NULL || rows == NULL) {
-        free(z);
-        free(rows);
-        return -5;
-    }
+    const long long n_rows = (long long)n_seq * W * n_q;
 
     int rc = 0;
-    for (int b = 0; b < n_seq && rc == 0; ++b) {
-        const int L = ctx_lens[b];
-        for (int w = 0; w < W && rc == 0; ++w) {
-            const int last = L - W + w; /* last visible cell */
-            for (int h = 0; h < n_q; ++h) {
-                double *o = out + (((size_t)b * W + w) * n_q + h) * hd;
-                const float *qv = q + (((size_t)b * W + w) * n_q + h) * hd;
-                for (int d = 0; d < hd; ++d)
-                    o[d] = 0.0;
-                if (last < 0)
-                    continue;
-                const int kvh = h / G;
-                const int n_vis = last + 1;
-
-                double zmax = -INFINITY;
-                for (int c = 0; c < n_vis; ++c) {
-                    const int64_t row = cell_row(block_table, max_blocks_per_seq, n_blocks,
-                                                 n_kv, block_size, b, c, kvh);
-                    if (row < 0) {
-                        rc = -3;
-                        break;
-                    }
-                    rows[c] = row;
-                    double dot = 0.0;
-                    for (int d = 0; d < hd; ++d)
-                        dot += (double)qv[d] * dequant(fmt, hd, k_data, k_scales, row, d);
-                    z[c] = (double)sm_scale * dot;
-                    if (z[c] > zmax)
-                        zmax = z[c];
-                }
-                if (rc != 0)
-                    break;
-
-                double den = 0.0;
-                for (int c = 0; c < n_vis; ++c) {
-                    const double e = exp(z[c] - zmax);
-                    den += e;
-                    for (int d = 0; d < hd; ++d)
-                        o[d] += e * dequant_v(fmt, hd, v_data, v_scales, rows[c], d);
-                }
-                for (int d = 0; d < hd; ++d)
-                    o[d] /= den;
-                if (fmt == KVO_FMT_K8V4)
-                    unrotate_f64(o, hd);
-            }
+#pragma omp parallel
+    {
+        double *z = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_len > 0 ? max_len : 1));
+        int my_rc = (z == NULL || rows == NULL) ? -5 : 0;
+#pragma omp for schedule(dynamic)
+        for (long long i = 0; i < n_rows; ++i) {
+            if (my_rc != 0)
+                continue;
+            const int h = (int)(i % n_q);
+            const int w = (int)((i / n_q) % W);
+            const int b = (int)(i / ((long long)n_q * W));
+            my_rc = attend_row(fmt, n_kv, hd, block_size, n_blocks, k_data, v_data, k_scales,
+                               v_scales, q, W, n_q, G, ctx_lens, block_table,
+                               max_blocks_per_seq, sm_scale, b, w, h, out, z, rows);
         }
+#pragma omp critical
+        {
+            if (my_rc != 0 && rc == 0)
+                rc = my_rc;
+        }
+        free(z);
+        free(rows);
     }
-    free(z);
-    free(rows);
     return rc;
+}
+
+/* Threads the attention rows may use (1 unless built with -fopenmp). */
+int kvo_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Ask for n threads (no effect unless built with -fopenmp). */
+void kvo_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
 }
 
 /* ------------------------------------------------------------------------ */

@@ -85,6 +85,11 @@ int kvo_attention(int fmt, int n_kv, int hd, int block_size, int n_blocks,
                   const int32_t *ctx_lens, const int32_t *block_table,
                   int max_blocks_per_seq, float sm_scale, double *out);
 
+/* Threads kvo_attention spreads its rows over: 1, or the OpenMP thread
+ * count of a build made with -fopenmp (the multi-core CPU baseline). */
+int kvo_threads(void);
+void kvo_set_threads(int n);
+
 /* Copy cells [0, n_cells) of one sequence out to contiguous fp16
  * out_k/out_v [n_kv][n_cells][hd] (fp16 bits). */
 int kvo_compact_f16(int fmt, int n_kv, int hd, int block_size, int n_blocks,

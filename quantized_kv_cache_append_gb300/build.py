@@ -40,6 +40,7 @@ def _sources():
 def _stamp(extra_flags) -> str:
     h = hashlib.sha256()
     for f in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
+            sorted(glob.glob(os.path.join(CSRC, "*.h"))) + \
             [os.path.join(INCLUDE, "kvq.h")]:
         h.update(f.encode())
         with open(f, "rb") as fh:

@@ -446,37 +446,31 @@ KVQ_API const char* kvq_status_string(int status) {
 // entry point keeps its scratch in one file-scope device array of
 // KVQ_STATIC_SCRATCH_BYTES, which exists on every device that loads the
 // library for as long as the process lives.  The first call on a device
-// looks the array's device address up (cudaGetSymbolAddress) and caches
-// it; make that first call before any stream capture.  All calls share the
-// array: two calls whose kernels overlap on the GPU (different streams,
-// no ordering between them) race on it.  Nothing in the array has to start
-// at zero: the partial kernel writes every slot the combine kernel reads.
+// (and the first after that device's context changes, e.g. after
+// cudaDeviceReset) looks the array's device address up
+// (cudaGetSymbolAddress) and caches it for that context; make that first
+// call before any stream capture.  All calls share the array: two calls
+// whose kernels overlap on the GPU (different streams, no ordering between
+// them) race on it; the lock below covers only the address lookup.  Nothing
+// in the array has to start at zero: the partial kernel writes every slot
+// the combine kernel reads.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace kvq {
 namespace {
 
 static __device__ __align__(256) unsigned char g_decode_scratch[KVQ_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
+ContextCache<void*> g_scratch_addr;
 
-// Device address of g_decode_scratch on the current device (set up once).
+// Device address of g_decode_scratch in the current context.
 kvq_status static_scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  const bool ok = per_context(g_scratch_addr, out, [](void** v) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
-      return KVQ_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
-  return KVQ_OK;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return false;
+    *v = p;
+    return true;
+  });
+  return ok ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 }  // namespace

@@ -341,12 +341,15 @@ bool make_span_map(CUtensorMap* map, const void* base, int sp, long long rows, i
 template <int HD>
 cudaError_t launch_hd(const ChunkArgs& a, cudaStream_t s) {
   using C = ChunkCfg<HD>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(chunk_attn<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  // the dynamic shared-memory limit, raised once per context
+  static ContextCache<int> limit_set;
+  int done = 0;
+  if (!per_context(limit_set, &done, [](int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(chunk_attn<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SMEM) == cudaSuccess;
+      }))
+    return cudaErrorInvalidConfiguration;
   ChunkMaps maps;
   memset(&maps, 0, sizeof(maps));
   const long long rows = (long long)a.n_kv * a.P;

@@ -1207,24 +1207,25 @@ const void* kernel_ptr() {
   return reinterpret_cast<const void*>(&decode_mma<FMT, HD, NT>);
 }
 
+// Resident CTAs per SM of one configuration (0 if it cannot run), after
+// raising its dynamic shared-memory limit; done once per context.
 template <int FMT, int HD, int NT>
 int ctas_per_sm_impl() {
-  static int occ = -1;
-  static std::once_flag once;
-  std::call_once(once, [] {
+  static ContextCache<int> cache;
+  int occ = 0;
+  const bool ok = per_context(cache, &occ, [](int* v) {
     using C = Cfg<FMT, HD, NT>;
     if (cudaFuncSetAttribute(decode_mma<FMT, HD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess) {
-      occ = 0;
-      return;
-    }
+                             C::SMEM) != cudaSuccess)
+      return false;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma<FMT, HD, NT>, kThreads,
                                                       C::SMEM) != cudaSuccess)
-      n = 0;
-    occ = n;
+      return false;
+    *v = n;
+    return true;
   });
-  return occ;
+  return ok ? occ : 0;
 }
 
 template <int FMT, int HD, int NT>
@@ -1292,6 +1293,34 @@ void* tensor_map_encoder() {
       fn = f;
   });
   return fn;
+}
+
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+    (void)cudaGetLastError();
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
 }
 
 bool mma_decode_supported(int fmt, int hd, int rows) {

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "kvq.h"
+#include "kvq_context_cache.h"
 
 namespace kvq {
 
@@ -189,6 +190,33 @@ cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, cons
 // The driver's cuTensorMapEncodeTiled (version 12000), looked up once; null
 // if the driver does not provide it.
 void* tensor_map_encoder();
+
+// Identity of the CUDA context current on the calling thread (cuCtxGetId),
+// 0 if none is current or the driver cannot say.  Kernel attributes, module
+// symbols and occupancy belong to a context: a process that drives several
+// devices, or that resets one (cudaDeviceReset makes a new context), needs
+// its one-time kernel setup redone for the new context.
+unsigned long long current_context_id();
+
+// One-time setup of a ContextCache (kvq_context_cache.h) for the current
+// device and context: `setup(T*) -> bool` runs when the device's slot was
+// filled under another context (or never); a failed setup leaves no sticky
+// runtime status behind.
+template <class T, class F>
+bool per_context(ContextCache<T>& cache, T* out, F setup) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return cache.get(dev, current_context_id(), out,
+                   [&](T* v) {
+                     if (setup(v)) return true;
+                     (void)cudaGetLastError();
+                     return false;
+                   },
+                   [] { return current_context_id(); });
+}
 
 // Block streaming (kvq_stream.cu): the residency plan (host only) and the
 // fetch of blocks from the host copy into window slots.

@@ -215,3 +215,21 @@ def test_compaction(fmt):
     if fmt == F16:   # a pure copy of the stored bits
         assert np.array_equal(ok.view(np.float16).astype(np.float32),
                               k.transpose(1, 0, 2).astype(np.float16).astype(np.float32))
+
+
+def test_parallel_build_is_bitwise_the_single_threaded_oracle():
+    """The OpenMP build (the multi-core CPU baseline) runs the same rows with
+    the same arithmetic, so its output equals the plain build's bit for bit."""
+    path = oracle.parallel_library(4)
+    if path is None:
+        pytest.skip("gcc without OpenMP")
+    lens, n_kv, hd, bs, G, W = [301, 77, 512], 2, 128, 32, 4, 3
+    for fmt in (F16, Q8):
+        k, v, table, nb, pool = _random_case(fmt, lens, n_kv, hd, bs, 7)
+        q = np.random.default_rng(8).standard_normal((len(lens), W, n_kv * G, hd)).astype(np.float32)
+        ctx = np.array(lens, np.int32)
+        ref = oracle.attention(pool, q, ctx, table, 0.0883883)
+        with oracle.use_library(path) as u:
+            assert u._lib.kvo_threads() == 4
+            par = oracle.attention(pool, q, ctx, table, 0.0883883)
+        assert np.array_equal(ref.view(np.uint64), par.view(np.uint64))

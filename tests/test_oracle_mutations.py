@@ -73,7 +73,7 @@ MUTATIONS = {
     "q4_scale_per_64_dims": ("+ d / KVO_Q4_BLOCK];", "+ d / KVO_GROUP];"),
     "hadamard_difference_reversed": ("x[j + h] = a - b;", "x[j + h] = b - a;"),
     "hadamard_skips_last_stage": ("for (int h = 1; h < n; h *= 2)", "for (int h = 1; h < n / 2; h *= 2)"),
-    "attention_no_unrotate": ("if (fmt == KVO_FMT_K8V4)\n                    unrotate_f64(o, hd);", ""),
+    "attention_no_unrotate": ("if (fmt == KVO_FMT_K8V4)\n        unrotate_f64(o, hd);\n    return 0;", "return 0;"),
     "unrotate_not_divided": ("o[d] /= (double)hd;", "o[d] /= 1.0;"),
     "unrotate_difference_reversed": ("o[j + h] = a - b;", "o[j + h] = b - a;"),
     "compact_v_not_rotated_back": ("kvo_hadamard_f32(w, hd);", ""),
