@@ -592,10 +592,10 @@ def _chunk_attn_bench(torch, kvq):
 
 
 def _decode_sources_sha() -> str:
-    """sha256[:16] over the decode kernel sources (the SIMT and tensor-core
-    partial kernels and the combine)."""
+    """sha256[:16] over the decode kernel sources (the partial kernel and
+    the combine, and the PTX helpers they use)."""
     h = hashlib.sha256()
-    for f in ("kvq_decode.cu", "kvq_decode_mma.cu", "kvq_ptx.cuh"):
+    for f in ("kvq_decode_mma.cu", "kvq_ptx.cuh"):
         h.update(open(os.path.join(ROOT, "quantized_kv_cache_append_gb300", "csrc", f),
                       "rb").read())
     return h.hexdigest()[:16]

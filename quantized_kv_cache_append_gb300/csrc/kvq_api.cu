@@ -69,25 +69,24 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Split plan: one wave of partial CTAs (as many as are resident per SM, on
 // every SM; four times that for batches, whose ragged lengths need short
-// splits to fill the tail of the launch)
-// over all (sequence, KV head) pairs, each split a whole number of cell
-// tiles.  The tensor-core kernel takes the shapes it covers; the CUDA-core
-// kernel the rest.  With max_bytes set, the split count is lowered until
-// the workspace fits (false if even one split per pair does not).
+// splits to fill the tail of the launch) over all (sequence, KV head, row
+// tile) items, each split a whole number of cell tiles.  A verify window
+// wider than one CTA's rows is cut into row tiles of mma_rows_per_cta rows.
+// With max_bytes set, the split count is lowered until the workspace fits
+// (false if even one split per pair does not).  use_mma is 0 when the
+// kernel's one-time setup failed.
 bool plan_decode(const kvq_cache* c, int n_seq, int W, int n_q, int max_ctx, DecodePlan* p,
                  size_t max_bytes = SIZE_MAX) {
   const int G = n_q / c->n_kv_heads;
   p->rows = G * W;
-  p->rows_pad = decode_rows_pad(c->head_dim, p->rows);
-  int per_sm = 0;
-  p->use_mma = 0;
-  if (mma_decode_supported(c->fmt, c->head_dim, p->rows)) {
-    per_sm = mma_ctas_per_sm(c->fmt, c->head_dim, p->rows);
-    p->use_mma = per_sm > 0;
-  }
-  if (!p->use_mma) per_sm = 4;
-  const int tile = p->use_mma ? mma_cell_tile() : decode_cell_tile();
-  const long long units = (long long)n_seq * c->n_kv_heads;
+  const int cta_rows = mma_rows_per_cta(c->head_dim);
+  p->rt_rows = p->rows < cta_rows ? p->rows : cta_rows;
+  p->n_rt = (p->rows + p->rt_rows - 1) / p->rt_rows;
+  int per_sm = mma_ctas_per_sm(c->fmt, c->head_dim, p->rt_rows);
+  p->use_mma = per_sm > 0;
+  if (!p->use_mma) per_sm = 1;   // still a plan (and a workspace size); the launch is refused
+  const int tile = mma_cell_tile();
+  const long long units = (long long)n_seq * c->n_kv_heads * p->n_rt;
   const int tiles = (max_ctx + tile - 1) / tile;
   int sms = sm_count();
   if (sms <= 0) sms = 148;
@@ -122,7 +121,7 @@ kvq_status check_decode_shape(const kvq_cache* c, int n_seq, int W, int n_q, int
   if ((long long)max_ctx > (long long)max_blocks * c->block_size) return KVQ_ERR_ARG;
   if (n_seq > 65535 || c->n_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   const int rows = (n_q / c->n_kv_heads) * W;
-  if (!decode_supported(c->fmt, c->head_dim, rows)) return KVQ_ERR_UNSUPPORTED;
+  if (!mma_decode_supported(c->fmt, c->head_dim, rows)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
@@ -220,7 +219,7 @@ kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W,
   if (!plan_decode(cache, n_seq, W, n_q, max_ctx, &plan, fit_plan ? workspace_bytes : SIZE_MAX))
     return fit_plan ? KVQ_ERR_WORKSPACE : KVQ_ERR_ARG;
   if (workspace_bytes < plan.bytes) return KVQ_ERR_WORKSPACE;
-  if (extra_tx != 0 && !plan.use_mma) return KVQ_ERR_UNSUPPORTED;  // no copy waits to run out
+  if (!plan.use_mma) return KVQ_ERR_CUDA;   // the kernels' one-time setup failed
   DecodeArgs a;
   a.pool = make_pool(cache);
   a.q = q;
@@ -234,14 +233,16 @@ kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W,
   a.n_q = n_q;
   a.G = n_q / cache->n_kv_heads;
   a.R = plan.rows;
+  a.RT = plan.rt_rows;
+  a.n_rt = plan.n_rt;
   a.max_blocks = max_blocks_per_seq;
   a.split_cells = plan.split_cells;
   a.nsplit = plan.nsplit;
   a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
   a.wait_limit = wait_limit;
   a.extra_tx = extra_tx;
-  const cudaError_t e =
-      launch_decode(cache->fmt, cache->head_dim, plan, a, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_decode_mma_partial(cache->fmt, cache->head_dim, plan, a,
+                                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

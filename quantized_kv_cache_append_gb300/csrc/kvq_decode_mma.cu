@@ -212,14 +212,22 @@ __device__ __forceinline__ bool item_of(const DecodeArgs& a, int c, int& b, int&
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int FMT, int HD, int NT>
+// HL (at most 4 query rows, NT = 1): the MMA's 8 columns carry the hi
+// parts of q (and of p) in columns 0-3 and the lo parts in columns 4-7, so
+// each k-step of q.k and each m-tile of p.v takes one MMA instead of two;
+// the hi and lo sums meet by one shuffle (lanes t and t ^ 2): per tile for
+// the logits, once per split for the output.  q's fragments stay in
+// registers.
+template <int FMT, int HD, int NT, bool HL>
 __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     decode_mma(const __grid_constant__ TmaMaps maps, DecodeArgs a) {
+  static_assert(!HL || NT == 1, "hi/lo columns need a single 8-column row tile");
   using C = Cfg<FMT, HD, NT>;
   constexpr int KS = HD / 16;   // k-steps of q.k, and m-tiles of p.v
   constexpr int RP = NT * 8;    // padded rows
   constexpr int MAXP = kTC / 16;
   constexpr float kNegInf = -INFINITY;
+  constexpr float kMStart = -1e30f;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -237,14 +245,38 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.v[0])) : "memory");
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // CTAs past the last item (splits beyond a sequence's context) have
-  // nothing to do; the combine kernel reads only the slots of live splits.
+  // One sequence: CTA c is split c / n_kv of KV head c % n_kv whatever the
+  // context length (the item order below reduces to that), so the block
+  // ids and the first copies need not wait for the length, which is only
+  // read after them; a split that turns out to lie past the context marks
+  // its slots empty.  A batch: CTAs past the last item (splits beyond a
+  // sequence's context) have nothing to do; the combine kernel reads only
+  // the slots of live splits.
+  // Row tiles: a work item's R query rows are cut into tiles of a.RT rows
+  // (a verify window wider than one CTA's accumulators), one CTA each; the
+  // CTAs of an item are neighbours in the grid, so all but the first find
+  // the item's K/V tiles in L2.
+  const int item = (int)blockIdx.x / a.n_rt;
+  const int r0 = ((int)blockIdx.x - item * a.n_rt) * a.RT;  // first query row of this CTA
+  const int Rc = min(a.RT, a.R - r0);                         // and its row count
   int b, kvh, split;
-  if (!item_of(a, blockIdx.x, b, kvh, split)) return;
-  const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
+  int L_raw = 0;
+  const bool single = a.n_seq == 1;
+  if (single) {
+    b = 0;
+    split = item / a.pool.n_kv;
+    kvh = item - split * a.pool.n_kv;
+    L_raw = __ldg(a.ctx_lens);
+  } else {
+    if (!item_of(a, item, b, kvh, split)) return;
+    L_raw = __ldg(a.ctx_lens + b);
+  }
   const int c_begin = split * a.split_cells;
-  const int c_end = min(L, c_begin + a.split_cells);
-  const int n_tiles = (c_end - c_begin + kTC - 1) / kTC;
+  // until the length is known (one sequence), copies stay inside the split
+  // and the block table
+  int c_end = min(clamp_len_mma(single ? INT_MAX : L_raw, a), c_begin + a.split_cells);
+  int n_tiles = (c_end - c_begin + kTC - 1) / kTC;
+  const int n_first = n_tiles < C::STAGES ? n_tiles : C::STAGES;   // tiles of the first wave
   const int pc_log2 = a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6;  // cells per TMA piece
   const int n_pieces = kTC >> pc_log2;
   const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
@@ -335,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         const int tt = (kq & 7) >> 1, e = kq & 1, hi8 = kq >> 3;
         dim = 16 * ks + 4 * tt + 2 * hi8 + e;
       }
-      if (r < a.R) {
-        const int w = r / a.G, gg = r - w * a.G;
+      if (r < Rc) {
+        const int w = (r0 + r) / a.G, gg = r0 + r - w * a.G;
         qv[u] = __ldg(a.q + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + dim);
       }
     }
@@ -361,22 +393,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       s_rel[s] = 0;
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-#pragma unroll
-    for (int it = 0; it < C::STAGES; ++it)
-      if (it < n_tiles) issue(it, fb[it]);
+    // the first tile now; the rest of the first wave after the barrier
+    // below, so that on every SM each CTA's first tile is queued for the
+    // copy engine ahead of the other tiles of the wave
+    if (n_first > 0) issue(0, fb[0]);
   }
   {
     unsigned char* qs = smem + C::SMEM_Q;
 #pragma unroll
     for (int u = 0; u < QPT; ++u) {
       const int i = threadIdx.x + u * kThreads;
-      if (i < RP * HD) {
+      if (i < RP * HD && (!HL || i / HD < 4)) {
         const int r = i / HD, k = i - r * HD;
         const float x = qv[u] * a.qscale;
         const __half h = __float2half_rn(x);
         const __half lo = __float2half_rn(x - __half2float(h));
         *reinterpret_cast<__half*>(qs + r * C::QROW + k * 2) = h;
-        *reinterpret_cast<__half*>(qs + (RP + r) * C::QROW + k * 2) = lo;
+        *reinterpret_cast<__half*>(qs + (HL ? 4 + r : RP + r) * C::QROW + k * 2) = lo;
         if constexpr (C::KI8) {
           // The 32 lanes of a warp hold 32 consecutive k of one row and one
           // 64-dim group (RP * HD is a multiple of 128): their sum of q,
@@ -397,6 +430,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     }
   }
   __syncthreads();
+  const int L = clamp_len_mma(L_raw, a);
+  if (single) {
+    c_end = min(L, c_begin + a.split_cells);
+    n_tiles = c_end > c_begin ? (c_end - c_begin + kTC - 1) / kTC : 0;
+    if (n_tiles == 0) {
+      // a split past the context: its slots tell the combine "no cells"
+      if (producer && n_first > 0) (void)mbar_wait(bar_full, 0, a.wait_limit);
+      const size_t slot0 = (((size_t)b * a.pool.n_kv + kvh) * a.nsplit + split) * a.R;
+      if (threadIdx.x < a.R)
+        *reinterpret_cast<float2*>(a.ws_ml + (slot0 + threadIdx.x) * 2) = make_float2(-INFINITY, 0.f);
+      return;
+    }
+  }
+  if (producer) {
+    for (int it = 1; it < n_first; ++it) {
+      int nb[MAXP];
+      tile_blks(it, blk_in_smem, nb);
+      issue(it, nb);
+    }
+  }
 
   // ---------------- consumer setup ----------------
   const int g = lane >> 2, t = lane & 3;
@@ -414,7 +467,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int i = ((nt * 8 + 2 * t + j) * C::NG + gq) * 2;
-          qcorr[gq][nt][j] = -(s_qc[i] + s_qc[i + 1]);
+          // (HL: the lo columns 4-7 start at 0; the hi ones carry the whole
+          // correction, the two meet in the logits)
+          qcorr[gq][nt][j] = (HL && t >= 2) ? 0.f : -(s_qc[i] + s_qc[i + 1]);
         }
   }
 
@@ -422,16 +477,34 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // k0-7, lo k8-15}, row lane&7.
   const uint32_t q_lane = qbase + (uint32_t)((lane >> 4) * RP + (lane & 7)) * C::QROW +
                           (uint32_t)((lane >> 3) & 1) * 16;
+  // HL: the B fragments of every k-step (rows 0-3 hi, 4-7 lo), kept in
+  // registers; one ldmatrix x4 covers two k-steps
+  uint32_t qreg[HL ? KS : 1][2];
+  if constexpr (HL) {
+    const uint32_t ql = qbase + (uint32_t)(lane & 7) * C::QROW + (uint32_t)(lane >> 3) * 16;
+#pragma unroll
+    for (int ks = 0; ks < KS; ks += 2) {
+      uint32_t r4[4];
+      ldsm_x4(r4, ql + ks * 32);
+      qreg[ks][0] = r4[0];
+      qreg[ks][1] = r4[1];
+      qreg[ks + 1][0] = r4[2];
+      qreg[ks + 1][1] = r4[3];
+    }
+  }
 
   // Last visible cell of each of this thread's rows (the verify window's
   // causal limit), or -1 for padding rows.
+  // the query row of this thread's column j of row tile nt (HL: lanes t
+  // and t ^ 2 hold the same rows, hi and lo halves)
+  auto row_of = [&](int nt, int j) -> int { return HL ? 2 * (t & 1) + j : nt * 8 + 2 * t + j; };
   int row_last[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int r = nt * 8 + 2 * t + j;
-      row_last[nt][j] = r < a.R ? L - a.W + r / a.G : -1;
+      const int r = row_of(nt, j);
+      row_last[nt][j] = r < Rc ? L - a.W + (r0 + r) / a.G : -1;
     }
 
   int row_last_min = INT_MAX;  // smallest causal limit among this thread's real rows
@@ -439,13 +512,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
-      if (nt * 8 + 2 * t + j < a.R) row_last_min = min(row_last_min, row_last[nt][j]);
+      if (row_of(nt, j) < Rc) row_last_min = min(row_last_min, row_last[nt][j]);
 
   float m[NT][2], l[NT][2];
   float o[KS][NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    m[nt][0] = m[nt][1] = kNegInf;
+    // a finite start, so p needs no "no maximum yet" test: the first tile
+    // with a visible cell always raises it
+    m[nt][0] = m[nt][1] = kMStart;
     l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
@@ -512,7 +587,21 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   auto qk = [&](int s, float (&z)[NT][4]) {
     const uint32_t st = sbase + s * C::STAGE_B;
   // ---------------- S^T = K . Q^T (four independent accumulators) ----------------
-  if constexpr (FMT == KVQ_F16) {
+  if constexpr (FMT == KVQ_F16 && HL) {
+    float acc[2][4];  // alternate k-steps, two independent chains
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t af[4];
+      ldsm_x4(af, st + kx[ks & 3] + (uint32_t)(ks >> 2) * kSpanB);
+      if (ks < 2) mma16816_zc(acc[ks & 1], af, qreg[ks][0], qreg[ks][1]);
+      else mma16816(acc[ks & 1], af, qreg[ks][0], qreg[ks][1]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float v = acc[0][k] + acc[1][k];
+      z[0][k] = v + __shfl_xor_sync(kFull, v, 2);  // hi columns + lo columns
+    }
+  } else if constexpr (FMT == KVQ_F16) {
     float acc[4][NT][4];
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -567,24 +656,40 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         af[2] = prmt(w[kk][0], kMagic, 0x4342u);
         af[1] = prmt(w[kk][1], kMagic, 0x4140u);
         af[3] = prmt(w[kk][1], kMagic, 0x4342u);
+        if constexpr (HL) {
+          // one chain: columns 0-3 hi (start at -1152 sum q), 4-7 lo (at 0)
+          mma16816(acc[0][0], af, qreg[gq * 4 + kk][0], qreg[gq * 4 + kk][1]);
+        } else {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          uint32_t qf[4];
-          ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + (gq * 4 + kk) * 32);
-          mma16816(acc[0][nt], af, qf[0], qf[1]);
-          if (kk == 0) mma16816_zc(acc[1][nt], af, qf[2], qf[3]);
-          else mma16816(acc[1][nt], af, qf[2], qf[3]);
+          for (int nt = 0; nt < NT; ++nt) {
+            uint32_t qf[4];
+            ldsm_x4(qf, q_lane + (uint32_t)(nt * 8) * C::QROW + (gq * 4 + kk) * 32);
+            mma16816(acc[0][nt], af, qf[0], qf[1]);
+            if (kk == 0) mma16816_zc(acc[1][nt], af, qf[2], qf[3]);
+            else mma16816(acc[1][nt], af, qf[2], qf[3]);
+          }
         }
       }
       const float s0 = __half2float(__ushort_as_half(ksc[(cl + g) * C::NG + gq]));
       const float s8 = __half2float(__ushort_as_half(ksc[(cl + g + 8) * C::NG + gq]));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        z[nt][0] = fmaf(s0, acc[0][nt][0] + acc[1][nt][0], z[nt][0]);
-        z[nt][1] = fmaf(s0, acc[0][nt][1] + acc[1][nt][1], z[nt][1]);
-        z[nt][2] = fmaf(s8, acc[0][nt][2] + acc[1][nt][2], z[nt][2]);
-        z[nt][3] = fmaf(s8, acc[0][nt][3] + acc[1][nt][3], z[nt][3]);
+        if constexpr (HL) {
+          z[nt][0] = fmaf(s0, acc[0][nt][0], z[nt][0]);
+          z[nt][1] = fmaf(s0, acc[0][nt][1], z[nt][1]);
+          z[nt][2] = fmaf(s8, acc[0][nt][2], z[nt][2]);
+          z[nt][3] = fmaf(s8, acc[0][nt][3], z[nt][3]);
+        } else {
+          z[nt][0] = fmaf(s0, acc[0][nt][0] + acc[1][nt][0], z[nt][0]);
+          z[nt][1] = fmaf(s0, acc[0][nt][1] + acc[1][nt][1], z[nt][1]);
+          z[nt][2] = fmaf(s8, acc[0][nt][2] + acc[1][nt][2], z[nt][2]);
+          z[nt][3] = fmaf(s8, acc[0][nt][3] + acc[1][nt][3], z[nt][3]);
+        }
       }
+    }
+    if constexpr (HL) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) z[0][k] += __shfl_xor_sync(kFull, z[0][k], 2);  // hi + lo columns
     }
   }
 
@@ -608,9 +713,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const bool none = m[nt][j] == kNegInf;
-        p[nt][j] = none ? 0.f : fast_exp2(z[nt][j] - m[nt][j]);
-        p[nt][2 + j] = none ? 0.f : fast_exp2(z[nt][2 + j] - m[nt][j]);
+        p[nt][j] = fast_exp2(z[nt][j] - m[nt][j]);
+        p[nt][2 + j] = fast_exp2(z[nt][2 + j] - m[nt][j]);
       }
   };
   float lmax[NT][2];
@@ -639,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
         if (tmax > m[nt][j] + kTau) {
-          const float alpha = m[nt][j] == kNegInf ? 0.f : fast_exp2(m[nt][j] - tmax);
+          const float alpha = fast_exp2(m[nt][j] - tmax);  // 0 from the finite start
           m[nt][j] = tmax;
           l[nt][j] *= alpha;
 #pragma unroll
@@ -670,10 +774,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       uint32_t h01, l01, h23, l23;
       split_pair(p[nt][0], p[nt][1], h01, l01);
       split_pair(p[nt][2], p[nt][3], h23, l23);
-      bh[nt][0] = movmatrix_t(h01);
-      bh[nt][1] = movmatrix_t(h23);
-      bl[nt][0] = movmatrix_t(l01);
-      bl[nt][1] = movmatrix_t(l23);
+      if constexpr (HL) {  // columns 0-3 hi, 4-7 lo
+        bh[nt][0] = movmatrix_t(t >= 2 ? l01 : h01);
+        bh[nt][1] = movmatrix_t(t >= 2 ? l23 : h23);
+      } else {
+        bh[nt][0] = movmatrix_t(h01);
+        bh[nt][1] = movmatrix_t(h23);
+        bl[nt][0] = movmatrix_t(l01);
+        bl[nt][1] = movmatrix_t(l23);
+      }
     }
     // V rows of cells past the valid ones may hold anything: zero them.
     const uint32_t mlo = (2 * t < nvalid ? 0xffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
@@ -692,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         mma16816(o[mt][nt], af, bh[nt][0], bh[nt][1]);
-        mma16816(o[mt][nt], af, bl[nt][0], bl[nt][1]);
+        if constexpr (!HL) mma16816(o[mt][nt], af, bl[nt][0], bl[nt][1]);
       }
     }
   } else if constexpr (C::V4) {
@@ -748,10 +857,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
           uint32_t h01, l01, h23, l23;
           split_pair(p[nt][0] * s0, p[nt][1] * s0, h01, l01);
           split_pair(p[nt][2] * s8, p[nt][3] * s8, h23, l23);
-          bh[nt][0] = movmatrix_t(h01);
-          bh[nt][1] = movmatrix_t(h23);
-          bl[nt][0] = movmatrix_t(l01);
-          bl[nt][1] = movmatrix_t(l23);
+          if constexpr (HL) {
+            bh[nt][0] = movmatrix_t(t >= 2 ? l01 : h01);
+            bh[nt][1] = movmatrix_t(t >= 2 ? l23 : h23);
+          } else {
+            bh[nt][0] = movmatrix_t(h01);
+            bh[nt][1] = movmatrix_t(h23);
+            bl[nt][0] = movmatrix_t(l01);
+            bl[nt][1] = movmatrix_t(l23);
+          }
         }
         const uint32_t wl = r[2 * jb], wh = r[2 * jb + 1];
         const uint32_t wl8 = wl >> 8, wh8 = wh >> 8;
@@ -762,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(o[2 * blk + h][nt], af, bh[nt][0], bh[nt][1]);
-            mma16816(o[2 * blk + h][nt], af, bl[nt][0], bl[nt][1]);
+            if constexpr (!HL) mma16816(o[2 * blk + h][nt], af, bl[nt][0], bl[nt][1]);
           }
         }
       }
@@ -787,10 +901,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         uint32_t h01, l01, h23, l23;
         split_pair(x0, x1, h01, l01);
         split_pair(x2, x3, h23, l23);
-        bh[nt][0] = movmatrix_t(h01);
-        bh[nt][1] = movmatrix_t(h23);
-        bl[nt][0] = movmatrix_t(l01);
-        bl[nt][1] = movmatrix_t(l23);
+        if constexpr (HL) {
+          bh[nt][0] = movmatrix_t(t >= 2 ? l01 : h01);
+          bh[nt][1] = movmatrix_t(t >= 2 ? l23 : h23);
+        } else {
+          bh[nt][0] = movmatrix_t(h01);
+          bh[nt][1] = movmatrix_t(h23);
+          bl[nt][0] = movmatrix_t(l01);
+          bl[nt][1] = movmatrix_t(l23);
+        }
       }
       // Two ldmatrix.trans x4 per 64-dim group, on byte pairs: register
       // i of chunk c holds (cell 2t, dims 16c + 2g, +1) and (cell 2t + 1,
@@ -812,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(o[c0 + h][nt], af, bh[nt][0], bh[nt][1]);
-            mma16816(o[c0 + h][nt], af, bl[nt][0], bl[nt][1]);
+            if constexpr (!HL) mma16816(o[c0 + h][nt], af, bl[nt][0], bl[nt][1]);
           }
         }
       }
@@ -887,7 +1006,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   if (producer) {
     // Every copy this CTA issued has landed before the CTA can exit (waits
     // return at once in normal runs; they are bounded after a lost wait).
-    for (int it = n_tiles > C::STAGES ? n_tiles - C::STAGES : 0; it < n_tiles; ++it)
+    const int n_all = n_tiles > n_first ? n_tiles : n_first;
+    for (int it = n_all > C::STAGES ? n_all - C::STAGES : 0; it < n_all; ++it)
       (void)mbar_wait(bar_full + 8 * (it % C::STAGES), (it / C::STAGES) & 1, a.wait_limit);
   }
 
@@ -897,6 +1017,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // its rows scaled to the CTA maximum into a slab of its own in the stage
   // memory; after a second barrier the 4 slabs are summed straight into the
   // split's partial in global memory.  A lost wait poisons the rows (NaN).
+  if constexpr (HL) {
+    // the hi and lo column sums of each row meet (lanes t < 2 keep them)
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[mt][0][k] += __shfl_xor_sync(kFull, o[mt][0][k], 2);
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -909,12 +1036,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     }
   float* s_wml = reinterpret_cast<float*>(smem + C::SMEM_WML);  // [warp][RP][m, l]
   const bool wlost = __any_sync(kFull, lost);
-  if (g == 0) {
+  if (g == 0 && (!HL || t < 2)) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int r = nt * 8 + 2 * t + j;
+        const int r = row_of(nt, j);
         s_wml[(warp * RP + r) * 2 + 0] = wlost ? __int_as_float(0x7fc00000) : m[nt][j];
         s_wml[(warp * RP + r) * 2 + 1] = l[nt][j];
       }
@@ -925,13 +1052,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int r = nt * 8 + 2 * t + j;
-      if (r < a.R) {
+      const int r = row_of(nt, j);
+      if (r < Rc && (!HL || t < 2)) {
         float M = s_wml[r * 2];
 #pragma unroll
         for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_wml[(w * RP + r) * 2]);
         const float wgt = (M == kNegInf || m[nt][j] == kNegInf) ? 0.f : fast_exp2(m[nt][j] - M);
-        float* orow = s_slab + (warp * a.R + r) * HD;
+        float* orow = s_slab + (warp * Rc + r) * HD;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           if constexpr (FMT == KVQ_F16) {  // m-tile rows g, g + 8 are dims 16 mt + g, + 8
@@ -948,14 +1075,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       }
     }
   __syncthreads();
-  const size_t slot0 = (((size_t)b * a.pool.n_kv + kvh) * a.nsplit + split) * a.R;
+  // this CTA's rows of the split's partial
+  const size_t row0 = (((size_t)b * a.pool.n_kv + kvh) * a.nsplit + split) * a.R + r0;
   if constexpr (C::V4) {
     // K8V4: the merged rows are in the rotated basis; one warp per row sums
     // the slabs, rotates the row back (Walsh-Hadamard, divided by HD) and
     // writes it.  The combine is linear in the partials, so it needs no
     // change.
     constexpr int U = HD >= 128 ? 4 : 2, NI = HD / (32 * U);
-    for (int r = warp; r < a.R; r += kConsumerWarps) {
+    for (int r = warp; r < Rc; r += kConsumerWarps) {
       float x[NI][U];
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
@@ -963,11 +1091,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
         for (int e = 0; e < U; ++e) {
           const float* col = s_slab + r * HD + d0 + e;
-          x[i][e] = (col[0] + col[a.R * HD]) + (col[2 * a.R * HD] + col[3 * a.R * HD]);
+          x[i][e] = (col[0] + col[Rc * HD]) + (col[2 * Rc * HD] + col[3 * Rc * HD]);
         }
       }
       wht_warp<U, NI>(x, lane);
-      float* dst = a.ws_o + (slot0 + r) * HD;
+      float* dst = a.ws_o + (row0 + r) * HD;
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
         const int d0 = U * lane + 32 * U * i;
@@ -980,16 +1108,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       }
     }
   } else
-  for (int i4 = threadIdx.x; i4 < a.R * HD / 4; i4 += kThreads) {
+  for (int i4 = threadIdx.x; i4 < Rc * HD / 4; i4 += kThreads) {
     const float4 v0 = reinterpret_cast<const float4*>(s_slab)[i4];
-    const float4 v1 = reinterpret_cast<const float4*>(s_slab + a.R * HD)[i4];
-    const float4 v2 = reinterpret_cast<const float4*>(s_slab + 2 * a.R * HD)[i4];
-    const float4 v3 = reinterpret_cast<const float4*>(s_slab + 3 * a.R * HD)[i4];
-    reinterpret_cast<float4*>(a.ws_o + slot0 * HD)[i4] =
+    const float4 v1 = reinterpret_cast<const float4*>(s_slab + Rc * HD)[i4];
+    const float4 v2 = reinterpret_cast<const float4*>(s_slab + 2 * Rc * HD)[i4];
+    const float4 v3 = reinterpret_cast<const float4*>(s_slab + 3 * Rc * HD)[i4];
+    reinterpret_cast<float4*>(a.ws_o + row0 * HD)[i4] =
         make_float4((v0.x + v1.x) + (v2.x + v3.x), (v0.y + v1.y) + (v2.y + v3.y),
                     (v0.z + v1.z) + (v2.z + v3.z), (v0.w + v1.w) + (v2.w + v3.w));
   }
-  if (threadIdx.x < a.R) {
+  if (threadIdx.x < Rc) {
     const int r = threadIdx.x;
     float M = s_wml[r * 2];
     bool bad = M != M;
@@ -1005,7 +1133,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
       const float mw = s_wml[(w * RP + r) * 2];
       if (M != kNegInf && mw != kNegInf) lsum = fmaf(s_wml[(w * RP + r) * 2 + 1], fast_exp2(mw - M), lsum);
     }
-    *reinterpret_cast<float2*>(a.ws_ml + (slot0 + r) * 2) =
+    *reinterpret_cast<float2*>(a.ws_ml + (row0 + r) * 2) =
         make_float2(bad ? __int_as_float(0x7fc00000) : M, lsum);
   }
 }
@@ -1041,8 +1169,11 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_partials(DecodeArg
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int dv = tid % DV, js = tid / DV;
   const int d = d0 + 4 * dv;
-  const int L = clamp_len_mma(__ldg(a.ctx_lens + b), a);
-  const int nlive = (L + a.split_cells - 1) / a.split_cells;
+  // one sequence: every split slot is written (splits past the context say
+  // "no cells"), so the context length need not be read
+  const int nlive = a.n_seq == 1 ? a.nsplit
+                                 : (clamp_len_mma(__ldg(a.ctx_lens + b), a) + a.split_cells - 1) /
+                                       a.split_cells;
   const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.nsplit;
 
   float M = kNegInf, lsum = 0.f;
@@ -1202,24 +1333,19 @@ bool make_map(CUtensorMap* map, const void* base, int span, int row_bytes, int s
   return r == CUDA_SUCCESS;
 }
 
-template <int FMT, int HD, int NT>
-const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_mma<FMT, HD, NT>);
-}
-
 // Resident CTAs per SM of one configuration (0 if it cannot run), after
 // raising its dynamic shared-memory limit; done once per context.
-template <int FMT, int HD, int NT>
+template <int FMT, int HD, int NT, bool HL>
 int ctas_per_sm_impl() {
   static ContextCache<int> cache;
   int occ = 0;
   const bool ok = per_context(cache, &occ, [](int* v) {
     using C = Cfg<FMT, HD, NT>;
-    if (cudaFuncSetAttribute(decode_mma<FMT, HD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(decode_mma<FMT, HD, NT, HL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return false;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma<FMT, HD, NT>, kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma<FMT, HD, NT, HL>, kThreads,
                                                       C::SMEM) != cudaSuccess)
       return false;
     *v = n;
@@ -1228,10 +1354,10 @@ int ctas_per_sm_impl() {
   return ok ? occ : 0;
 }
 
-template <int FMT, int HD, int NT>
+template <int FMT, int HD, int NT, bool HL>
 cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s) {
   using C = Cfg<FMT, HD, NT>;
-  if (ctas_per_sm_impl<FMT, HD, NT>() <= 0) return cudaErrorInvalidConfiguration;
+  if (ctas_per_sm_impl<FMT, HD, NT, HL>() <= 0) return cudaErrorInvalidConfiguration;
   const long long rows = (long long)a.pool.n_blocks * a.pool.n_kv << a.pool.bs_log2;
   const int piece = 1 << (a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6);
   TmaMaps maps;
@@ -1241,7 +1367,7 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
   for (int sp = 0; sp < C::VNCH; ++sp)
     if (!make_map(&maps.v[sp], a.pool.v, C::VSWB, C::VROWB, sp, rows, piece)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  const long long items = (long long)p.nsplit * a.pool.n_kv * a.n_seq;
+  const long long items = (long long)p.nsplit * a.pool.n_kv * a.n_seq * a.n_rt;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   cfg.gridDim = dim3((unsigned)items);
   cfg.blockDim = dim3(kThreads);
@@ -1252,32 +1378,37 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma<FMT, HD, NT>, maps, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma<FMT, HD, NT, HL>, maps, a);
   if (e != cudaSuccess) return e;
   return launch_combine<HD>(a, s);
 }
 
+// Kernel shape of a row count: 0 = one 8-column tile with hi/lo columns
+// (at most 4 rows), else the number of 8-row tiles.
+int tile_code(int rows) { return rows <= 4 ? 0 : rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : -1; }
+int n_tiles_for(int rows) { const int c = tile_code(rows); return c == 0 ? 1 : c < 0 ? 0 : c; }
+
 template <int FMT, int HD>
-int ctas_per_sm_hd(int nt) {
-  switch (nt) {
-    case 1: return ctas_per_sm_impl<FMT, HD, 1>();
-    case 2: if constexpr (HD <= 128) return ctas_per_sm_impl<FMT, HD, 2>(); break;
-    case 4: if constexpr (HD <= 64) return ctas_per_sm_impl<FMT, HD, 4>(); break;
+int ctas_per_sm_hd(int code) {
+  switch (code) {
+    case 0: return ctas_per_sm_impl<FMT, HD, 1, true>();
+    case 1: return ctas_per_sm_impl<FMT, HD, 1, false>();
+    case 2: if constexpr (HD <= 128) return ctas_per_sm_impl<FMT, HD, 2, false>(); break;
+    case 4: if constexpr (HD <= 64) return ctas_per_sm_impl<FMT, HD, 4, false>(); break;
   }
   return 0;
 }
 
 template <int FMT, int HD>
-cudaError_t launch_hd(int nt, const DecodePlan& p, const DecodeArgs& a, cudaStream_t s) {
-  switch (nt) {
-    case 1: return launch_impl<FMT, HD, 1>(p, a, s);
-    case 2: if constexpr (HD <= 128) return launch_impl<FMT, HD, 2>(p, a, s); break;
-    case 4: if constexpr (HD <= 64) return launch_impl<FMT, HD, 4>(p, a, s); break;
+cudaError_t launch_hd(int code, const DecodePlan& p, const DecodeArgs& a, cudaStream_t s) {
+  switch (code) {
+    case 0: return launch_impl<FMT, HD, 1, true>(p, a, s);
+    case 1: return launch_impl<FMT, HD, 1, false>(p, a, s);
+    case 2: if constexpr (HD <= 128) return launch_impl<FMT, HD, 2, false>(p, a, s); break;
+    case 4: if constexpr (HD <= 64) return launch_impl<FMT, HD, 4, false>(p, a, s); break;
   }
   return cudaErrorInvalidValue;
 }
-
-int n_tiles_for(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 0; }
 
 }  // namespace
 
@@ -1324,17 +1455,20 @@ unsigned long long current_context_id() {
 }
 
 bool mma_decode_supported(int fmt, int hd, int rows) {
-  const int nt = n_tiles_for(rows);
-  if (nt == 0 || rows < 1) return false;
+  if (rows < 1 || rows > 32) return false;
   if (hd != 64 && hd != 128 && hd != 256) return false;
-  if (fmt != KVQ_F16 && fmt != KVQ_Q8 && fmt != KVQ_K8V4) return false;
-  return nt * hd <= 256;
+  return fmt == KVQ_F16 || fmt == KVQ_Q8 || fmt == KVQ_K8V4;
 }
+
+// Query rows one CTA holds: 8-row MMA tiles while their fp32 accumulators
+// (HD / 16 m-tiles x 4 floats per tile and thread) stay at 32 per thread
+// or fewer -- 32 rows at head_dim 64, 16 at 128, 8 at 256.
+int mma_rows_per_cta(int hd) { return 8 * (256 / hd); }
 
 int mma_cell_tile() { return kTC; }
 
 int mma_ctas_per_sm(int fmt, int hd, int rows) {
-  const int nt = n_tiles_for(rows);
+  const int nt = tile_code(rows);
   if (fmt == KVQ_F16) {
     if (hd == 64) return ctas_per_sm_hd<KVQ_F16, 64>(nt);
     if (hd == 128) return ctas_per_sm_hd<KVQ_F16, 128>(nt);
@@ -1352,7 +1486,7 @@ int mma_ctas_per_sm(int fmt, int hd, int rows) {
 
 cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, const DecodeArgs& a,
                                       cudaStream_t s) {
-  const int nt = n_tiles_for(p.rows);
+  const int nt = tile_code(p.rt_rows);
   if (fmt == KVQ_F16) {
     if (hd == 64) return launch_hd<KVQ_F16, 64>(nt, p, a, s);
     if (hd == 128) return launch_hd<KVQ_F16, 128>(nt, p, a, s);

@@ -121,9 +121,10 @@ struct AppendArgs {
 // is cut into nsplit ranges of split_cells cells; each range is one CTA of
 // the partial kernel.
 struct DecodePlan {
-  int use_mma;         // 1: tensor-core partial kernel (kvq_decode_mma.cu)
+  int use_mma;         // 1: the tensor-core kernels can run (their setup succeeded)
   int rows;            // R = G * W query rows per (sequence, KV head)
-  int rows_pad;        // R rounded up to the kernel's row tile
+  int rt_rows;         // rows per CTA (R, or the widest row tile the head dim allows)
+  int n_rt;            // row tiles per work item: ceil(R / rt_rows)
   int split_cells;     // cells per split (a multiple of the cell tile)
   int nsplit;          // splits per (sequence, KV head), one partial each
   size_t off_o, off_ml, bytes;  // workspace layout
@@ -138,6 +139,7 @@ struct DecodeArgs {
   float* ws_o;         // [n_seq][n_kv][nsplit][R][hd]   unnormalised partial outputs
   float* ws_ml;        // [n_seq][n_kv][nsplit][R][2]    (running max, sum), log2 domain
   int n_seq, W, n_q, G, R, max_blocks, split_cells, nsplit;
+  int RT, n_rt;        // query rows per CTA and CTAs (row tiles) per work item
   float qscale;        // sm_scale * log2(e): logits come out in the log2 domain
   uint32_t wait_limit; // polls of a copy wait before it is declared lost
   uint32_t extra_tx;   // bytes added to each stage's expected count (0; >0 only
@@ -172,17 +174,13 @@ struct PersistArgs {
 cudaError_t launch_append(int fmt, int hd, const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_compact(int fmt, int hd, const CompactArgs& a, cudaStream_t s);
 cudaError_t launch_persist(int fmt, int hd, bool gather, const PersistArgs& a, cudaStream_t s);
-bool decode_supported(int fmt, int hd, int rows);
-int decode_rows_pad(int hd, int rows);
-int decode_cell_tile();
-cudaError_t launch_decode(int fmt, int hd, const DecodePlan& plan, const DecodeArgs& a,
-                          cudaStream_t s);
 
-// Tensor-core partial kernel (kvq_decode_mma.cu): shapes it covers, its cell
-// tile, resident CTAs per SM (0 if unavailable), and its launcher (partial +
-// combine).
+// Split-K decode (kvq_decode_mma.cu): shapes it covers, its cell tile, the
+// query rows one CTA holds, resident CTAs per SM of the kernel serving a
+// row count (0 if unavailable), and its launcher (partial + combine).
 bool mma_decode_supported(int fmt, int hd, int rows);
 int mma_cell_tile();
+int mma_rows_per_cta(int hd);
 int mma_ctas_per_sm(int fmt, int hd, int rows);
 cudaError_t launch_decode_mma_partial(int fmt, int hd, const DecodePlan& p, const DecodeArgs& a,
                                       cudaStream_t s);

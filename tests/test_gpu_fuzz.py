@@ -33,7 +33,7 @@ def _case(seed):
     hd = int(rng.choice([64, 128, 256]))
     bs = int(rng.choice([16, 32, 64, 256, 1024]))
     n_kv = int(rng.choice([1, 2, 3, 4, 8]))
-    max_rows = 32 if hd == 64 else (16 if hd == 128 else 8)
+    max_rows = 32   # rows beyond one CTA's tile (16 at head_dim 128, 8 at 256) run as row tiles
     while True:
         G = int(rng.choice([1, 2, 3, 4, 8]))
         W = int(rng.choice([1, 1, 2, 4, 8, 16]))

@@ -133,6 +133,26 @@ def test_shapes(fmt, hd, bs, n_kv, G, W):
 
 
 @pytest.mark.parametrize("fmt", ["f16", "q8", "k8v4"])
+@pytest.mark.parametrize("hd,n_kv,G,W", [
+    (256, 2, 8, 2), (256, 2, 8, 4), (256, 1, 4, 4), (256, 1, 2, 16),   # 16, 32, 16, 32 rows
+    (128, 2, 8, 4), (128, 1, 4, 8), (128, 3, 2, 16), (128, 1, 8, 3),   # 32, 32, 32, 24 rows
+    (64, 2, 8, 4), (64, 1, 4, 8),                                      # 32 rows in one CTA
+])
+def test_wide_verify_windows(fmt, hd, n_kv, G, W):
+    """Verify windows whose G * W query rows exceed one CTA's row tile (8
+    rows at head_dim 256, 16 at 128) are cut into row tiles; every tile
+    must give the oracle's attention, causal limits included (#711 kv:
+    --kv k8v4 streams with --kv-resident, "How": verify-window appends;
+    "Measured": spec 4)."""
+    lens = [W, 2 * W + 5, 700, 3001]
+    p, rng = _random_pair(fmt, lens, n_kv, hd, 64, seed=hd + 11 * G + W + n_kv)
+    q = rng.standard_normal((len(lens), W, n_kv * G, hd)).astype(np.float32)
+    sm = workloads.sm_scale_for(hd)
+    p.check_decode(q, lens, sm)
+    p.check_decode(q, lens, sm, max_ctx=p.bt_host.shape[1] * 64)   # widest allowed plan
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8", "k8v4"])
 def test_single_cell_outputs_its_value(fmt):
     p, rng = _random_pair(fmt, [1], 2, 128, 16, seed=3)
     q = rng.standard_normal((1, 1, 8, 128)).astype(np.float32)

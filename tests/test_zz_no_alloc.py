@@ -10,8 +10,10 @@ the library keeps in a device array of its own.
 This file checks, through the C ABI, that it returns what kvq_decode_attn
 (with a caller-provided workspace) returns, on two calls in a row with
 different shapes (the second call finds the first call's leftovers in the
-shared scratch), and that a request larger than the array is refused
-before anything runs.  It is collected last so that a run stopping at the
+shared scratch), that a request whose full split plan does not fit the
+array is cut into fewer splits and still matches the float64 oracle, and
+that a request too large even with one split per (sequence, KV head) is
+refused before anything runs.  It is collected last so that a run stopping at the
 first failure has run every other test first; it also passes on its own.
 """
 import numpy as np
@@ -123,3 +125,52 @@ def test_request_beyond_the_static_scratch_is_refused():
     assert st == kvq.KVQ_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert not out.any()
+
+
+def test_plan_lowered_to_fit_the_static_scratch_matches_the_oracle():
+    # A verify window of 4 tokens on 32 ragged int8 sequences: the full split
+    # plan needs more partials than the 8 MiB array holds, so the call cuts
+    # the context into fewer splits until they fit.  Its output must still be
+    # the attention the pages define (the float64 oracle on its own cache,
+    # fed the same cells; same bar as every other decode) and agree with the
+    # workspace entry point.
+    import oracle
+    from tests.gpu_pairs import Pair, assert_attention_close, dev
+
+    n_seq, n_kv, G, W, hd, bs = 32, 8, 4, 4, 128, 256
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1024, 8193, n_seq).astype(np.int32)
+    max_ctx = int(lens.max())
+    nbs = [-(-int(L) // bs) for L in lens]
+    perm = rng.permutation(sum(nbs)).astype(np.int32)
+    table = np.full((n_seq, max(nbs)), -1, np.int32)
+    at = 0
+    for b, n in enumerate(nbs):
+        table[b, :n] = perm[at:at + n]
+        at += n
+    pair = Pair("q8", n_kv, hd, bs, sum(nbs), table)
+    n_tok = int(lens.sum())
+    k = rng.standard_normal((n_tok, n_kv, hd)).astype(np.float32)
+    v = rng.standard_normal((n_tok, n_kv, hd)).astype(np.float32)
+    seq = np.concatenate([np.full(L, b, np.int32) for b, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
+    pair.append(k, v, seq, pos)
+    q = rng.standard_normal((n_seq, W, n_kv * G, hd)).astype(np.float32)
+    sm = float(np.float32(1.0) / np.sqrt(np.float32(hd)))
+
+    pool = pair.gpu
+    need = kvq.kvq_decode_workspace_bytes(pool.cache, n_seq, W, n_kv * G, max_ctx)
+    assert need > kvq.KVQ_STATIC_SCRATCH_BYTES
+    qd, ctx = dev(q), dev(lens)
+    got = _static(pool, qd, ctx, max_ctx, pair.bt, sm)
+    ref = _with_workspace(pool, qd, ctx, max_ctx, pair.bt, sm)
+    torch.cuda.synchronize()
+    _close(got, ref)
+
+    path = oracle.parallel_library(8)   # the same oracle on 8 threads (bitwise equal)
+    if path is not None:
+        with oracle.use_library(path):
+            want = pair.decode_oracle(q, lens, sm)
+    else:
+        want = pair.decode_oracle(q, lens, sm)
+    assert_attention_close(got.cpu().numpy(), want)
