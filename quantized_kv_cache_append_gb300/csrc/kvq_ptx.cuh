@@ -43,6 +43,14 @@ static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// A hint to bring bytes [src, src + bytes) into L2 (16-byte aligned, a
+// multiple of 16 bytes); no data moves to the SM and nothing waits on it.
+static __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 static __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
