@@ -588,7 +588,8 @@ def _chunk_attn_bench(torch, kvq):
     return {"workload": "4096-token chunk over 131072 cells, 32/8 heads, head_dim 128",
             "ms": round(ms, 3), "TFLOP/s": round(tflops, 1), "peak_TFLOP/s": peak,
             "peak_kind": kind, "frac": round(tflops / peak, 4),
-            "note": "mma.sync m16n8k16 with fp16 hi+lo q and p: 2 MMAs per algorithmic one"}
+            "note": "tcgen05 MMAs (fp32 accumulators in tensor memory); q as fp16 hi+lo "
+                    "(two MMAs for q.k), p as one fp16 value (one MMA for p.v)"}
 
 
 def _decode_sources_sha() -> str:

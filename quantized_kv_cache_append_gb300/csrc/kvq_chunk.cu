@@ -37,6 +37,7 @@
 
 #include "kvq_internal.cuh"
 #include "kvq_ptx.cuh"
+#include "kvq_tc.cuh"
 
 namespace kvq {
 namespace {
@@ -323,14 +324,292 @@ __global__ void __launch_bounds__(kThr, HD == 64 ? 4 : (HD == 128 ? 2 : 1))
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// head_dim 128 on the fifth-generation tensor cores (tcgen05, TMEM).
+//
+// One CTA per (128 query rows, KV head), six warps:
+//   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads
+//              its row of S from tensor memory, masks, keeps the running
+//              maximum (raised lazily; the rare raise rescales its row of O
+//              in tensor memory after the previous P V has finished), writes
+//              P = 2^(S - m) as fp16 over the first 64 columns of the same
+//              S buffer, and at the end divides its row of O by the sum.
+//   warp 4     TMA producer: 128-key K and V tiles (two stages each).
+//   warp 5     allocates the 512 TMEM columns and issues the MMAs from one
+//              thread: S_j = Q K_j^T (M = N = 128, fp32 in TMEM, three S
+//              buffers) as Q_hi K^T + Q_lo K^T, and O += P_j V_j with P read
+//              from tensor memory and V as an MN-major operand.
+// The issue order S_0, S_1, PV_0, S_2, PV_1, S_3, ... keeps the tensor pipe
+// fed while the softmax of one tile overlaps the MMAs of its neighbours.
+// q * sm_scale * log2(e) enters as fp16 hi + lo (the logits need the bits:
+// K's large channels magnify q's rounding), p as one fp16 value.
+// ---------------------------------------------------------------------------
+namespace tcc {
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int HDT = 128;
+constexpr int kSoftWarps = 4;
+constexpr int kProdWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 192;
+constexpr int SPAN_B = BN * 128;            // one 128-byte span of a 128-row tile
+constexpr int TILE_B = 2 * SPAN_B;          // 128 rows x 256 bytes
+constexpr int OFF_QH = 0, OFF_QL = TILE_B;  // q hi / lo, [span][row][128 B], 128-byte swizzle
+constexpr int OFF_K = 2 * TILE_B;           // two K stages
+constexpr int OFF_V = OFF_K + 2 * TILE_B;   // two V stages
+constexpr int OFF_BAR = OFF_V + 2 * TILE_B;
+// barriers
+constexpr int KFULL = 0, KEMPTY = 2, VFULL = 4, VEMPTY = 6, SFULL = 8, PFULL = 11, SFREE = 14,
+              ODONE = 17, QREADY = 18, NBAR = 19;
+constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
+constexpr int SMEM = OFF_TSLOT + 16 + 1024;   // + alignment slack
+constexpr uint32_t TMEM_COLS = 512;             // S buffers at columns 0, 128, 256; O at 384
+constexpr uint32_t COL_O = 384;
+static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+
+// byte offset of (row r, byte b) of a [span][128 rows][128 B] tile
+__device__ __forceinline__ uint32_t sw(int r, int b) {
+  return (uint32_t)((b >> 7) * SPAN_B + r * 128) + ((uint32_t)(((b >> 4) & 7) ^ (r & 7)) << 4) +
+         (uint32_t)(b & 15);
+}
+}  // namespace tcc
+
+__global__ void __launch_bounds__(tcc::kThreads, 1)
+    chunk_attn_tc(const __grid_constant__ ChunkMaps maps, ChunkArgs a) {
+  using namespace tcc;
+  constexpr float kNegInf = -INFINITY;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.y;
+  const int r0 = blockIdx.x * BM;
+  const int n_rows = a.T * a.G;
+  const int P0 = a.P - a.T;                 // cells before the chunk
+  const int t_last = min(a.T - 1, (min(r0 + BM, n_rows) - 1) / a.G);
+  const int n_tiles = (P0 + t_last + 1 + BN - 1) / BN;   // key tiles the CTA's rows see
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(KFULL + i), 1);
+      mbar_init(bar(KEMPTY + i), 1);
+      mbar_init(bar(VFULL + i), 1);
+      mbar_init(bar(VEMPTY + i), 1);
+    }
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(bar(SFULL + i), 1);
+      mbar_init(bar(PFULL + i), kSoftWarps * 32);
+      mbar_init(bar(SFREE + i), 1);
+    }
+    mbar_init(bar(ODONE), 1);
+    mbar_init(bar(QREADY), kSoftWarps * 32);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) tmem_alloc(sbase + OFF_TSLOT, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TSLOT);
+  bool lost = false;
+
+  if (warp == kProdWarp) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.k[0])) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.v[0])) : "memory");
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j & 1;
+        const int row = kvh * a.P + j * BN;
+        if (j >= 2 && !mbar_wait(bar(KEMPTY + s), ((j >> 1) - 1) & 1)) break;
+        mbar_expect_tx(bar(KFULL + s), (uint32_t)TILE_B);
+        tma_load_2d(sbase + OFF_K + s * TILE_B, &maps.k[0], 0, row, bar(KFULL + s));
+        tma_load_2d(sbase + OFF_K + s * TILE_B + SPAN_B, &maps.k[1], 0, row, bar(KFULL + s));
+        if (j >= 2 && !mbar_wait(bar(VEMPTY + s), ((j >> 1) - 1) & 1)) break;
+        mbar_expect_tx(bar(VFULL + s), (uint32_t)TILE_B);
+        tma_load_2d(sbase + OFF_V + s * TILE_B, &maps.v[0], 0, row, bar(VFULL + s));
+        tma_load_2d(sbase + OFF_V + s * TILE_B + SPAN_B, &maps.v[1], 0, row, bar(VFULL + s));
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t IS = umma_idesc_f16(BM, BN, false, false);   // Q, K both K-major
+      constexpr uint32_t IO = umma_idesc_f16(BM, HDT, false, true);   // P (TMEM), V MN-major
+      auto issue_s = [&](int j) -> bool {
+        const int s = j & 1, b = j % 3;
+        if (!mbar_wait(bar(KFULL + s), (j >> 1) & 1)) return false;
+        if (j >= 3 && !mbar_wait(bar(SFREE + b), (j / 3 - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)b * 128;
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+          for (int kk = 0; kk < HDT / 16; ++kk) {
+            const uint32_t off = (uint32_t)(kk >> 2) * SPAN_B + (uint32_t)(kk & 3) * 32;
+            umma_ss(d, umma_desc_sw128(sbase + (hl ? OFF_QL : OFF_QH) + off, 16, 1024),
+                    umma_desc_sw128(sbase + OFF_K + s * TILE_B + off, 16, 1024), IS, hl + kk > 0);
+          }
+        umma_commit(bar(SFULL + b));
+        umma_commit(bar(KEMPTY + s));
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j & 1, b = j % 3;
+        if (!mbar_wait(bar(PFULL + b), (j / 3) & 1)) return false;
+        if (!mbar_wait(bar(VFULL + s), (j >> 1) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys: P columns 8 kk .. + 7, two V atoms
+          umma_ts(tmem + COL_O, tmem + (uint32_t)b * 128 + (uint32_t)kk * 8,
+                  umma_desc_sw128(sbase + OFF_V + s * TILE_B + kk * 2048, SPAN_B, 1024), IO,
+                  j > 0 || kk > 0);
+        umma_commit(bar(SFREE + b));
+        umma_commit(bar(VEMPTY + s));
+        umma_commit(bar(ODONE));
+        return true;
+      };
+      bool ok = mbar_wait(bar(QREADY), 0);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0) && (n_tiles < 2 || issue_s(1));
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        ok = issue_pv(j);
+        if (ok && j + 2 < n_tiles) ok = issue_s(j + 2);
+      }
+    }
+  } else {
+    // ---------------- softmax warps: thread = query row ----------------
+    const int row = threadIdx.x;
+    const int gr = r0 + row;
+    const bool valid = gr < n_rows;
+    const int tok = valid ? gr / a.G : 0;
+    const int gg = valid ? gr - tok * a.G : 0;
+    const int lim = valid ? P0 + tok : -1;                  // last key this row sees
+    {
+      // q * sm_scale * log2(e) -> fp16 hi + lo rows of the A operand
+      const float* qrow = a.q + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HDT;
+#pragma unroll 4
+      for (int c = 0; c < HDT / 8; ++c) {
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (valid) {
+          x0 = __ldg(reinterpret_cast<const float4*>(qrow + 8 * c));
+          x1 = __ldg(reinterpret_cast<const float4*>(qrow + 8 * c + 4));
+        }
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          split_pair(x[2 * e] * a.qscale, x[2 * e + 1] * a.qscale, hi[e], lo[e]);
+        *reinterpret_cast<uint4*>(smem + OFF_QH + sw(row, c * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + OFF_QL + sw(row, c * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(QREADY)) : "memory");
+    }
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m = -1e30f, l = 0.f;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j % 3;
+      lost = __any_sync(kAll, !mbar_wait(bar(SFULL + b), (j / 3) & 1));
+      if (lost) break;
+      tc_fence_after();
+      float sv[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32)
+        tmem_ld32(tmem + lane_base + (uint32_t)b * 128 + c0, *reinterpret_cast<uint32_t(*)[32]>(sv + c0));
+      tmem_wait_ld();
+      const int key0 = j * BN;
+      if (key0 + BN - 1 > lim) {   // keys past this row's causal limit
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (key0 + c > lim) sv[c] = kNegInf;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+      const bool rise = mx > m + kTauC;
+      float alpha = 1.f;
+      if (rise) {
+        alpha = fast_exp2(m - mx);   // 0 from the finite start
+        m = mx;
+        l *= alpha;
+      }
+      if (j > 0 && __any_sync(kAll, rise)) {
+        // O holds P V of the tiles so far: wait for the last one, rescale
+        lost = __any_sync(kAll, !mbar_wait(bar(ODONE), (j - 1) & 1));
+        if (lost) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < HDT; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + COL_O + c0, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(tmem + lane_base + COL_O + c0, ov);
+        }
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {   // keys 64 h .. + 63 -> P columns 32 h .. + 31
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = fast_exp2(sv[64 * h + 2 * e] - m);
+          const float p1 = fast_exp2(sv[64 * h + 2 * e + 1] - m);
+          sum += p0 + p1;
+          pk[e] = pack_half2(p0, p1);
+        }
+        tmem_st32(tmem + lane_base + (uint32_t)b * 128 + 32 * h, pk);
+      }
+      l += sum;
+      tmem_wait_st();
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(PFULL + b)) : "memory");
+    }
+    if (!lost && n_tiles > 0) lost = __any_sync(kAll, !mbar_wait(bar(ODONE), (n_tiles - 1) & 1));
+    tc_fence_after();
+    float* orow = a.out + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HDT;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < HDT; c0 += 32) {
+      uint32_t ov[32];
+      tmem_ld32(tmem + lane_base + COL_O + c0, ov);
+      tmem_wait_ld();
+      if (valid) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          float4 r4 = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                  __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+          if (lost) {
+            const float nan = __int_as_float(0x7fc00000);
+            r4 = make_float4(nan, nan, nan, nan);
+          }
+          *reinterpret_cast<float4*>(orow + c0 + e) = r4;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // One 2D tensor map per 128-byte span of a staging row: [n_kv * P rows]
-// [128 bytes], row stride HD * 2 bytes, box 128 bytes x 64 rows.
-bool make_span_map(CUtensorMap* map, const void* base, int sp, long long rows, int row_bytes) {
+// [128 bytes], row stride HD * 2 bytes, box 128 bytes x box_rows rows.
+bool make_span_map(CUtensorMap* map, const void* base, int sp, long long rows, int row_bytes,
+                   int box_rows = kBN) {
   auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  const cuuint32_t box[2] = {128, (cuuint32_t)kBN};
+  const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   void* span = static_cast<char*>(const_cast<void*>(base)) + (size_t)sp * 128;
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, span, dims, strides, box, estr,
@@ -364,12 +643,38 @@ cudaError_t launch_hd(const ChunkArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+
+// head_dim 128: the tcgen05 kernel, one CTA of 192 threads per (128 rows,
+// KV head), 128-key tiles.
+cudaError_t launch_tc128(const ChunkArgs& a, cudaStream_t s) {
+  static ContextCache<int> limit_set;
+  int done = 0;
+  if (!per_context(limit_set, &done, [](int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(chunk_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    tcc::SMEM) == cudaSuccess;
+      }))
+    return cudaErrorInvalidConfiguration;
+  ChunkMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const long long rows = (long long)a.n_kv * a.P;
+  for (int sp = 0; sp < 2; ++sp) {
+    if (!make_span_map(&maps.k[sp], a.k16, sp, rows, 256, tcc::BN) ||
+        !make_span_map(&maps.v[sp], a.v16, sp, rows, 256, tcc::BN))
+      return cudaErrorInvalidValue;
+  }
+  const long long row_tiles = ((long long)a.T * a.G + tcc::BM - 1) / tcc::BM;
+  if (row_tiles > 0x7fffffffLL || a.n_kv > 65535) return cudaErrorInvalidValue;
+  chunk_attn_tc<<<dim3((unsigned)row_tiles, (unsigned)a.n_kv), tcc::kThreads, tcc::SMEM, s>>>(maps, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_chunk_attn(int hd, const ChunkArgs& a, cudaStream_t s) {
   switch (hd) {
     case 64: return launch_hd<64>(a, s);
-    case 128: return launch_hd<128>(a, s);
+    case 128: return launch_tc128(a, s);
     case 256: return launch_hd<256>(a, s);
     default: return cudaErrorInvalidValue;
   }
