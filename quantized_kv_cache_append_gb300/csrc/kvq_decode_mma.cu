@@ -30,7 +30,8 @@
 //               (Walsh-Hadamard, / HD) before it is written.
 //
 // q and p enter the tensor cores as fp16 hi + lo pairs (about 22 significant
-// bits), K and V as exact fp16 values.
+// bits), K and V as exact fp16 values.  The copies carry an evict-first L2
+// policy: the cache is read once per call.
 //
 // The CTA's 4 warps merge their states through shared memory into one
 // partial (o, m, l) per row of the split; the combine kernel below merges
@@ -307,6 +308,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   const int n_pieces = kTC >> pc_log2;
   const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
   const bool producer = threadIdx.x == 0;
+  // the cache is read once per call: its lines leave L2 first
+  const uint64_t pol = l2_evict_first_policy();
   // Let the combine grid be scheduled as soon as SMs free up; it still waits
   // (griddepcontrol.wait) for this whole grid to finish before reading.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -352,18 +355,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
       for (int sp = 0; sp < C::NCH; ++sp) {
         const uint32_t so = (uint32_t)(sp * kTC + (p << pc_log2)) * C::SWB;
-        tma_load_2d(st + so, &maps.k[sp], 0, row, full);
+        tma_load_2d_hint(st + so, &maps.k[sp], 0, row, full, pol);
       }
 #pragma unroll
       for (int sp = 0; sp < C::VNCH; ++sp) {
         const uint32_t so = (uint32_t)(sp * kTC + (p << pc_log2)) * C::VSWB;
-        tma_load_2d(st + C::OFF_V + so, &maps.v[sp], 0, row, full);
+        tma_load_2d_hint(st + C::OFF_V + so, &maps.v[sp], 0, row, full, pol);
       }
       if constexpr (C::KI8) {
         const uint32_t sbk = (uint32_t)pc * C::NG * 2, sbv = (uint32_t)pc * C::VNS * 2;
         const uint32_t sc = sbase + C::SMEM_SC + (uint32_t)s * C::SC_STAGE_B;
-        bulk_load(sc + (uint32_t)p * sbk, a.pool.ks + (size_t)row * C::NG, sbk, full);
-        bulk_load(sc + C::KSCALE_B + (uint32_t)p * sbv, a.pool.vs + (size_t)row * C::VNS, sbv, full);
+        bulk_load_hint(sc + (uint32_t)p * sbk, a.pool.ks + (size_t)row * C::NG, sbk, full, pol);
+        bulk_load_hint(sc + C::KSCALE_B + (uint32_t)p * sbv, a.pool.vs + (size_t)row * C::VNS, sbv, full, pol);
       }
     }
   };

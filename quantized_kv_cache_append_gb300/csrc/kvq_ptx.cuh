@@ -1,5 +1,6 @@
 // kvq_ptx.cuh -- small inline-PTX wrappers shared by the library's kernels:
-// mbarrier waits with a poll limit, TMA and bulk copies into shared memory,
+// mbarrier waits with a poll limit, TMA and bulk copies into shared memory
+// (with an optional L2 eviction policy),
 // ldmatrix / movmatrix, mma.sync.m16n8k16 (f16 in, f32 accumulate), byte
 // permutes and fp16 pair arithmetic.  Each is one or two PTX instructions.
 #pragma once
@@ -66,6 +67,34 @@ static __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, 
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// An L2 policy that marks the lines a copy brings in as the first to go:
+// for data read once (a cache streamed by decode), so it does not push out
+// the small inputs and partials that later kernels read again.
+static __device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tma_load_2d / bulk_load with an L2 cache policy
+static __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                        uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+static __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                                      uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
       : "memory");
 }
 
