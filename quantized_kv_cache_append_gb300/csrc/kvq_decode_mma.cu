@@ -244,18 +244,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.k[0])) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.v[0])) : "memory");
-    // One sequence: while the previous kernel finishes, the first tile of
-    // this CTA's split is brought into L2.  Only a hint: the block id read
-    // here may still change before the wait below (the copies read it
-    // again after the wait), and a prefetch of the wrong rows costs
-    // bandwidth, nothing else.
+    // One sequence: while the previous kernel finishes, the first two tiles
+    // of this CTA's split are brought into L2.  Only a hint: the block
+    // ids read here may still change before the wait below (the copies
+    // read them again after the wait), and a prefetch of the wrong rows
+    // costs bandwidth, nothing else.
     if (a.n_seq == 1 && a.n_rt == 1) {
       const int split0 = (int)blockIdx.x / a.pool.n_kv, kvh0 = (int)blockIdx.x - split0 * a.pool.n_kv;
       const int c0 = split0 * a.split_cells;
       const int pcl = a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6;
       const int cap = clamp_len_mma(INT_MAX, a);   // cells the table row can address
       if (c0 < cap) {
-        for (int p = 0; p < (kTC >> pcl) && c0 + (p << pcl) < cap; ++p) {
+        constexpr int kPrefetchTiles = 2;
+        for (int p = 0; p < kPrefetchTiles * (kTC >> pcl) && (p << pcl) < a.split_cells && c0 + (p << pcl) < cap;
+             ++p) {
           const int blk = a.block_table[(c0 + (p << pcl)) >> a.pool.bs_log2];
           if (blk < 0 || blk >= a.pool.n_blocks) continue;
           const size_t row =
