@@ -3,8 +3,8 @@
 Workload (one step): batch 1, 32 query / 8 KV heads, head_dim 128, a
 32768-cell context; append one cell (K and V) and decode one token, on an
 FP16 cache and on an int8 cache (both formats every step).  The context
-grows by one cell per step for 64 steps, as the workload states.  Eight
-layer caches (8 x 203 MB = 1.6 GB, far above the 129 MB L2) are visited in
+grows by one cell per step for 64 steps, as the workload states.  32 layer
+caches (32 x 203 MB = 6.5 GB, far above the 129 MB L2) are visited in
 turn, so no step reads a cache that is still in L2.
 
 Printed: one JSON line.  `value` = cache bytes the two decodes read per step
@@ -13,7 +13,10 @@ The timed region replays CUDA graphs of the captured steps (the library's C
 entry points, called through the binding while capturing); `e2e` repeats
 the measurement through the same public calls without graphs, with the
 step's inputs copied from pinned host memory (one packed copy) and both
-outputs read back (one copy) every step.  `--impl reference` times the CPU oracle on the same workload.
+outputs read back (one copy) every step, and once more from plain C
+(tests/e2e_host.c: the same calls through the C ABI and the CUDA runtime),
+so that the record splits its host cost into the binding's share and the
+rest.  `--impl reference` times the CPU oracle on the same workload.
 
 Beside the step (not in `value`): the K8V4 format (int8 K, rotated 4-bit V)
 on the same workload -- decode, one-cell and bulk append, compaction and
@@ -188,10 +191,13 @@ def run_kvq(args):
     from quantized_kv_cache_append_gb300.pool import PagedPool, row_layout
 
     rank, world, local = _dist()
+    kvq.build()
+    # the e2e step from plain C runs first, while this process holds no CUDA
+    # context on the device (a second live context slowed it 18x)
+    c_leg = _e2e_c_leg(min(args.steps, 512), min(args.warmup, 32), local) if rank == 0 else None
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    kvq.build()
     kvq.load_library()
 
     wl = workloads.make("gqa32k")
@@ -399,6 +405,18 @@ def run_kvq(args):
     # end to end through the public calls, host buffers, no graphs
     e2e = _e2e(step_fn=None, torch=torch, layers=layers, wl=wl, bt=bt, cap=cap, L=L,
                n_kv=n_kv, hd=hd, K=min(K, 512), W=min(W, 32), world=world, dist=dist)
+    if rank == 0:
+        ok = "ms_per_step" in c_leg
+        e2e["breakdown"] = {
+            "device_ms_per_step": round(ms / K, 4),
+            "c_abi": c_leg,
+            "binding_ms_per_step": round(e2e["ms_per_step"] - c_leg["ms_per_step"], 4) if ok else None,
+            "note": ("device: the step's kernels in CUDA graphs; c_abi: the same e2e step from plain C "
+                     "(tests/e2e_host.c) through the C ABI, host buffers, no graphs, with its host "
+                     "microseconds per step in the copies' enqueue, the four library calls and the "
+                     "synchronize; binding: this e2e leg minus the C one (ctypes marshalling and the "
+                     "Python around the calls)"),
+        }
 
     result = None
     if rank == 0:
@@ -626,6 +644,30 @@ def _ncu_traffic(fmt: str):
         return int(float(fields[f"traffic_bytes_per_launch_{fmt}"]))
     except Exception:
         return None
+
+
+def _e2e_c_leg(K: int, W: int, device: int) -> dict:
+    """The e2e step driven from plain C (tests/e2e_host.c) through the C ABI
+    and the CUDA runtime, in its own process with caches of the same
+    geometry: its printed name-value pairs (ms_per_step and the host time
+    split), or {"error": why} if it cannot be built or run."""
+    import importlib
+    kb = importlib.import_module("quantized_kv_cache_append_gb300.build")   # the module, not build()
+    src = os.path.join(ROOT, "tests", "e2e_host.c")
+    exe = os.path.join(kb.BUILD_DIR, "e2e_host")
+    r = subprocess.run([kb._nvcc(), "-O2", "-o", exe, src, "-I", kb.INCLUDE, "-L", kb.BUILD_DIR, "-lkvq",
+                        "-Xlinker", f"-rpath,{kb.BUILD_DIR}"], capture_output=True, text=True)
+    if r.returncode != 0:
+        return {"error": "build: " + (r.stderr or r.stdout).strip()[-200:]}
+    try:
+        r = subprocess.run([exe, str(K), str(W), str(LAYERS), str(device)], capture_output=True,
+                           text=True, timeout=900)
+    except subprocess.TimeoutExpired:
+        return {"error": "timed out"}
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip()[-200:]}
+    f = r.stdout.split()
+    return {k: round(float(v), 4) for k, v in zip(f[::2], f[1::2])}
 
 
 def _e2e(step_fn, torch, layers, wl, bt, cap, L, n_kv, hd, K, W, world, dist):

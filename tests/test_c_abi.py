@@ -49,3 +49,22 @@ def test_residency_plan_from_c(program):
     # the row's entries: blocks 4, 1, 5 in slots 0, 1, 2; block 2 not resident
     assert program["slots"].split() == ["0", "1", "2", "-1"]
     assert program["again"].split() == ["0", "fetch", "0", "hits", "3"]
+
+
+def test_e2e_host_program_builds_and_refuses_bad_arguments(tmp_path):
+    """tests/e2e_host.c (the bench's end-to-end step from plain C) compiles
+    against the header and the library; without arguments it prints its
+    usage and exits 1 before touching a device."""
+    import importlib
+    kb = importlib.import_module("quantized_kv_cache_append_gb300.build")   # the module, not build()
+    if not os.path.exists(kb._nvcc()):
+        pytest.skip("no nvcc")
+    kvq.build()
+    exe = str(tmp_path / "e2e_host")
+    subprocess.run([kb._nvcc(), "-O2", "-o", exe, os.path.join(ROOT, "tests", "e2e_host.c"), "-I",
+                    kb.INCLUDE, "-L", kb.BUILD_DIR, "-lkvq", "-Xlinker", f"-rpath,{kb.BUILD_DIR}"],
+                   check=True, capture_output=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 1 and "usage" in r.stderr
+    r = subprocess.run([exe, "0", "1", "1"], capture_output=True, text=True)
+    assert r.returncode == 1
