@@ -526,9 +526,18 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (key0 + c > lim) sv[c] = kNegInf;
       }
-      float mx = sv[0];
+      // the row maximum and (below) the row sum over 8 independent
+      // chains: a single chain of 127 dependent steps is what one warp per
+      // scheduler cannot hide
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+      for (int e = 0; e < 8; ++e) mx8[e] = sv[e];
+#pragma unroll
+      for (int c = 8; c < BN; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], sv[c + e]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const bool rise = mx > m + kTauC;
       float alpha = 1.f;
       if (rise) {
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
           tmem_st32(tmem + lane_base + COL_O + c0, ov);
         }
       }
-      float sum = 0.f;
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {   // keys 64 h .. + 63 -> P columns 32 h .. + 31
         uint32_t pk[32];
@@ -559,12 +568,12 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
         for (int e = 0; e < 32; ++e) {
           const float p0 = fast_exp2(sv[64 * h + 2 * e] - m);
           const float p1 = fast_exp2(sv[64 * h + 2 * e + 1] - m);
-          sum += p0 + p1;
+          sum8[e & 7] += p0 + p1;
           pk[e] = pack_half2(p0, p1);
         }
         tmem_st32(tmem + lane_base + (uint32_t)b * 128 + 32 * h, pk);
       }
-      l += sum;
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tmem_wait_st();
       tc_fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(PFULL + b)) : "memory");
