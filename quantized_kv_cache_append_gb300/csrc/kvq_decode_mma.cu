@@ -59,7 +59,8 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = kConsumerWarps * 32;  // thread 0 also issues the copies
-constexpr int kTC = 64;                      // cells per pipeline stage
+constexpr int kTC = 64;                      // cells per pipeline stage (a piece index is
+                                             // split by shifts: 64 = 2^6)
 constexpr int kCellsPerWarp = kTC / kConsumerWarps;
 constexpr float kTau = 8.0f;                 // lazy rescale threshold (log2 units)
 constexpr unsigned kFull = 0xffffffffu;
@@ -148,6 +149,14 @@ __device__ __forceinline__ uint32_t swz_off(int c, int b, int sw) {
 template <int FMT, int HD>
 __device__ __forceinline__ uint32_t tile_off(int c, int b) {
   return swz_off(c, b, Cfg<FMT, HD, 1>::SWB);
+}
+
+// r / G for a query row index r (r < 32 <= 2^32 / G): a multiply by the
+// host's ceil(2^32 / G) instead of a division by a run-time value, which
+// sat on the path to each CTA's first copy (8 q loads a thread, each with
+// a row index to divide)
+__device__ __forceinline__ int div_g(const DecodeArgs& a, int r) {
+  return (int)(((unsigned long long)(unsigned)r * a.g_magic) >> 32);
 }
 
 __device__ __forceinline__ int clamp_len_mma(int L, const DecodeArgs& a) {
@@ -399,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         dim = 16 * ks + 4 * tt + 2 * hi8 + e;
       }
       if (r < Rc) {
-        const int w = (r0 + r) / a.G, gg = r0 + r - w * a.G;
+        const int w = div_g(a, r0 + r), gg = r0 + r - w * a.G;
         qv[u] = __ldg(a.q + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD + dim);
       }
     }
@@ -409,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   for (int u = 0; u < BPT; ++u) {
     const int i = threadIdx.x + u * kThreads;
     bv[u] = (blk_in_smem && i < n_entries)
-                ? block_of(a, bt, c_begin + (i / n_pieces) * kTC + ((i % n_pieces) << pc_log2), c_end)
+                ? block_of(a, bt, c_begin + (i >> (6 - pc_log2)) * kTC + ((i & (n_pieces - 1)) << pc_log2), c_end)
                 : -1;
   }
   bool lost = false;
@@ -535,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int r = row_of(nt, j);
-      row_last[nt][j] = r < Rc ? L - a.W + (r0 + r) / a.G : -1;
+      row_last[nt][j] = r < Rc ? L - a.W + div_g(a, r0 + r) : -1;
     }
 
   int row_last_min = INT_MAX;  // smallest causal limit among this thread's real rows
@@ -1304,7 +1313,7 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_partials(DecodeArg
       const float nan = __int_as_float(0x7fc00000);
       res = make_float4(nan, nan, nan, nan);
     }
-    const int w = r / a.G, gg = r - w * a.G;
+    const int w = div_g(a, r), gg = r - w * a.G;
     *reinterpret_cast<float4*>(a.out + (((size_t)b * a.W + w) * a.n_q + (size_t)kvh * a.G + gg) * HD +
                                d0 + 4 * tid) = res;
   }

@@ -140,6 +140,8 @@ struct DecodeArgs {
   float* ws_ml;        // [n_seq][n_kv][nsplit][R][2]    (running max, sum), log2 domain
   int n_seq, W, n_q, G, R, max_blocks, split_cells, nsplit;
   int RT, n_rt;        // query rows per CTA and CTAs (row tiles) per work item
+  unsigned long long g_magic;  // ceil(2^32 / G): (r * g_magic) >> 32 == r / G for
+                               // every row index r < 2^32 / G (rows are < 32)
   float qscale;        // sm_scale * log2(e): logits come out in the log2 domain
   uint32_t wait_limit; // polls of a copy wait before it is declared lost
   uint32_t extra_tx;   // bytes added to each stage's expected count (0; >0 only
