@@ -233,6 +233,9 @@ kvq_status decode_impl(const kvq_cache* cache, const float* q, int n_seq, int W,
   a.n_q = n_q;
   a.G = n_q / cache->n_kv_heads;
   a.g_magic = (0x100000000ull + (unsigned long long)a.G - 1) / (unsigned long long)a.G;
+  a.div_nkv = make_fastdiv((unsigned)cache->n_kv_heads);
+  a.div_nrt = make_fastdiv((unsigned)plan.n_rt);
+  a.div_split = make_fastdiv((unsigned)plan.split_cells);
   a.R = plan.rows;
   a.RT = plan.rt_rows;
   a.n_rt = plan.n_rt;

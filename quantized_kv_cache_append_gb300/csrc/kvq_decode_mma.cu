@@ -189,7 +189,8 @@ __device__ __forceinline__ bool item_of(const DecodeArgs& a, int c, int& b, int&
       int n = 0, Lb = 0;
       if (bb < a.n_seq) {
         Lb = clamp_len_mma(__ldg(a.ctx_lens + bb), a);
-        n = pass == 0 ? Lb / S * nkv : (Lb % S != 0 ? nkv : 0);
+        const int qs = (int)fdiv((unsigned)Lb, a.div_split);   // Lb / S (Lb >= 0)
+        n = pass == 0 ? qs * nkv : (Lb - qs * S != 0 ? nkv : 0);
       }
       int incl = n;
 #pragma unroll
@@ -205,10 +206,10 @@ __device__ __forceinline__ bool item_of(const DecodeArgs& a, int c, int& b, int&
         const int Ls = __shfl_sync(kFull, Lb, src);
         b = b0 + src;
         if (pass == 0) {
-          split = k / nkv;
+          split = (int)fdiv((unsigned)k, a.div_nkv);
           kvh = k - split * nkv;
         } else {
-          split = Ls / S;
+          split = (int)fdiv((unsigned)Ls, a.div_split);
           kvh = k;
         }
         return true;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
     // read them again after the wait), and a prefetch of the wrong rows
     // costs bandwidth, nothing else.
     if (a.n_seq == 1 && a.n_rt == 1) {
-      const int split0 = (int)blockIdx.x / a.pool.n_kv, kvh0 = (int)blockIdx.x - split0 * a.pool.n_kv;
+      const int split0 = (int)fdiv(blockIdx.x, a.div_nkv), kvh0 = (int)blockIdx.x - split0 * a.pool.n_kv;
       const int c0 = split0 * a.split_cells;
       const int pcl = a.pool.bs_log2 < 6 ? a.pool.bs_log2 : 6;
       const int cap = clamp_len_mma(INT_MAX, a);   // cells the table row can address
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   // (a verify window wider than one CTA's accumulators), one CTA each; the
   // CTAs of an item are neighbours in the grid, so all but the first find
   // the item's K/V tiles in L2.
-  const int item = (int)blockIdx.x / a.n_rt;
+  const int item = (int)fdiv(blockIdx.x, a.div_nrt);
   const int r0 = ((int)blockIdx.x - item * a.n_rt) * a.RT;  // first query row of this CTA
   const int Rc = min(a.RT, a.R - r0);                         // and its row count
   int b, kvh, split;
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
   const bool single = a.n_seq == 1;
   if (single) {
     b = 0;
-    split = item / a.pool.n_kv;
+    split = (int)fdiv((unsigned)item, a.div_nkv);
     kvh = item - split * a.pool.n_kv;
     L_raw = __ldg(a.ctx_lens);
   } else {
@@ -1212,8 +1213,9 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_partials(DecodeArg
   // one sequence: every split slot is written (splits past the context say
   // "no cells"), so the context length need not be read
   const int nlive = a.n_seq == 1 ? a.nsplit
-                                 : (clamp_len_mma(__ldg(a.ctx_lens + b), a) + a.split_cells - 1) /
-                                       a.split_cells;
+                                 : (int)fdiv((unsigned)(clamp_len_mma(__ldg(a.ctx_lens + b), a) +
+                                                        a.split_cells - 1),
+                                             a.div_split);
   const size_t base0 = ((size_t)b * a.pool.n_kv + kvh) * a.nsplit;
 
   float M = kNegInf, lsum = 0.f;

@@ -130,6 +130,29 @@ struct DecodePlan {
   size_t off_o, off_ml, bytes;  // workspace layout
 };
 
+// Division of a 32-bit x by a divisor d fixed per call: q = x / d is the
+// high 64 bits of x * ceil(2^64 / d), exact for every x < 2^64 / d, so for
+// every 32-bit x (d = 1 keeps m = 0 and q = x).  Built on the host; on the
+// device one multiply replaces the instruction sequence of a division by a
+// run-time value.
+struct FastDiv {
+  unsigned long long m;
+  unsigned d;
+};
+
+inline FastDiv make_fastdiv(unsigned d) {
+  FastDiv f;
+  f.d = d;
+  f.m = d <= 1 ? 0ull : ~0ull / d + 1ull;
+  return f;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned fdiv(unsigned x, const FastDiv& f) {
+  return f.d <= 1 ? x : (unsigned)__umul64hi((unsigned long long)x, f.m);
+}
+#endif
+
 struct DecodeArgs {
   Pool pool;
   const float* q;      // [n_seq][W][n_q][hd]
@@ -142,6 +165,7 @@ struct DecodeArgs {
   int RT, n_rt;        // query rows per CTA and CTAs (row tiles) per work item
   unsigned long long g_magic;  // ceil(2^32 / G): (r * g_magic) >> 32 == r / G for
                                // every row index r < 2^32 / G (rows are < 32)
+  FastDiv div_nkv, div_nrt, div_split;  // n_kv, n_rt, split_cells
   float qscale;        // sm_scale * log2(e): logits come out in the log2 domain
   uint32_t wait_limit; // polls of a copy wait before it is declared lost
   uint32_t extra_tx;   // bytes added to each stage's expected count (0; >0 only
