@@ -268,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FMT, HD, NT>::MIN_CTAS)
         constexpr int kPrefetchTiles = 2;
         for (int p = 0; p < kPrefetchTiles * (kTC >> pcl) && (p << pcl) < a.split_cells && c0 + (p << pcl) < cap;
              ++p) {
-          const int blk = a.block_table[(c0 + (p << pcl)) >> a.pool.bs_log2];
+          // read at L2 (no L1 line: the reads after the wait must not
+          // find a copy taken before the previous kernel's writes)
+          const int blk = __ldcg(a.block_table + ((c0 + (p << pcl)) >> a.pool.bs_log2));
           if (blk < 0 || blk >= a.pool.n_blocks) continue;
           const size_t row =
               ((size_t)blk * a.pool.n_kv + kvh0) * (1u << a.pool.bs_log2) + ((c0 + (p << pcl)) & ((1 << a.pool.bs_log2) - 1));
