@@ -580,43 +580,59 @@ def _chunk_attn_bench(torch, kvq):
     at the end of 131072 cells, 32/8 heads, head_dim 128, over fp16 staging;
     synthetic N(0, 1) staging and queries.  Tensor-bound: algorithmic flops
     are 4 * head_dim per (query head, visible cell) -- q.k and p.v -- against
-    the measured dense bf16 peak (fp16 runs at the same nominal rate)."""
-    n_kv, n_q, hd, P, T = 8, 32, 128, 131072, 4096
-    g = torch.Generator(device="cuda").manual_seed(1005)
-    k16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
-    v16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
-    q = torch.randn(T, n_q, hd, device="cuda", generator=g)
-    out = torch.empty_like(q)
-    sm = float(1.0 / np.sqrt(hd))
-
-    def run():
-        st = kvq.kvq_chunk_attn(k16, v16, n_kv, P, hd, q, T, n_q, sm, out)
-        if st != kvq.KVQ_OK:
-            raise RuntimeError(kvq.kvq_status_string(st))
-
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 5
-    a.record()
-    for _ in range(reps):
-        run()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
-    flops = 4.0 * hd * n_q * (T * (P - T) + T * (T + 1) / 2)
-    tflops = flops / (ms * 1e-3) / 1e12
+    the measured dense bf16 peak (fp16 runs at the same nominal rate).  The
+    other head dims the call serves (64 on the same tcgen05 kernel, 256 on
+    the mma.sync one) are timed beside it on a 4096-token chunk over 32768
+    cells (16/4 and 16/2 heads)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             peak, kind = float(json.load(f)["bf16_tflops"]), "measured bf16 dense"
     except Exception:
         peak, kind = 1900.0, "fallback bf16 dense"
+
+    def timed(n_kv, n_q, hd, P, T, seed):
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        k16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
+        v16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
+        q = torch.randn(T, n_q, hd, device="cuda", generator=g)
+        out = torch.empty_like(q)
+        sm = float(1.0 / np.sqrt(hd))
+
+        def run():
+            st = kvq.kvq_chunk_attn(k16, v16, n_kv, P, hd, q, T, n_q, sm, out)
+            if st != kvq.KVQ_OK:
+                raise RuntimeError(kvq.kvq_status_string(st))
+
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        a.record()
+        for _ in range(reps):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        flops = 4.0 * hd * n_q * (T * (P - T) + T * (T + 1) / 2)
+        tflops = flops / (ms * 1e-3) / 1e12
+        return ms, tflops
+
+    ms, tflops = timed(8, 32, 128, 131072, 4096, 1005)
+    others = {}
+    for hd, n_kv, n_q in ((64, 4, 16), (256, 2, 16)):
+        ms_o, tf_o = timed(n_kv, n_q, hd, 32768, 4096, 1005 + hd)
+        kind_k = "tcgen05" if hd == 64 else "mma.sync"
+        others[f"hd{hd}"] = {"workload": f"4096-token chunk over 32768 cells, {n_q}/{n_kv} heads, "
+                                         f"head_dim {hd} ({kind_k})",
+                             "ms": round(ms_o, 3), "TFLOP/s": round(tf_o, 1),
+                             "frac": round(tf_o / peak, 4)}
     return {"workload": "4096-token chunk over 131072 cells, 32/8 heads, head_dim 128",
             "ms": round(ms, 3), "TFLOP/s": round(tflops, 1), "peak_TFLOP/s": peak,
             "peak_kind": kind, "frac": round(tflops / peak, 4),
             "note": "tcgen05 MMAs (fp32 accumulators in tensor memory); q as fp16 hi+lo "
-                    "(two MMAs for q.k), p as one fp16 value (one MMA for p.v)"}
+                    "(two MMAs for q.k), p as one fp16 value (one MMA for p.v)",
+            "other_head_dims": others}
 
 
 def _decode_sources_sha() -> str:

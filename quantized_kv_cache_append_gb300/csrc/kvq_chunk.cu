@@ -8,6 +8,10 @@
 // step appends before it attends), so token t attends to cells
 // [0, P - T + t]; query head h reads KV head h / (n_q / n_kv).
 //
+// Two kernels: head_dim 64 and 128 run on the fifth-generation tensor cores
+// (chunk_attn_tc below); head_dim 256, whose q halves alone would fill an
+// SM's shared memory there, runs on mma.sync (chunk_attn, described here).
+//
 // One CTA of 4 warps per (64 query rows, KV head); a row is a (chunk token,
 // head of the GQA group) pair, so the G heads of a token share every K/V
 // tile.  Each warp owns 16 rows and walks the key tiles its rows can see:
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(kThr, HD == 64 ? 4 : (HD == 128 ? 2 : 1))
 
 
 // ---------------------------------------------------------------------------
-// head_dim 128 on the fifth-generation tensor cores (tcgen05, TMEM).
+// head_dim 64 and 128 on the fifth-generation tensor cores (tcgen05, TMEM).
 //
 // One CTA per (128 query rows, KV head), six warps:
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads
@@ -335,7 +339,8 @@ __global__ void __launch_bounds__(kThr, HD == 64 ? 4 : (HD == 128 ? 2 : 1))
 //              in tensor memory after the previous P V has finished), writes
 //              P = 2^(S - m) as fp16 over the first 64 columns of the same
 //              S buffer, and at the end divides its row of O by the sum.
-//   warp 4     TMA producer: 128-key K and V tiles (two stages each).
+//   warp 4     TMA producer: 128-key K and V tiles (two stages each; a
+//              tile is head_dim / 64 boxes of 128 bytes by 128 rows).
 //   warp 5     allocates the 512 TMEM columns and issues the MMAs from one
 //              thread: S_j = Q K_j^T (M = N = 128, fp32 in TMEM, three S
 //              buffers) as Q_hi K^T + Q_lo K^T, and O += P_j V_j with P read
@@ -348,25 +353,34 @@ __global__ void __launch_bounds__(kThr, HD == 64 ? 4 : (HD == 128 ? 2 : 1))
 namespace tcc {
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int HDT = 128;
 constexpr int kSoftWarps = 4;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 192;
 constexpr int SPAN_B = BN * 128;            // one 128-byte span of a 128-row tile
-constexpr int TILE_B = 2 * SPAN_B;          // 128 rows x 256 bytes
-constexpr int OFF_QH = 0, OFF_QL = TILE_B;  // q hi / lo, [span][row][128 B], 128-byte swizzle
-constexpr int OFF_K = 2 * TILE_B;           // two K stages
-constexpr int OFF_V = OFF_K + 2 * TILE_B;   // two V stages
-constexpr int OFF_BAR = OFF_V + 2 * TILE_B;
 // barriers
 constexpr int KFULL = 0, KEMPTY = 2, VFULL = 4, VEMPTY = 6, SFULL = 8, PFULL = 11, SFREE = 14,
               ODONE = 17, QREADY = 18, NBAR = 19;
-constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
-constexpr int SMEM = OFF_TSLOT + 16 + 1024;   // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;             // S buffers at columns 0, 128, 256; O at 384
 constexpr uint32_t COL_O = 384;
-static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+
+// Shared memory of the head_dim-HD kernel: q hi and lo, two K and two V
+// stages, each a tile of HD / 64 spans ([span][row][128 B], 128-byte
+// swizzle), then the barriers and the tensor-memory address slot.
+template <int HD>
+struct TcLayout {
+  static constexpr int NSP = HD / 64;               // 128-byte spans per row
+  static constexpr int TILE_B = NSP * SPAN_B;       // 128 rows x 2 HD bytes
+  static constexpr int OFF_QH = 0, OFF_QL = TILE_B;
+  static constexpr int OFF_K = 2 * TILE_B;          // two K stages
+  static constexpr int OFF_V = OFF_K + 2 * TILE_B;  // two V stages
+  static constexpr int OFF_BAR = OFF_V + 2 * TILE_B;
+  static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TSLOT + 16 + 1024;   // + alignment slack
+  static_assert(HD == 64 || HD == 128, "q hi + lo and two K and V stages fit one SM up to head_dim 128");
+  static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+  static_assert(COL_O + HD <= TMEM_COLS, "O fits tensor memory beside the three S buffers");
+};
 
 // byte offset of (row r, byte b) of a [span][128 rows][128 B] tile
 __device__ __forceinline__ uint32_t sw(int r, int b) {
@@ -375,9 +389,13 @@ __device__ __forceinline__ uint32_t sw(int r, int b) {
 }
 }  // namespace tcc
 
+template <int HD>
 __global__ void __launch_bounds__(tcc::kThreads, 1)
     chunk_attn_tc(const __grid_constant__ ChunkMaps maps, ChunkArgs a) {
   using namespace tcc;
+  using Lay = TcLayout<HD>;
+  constexpr int TILE_B = Lay::TILE_B, OFF_QH = Lay::OFF_QH, OFF_QL = Lay::OFF_QL, OFF_K = Lay::OFF_K,
+                OFF_V = Lay::OFF_V, OFF_BAR = Lay::OFF_BAR, OFF_TSLOT = Lay::OFF_TSLOT;
   constexpr float kNegInf = -INFINITY;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -424,18 +442,20 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
         const int row = kvh * a.P + j * BN;
         if (j >= 2 && !mbar_wait(bar(KEMPTY + s), ((j >> 1) - 1) & 1)) break;
         mbar_expect_tx(bar(KFULL + s), (uint32_t)TILE_B);
-        tma_load_2d(sbase + OFF_K + s * TILE_B, &maps.k[0], 0, row, bar(KFULL + s));
-        tma_load_2d(sbase + OFF_K + s * TILE_B + SPAN_B, &maps.k[1], 0, row, bar(KFULL + s));
+#pragma unroll
+        for (int sp = 0; sp < Lay::NSP; ++sp)
+          tma_load_2d(sbase + OFF_K + s * TILE_B + sp * SPAN_B, &maps.k[sp], 0, row, bar(KFULL + s));
         if (j >= 2 && !mbar_wait(bar(VEMPTY + s), ((j >> 1) - 1) & 1)) break;
         mbar_expect_tx(bar(VFULL + s), (uint32_t)TILE_B);
-        tma_load_2d(sbase + OFF_V + s * TILE_B, &maps.v[0], 0, row, bar(VFULL + s));
-        tma_load_2d(sbase + OFF_V + s * TILE_B + SPAN_B, &maps.v[1], 0, row, bar(VFULL + s));
+#pragma unroll
+        for (int sp = 0; sp < Lay::NSP; ++sp)
+          tma_load_2d(sbase + OFF_V + s * TILE_B + sp * SPAN_B, &maps.v[sp], 0, row, bar(VFULL + s));
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t IS = umma_idesc_f16(BM, BN, false, false);   // Q, K both K-major
-      constexpr uint32_t IO = umma_idesc_f16(BM, HDT, false, true);   // P (TMEM), V MN-major
+      constexpr uint32_t IO = umma_idesc_f16(BM, HD, false, true);   // P (TMEM), V MN-major
       auto issue_s = [&](int j) -> bool {
         const int s = j & 1, b = j % 3;
         if (!mbar_wait(bar(KFULL + s), (j >> 1) & 1)) return false;
@@ -445,7 +465,7 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
 #pragma unroll
         for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-          for (int kk = 0; kk < HDT / 16; ++kk) {
+          for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (uint32_t)(kk >> 2) * SPAN_B + (uint32_t)(kk & 3) * 32;
             umma_ss(d, umma_desc_sw128(sbase + (hl ? OFF_QL : OFF_QH) + off, 16, 1024),
                     umma_desc_sw128(sbase + OFF_K + s * TILE_B + off, 16, 1024), IS, hl + kk > 0);
@@ -489,9 +509,9 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
     const int lim = valid ? P0 + tok : -1;                  // last key this row sees
     {
       // q * sm_scale * log2(e) -> fp16 hi + lo rows of the A operand
-      const float* qrow = a.q + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HDT;
+      const float* qrow = a.q + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HD;
 #pragma unroll 4
-      for (int c = 0; c < HDT / 8; ++c) {
+      for (int c = 0; c < HD / 8; ++c) {
         float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
         if (valid) {
           x0 = __ldg(reinterpret_cast<const float4*>(qrow + 8 * c));
@@ -551,7 +571,7 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
         if (lost) break;
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < HDT; c0 += 32) {
+        for (int c0 = 0; c0 < HD; c0 += 32) {
           uint32_t ov[32];
           tmem_ld32(tmem + lane_base + COL_O + c0, ov);
           tmem_wait_ld();
@@ -580,10 +600,10 @@ __global__ void __launch_bounds__(tcc::kThreads, 1)
     }
     if (!lost && n_tiles > 0) lost = __any_sync(kAll, !mbar_wait(bar(ODONE), (n_tiles - 1) & 1));
     tc_fence_after();
-    float* orow = a.out + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HDT;
+    float* orow = a.out + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HD;
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-    for (int c0 = 0; c0 < HDT; c0 += 32) {
+    for (int c0 = 0; c0 < HD; c0 += 32) {
       uint32_t ov[32];
       tmem_ld32(tmem + lane_base + COL_O + c0, ov);
       tmem_wait_ld();
@@ -653,28 +673,30 @@ cudaError_t launch_hd(const ChunkArgs& a, cudaStream_t s) {
 }
 
 
-// head_dim 128: the tcgen05 kernel, one CTA of 192 threads per (128 rows,
-// KV head), 128-key tiles.
-cudaError_t launch_tc128(const ChunkArgs& a, cudaStream_t s) {
+// head_dim 64 and 128: the tcgen05 kernel, one CTA of 192 threads per (128
+// rows, KV head), 128-key tiles.
+template <int HD>
+cudaError_t launch_tc(const ChunkArgs& a, cudaStream_t s) {
+  using Lay = tcc::TcLayout<HD>;
   static ContextCache<int> limit_set;
   int done = 0;
   if (!per_context(limit_set, &done, [](int* v) {
         *v = 1;
-        return cudaFuncSetAttribute(chunk_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    tcc::SMEM) == cudaSuccess;
+        return cudaFuncSetAttribute(chunk_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Lay::SMEM) == cudaSuccess;
       }))
     return cudaErrorInvalidConfiguration;
   ChunkMaps maps;
   memset(&maps, 0, sizeof(maps));
   const long long rows = (long long)a.n_kv * a.P;
-  for (int sp = 0; sp < 2; ++sp) {
-    if (!make_span_map(&maps.k[sp], a.k16, sp, rows, 256, tcc::BN) ||
-        !make_span_map(&maps.v[sp], a.v16, sp, rows, 256, tcc::BN))
+  for (int sp = 0; sp < Lay::NSP; ++sp) {
+    if (!make_span_map(&maps.k[sp], a.k16, sp, rows, HD * 2, tcc::BN) ||
+        !make_span_map(&maps.v[sp], a.v16, sp, rows, HD * 2, tcc::BN))
       return cudaErrorInvalidValue;
   }
   const long long row_tiles = ((long long)a.T * a.G + tcc::BM - 1) / tcc::BM;
   if (row_tiles > 0x7fffffffLL || a.n_kv > 65535) return cudaErrorInvalidValue;
-  chunk_attn_tc<<<dim3((unsigned)row_tiles, (unsigned)a.n_kv), tcc::kThreads, tcc::SMEM, s>>>(maps, a);
+  chunk_attn_tc<HD><<<dim3((unsigned)row_tiles, (unsigned)a.n_kv), tcc::kThreads, Lay::SMEM, s>>>(maps, a);
   return cudaGetLastError();
 }
 
@@ -682,8 +704,8 @@ cudaError_t launch_tc128(const ChunkArgs& a, cudaStream_t s) {
 
 cudaError_t launch_chunk_attn(int hd, const ChunkArgs& a, cudaStream_t s) {
   switch (hd) {
-    case 64: return launch_hd<64>(a, s);
-    case 128: return launch_tc128(a, s);
+    case 64: return launch_tc<64>(a, s);
+    case 128: return launch_tc<128>(a, s);
     case 256: return launch_hd<256>(a, s);
     default: return cudaErrorInvalidValue;
   }
