@@ -581,9 +581,9 @@ def _chunk_attn_bench(torch, kvq):
     synthetic N(0, 1) staging and queries.  Tensor-bound: algorithmic flops
     are 4 * head_dim per (query head, visible cell) -- q.k and p.v -- against
     the measured dense bf16 peak (fp16 runs at the same nominal rate).  The
-    other head dims the call serves (64 on the same tcgen05 kernel, 256 on
-    the mma.sync one) are timed beside it on a 4096-token chunk over 32768
-    cells (16/4 and 16/2 heads)."""
+    other head dims the call serves (64 and 256, on the same tcgen05
+    kernel) are timed beside it on a 4096-token chunk over 32768 cells
+    (16/4 and 16/2 heads)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             peak, kind = float(json.load(f)["bf16_tflops"]), "measured bf16 dense"
@@ -622,7 +622,7 @@ def _chunk_attn_bench(torch, kvq):
     others = {}
     for hd, n_kv, n_q in ((64, 4, 16), (256, 2, 16)):
         ms_o, tf_o = timed(n_kv, n_q, hd, 32768, 4096, 1005 + hd)
-        kind_k = "tcgen05" if hd == 64 else "mma.sync"
+        kind_k = "tcgen05"
         others[f"hd{hd}"] = {"workload": f"4096-token chunk over 32768 cells, {n_q}/{n_kv} heads, "
                                          f"head_dim {hd} ({kind_k})",
                              "ms": round(ms_o, 3), "TFLOP/s": round(tf_o, 1),

@@ -71,6 +71,8 @@ def _gpu_chunk(k16, v16, q, sm):
     (oracle.FMT_K8V4, 2, 4, 128, 1000, 128),   # staging of a K8V4 cache (V rotated back)
     (oracle.FMT_F16, 2, 4, 64, 4096, 512),     # head_dim 64 on tensor memory: many key and row tiles
     (oracle.FMT_Q8, 3, 2, 64, 1500, 700),      # head_dim 64, ragged tiles, rows spanning tokens
+    (oracle.FMT_F16, 2, 4, 256, 2000, 400),    # head_dim 256: 64-key tiles, one V stage, many tiles
+    (oracle.FMT_K8V4, 1, 3, 256, 900, 333),    # head_dim 256, G = 3, ragged key and row tiles
 ])
 def test_chunk_matches_oracle(fmt, n_kv, G, hd, P, T):
     k16, v16 = _staging_from_oracle_pool(fmt, n_kv, hd, P, 31 + hd + T)
