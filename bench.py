@@ -862,10 +862,13 @@ def run_profile_case(args):
 
     kvq.build()
     kvq.load_library()
-    if args.profile_workload == "chunk":
+    chunk_cases = {"chunk": (8, 32, 128), "chunk64": (4, 16, 64), "chunk256": (2, 16, 256)}
+    if args.profile_workload in chunk_cases:
         # prompt-chunk attention: a 4096-token chunk over 32768 cells of fp16
-        # staging, 32/8 heads, head_dim 128 (134 MB of staging, above L2)
-        n_kv, n_q, hd, P, T = 8, 32, 128, 32768, 4096
+        # staging; 32/8 heads at head_dim 128 (134 MB of staging, above L2),
+        # 16/4 at 64, 16/2 at 256 (the bench's other head dims)
+        n_kv, n_q, hd = chunk_cases[args.profile_workload]
+        P, T = 32768, 4096
         g = torch.Generator(device="cuda").manual_seed(1005)
         k16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
         v16 = torch.randn(n_kv, P, hd, device="cuda", generator=g).half()
@@ -875,7 +878,7 @@ def run_profile_case(args):
             st = kvq.kvq_chunk_attn(k16, v16, n_kv, P, hd, q, T, n_q, float(1 / np.sqrt(hd)), out)
             assert st == kvq.KVQ_OK, kvq.kvq_status_string(st)
         torch.cuda.synchronize()
-        print(json.dumps({"profile_case": "chunk", "reps": args.profile_reps}))
+        print(json.dumps({"profile_case": args.profile_workload, "reps": args.profile_reps}))
         return
     if args.profile_workload == "stream":
         # block streaming: one gqa32k int8 layer (128 blocks, 70 MB) in a

@@ -204,20 +204,25 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IS = umma_idesc_f16(BM, BN, false, false);   // Q, K both K-major
       constexpr uint32_t IO = umma_idesc_f16(BM, HD, false, true);   // P (TMEM), V MN-major
+      // operand descriptors built once, stepped per MMA by constant offsets
+      const uint64_t dq[2] = {umma_desc_sw128(sbase + OFF_QH, 16, 1024),
+                              umma_desc_sw128(sbase + OFF_QL, 16, 1024)};
+      const uint64_t dk0 = umma_desc_sw128(sbase + OFF_K, 16, 1024);
+      const uint64_t dv0 = umma_desc_sw128(sbase + OFF_V, KSPAN_B, 1024);
       auto issue_s = [&](int j) -> bool {
         const int ks = j % KST, b = j % 3;
         if (!mbar_wait(bar(KFULL + ks), (j / KST) & 1)) return false;
         if (j >= 3 && !mbar_wait(bar(SFREE + b), (j / 3 - 1) & 1)) return false;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * BN);
+        const uint64_t dk = umma_desc_step(dk0, (uint32_t)(ks * KTILE_B));
 #pragma unroll
         for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t in = (uint32_t)(kk & 3) * 32;   // 16 dims: 32 bytes into a span
-            umma_ss(d, umma_desc_sw128(sbase + (hl ? OFF_QL : OFF_QH) + (kk >> 2) * QSPAN_B + in, 16, 1024),
-                    umma_desc_sw128(sbase + OFF_K + ks * KTILE_B + (kk >> 2) * KSPAN_B + in, 16, 1024), IS,
-                    hl + kk > 0);
+            umma_ss(d, umma_desc_step(dq[hl], (kk >> 2) * QSPAN_B + in),
+                    umma_desc_step(dk, (kk >> 2) * KSPAN_B + in), IS, hl + kk > 0);
           }
         umma_commit(bar(SFULL + b));
         umma_commit(bar(KEMPTY + ks));
@@ -228,11 +233,11 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         if (!mbar_wait(bar(PFULL + b), (j / 3) & 1)) return false;
         if (!mbar_wait(bar(VFULL + vs), (j / VST) & 1)) return false;
         tc_fence_after();
+        const uint32_t pa = tmem + (uint32_t)(b * BN);
+        const uint64_t dv = umma_desc_step(dv0, (uint32_t)(vs * KTILE_B));
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys: P columns 8 kk .. + 7, two V atoms
-          umma_ts(tmem + COL_O, tmem + (uint32_t)(b * BN) + (uint32_t)kk * 8,
-                  umma_desc_sw128(sbase + OFF_V + vs * KTILE_B + kk * 2048, KSPAN_B, 1024), IO,
-                  j > 0 || kk > 0);
+          umma_ts(tmem + COL_O, pa + (uint32_t)kk * 8, umma_desc_step(dv, kk * 2048), IO, j > 0 || kk > 0);
         umma_commit(bar(SFREE + b));
         umma_commit(bar(VEMPTY + vs));
         umma_commit(bar(ODONE));
