@@ -52,14 +52,16 @@ struct ChunkMaps {
 //   warp 4     TMA producer of the K tiles (two stages; a tile is
 //              head_dim / 64 boxes of 128 bytes by BN rows, 128-byte
 //              swizzle), and of the V tiles too at head_dim 64 and 128 (two
-//              stages); at 256, V has one stage and warp 6 fetches it.
-//   warp 5     allocates the 512 TMEM columns and issues the MMAs from one
-//              thread: S_j = Q K_j^T (M = 128, N = BN, fp32 in TMEM, three S
-//              buffers) as Q_hi K^T + Q_lo K^T, and O += P_j V_j (N =
-//              head_dim) with P read from tensor memory and V as an MN-major
-//              operand.
-// The issue order S_0, S_1, PV_0, S_2, PV_1, S_3, ... keeps the tensor pipe
-// fed while the softmax of one tile overlaps the MMAs of its neighbours.
+//              stages); at 256, V has one stage and warp 7 fetches it.
+//   warp 5     allocates the 512 TMEM columns; one thread issues
+//              S_j = Q K_j^T (M = 128, N = BN, fp32 in TMEM, three S
+//              buffers) as Q_hi K^T + Q_lo K^T, up to three tiles ahead.
+//   warp 6     one thread issues O += P_j V_j (N = head_dim) with P read
+//              from tensor memory and V as an MN-major operand.
+// Two issuing threads keep the tensor pipe fed: it holds only an MMA or two
+// beyond the last one issued, so while one thread checks its barriers the
+// other's MMAs run, and the softmax of one tile overlaps the MMAs of its
+// neighbours.
 // q * sm_scale * log2(e) enters as fp16 hi + lo (about 22 significant bits:
 // K's large channels magnify q's rounding), K and V as the exact staging
 // values, p as one fp16 value.
@@ -68,16 +70,18 @@ namespace tcc {
 constexpr int BM = 128;
 constexpr int kSoftWarps = 4;
 constexpr int kProdWarp = 4;    // K tiles (and V tiles unless a warp of their own)
-constexpr int kMmaWarp = 5;
-constexpr int kProdWarpV = 6;   // V tiles, when V has a single stage
+constexpr int kMmaWarp = 5;     // S MMAs; owns the tensor memory
+constexpr int kPvWarp = 6;      // P V MMAs
+constexpr int kProdWarpV = 7;   // V tiles, when V has a single stage
 constexpr int QSPAN_B = BM * 128;   // one 128-byte span of the 128 q rows
-// barriers
-// ODONE completes once per P V product (the rescale waits for the previous
-// tile's, when at most that one is still running); ALLDONE once, after the
-// last: when the last p is written, two products can still be running, one
-// more than a parity wait tells apart.
+// barriers.  SFREE[b] completes when the P V product that read S buffer b
+// has (so the rescale of O before tile j's P waits on SFREE[(j - 1) % 3]:
+// never more than one phase behind, as the S MMAs of tile j - 1 waited for
+// the product three tiles before it).  ALLDONE completes once, after the
+// last product: when the last p is written, the last two products can still
+// be running, one more than a parity wait on a per-tile barrier tells apart.
 constexpr int KFULL = 0, KEMPTY = 2, VFULL = 4, VEMPTY = 6, SFULL = 8, PFULL = 11, SFREE = 14,
-              ODONE = 17, QREADY = 18, ALLDONE = 19, NBAR = 20;
+              QREADY = 17, ALLDONE = 18, NBAR = 19;
 constexpr uint32_t TMEM_COLS = 512;
 
 // The head_dim-HD kernel's tiles and memory.  Shared memory: q hi and lo
@@ -91,8 +95,8 @@ template <int HD>
 struct TcLayout {
   static constexpr int BN = HD == 256 ? 64 : 128;     // keys per tile
   static constexpr int KST = 2, VST = HD == 256 ? 1 : 2;
-  static constexpr bool SPLIT_PROD = VST == 1;        // V from warp 6
-  static constexpr int THREADS = SPLIT_PROD ? 224 : 192;
+  static constexpr bool SPLIT_PROD = VST == 1;        // V from warp 7
+  static constexpr int THREADS = SPLIT_PROD ? 256 : 224;
   static constexpr int NSP = HD / 64;                 // 128-byte spans per row
   static constexpr int QTILE_B = NSP * QSPAN_B;       // 128 q rows x 2 HD bytes
   static constexpr int KSPAN_B = BN * 128;            // one span of a key tile
@@ -153,7 +157,6 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       mbar_init(bar(PFULL + i), kSoftWarps * 32);
       mbar_init(bar(SFREE + i), 1);
     }
-    mbar_init(bar(ODONE), 1);
     mbar_init(bar(ALLDONE), 1);
     mbar_init(bar(QREADY), kSoftWarps * 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
   bool lost = false;
 
   if (warp == kProdWarp || (Lay::SPLIT_PROD && warp == kProdWarpV)) {
-    // K tiles from warp 4; V tiles from warp 4 too, or from warp 6 when V has
+    // K tiles from warp 4; V tiles from warp 4 too, or from warp 7 when V has
     // a single stage (its refill waits for P V, which must not hold K back)
     if (lane == 0) {
       const bool do_k = warp == kProdWarp, do_v = !Lay::SPLIT_PROD || warp == kProdWarpV;
@@ -201,18 +204,20 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         (void)mbar_wait(bar(VFULL + j % VST), (j / VST) & 1);
     }
   } else if (warp == kMmaWarp) {
+    // S_j = Q_hi K_j^T + Q_lo K_j^T, up to three tiles ahead of the P V
+    // products (one per S buffer)
     if (lane == 0) {
       constexpr uint32_t IS = umma_idesc_f16(BM, BN, false, false);   // Q, K both K-major
-      constexpr uint32_t IO = umma_idesc_f16(BM, HD, false, true);   // P (TMEM), V MN-major
       // operand descriptors built once, stepped per MMA by constant offsets
       const uint64_t dq[2] = {umma_desc_sw128(sbase + OFF_QH, 16, 1024),
                               umma_desc_sw128(sbase + OFF_QL, 16, 1024)};
       const uint64_t dk0 = umma_desc_sw128(sbase + OFF_K, 16, 1024);
-      const uint64_t dv0 = umma_desc_sw128(sbase + OFF_V, KSPAN_B, 1024);
-      auto issue_s = [&](int j) -> bool {
+      bool ok = mbar_wait(bar(QREADY), 0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
         const int ks = j % KST, b = j % 3;
-        if (!mbar_wait(bar(KFULL + ks), (j / KST) & 1)) return false;
-        if (j >= 3 && !mbar_wait(bar(SFREE + b), (j / 3 - 1) & 1)) return false;
+        ok = mbar_wait(bar(KFULL + ks), (j / KST) & 1) &&
+             (j < 3 || mbar_wait(bar(SFREE + b), (j / 3 - 1) & 1));
+        if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * BN);
         const uint64_t dk = umma_desc_step(dk0, (uint32_t)(ks * KTILE_B));
@@ -226,12 +231,21 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
           }
         umma_commit(bar(SFULL + b));
         umma_commit(bar(KEMPTY + ks));
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
+      }
+    }
+  } else if (warp == kPvWarp) {
+    // O += P_j V_j.  A thread of its own: while it waits for a tile's p,
+    // the S thread keeps the tensor pipe fed, and the other way round (the
+    // pipe holds only an MMA or two beyond the last one issued, so a single
+    // issuing thread's barrier checks left it idle)
+    if (lane == 0) {
+      constexpr uint32_t IO = umma_idesc_f16(BM, HD, false, true);   // P (TMEM), V MN-major
+      const uint64_t dv0 = umma_desc_sw128(sbase + OFF_V, KSPAN_B, 1024);
+      bool ok = true;
+      for (int j = 0; ok && j < n_tiles; ++j) {
         const int vs = j % VST, b = j % 3;
-        if (!mbar_wait(bar(PFULL + b), (j / 3) & 1)) return false;
-        if (!mbar_wait(bar(VFULL + vs), (j / VST) & 1)) return false;
+        ok = mbar_wait(bar(PFULL + b), (j / 3) & 1) && mbar_wait(bar(VFULL + vs), (j / VST) & 1);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t pa = tmem + (uint32_t)(b * BN);
         const uint64_t dv = umma_desc_step(dv0, (uint32_t)(vs * KTILE_B));
@@ -240,17 +254,6 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
           umma_ts(tmem + COL_O, pa + (uint32_t)kk * 8, umma_desc_step(dv, kk * 2048), IO, j > 0 || kk > 0);
         umma_commit(bar(SFREE + b));
         umma_commit(bar(VEMPTY + vs));
-        umma_commit(bar(ODONE));
-        return true;
-      };
-      bool ok = mbar_wait(bar(QREADY), 0);
-      if (ok) {
-        tc_fence_after();
-        ok = issue_s(0) && (n_tiles < 2 || issue_s(1));
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        ok = issue_pv(j);
-        if (ok && j + 2 < n_tiles) ok = issue_s(j + 2);
       }
       if (ok) umma_commit(bar(ALLDONE));   // every product above has completed
     }
@@ -302,17 +305,18 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
           if (key0 + c > lim) sv[c] = kNegInf;
       }
       // the row maximum and (below) the row sum over 8 independent
-      // chains: a single chain of 127 dependent steps is what one warp per
-      // scheduler cannot hide
+      // chains (a single chain of dependent steps is what one warp per
+      // scheduler cannot hide); three-input maxima take two logits a step,
+      // packed fp32 adds two subtractions or sums an instruction
       float mx8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = sv[e];
+      for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(sv[e], sv[8 + e]);
 #pragma unroll
-      for (int c = 8; c < BN; c += 8)
+      for (int c = 16; c < BN; c += 16)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], sv[c + e]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int e = 0; e < 8; ++e) mx8[e] = max3f(mx8[e], sv[c + e], sv[c + 8 + e]);
+      const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const bool rise = mx > m + kTauC;
       float alpha = 1.f;
       if (rise) {
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       }
       if (j > 0 && __any_sync(kAll, rise)) {
         // O holds P V of the tiles so far: wait for the last one, rescale
-        lost = __any_sync(kAll, !mbar_wait(bar(ODONE), (j - 1) & 1));
+        lost = __any_sync(kAll, !mbar_wait(bar(SFREE + (j - 1) % 3), ((j - 1) / 3) & 1));
         if (lost) break;
         tc_fence_after();
 #pragma unroll
@@ -336,14 +340,17 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         }
       }
       float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const float nm = -m;
 #pragma unroll
       for (int h = 0; h < BN / 64; ++h) {   // keys 64 h .. + 63 -> P columns 32 h .. + 31
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = fast_exp2(sv[64 * h + 2 * e] - m);
-          const float p1 = fast_exp2(sv[64 * h + 2 * e + 1] - m);
-          sum8[e & 7] += p0 + p1;
+          float x0, x1;
+          add_f32x2(x0, x1, sv[64 * h + 2 * e], sv[64 * h + 2 * e + 1], nm, nm);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          const int c = 2 * (e & 3);
+          add_f32x2(sum8[c], sum8[c + 1], sum8[c], sum8[c + 1], p0, p1);
           pk[e] = pack_half2(p0, p1);
         }
         tmem_st32(tmem + lane_base + (uint32_t)(b * BN) + 32 * h, pk);
@@ -401,8 +408,8 @@ bool make_span_map(CUtensorMap* map, const void* base, int sp, long long rows, i
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One CTA per (128 query rows, KV head): 192 threads at head_dim 64 and 128,
-// 224 at 256.
+// One CTA per (128 query rows, KV head): 224 threads at head_dim 64 and 128,
+// 256 at 256.
 template <int HD>
 cudaError_t launch_tc(const ChunkArgs& a, cudaStream_t s) {
   using Lay = tcc::TcLayout<HD>;

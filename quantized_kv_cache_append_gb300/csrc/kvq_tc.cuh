@@ -2,8 +2,9 @@
 // (tcgen05) used by the prompt-chunk attention: tensor-memory allocation,
 // MMA with the A operand in shared or tensor memory, commit to an
 // mbarrier, tensor-memory loads and stores, and the shared-memory and
-// instruction descriptors those MMAs take.  Each wrapper is one PTX
-// instruction.
+// instruction descriptors those MMAs take; and two Blackwell arithmetic
+// forms the chunk softmax uses (three-input max, packed fp32 add).  Each
+// wrapper is one PTX instruction.
 #pragma once
 
 #include <stdint.h>
@@ -112,6 +113,23 @@ static __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t 
       "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
       "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+
+// max(a, b, c) in one instruction (three-input form, sm_100 and later).
+static __device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a0 + b0, a1 + b1), each rounded to nearest, in one packed fp32
+// instruction (sm_100 and later).
+static __device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1, float b0,
+                                                 float b1) {
+  asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+      " add.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 static __device__ __forceinline__ void tmem_wait_ld() {
