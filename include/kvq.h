@@ -276,7 +276,7 @@ kvq_status kvq_compact_f16(const kvq_cache *cache, const int32_t *block_table_ro
  * Token t attends to cells [0, P - T + t] (causal); query head h reads KV
  * head h / (n_q / n_kv_heads).  out = softmax(sm_scale * q . K^T) V with
  * fp32 accumulation (q enters the tensor cores as an fp16 hi + lo pair, the
- * softmax weights likewise).  head_dim in {64, 128, 256}; 1 <= T <= P;
+ * softmax weights as one fp16 value).  head_dim in {64, 128, 256}; 1 <= T <= P;
  * n_q a multiple of n_kv_heads; n_kv_heads * P < 2^31.  Invalid arguments
  * return KVQ_ERR_ARG / KVQ_ERR_UNSUPPORTED before any launch.  Asynchronous
  * on `stream`; the library allocates nothing.
