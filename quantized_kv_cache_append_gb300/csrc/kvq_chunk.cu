@@ -80,8 +80,10 @@ constexpr int QSPAN_B = BM * 128;   // one 128-byte span of the 128 q rows
 // the product three tiles before it).  ALLDONE completes once, after the
 // last product: when the last p is written, the last two products can still
 // be running, one more than a parity wait on a per-tile barrier tells apart.
+// SDRAIN / PDRAIN: each issuing thread's last commit, waited on before the
+// tensor memory is freed (after a lost wait too).
 constexpr int KFULL = 0, KEMPTY = 2, VFULL = 4, VEMPTY = 6, SFULL = 8, PFULL = 11, SFREE = 14,
-              QREADY = 17, ALLDONE = 18, NBAR = 19;
+              QREADY = 17, ALLDONE = 18, SDRAIN = 19, PDRAIN = 20, NBAR = 21;
 constexpr uint32_t TMEM_COLS = 512;
 
 // The head_dim-HD kernel's tiles and memory.  Shared memory: q hi and lo
@@ -158,6 +160,8 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       mbar_init(bar(SFREE + i), 1);
     }
     mbar_init(bar(ALLDONE), 1);
+    mbar_init(bar(SDRAIN), 1);
+    mbar_init(bar(PDRAIN), 1);
     mbar_init(bar(QREADY), kSoftWarps * 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -232,6 +236,10 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         umma_commit(bar(SFULL + b));
         umma_commit(bar(KEMPTY + ks));
       }
+      // every MMA this thread issued has completed before the CTA frees the
+      // tensor memory (at once in normal runs; bounded after a lost wait)
+      umma_commit(bar(SDRAIN));
+      (void)mbar_wait(bar(SDRAIN), 0);
     }
   } else if (warp == kPvWarp) {
     // O += P_j V_j.  A thread of its own: while it waits for a tile's p,
@@ -256,6 +264,8 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         umma_commit(bar(VEMPTY + vs));
       }
       if (ok) umma_commit(bar(ALLDONE));   // every product above has completed
+      umma_commit(bar(PDRAIN));
+      (void)mbar_wait(bar(PDRAIN), 0);
     }
   } else {
     // ---------------- softmax warps: thread = query row ----------------
