@@ -141,7 +141,10 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y;
-  const int r0 = blockIdx.x * BM;
+  // row tiles in descending order: the last ones (later tokens) see the
+  // most keys, so the longest CTAs start first and the grid's last, partial
+  // wave holds the shortest
+  const int r0 = (int)(gridDim.x - 1 - blockIdx.x) * BM;
   const int n_rows = a.T * a.G;
   const int P0 = a.P - a.T;                 // cells before the chunk
   const int t_last = min(a.T - 1, (min(r0 + BM, n_rows) - 1) / a.G);

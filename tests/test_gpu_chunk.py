@@ -101,6 +101,27 @@ def test_full_chunk_sampled_tokens():
         assert_attention_close(got[t:t + 1], ref)
 
 
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_chunk_rising_logits(hd):
+    # logits that climb along the keys (a ramp in one K channel, q aligned
+    # with it): the running maximum rises past the lazy threshold every
+    # couple of key tiles, so O is rescaled in tensor memory again and
+    # again, each time after the previous tile's P V has completed
+    n_kv, G, P, T = 2, 4, 2048, 512
+    rng = np.random.default_rng(4242 + hd)
+    k = rng.standard_normal((n_kv, P, hd)).astype(np.float32)
+    v = rng.standard_normal((n_kv, P, hd)).astype(np.float32)
+    sm = _sm(hd)
+    # + 8 in the log2 domain every 256 keys
+    k[:, :, 0] = np.arange(P, dtype=np.float32) * (8.0 / 256) / (sm * np.log2(np.e))
+    q = rng.standard_normal((T, n_kv * G, hd)).astype(np.float32) * 0.1
+    q[:, :, 0] = 1.0
+    k16, v16 = oracle.fp16_bits(k), oracle.fp16_bits(v)
+    got = _gpu_chunk(k16, v16, q, sm)
+    ref = oracle.chunk_attention(k16, v16, q, sm)
+    assert_attention_close(got, ref)
+
+
 def test_chunk_refuses_bad_arguments():
     k = torch.zeros(1, 64, 128, dtype=torch.float16, device="cuda")
     q = torch.zeros(4, 4, 128, device="cuda")
