@@ -11,12 +11,13 @@ Printed: one JSON line.  `value` = cache bytes the two decodes read per step
 (every visible cell, K + V, codes + scales) / step time, over all ranks.
 The timed region replays CUDA graphs of the captured steps (the library's C
 entry points, called through the binding while capturing); `e2e` repeats
-the measurement through the same public calls without graphs, with the
-step's inputs copied from pinned host memory (one packed copy) and both
-outputs read back (one copy) every step, and once more from plain C
-(tests/e2e_host.c: the same calls through the C ABI and the CUDA runtime),
-so that the record splits its host cost into the binding's share and the
-rest.  `--impl reference` times the CPU oracle on the same workload.
+the measurement through the C ABI without graphs (tests/e2e_host.c, plain C
+and the CUDA runtime, in its own process), with the step's inputs copied
+from pinned host memory (one packed copy) and both outputs read back (one
+copy) every step; the same step through the Python binding is timed too,
+and the record splits the host cost into the binding's share and the rest
+(with more than one rank, or without the C leg, `e2e` is the binding's
+leg).  `--impl reference` times the CPU oracle on the same workload.
 
 Beside the step (not in `value`): the K8V4 format (int8 K, rotated 4-bit V)
 on the same workload -- decode, one-cell and bulk append, compaction and
@@ -402,21 +403,39 @@ def run_kvq(args):
     dominant = max(("f16", "q8"), key=kernel_ms.get)   # of the step's two formats
     traffic = _ncu_traffic(dominant)
 
-    # end to end through the public calls, host buffers, no graphs
-    e2e = _e2e(step_fn=None, torch=torch, layers=layers, wl=wl, bt=bt, cap=cap, L=L,
-               n_kv=n_kv, hd=hd, K=min(K, 512), W=min(W, 32), world=world, dist=dist)
+    # end to end, host buffers, no graphs: through the C ABI (the C leg, run
+    # above in its own process) and through the Python binding
+    K_e2e = min(K, 512)
+    e2e_py = _e2e(step_fn=None, torch=torch, layers=layers, wl=wl, bt=bt, cap=cap, L=L,
+                  n_kv=n_kv, hd=hd, K=K_e2e, W=min(W, 32), world=world, dist=dist)
+    e2e = e2e_py
     if rank == 0:
         ok = "ms_per_step" in c_leg
-        e2e["breakdown"] = {
+        breakdown = {
             "device_ms_per_step": round(ms / K, 4),
             "c_abi": c_leg,
-            "binding_ms_per_step": round(e2e["ms_per_step"] - c_leg["ms_per_step"], 4) if ok else None,
-            "note": ("device: the step's kernels in CUDA graphs; c_abi: the same e2e step from plain C "
+            "binding_ms_per_step": round(e2e_py["ms_per_step"] - c_leg["ms_per_step"], 4) if ok else None,
+            "note": ("device: the step's kernels in CUDA graphs; c_abi: the e2e step from plain C "
                      "(tests/e2e_host.c) through the C ABI, host buffers, no graphs, with its host "
                      "microseconds per step in the copies' enqueue, the four library calls and the "
-                     "synchronize; binding: this e2e leg minus the C one (ctypes marshalling and the "
-                     "Python around the calls)"),
+                     "synchronize; binding: the Python binding's leg minus the C one (ctypes "
+                     "marshalling and the Python around the calls)"),
         }
+        if ok and world == 1:
+            # the C ABI leg is the e2e figure: the same steps (context lengths,
+            # layers) as the binding's leg, so the same bytes per step
+            total = sum(_step_ctx(s, L) * n_kv * (_row_bytes(False, hd) + _row_bytes(True, hd))
+                        for s in range(K_e2e))
+            e2e = {"value": round(total / (K_e2e * c_leg["ms_per_step"] * 1e-3) / 1e9, 2),
+                   "unit": "GB/s", "steps": K_e2e,
+                   "h2d_bytes_per_step": int(c_leg["h2d_bytes"]),
+                   "d2h_bytes_per_step": int(c_leg["d2h_bytes"]),
+                   "ms_per_step": c_leg["ms_per_step"],
+                   "path": "C ABI (tests/e2e_host.c), pinned host buffers, copies in the timed region",
+                   "python_binding": {k: e2e_py[k] for k in ("value", "unit", "ms_per_step")}}
+        else:
+            e2e["path"] = "Python binding, pinned host buffers, copies in the timed region"
+        e2e["breakdown"] = breakdown
 
     result = None
     if rank == 0:
@@ -725,13 +744,16 @@ def _e2e(step_fn, torch, layers, wl, bt, cap, L, n_kv, hd, K, W, world, dist):
     h2d = words * 4
     d2h = hout.numel() * 4
 
+    douts = (dout[0], dout[1])   # the two formats' output views, made once
+    hins = [hin[j] for j in range(STEPS_PER_LAYER)]
+
     def one(s):
         j = (s // LAYERS) % STEPS_PER_LAYER
-        din.copy_(hin[j], non_blocking=True)
+        din.copy_(hins[j], non_blocking=True)
         for i, name in enumerate(("f16", "q8")):
             pool, ws, _ = layers[s % LAYERS][name]
             pool.append(dk, dv, seq0, dpos, bt)
-            pool.decode(dq, dctx, cap, bt, wl.sm_scale, out=dout[i], workspace=ws)
+            pool.decode(dq, dctx, cap, bt, wl.sm_scale, out=douts[i], workspace=ws)
         hout.copy_(dout, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 

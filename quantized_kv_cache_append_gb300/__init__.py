@@ -125,13 +125,17 @@ def _ptr(x):
     """Device (or host) address of a tensor / int / None."""
     if x is None:
         return None
+    data_ptr = getattr(x, "data_ptr", None)   # torch tensors: the common case first
+    if data_ptr is not None:
+        return data_ptr()
     if isinstance(x, int):
         return x
-    if hasattr(x, "data_ptr"):
-        return x.data_ptr()
     if hasattr(x, "ctypes") and hasattr(x, "dtype"):   # numpy (host) array
         return x.ctypes.data
     raise TypeError(f"cannot take the address of {type(x)}")
+
+
+_current_stream = None   # () -> cudaStream_t of torch's current stream, set on first use
 
 
 def _stream(stream):
@@ -139,11 +143,16 @@ def _stream(stream):
     current stream on the current device (read without building a Stream
     object, which costs a few microseconds a call)."""
     if stream is None:
-        import torch
-        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-        if raw is not None:
-            return raw(torch.cuda.current_device())
-        return torch.cuda.current_stream().cuda_stream
+        global _current_stream
+        if _current_stream is None:
+            import torch
+            raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
+            if raw is not None:
+                _current_stream = lambda: raw(device())
+            else:
+                _current_stream = lambda: torch.cuda.current_stream().cuda_stream
+        return _current_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
