@@ -18,8 +18,6 @@
 #include <math.h>
 #include <string.h>
 
-#include <mutex>
-
 #include "kvq_internal.cuh"
 #include "kvq_ptx.cuh"
 #include "kvq_tc.cuh"
