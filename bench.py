@@ -638,6 +638,9 @@ def _chunk_attn_bench(torch, kvq):
         return ms, tflops
 
     ms, tflops = timed(8, 32, 128, 131072, 4096, 1005)
+    # a short chunk (the tail of a long prompt): 64 (row tile, KV head)
+    # CTAs, so each one's key tiles are split over a cluster
+    ms_s, tf_s = timed(8, 32, 128, 131072, 256, 1777)
     others = {}
     for hd, n_kv, n_q in ((64, 4, 16), (256, 2, 16)):
         ms_o, tf_o = timed(n_kv, n_q, hd, 32768, 4096, 1005 + hd)
@@ -651,7 +654,10 @@ def _chunk_attn_bench(torch, kvq):
             "peak_kind": kind, "frac": round(tflops / peak, 4),
             "note": "tcgen05 MMAs (fp32 accumulators in tensor memory); q as fp16 hi+lo "
                     "(two MMAs for q.k), p as one fp16 value (one MMA for p.v)",
-            "other_head_dims": others}
+            "other_head_dims": others,
+            "short_chunk": {"workload": "256-token chunk over 131072 cells, 32/8 heads, head_dim 128 "
+                                        "(key tiles split over clusters of CTAs)",
+                            "ms": round(ms_s, 3), "TFLOP/s": round(tf_s, 1), "frac": round(tf_s / peak, 4)}}
 
 
 def _decode_sources_sha() -> str:

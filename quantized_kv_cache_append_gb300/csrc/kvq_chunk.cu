@@ -26,6 +26,7 @@ namespace kvq {
 namespace {
 
 constexpr float kTauC = 8.0f;     // lazy rescale threshold (log2 units)
+constexpr int kMaxKeySplits = 8;  // CTAs of a key-split cluster (the portable maximum)
 constexpr unsigned kAll = 0xffffffffu;
 
 struct ChunkMaps {
@@ -146,7 +147,13 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
   const int n_rows = a.T * a.G;
   const int P0 = a.P - a.T;                 // cells before the chunk
   const int t_last = min(a.T - 1, (min(r0 + BM, n_rows) - 1) / a.G);
-  const int n_tiles = (P0 + t_last + 1 + BN - 1) / BN;   // key tiles the CTA's rows see
+  const int n_all = (P0 + t_last + 1 + BN - 1) / BN;     // key tiles the CTA's rows see
+  // key splits: the gridDim.z CTAs of a (row tile, KV head) form a cluster,
+  // each takes a contiguous share of the key tiles, and they merge at the end
+  const int n_split = (int)gridDim.z;
+  const int per = (n_all + n_split - 1) / n_split;
+  const int j0 = min(n_all, (int)blockIdx.z * per);     // this CTA's first key tile
+  const int n_tiles = min(n_all, j0 + per) - j0;         // and its count (0 possible)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -172,6 +179,15 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TSLOT);
   bool lost = false;
+  // softmax threads: thread = query row (TMEM lane); the running maximum m
+  // and sum l outlive the softmax section for the output and the merge
+  const int row = threadIdx.x;
+  const int gr = r0 + row;
+  const bool valid = row < BM && gr < n_rows;
+  const int tok = valid ? gr / a.G : 0;
+  const int gg = valid ? gr - tok * a.G : 0;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  float m = -1e30f, l = 0.f;
 
   if (warp == kProdWarp || (Lay::SPLIT_PROD && warp == kProdWarpV)) {
     // K tiles from warp 4; V tiles from warp 4 too, or from warp 7 when V has
@@ -183,13 +199,13 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
         const int ks = j % KST, vs = j % VST;
-        const int row = kvh * a.P + j * BN;
+        const int krow = kvh * a.P + (j0 + j) * BN;   // first staging row of the tile
         if (do_k) {
           if (j >= KST && !mbar_wait(bar(KEMPTY + ks), (j / KST - 1) & 1)) break;
           mbar_expect_tx(bar(KFULL + ks), (uint32_t)KTILE_B);
 #pragma unroll
           for (int sp = 0; sp < Lay::NSP; ++sp)
-            tma_load_2d(sbase + OFF_K + ks * KTILE_B + sp * KSPAN_B, &maps.k[sp], 0, row, bar(KFULL + ks));
+            tma_load_2d(sbase + OFF_K + ks * KTILE_B + sp * KSPAN_B, &maps.k[sp], 0, krow, bar(KFULL + ks));
           k_issued = j + 1;
         }
         if (do_v) {
@@ -197,7 +213,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
           mbar_expect_tx(bar(VFULL + vs), (uint32_t)KTILE_B);
 #pragma unroll
           for (int sp = 0; sp < Lay::NSP; ++sp)
-            tma_load_2d(sbase + OFF_V + vs * KTILE_B + sp * KSPAN_B, &maps.v[sp], 0, row, bar(VFULL + vs));
+            tma_load_2d(sbase + OFF_V + vs * KTILE_B + sp * KSPAN_B, &maps.v[sp], 0, krow, bar(VFULL + vs));
           v_issued = j + 1;
         }
       }
@@ -270,11 +286,6 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
     }
   } else {
     // ---------------- softmax warps: thread = query row ----------------
-    const int row = threadIdx.x;
-    const int gr = r0 + row;
-    const bool valid = gr < n_rows;
-    const int tok = valid ? gr / a.G : 0;
-    const int gg = valid ? gr - tok * a.G : 0;
     const int lim = valid ? P0 + tok : -1;                  // last key this row sees
     {
       // q * sm_scale * log2(e) -> fp16 hi + lo rows of the A operand
@@ -297,8 +308,6 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(QREADY)) : "memory");
     }
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m = -1e30f, l = 0.f;
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j % 3;
       lost = __any_sync(kAll, !mbar_wait(bar(SFULL + b), (j / 3) & 1));
@@ -309,7 +318,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       for (int c0 = 0; c0 < BN; c0 += 32)
         tmem_ld32(tmem + lane_base + (uint32_t)(b * BN) + c0, *reinterpret_cast<uint32_t(*)[32]>(sv + c0));
       tmem_wait_ld();
-      const int key0 = j * BN;
+      const int key0 = (j0 + j) * BN;
       if (key0 + BN - 1 > lim) {   // keys past this row's causal limit
 #pragma unroll
         for (int c = 0; c < BN; ++c)
@@ -372,27 +381,91 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(PFULL + b)) : "memory");
     }
     if (!lost && n_tiles > 0) lost = __any_sync(kAll, !mbar_wait(bar(ALLDONE), 0));
-    tc_fence_after();
-    float* orow = a.out + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HD;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+  }
+  // every copy and MMA of the CTA has completed (each role drained its own)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const bool soft = warp < kSoftWarps;
+  float* orow = a.out + ((size_t)tok * a.n_q + (size_t)kvh * a.G + gg) * HD;
+  const float nan = __int_as_float(0x7fc00000);
+  if (n_split == 1) {
+    if (soft) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-    for (int c0 = 0; c0 < HD; c0 += 32) {
-      uint32_t ov[32];
-      tmem_ld32(tmem + lane_base + COL_O + c0, ov);
-      tmem_wait_ld();
-      if (valid) {
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + lane_base + COL_O + c0, ov);
+        tmem_wait_ld();
+        if (valid) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float4 r4 = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
-                                  __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
-          if (lost) {
-            const float nan = __int_as_float(0x7fc00000);
-            r4 = make_float4(nan, nan, nan, nan);
+          for (int e = 0; e < 32; e += 4) {
+            float4 r4 = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                    __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+            if (lost) r4 = make_float4(nan, nan, nan, nan);
+            *reinterpret_cast<float4*>(orow + c0 + e) = r4;
           }
-          *reinterpret_cast<float4*>(orow + c0 + e) = r4;
         }
       }
     }
+  } else {
+    // Merge of the cluster's key splits through distributed shared memory
+    // (the q and K stage areas are free now): (m, l) of every row first,
+    // then each CTA's O scaled by 2^(m - M) / L, then each CTA sums a slice
+    // of the columns over the cluster and writes it.  Every thread of every
+    // CTA passes the three cluster barriers exactly once.
+    float2* s_ml = reinterpret_cast<float2*>(smem + OFF_K);   // [BM]: (m, l) of each row
+    const uint32_t s_o = sbase + OFF_QH;                     // [BM][HD] fp32, 16-byte chunks swizzled
+    auto o_chunk = [&](int r, int ch) -> uint32_t {          // byte offset of chunk ch of row r
+      return (uint32_t)(r * HD * 4) + ((uint32_t)(ch ^ (r & 7)) << 4);
+    };
+    if (soft) s_ml[row] = make_float2(m, lost ? nan : l);   // a lost wait: NaN through L
+    cluster_sync_all();
+    if (soft) {
+      float M = -INFINITY;
+      for (int z = 0; z < n_split; ++z) M = fmaxf(M, ld_dsmem_f32(smem_u32(&s_ml[row].x), z));
+      float L = 0.f;
+      for (int z = 0; z < n_split; ++z) {
+        const float mz = ld_dsmem_f32(smem_u32(&s_ml[row].x), z), lz = ld_dsmem_f32(smem_u32(&s_ml[row].y), z);
+        L += lz * fast_exp2(mz - M);
+      }
+      const float c = fast_exp2(m - M) / L;   // this split's weight (rows that see no key: unused)
+#pragma unroll
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t ov[32];
+        if (n_tiles > 0) {
+          tmem_ld32(tmem + lane_base + COL_O + c0, ov);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 r4 = n_tiles > 0
+              ? make_float4(__uint_as_float(ov[e]) * c, __uint_as_float(ov[e + 1]) * c,
+                            __uint_as_float(ov[e + 2]) * c, __uint_as_float(ov[e + 3]) * c)
+              : make_float4(0.f, 0.f, 0.f, 0.f);
+          st_shared_v4(s_o + o_chunk(row, (c0 + e) >> 2), r4);
+        }
+      }
+    }
+    cluster_sync_all();
+    if (soft && valid) {
+      // this CTA's slice of the row's 16-byte chunks, summed over the cluster
+      constexpr int NCH = HD / 4;
+      const int z0 = (int)blockIdx.z;
+      const int ch_b = z0 * NCH / n_split, ch_e = (z0 + 1) * NCH / n_split;
+      for (int ch = ch_b; ch < ch_e; ++ch) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int z = 0; z < n_split; ++z) {
+          const float4 v4 = ld_dsmem_v4(s_o + o_chunk(row, ch), z);
+          acc.x += v4.x;
+          acc.y += v4.y;
+          acc.z += v4.z;
+          acc.w += v4.w;
+        }
+        *reinterpret_cast<float4*>(orow + 4 * ch) = acc;
+      }
+    }
+    cluster_sync_all();   // no CTA leaves while a peer reads its shared memory
   }
   tc_fence_before();
   __syncthreads();
@@ -419,8 +492,76 @@ bool make_span_map(CUtensorMap* map, const void* base, int sp, long long rows, i
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One CTA per (128 query rows, KV head): 224 threads at head_dim 64 and 128,
-// 256 at 256.
+// The cluster launch of chunk_attn_tc<HD> with n_split CTAs per cluster
+// (along z); 1: a plain launch.
+template <int HD>
+cudaLaunchConfig_t tc_config(dim3 grid, int n_split, cudaStream_t s, cudaLaunchAttribute* attr) {
+  using Lay = tcc::TcLayout<HD>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(Lay::THREADS);
+  cfg.dynamicSmemBytes = Lay::SMEM;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)n_split;
+  cfg.attrs = attr;
+  cfg.numAttrs = n_split > 1 ? 1 : 0;
+  return cfg;
+}
+
+// Clusters of n_split CTAs that can be resident at once (the occupancy
+// query, once per context); 0 if none or unknown.
+template <int HD>
+int tc_max_clusters(int n_split) {
+  static ContextCache<int> cache[kMaxKeySplits + 1];
+  int v = 0;
+  if (!per_context(cache[n_split], &v, [n_split](int* out) {
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t cfg = tc_config<HD>(dim3(1, 1, n_split), n_split, nullptr, attr);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, (const void*)chunk_attn_tc<HD>, &cfg) != cudaSuccess)
+          return false;
+        *out = n;
+        return true;
+      }))
+    return 0;
+  return v;
+}
+
+// Key splits per (row tile, KV head).  A chunk with enough row tiles fills
+// the SMs by itself (1).  A short one over a long context would leave most
+// SMs idle, each CTA streaming every key tile: its key tiles are then split
+// over a cluster of up to kMaxKeySplits CTAs, the count that minimises
+// (waves of clusters) x (tiles per split), with the waves counted in the
+// clusters the occupancy query says can be resident and a split costing
+// about two tiles more for its merge; each split keeps at least four tiles.
+template <int HD>
+int tc_key_splits(long long base, int n_all) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  if (base >= sms) return 1;
+  double best_t = (double)((base + sms - 1) / sms) * n_all;
+  int best = 1;
+  for (int ns = 2; ns <= kMaxKeySplits && n_all >= 4 * ns; ++ns) {
+    const int maxc = tc_max_clusters<HD>(ns);
+    if (maxc <= 0) continue;
+    const double t = (double)((base + maxc - 1) / maxc) * ((n_all + ns - 1) / ns) + 2.0;
+    if (t < best_t) {
+      best_t = t;
+      best = ns;
+    }
+  }
+  return best;
+}
+
+// One CTA per (128 query rows, KV head, key split): 224 threads at head_dim
+// 64 and 128, 256 at 256.
 template <int HD>
 cudaError_t launch_tc(const ChunkArgs& a, cudaStream_t s) {
   using Lay = tcc::TcLayout<HD>;
@@ -442,8 +583,11 @@ cudaError_t launch_tc(const ChunkArgs& a, cudaStream_t s) {
   }
   const long long row_tiles = ((long long)a.T * a.G + tcc::BM - 1) / tcc::BM;
   if (row_tiles > 0x7fffffffLL || a.n_kv > 65535) return cudaErrorInvalidValue;
-  chunk_attn_tc<HD><<<dim3((unsigned)row_tiles, (unsigned)a.n_kv), Lay::THREADS, Lay::SMEM, s>>>(maps, a);
-  return cudaGetLastError();
+  const int n_split = tc_key_splits<HD>(row_tiles * a.n_kv, (a.P + Lay::BN - 1) / Lay::BN);
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      tc_config<HD>(dim3((unsigned)row_tiles, (unsigned)a.n_kv, (unsigned)n_split), n_split, s, attr);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_tc<HD>, maps, a);
 }
 
 }  // namespace

@@ -2,9 +2,10 @@
 // (tcgen05) used by the prompt-chunk attention: tensor-memory allocation,
 // MMA with the A operand in shared or tensor memory, commit to an
 // mbarrier, tensor-memory loads and stores, and the shared-memory and
-// instruction descriptors those MMAs take; and two Blackwell arithmetic
-// forms the chunk softmax uses (three-input max, packed fp32 add).  Each
-// wrapper is one PTX instruction.
+// instruction descriptors those MMAs take; two Blackwell arithmetic forms
+// the chunk softmax uses (three-input max, packed fp32 add); and the
+// cluster barrier and distributed-shared-memory loads of the key-split
+// merge.  Each wrapper is one or two PTX instructions.
 #pragma once
 
 #include <stdint.h>
@@ -130,6 +131,44 @@ static __device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0,
       " add.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// A barrier over every thread of every CTA of the cluster, ordering the
+// shared-memory accesses before it (release) against those after it
+// (acquire).  Each thread of the cluster must reach it the same number of
+// times; the warp is converged first (the instructions are .aligned).
+static __device__ __forceinline__ void cluster_sync_all() {
+  __syncwarp();
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Loads from the shared memory of the cluster's CTA `rank` at the offset
+// that smem_addr (a shared-window address of this CTA) has here.
+static __device__ __forceinline__ float ld_dsmem_f32(uint32_t smem_addr, int rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+static __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t smem_addr, int rank) {
+  uint32_t remote;
+  float4 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+static __device__ __forceinline__ void st_shared_v4(uint32_t smem_addr, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
 }
 
 static __device__ __forceinline__ void tmem_wait_ld() {

@@ -73,6 +73,15 @@ def _gpu_chunk(k16, v16, q, sm):
     (oracle.FMT_Q8, 3, 2, 64, 1500, 700),      # head_dim 64, ragged tiles, rows spanning tokens
     (oracle.FMT_F16, 2, 4, 256, 2000, 400),    # head_dim 256: 64-key tiles, one V stage, many tiles
     (oracle.FMT_K8V4, 1, 3, 256, 900, 333),    # head_dim 256, G = 3, ragged key and row tiles
+    # short chunks over long contexts: few row tiles, so the key tiles are
+    # split over a cluster of CTAs that merge through distributed shared memory
+    (oracle.FMT_F16, 2, 4, 128, 8192, 64),
+    (oracle.FMT_Q8, 1, 8, 64, 5000, 40),
+    (oracle.FMT_K8V4, 2, 2, 256, 3000, 100),
+    (oracle.FMT_F16, 1, 1, 128, 4096, 1),      # one token, one row
+    # 160 (row tile, KV head) CTAs: no key split
+    (oracle.FMT_F16, 8, 4, 64, 700, 640),
+    (oracle.FMT_Q8, 8, 4, 256, 700, 640),
 ])
 def test_chunk_matches_oracle(fmt, n_kv, G, hd, P, T):
     k16, v16 = _staging_from_oracle_pool(fmt, n_kv, hd, P, 31 + hd + T)
