@@ -602,7 +602,8 @@ def _chunk_attn_bench(torch, kvq):
     the measured dense bf16 peak (fp16 runs at the same nominal rate).  The
     other head dims the call serves (64 and 256, on the same tcgen05
     kernel) are timed beside it on a 4096-token chunk over 32768 cells
-    (16/4 and 16/2 heads)."""
+    (16/4 and 16/2 heads), and so is a 256-token chunk over the 131072
+    cells (few row tiles: its key tiles are split over clusters of CTAs)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             peak, kind = float(json.load(f)["bf16_tflops"]), "measured bf16 dense"
@@ -644,9 +645,8 @@ def _chunk_attn_bench(torch, kvq):
     others = {}
     for hd, n_kv, n_q in ((64, 4, 16), (256, 2, 16)):
         ms_o, tf_o = timed(n_kv, n_q, hd, 32768, 4096, 1005 + hd)
-        kind_k = "tcgen05"
         others[f"hd{hd}"] = {"workload": f"4096-token chunk over 32768 cells, {n_q}/{n_kv} heads, "
-                                         f"head_dim {hd} ({kind_k})",
+                                         f"head_dim {hd} (tcgen05)",
                              "ms": round(ms_o, 3), "TFLOP/s": round(tf_o, 1),
                              "frac": round(tf_o / peak, 4)}
     return {"workload": "4096-token chunk over 131072 cells, 32/8 heads, head_dim 128",
