@@ -286,6 +286,25 @@ kvq_status kvq_chunk_attn(const void *k16, const void *v16, int n_kv_heads, int 
                           void *stream);
 
 /*
+ * kvq_chunk_attn with the failure path of its waits exercised, for tests of
+ * that path only.  Every mbarrier wait of the chunk kernel is bounded; a
+ * wait that runs out turns the CTA's rows into NaN (through the merge too,
+ * when a short chunk's key tiles are split over a cluster of CTAs), and
+ * each role still waits (bounded) for its own copies and MMAs before the
+ * CTA exits, so the context stays usable.  This call adds extra_tx_bytes
+ * (a multiple of 16 in [16, 4096]) to the byte count every K and V stage
+ * expects, bytes no copy ever delivers, and bounds each wait by wait_limit
+ * polls (1 .. 2^25; kvq_chunk_attn uses 2^25): every wait runs out, and a
+ * correct failure path returns KVQ_OK with NaN in every output row.  No
+ * fault, trap or unbounded wait is involved.  Other arguments, checks and
+ * errors as kvq_chunk_attn.
+ */
+kvq_status kvq_chunk_attn_lost_wait_test(const void *k16, const void *v16, int n_kv_heads, int P,
+                                         int head_dim, const float *q, int T, int n_q,
+                                         float sm_scale, float *out, uint32_t wait_limit,
+                                         uint32_t extra_tx_bytes, void *stream);
+
+/*
  * Persistence of one sequence: cells [0, n_cells) gathered out of the pool
  * into token-major runs, and scattered back into a pool (Path F format v3:
  * persist per-head INT8 KV scales for INT8 + persistent KV interop,

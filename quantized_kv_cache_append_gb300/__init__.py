@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "kvq_decode_attn_lost_wait_test",
     "kvq_compact_f16",
     "kvq_chunk_attn",
+    "kvq_chunk_attn_lost_wait_test",
     "kvq_gather_cells",
     "kvq_scatter_cells",
     "kvq_stream_plan",
@@ -104,6 +105,9 @@ def load_library(path: Optional[str] = None):
     lib.kvq_compact_f16.argtypes = [CP, P, I, P, P, P]
     lib.kvq_chunk_attn.restype = I
     lib.kvq_chunk_attn.argtypes = [P, P, I, I, I, P, I, I, ctypes.c_float, P, P]
+    lib.kvq_chunk_attn_lost_wait_test.restype = I
+    lib.kvq_chunk_attn_lost_wait_test.argtypes = [P, P, I, I, I, P, I, I, ctypes.c_float, P,
+                                                  ctypes.c_uint32, ctypes.c_uint32, P]
     lib.kvq_gather_cells.restype = I
     lib.kvq_gather_cells.argtypes = [CP, P, I, P, P, P, P, P]
     lib.kvq_scatter_cells.restype = I
@@ -202,6 +206,14 @@ def kvq_chunk_attn(k16, v16, n_kv_heads: int, P: int, head_dim: int, q, T: int, 
                    sm_scale: float, out, stream=None) -> int:
     return load_library().kvq_chunk_attn(_ptr(k16), _ptr(v16), n_kv_heads, P, head_dim, _ptr(q),
                                          T, n_q, float(sm_scale), _ptr(out), _stream(stream))
+
+
+def kvq_chunk_attn_lost_wait_test(k16, v16, n_kv_heads: int, P: int, head_dim: int, q, T: int,
+                                  n_q: int, sm_scale: float, out, wait_limit: int,
+                                  extra_tx_bytes: int, stream=None) -> int:
+    return load_library().kvq_chunk_attn_lost_wait_test(
+        _ptr(k16), _ptr(v16), n_kv_heads, P, head_dim, _ptr(q), T, n_q, float(sm_scale), _ptr(out),
+        wait_limit, extra_tx_bytes, _stream(stream))
 
 
 def kvq_gather_cells(cache: kvq_cache, block_table_row, n_cells: int, codes_k, codes_v,

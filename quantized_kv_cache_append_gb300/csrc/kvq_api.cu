@@ -348,9 +348,11 @@ KVQ_API kvq_status kvq_scatter_cells(const kvq_cache* cache, const int32_t* bloc
                            false, stream);
 }
 
-KVQ_API kvq_status kvq_chunk_attn(const void* k16, const void* v16, int n_kv_heads, int P,
-                                  int head_dim, const float* q, int T, int n_q, float sm_scale,
-                                  float* out, void* stream) {
+namespace kvq {
+namespace {
+kvq_status chunk_impl(const void* k16, const void* v16, int n_kv_heads, int P, int head_dim,
+                      const float* q, int T, int n_q, float sm_scale, float* out, void* stream,
+                      uint32_t wait_limit = kDefaultWaitLimit, uint32_t extra_tx = 0) {
   if (k16 == nullptr || v16 == nullptr || q == nullptr || out == nullptr) return KVQ_ERR_ARG;
   if (!aligned(k16, 16) || !aligned(v16, 16) || !aligned(q, 16) || !aligned(out, 16))
     return KVQ_ERR_ARG;
@@ -372,8 +374,28 @@ KVQ_API kvq_status kvq_chunk_attn(const void* k16, const void* v16, int n_kv_hea
   a.n_q = n_q;
   a.G = n_q / n_kv_heads;
   a.qscale = sm_scale * 1.4426950408889634f;  // log2(e)
+  a.wait_limit = wait_limit;
+  a.extra_tx = extra_tx;
   const cudaError_t e = launch_chunk_attn(head_dim, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+}  // namespace
+}  // namespace kvq
+
+KVQ_API kvq_status kvq_chunk_attn(const void* k16, const void* v16, int n_kv_heads, int P,
+                                  int head_dim, const float* q, int T, int n_q, float sm_scale,
+                                  float* out, void* stream) {
+  return kvq::chunk_impl(k16, v16, n_kv_heads, P, head_dim, q, T, n_q, sm_scale, out, stream);
+}
+
+KVQ_API kvq_status kvq_chunk_attn_lost_wait_test(const void* k16, const void* v16, int n_kv_heads,
+                                                 int P, int head_dim, const float* q, int T, int n_q,
+                                                 float sm_scale, float* out, uint32_t wait_limit,
+                                                 uint32_t extra_tx_bytes, void* stream) {
+  if (wait_limit == 0 || wait_limit > kDefaultWaitLimit) return KVQ_ERR_ARG;
+  if (extra_tx_bytes == 0 || extra_tx_bytes > 4096 || extra_tx_bytes % 16 != 0) return KVQ_ERR_ARG;
+  return kvq::chunk_impl(k16, v16, n_kv_heads, P, head_dim, q, T, n_q, sm_scale, out, stream,
+                         wait_limit, extra_tx_bytes);
 }
 
 KVQ_API kvq_status kvq_stream_plan(int n_host_blocks, int n_slots, int32_t* slot_of_block,

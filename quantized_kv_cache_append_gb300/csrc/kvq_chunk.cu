@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y;
+  const uint32_t wl = a.wait_limit;   // polls before a wait is declared lost
   // row tiles in descending order: the last ones (later tokens) see the
   // most keys, so the longest CTAs start first and the grid's last, partial
   // wave holds the shortest
@@ -201,16 +202,16 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         const int ks = j % KST, vs = j % VST;
         const int krow = kvh * a.P + (j0 + j) * BN;   // first staging row of the tile
         if (do_k) {
-          if (j >= KST && !mbar_wait(bar(KEMPTY + ks), (j / KST - 1) & 1)) break;
-          mbar_expect_tx(bar(KFULL + ks), (uint32_t)KTILE_B);
+          if (j >= KST && !mbar_wait(bar(KEMPTY + ks), (j / KST - 1) & 1, wl)) break;
+          mbar_expect_tx(bar(KFULL + ks), (uint32_t)KTILE_B + a.extra_tx);
 #pragma unroll
           for (int sp = 0; sp < Lay::NSP; ++sp)
             tma_load_2d(sbase + OFF_K + ks * KTILE_B + sp * KSPAN_B, &maps.k[sp], 0, krow, bar(KFULL + ks));
           k_issued = j + 1;
         }
         if (do_v) {
-          if (j >= VST && !mbar_wait(bar(VEMPTY + vs), (j / VST - 1) & 1)) break;
-          mbar_expect_tx(bar(VFULL + vs), (uint32_t)KTILE_B);
+          if (j >= VST && !mbar_wait(bar(VEMPTY + vs), (j / VST - 1) & 1, wl)) break;
+          mbar_expect_tx(bar(VFULL + vs), (uint32_t)KTILE_B + a.extra_tx);
 #pragma unroll
           for (int sp = 0; sp < Lay::NSP; ++sp)
             tma_load_2d(sbase + OFF_V + vs * KTILE_B + sp * KSPAN_B, &maps.v[sp], 0, krow, bar(VFULL + vs));
@@ -220,9 +221,9 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       // every copy has landed before the CTA can exit (the waits return at
       // once in normal runs; they are bounded after a lost wait)
       for (int j = k_issued > KST ? k_issued - KST : 0; j < k_issued; ++j)
-        (void)mbar_wait(bar(KFULL + j % KST), (j / KST) & 1);
+        (void)mbar_wait(bar(KFULL + j % KST), (j / KST) & 1, wl);
       for (int j = v_issued > VST ? v_issued - VST : 0; j < v_issued; ++j)
-        (void)mbar_wait(bar(VFULL + j % VST), (j / VST) & 1);
+        (void)mbar_wait(bar(VFULL + j % VST), (j / VST) & 1, wl);
     }
   } else if (warp == kMmaWarp) {
     // S_j = Q_hi K_j^T + Q_lo K_j^T, up to three tiles ahead of the P V
@@ -233,11 +234,11 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       const uint64_t dq[2] = {umma_desc_sw128(sbase + OFF_QH, 16, 1024),
                               umma_desc_sw128(sbase + OFF_QL, 16, 1024)};
       const uint64_t dk0 = umma_desc_sw128(sbase + OFF_K, 16, 1024);
-      bool ok = mbar_wait(bar(QREADY), 0);
+      bool ok = mbar_wait(bar(QREADY), 0, wl);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int ks = j % KST, b = j % 3;
-        ok = mbar_wait(bar(KFULL + ks), (j / KST) & 1) &&
-             (j < 3 || mbar_wait(bar(SFREE + b), (j / 3 - 1) & 1));
+        ok = mbar_wait(bar(KFULL + ks), (j / KST) & 1, wl) &&
+             (j < 3 || mbar_wait(bar(SFREE + b), (j / 3 - 1) & 1, wl));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * BN);
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       // every MMA this thread issued has completed before the CTA frees the
       // tensor memory (at once in normal runs; bounded after a lost wait)
       umma_commit(bar(SDRAIN));
-      (void)mbar_wait(bar(SDRAIN), 0);
+      (void)mbar_wait(bar(SDRAIN), 0, wl);
     }
   } else if (warp == kPvWarp) {
     // O += P_j V_j.  A thread of its own: while it waits for a tile's p,
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       bool ok = true;
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int vs = j % VST, b = j % 3;
-        ok = mbar_wait(bar(PFULL + b), (j / 3) & 1) && mbar_wait(bar(VFULL + vs), (j / VST) & 1);
+        ok = mbar_wait(bar(PFULL + b), (j / 3) & 1, wl) && mbar_wait(bar(VFULL + vs), (j / VST) & 1, wl);
         if (!ok) break;
         tc_fence_after();
         const uint32_t pa = tmem + (uint32_t)(b * BN);
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       }
       if (ok) umma_commit(bar(ALLDONE));   // every product above has completed
       umma_commit(bar(PDRAIN));
-      (void)mbar_wait(bar(PDRAIN), 0);
+      (void)mbar_wait(bar(PDRAIN), 0, wl);
     }
   } else {
     // ---------------- softmax warps: thread = query row ----------------
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
     }
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j % 3;
-      lost = __any_sync(kAll, !mbar_wait(bar(SFULL + b), (j / 3) & 1));
+      lost = __any_sync(kAll, !mbar_wait(bar(SFULL + b), (j / 3) & 1, wl));
       if (lost) break;
       tc_fence_after();
       float sv[BN];
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       }
       if (j > 0 && __any_sync(kAll, rise)) {
         // O holds P V of the tiles so far: wait for the last one, rescale
-        lost = __any_sync(kAll, !mbar_wait(bar(SFREE + (j - 1) % 3), ((j - 1) / 3) & 1));
+        lost = __any_sync(kAll, !mbar_wait(bar(SFREE + (j - 1) % 3), ((j - 1) / 3) & 1, wl));
         if (lost) break;
         tc_fence_after();
 #pragma unroll
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
       tc_fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(PFULL + b)) : "memory");
     }
-    if (!lost && n_tiles > 0) lost = __any_sync(kAll, !mbar_wait(bar(ALLDONE), 0));
+    if (!lost && n_tiles > 0) lost = __any_sync(kAll, !mbar_wait(bar(ALLDONE), 0, wl));
   }
   // every copy and MMA of the CTA has completed (each role drained its own)
   tc_fence_before();

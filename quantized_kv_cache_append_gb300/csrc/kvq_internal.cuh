@@ -260,6 +260,9 @@ struct ChunkArgs {
   float* out;          // [T][n_q][hd]
   int n_kv, P, T, n_q, G;
   float qscale;        // sm_scale * log2(e)
+  uint32_t wait_limit; // polls of an mbarrier wait before it is declared lost
+  uint32_t extra_tx;   // bytes added to each K / V stage's expected count (0; >0 only
+                       // in the lost-wait test, which makes every copy wait run out)
 };
 cudaError_t launch_chunk_attn(int hd, const ChunkArgs& a, cudaStream_t s);
 
