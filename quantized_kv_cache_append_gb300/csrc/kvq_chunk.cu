@@ -122,7 +122,10 @@ __device__ __forceinline__ uint32_t sw(int r, int b) {
 }
 }  // namespace tcc
 
-template <int HD>
+// LW: the lost-wait test's instantiation, whose waits take their poll limit
+// from the call and whose stages expect a.extra_tx bytes more than any copy
+// delivers; the ordinary one keeps the constant limit in its hot loops.
+template <int HD, bool LW>
 __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
     chunk_attn_tc(const __grid_constant__ ChunkMaps maps, ChunkArgs a) {
   using namespace tcc;
@@ -140,7 +143,8 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y;
-  const uint32_t wl = a.wait_limit;   // polls before a wait is declared lost
+  const uint32_t wl = LW ? a.wait_limit : kDefaultWaitLimit;   // polls before a wait is lost
+  const uint32_t extra_tx = LW ? a.extra_tx : 0u;
   // row tiles in descending order: the last ones (later tokens) see the
   // most keys, so the longest CTAs start first and the grid's last, partial
   // wave holds the shortest
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         const int krow = kvh * a.P + (j0 + j) * BN;   // first staging row of the tile
         if (do_k) {
           if (j >= KST && !mbar_wait(bar(KEMPTY + ks), (j / KST - 1) & 1, wl)) break;
-          mbar_expect_tx(bar(KFULL + ks), (uint32_t)KTILE_B + a.extra_tx);
+          mbar_expect_tx(bar(KFULL + ks), (uint32_t)KTILE_B + extra_tx);
 #pragma unroll
           for (int sp = 0; sp < Lay::NSP; ++sp)
             tma_load_2d(sbase + OFF_K + ks * KTILE_B + sp * KSPAN_B, &maps.k[sp], 0, krow, bar(KFULL + ks));
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(tcc::TcLayout<HD>::THREADS, 1)
         }
         if (do_v) {
           if (j >= VST && !mbar_wait(bar(VEMPTY + vs), (j / VST - 1) & 1, wl)) break;
-          mbar_expect_tx(bar(VFULL + vs), (uint32_t)KTILE_B + a.extra_tx);
+          mbar_expect_tx(bar(VFULL + vs), (uint32_t)KTILE_B + extra_tx);
 #pragma unroll
           for (int sp = 0; sp < Lay::NSP; ++sp)
             tma_load_2d(sbase + OFF_V + vs * KTILE_B + sp * KSPAN_B, &maps.v[sp], 0, krow, bar(VFULL + vs));
@@ -514,7 +518,7 @@ cudaLaunchConfig_t tc_config(dim3 grid, int n_split, cudaStream_t s, cudaLaunchA
 
 // Clusters of n_split CTAs that can be resident at once (the occupancy
 // query, once per context); 0 if none or unknown.
-template <int HD>
+template <int HD, bool LW>
 int tc_max_clusters(int n_split) {
   static ContextCache<int> cache[kMaxKeySplits + 1];
   int v = 0;
@@ -522,7 +526,7 @@ int tc_max_clusters(int n_split) {
         cudaLaunchAttribute attr[1];
         const cudaLaunchConfig_t cfg = tc_config<HD>(dim3(1, 1, n_split), n_split, nullptr, attr);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, (const void*)chunk_attn_tc<HD>, &cfg) != cudaSuccess)
+        if (cudaOccupancyMaxActiveClusters(&n, (const void*)chunk_attn_tc<HD, LW>, &cfg) != cudaSuccess)
           return false;
         *out = n;
         return true;
@@ -538,7 +542,7 @@ int tc_max_clusters(int n_split) {
 // (waves of clusters) x (tiles per split), with the waves counted in the
 // clusters the occupancy query says can be resident and a split costing
 // about two tiles more for its merge; each split keeps at least four tiles.
-template <int HD>
+template <int HD, bool LW>
 int tc_key_splits(long long base, int n_all) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -550,7 +554,7 @@ int tc_key_splits(long long base, int n_all) {
   double best_t = (double)((base + sms - 1) / sms) * n_all;
   int best = 1;
   for (int ns = 2; ns <= kMaxKeySplits && n_all >= 4 * ns; ++ns) {
-    const int maxc = tc_max_clusters<HD>(ns);
+    const int maxc = tc_max_clusters<HD, LW>(ns);
     if (maxc <= 0) continue;
     const double t = (double)((base + maxc - 1) / maxc) * ((n_all + ns - 1) / ns) + 2.0;
     if (t < best_t) {
@@ -563,14 +567,14 @@ int tc_key_splits(long long base, int n_all) {
 
 // One CTA per (128 query rows, KV head, key split): 224 threads at head_dim
 // 64 and 128, 256 at 256.
-template <int HD>
-cudaError_t launch_tc(const ChunkArgs& a, cudaStream_t s) {
+template <int HD, bool LW>
+cudaError_t launch_tc_kernel(const ChunkArgs& a, cudaStream_t s) {
   using Lay = tcc::TcLayout<HD>;
   static ContextCache<int> limit_set;
   int done = 0;
   if (!per_context(limit_set, &done, [](int* v) {
         *v = 1;
-        return cudaFuncSetAttribute(chunk_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(chunk_attn_tc<HD, LW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Lay::SMEM) == cudaSuccess;
       }))
     return cudaErrorInvalidConfiguration;
@@ -584,11 +588,16 @@ cudaError_t launch_tc(const ChunkArgs& a, cudaStream_t s) {
   }
   const long long row_tiles = ((long long)a.T * a.G + tcc::BM - 1) / tcc::BM;
   if (row_tiles > 0x7fffffffLL || a.n_kv > 65535) return cudaErrorInvalidValue;
-  const int n_split = tc_key_splits<HD>(row_tiles * a.n_kv, (a.P + Lay::BN - 1) / Lay::BN);
+  const int n_split = tc_key_splits<HD, LW>(row_tiles * a.n_kv, (a.P + Lay::BN - 1) / Lay::BN);
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg =
       tc_config<HD>(dim3((unsigned)row_tiles, (unsigned)a.n_kv, (unsigned)n_split), n_split, s, attr);
-  return cudaLaunchKernelEx(&cfg, chunk_attn_tc<HD>, maps, a);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_tc<HD, LW>, maps, a);
+}
+
+template <int HD>
+cudaError_t launch_tc(const ChunkArgs& a, cudaStream_t s) {
+  return a.extra_tx != 0 ? launch_tc_kernel<HD, true>(a, s) : launch_tc_kernel<HD, false>(a, s);
 }
 
 }  // namespace

@@ -1430,7 +1430,6 @@ cudaError_t launch_impl(const DecodePlan& p, const DecodeArgs& a, cudaStream_t s
 // Kernel shape of a row count: 0 = one 8-column tile with hi/lo columns
 // (at most 4 rows), else the number of 8-row tiles.
 int tile_code(int rows) { return rows <= 4 ? 0 : rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : -1; }
-int n_tiles_for(int rows) { const int c = tile_code(rows); return c == 0 ? 1 : c < 0 ? 0 : c; }
 
 template <int FMT, int HD>
 int ctas_per_sm_hd(int code) {
