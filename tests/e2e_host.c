@@ -23,6 +23,8 @@
  * the four library calls and waiting in the synchronize; exit status 0 on
  * success, 1 on any CUDA or library error (with a message on stderr).
  */
+#define _POSIX_C_SOURCE 199309L /* clock_gettime in strict C */
+
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
