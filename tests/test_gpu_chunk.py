@@ -110,6 +110,27 @@ def test_full_chunk_sampled_tokens():
         assert_attention_close(got[t:t + 1], ref)
 
 
+def test_short_chunk_sampled_tokens():
+    # the benchmark's short chunk: 256 tokens over 131072 cells, 32/8 heads,
+    # head_dim 128 -- 64 (row tile, KV head) pairs, so the key tiles are
+    # split over clusters of CTAs and merged through distributed shared
+    # memory; sampled tokens against the oracle over exactly their cells
+    n_kv, G, hd, P, T = 8, 4, 128, 131072, 256
+    g = torch.Generator().manual_seed(1777)
+    kf = torch.randn(n_kv, P, hd, generator=g)
+    vf = torch.randn(n_kv, P, hd, generator=g)
+    q = torch.randn(T, n_kv * G, hd, generator=g).numpy()
+    k16 = oracle.fp16_bits(kf.numpy())
+    v16 = oracle.fp16_bits(vf.numpy())
+    got = _gpu_chunk(k16, v16, q, _sm(hd))
+    assert np.isfinite(got).all()
+    for t in (0, 1, 127, 128, 255):
+        n_vis = P - T + t + 1
+        ref = oracle.chunk_attention(np.ascontiguousarray(k16[:, :n_vis]),
+                                     np.ascontiguousarray(v16[:, :n_vis]), q[t:t + 1], _sm(hd))
+        assert_attention_close(got[t:t + 1], ref)
+
+
 @pytest.mark.parametrize("hd", [64, 128, 256])
 def test_chunk_rising_logits(hd):
     # logits that climb along the keys (a ramp in one K channel, q aligned
