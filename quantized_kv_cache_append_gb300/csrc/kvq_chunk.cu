@@ -19,6 +19,7 @@
 #include <string.h>
 
 #include "kvq_internal.cuh"
+#include "kvq_key_splits.h"
 #include "kvq_ptx.cuh"
 #include "kvq_tc.cuh"
 
@@ -26,7 +27,6 @@ namespace kvq {
 namespace {
 
 constexpr float kTauC = 8.0f;     // lazy rescale threshold (log2 units)
-constexpr int kMaxKeySplits = 8;  // CTAs of a key-split cluster (the portable maximum)
 constexpr unsigned kAll = 0xffffffffu;
 
 struct ChunkMaps {
@@ -535,13 +535,8 @@ int tc_max_clusters(int n_split) {
   return v;
 }
 
-// Key splits per (row tile, KV head).  A chunk with enough row tiles fills
-// the SMs by itself (1).  A short one over a long context would leave most
-// SMs idle, each CTA streaming every key tile: its key tiles are then split
-// over a cluster of up to kMaxKeySplits CTAs, the count that minimises
-// (waves of clusters) x (tiles per split), with the waves counted in the
-// clusters the occupancy query says can be resident and a split costing
-// about two tiles more for its merge; each split keeps at least four tiles.
+// Key splits per (row tile, KV head) (choose_key_splits), with the clusters
+// that can be resident taken from the occupancy query.
 template <int HD, bool LW>
 int tc_key_splits(long long base, int n_all) {
   int dev = 0, sms = 0;
@@ -550,19 +545,7 @@ int tc_key_splits(long long base, int n_all) {
     (void)cudaGetLastError();
     return 1;
   }
-  if (base >= sms) return 1;
-  double best_t = (double)((base + sms - 1) / sms) * n_all;
-  int best = 1;
-  for (int ns = 2; ns <= kMaxKeySplits && n_all >= 4 * ns; ++ns) {
-    const int maxc = tc_max_clusters<HD, LW>(ns);
-    if (maxc <= 0) continue;
-    const double t = (double)((base + maxc - 1) / maxc) * ((n_all + ns - 1) / ns) + 2.0;
-    if (t < best_t) {
-      best_t = t;
-      best = ns;
-    }
-  }
-  return best;
+  return choose_key_splits(base, n_all, sms, [](int ns) { return tc_max_clusters<HD, LW>(ns); });
 }
 
 // One CTA per (128 query rows, KV head, key split): 224 threads at head_dim
