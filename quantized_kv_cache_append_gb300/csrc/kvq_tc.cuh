@@ -5,7 +5,7 @@
 // instruction descriptors those MMAs take; two Blackwell arithmetic forms
 // the chunk softmax uses (three-input max, packed fp32 add); and the
 // cluster barrier and distributed-shared-memory loads of the key-split
-// merge.  Each wrapper is one or two PTX instructions.
+// merge.  Each wrapper is one or a few PTX instructions.
 #pragma once
 
 #include <stdint.h>
@@ -30,8 +30,9 @@ static __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr, u
 // stay below 2^18, so the sum never carries into the next field.  Building
 // each operand's descriptor once and stepping it by compile-time offsets
 // keeps the issuing thread's work between MMAs to one 64-bit add per
-// operand: with the full construction per MMA, an M = 128, N = 128 MMA
-// issued every 116-119 cycles instead of the tensor core's 64.
+// operand: in a probe that built both descriptors in full before every MMA,
+// one M = 128, N = 128 MMA was issued every 119 cycles instead of the
+// tensor core's 64.
 static __device__ __forceinline__ uint64_t umma_desc_step(uint64_t desc, uint32_t bytes) {
   return desc + (uint64_t)(bytes >> 4);
 }
